@@ -1,0 +1,109 @@
+/*
+ * swa_attn.h — C ABI of libswa.so: memory-linear causal sliding-window attention with grouped-query
+ * heads, forward and backward, hand-written for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (per batch b and query head hq, with kv head hk = hq / (Hq / Hkv)):
+ *
+ *     visible(i, j) <=> 0 <= i - j < window          (each query sees itself and the window-1
+ *                                                     keys before it; window >= N is plain causal)
+ *     S[i, j] = scale * <Q[i], K[j]>  (visible cells only)
+ *     LSE[i]  = ln sum_j exp(S[i, j]),  P = exp(S - LSE),  O = P V
+ *
+ * This is the attention of "Off NVIDIA, you fix the platform yourself" (Layer2C Lab 28), section
+ * "What was broken?": a score table with one row per token and one column per earlier token, where
+ * under a sliding window each token sees only the W tokens before it.  As in the mlx-train-perf
+ * README (flash-attention section) only O and the per-row log-sum-exp are saved by the forward,
+ * and the backward recomputes the score tiles it needs; the N x N matrix is never stored.
+ *
+ * Layout: every tensor is contiguous, row-major.
+ *     q, o, dO, dq     bf16  [B, Hq,  N, D]
+ *     k, v, dk, dv     bf16  [B, Hkv, N, D]
+ *     lse              fp32  [B, Hq,  N]      natural log, over the scaled scores
+ * Supported: D in {64, 128}; Hq % Hkv == 0; N >= 1; B >= 1; window >= 1; scale finite and > 0.
+ * All device pointers must be 16-byte aligned.
+ *
+ * Ownership: the caller allocates every buffer (device memory), including the backward workspace.
+ * The library allocates no device memory, keeps no per-call state, and never synchronizes the
+ * stream; calls are asynchronous on `stream` (0 = the legacy default stream).
+ *
+ * Errors: arguments are checked on the host before anything is launched; a bad argument returns
+ * its code and launches nothing.  Launch failures return SWA_ERR_CUDA.  The entry points never
+ * throw, abort or print.  Every wait inside the kernels is bounded; a kernel whose wait runs out
+ * records it in a per-device error word and returns early — read it with swa_check_device().
+ */
+#ifndef SWA_ATTN_H
+#define SWA_ATTN_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SWA_OK = 0,
+    SWA_ERR_INVALID_ARG = 1,    /* a size, window or scale outside its domain, or a null pointer  */
+    SWA_ERR_UNSUPPORTED = 2,    /* D not in {64, 128}, or no sm_100-family device current         */
+    SWA_ERR_MISALIGNED = 3,     /* a tensor pointer not 16-byte aligned                          */
+    SWA_ERR_CUDA = 4,           /* a CUDA runtime / driver call or a launch failed               */
+    SWA_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait ran out (reported by swa_check_device) */
+    SWA_ERR_WORKSPACE = 6       /* backward workspace null or smaller than required              */
+} swa_status;
+
+/*
+ * Forward.  Writes o [B,Hq,N,D] bf16 and lse [B,Hq,N] fp32.
+ *   q, k, v : inputs (device, bf16, layout above); not modified.
+ *   o, lse  : outputs (device); fully overwritten for rows 0..N-1.
+ *   window  : W >= 1; values >= N mean full causal attention.
+ *   scale   : softmax scale applied to <q, k> (typically 1/sqrt(D)).
+ * Saved state for the backward is exactly (o, lse) — the lab's windowed forward that "may emit the
+ * logsumexp under a window" (Lab 28, "Method and disclosure").
+ */
+swa_status swa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int Hq, int Hkv, int N, int D, int window, float scale,
+                        cudaStream_t stream);
+
+/*
+ * Bytes of device workspace swa_attn_bwd needs: one fp32 Delta = rowsum(dO * O) per query row,
+ * B*Hq*N*4 bytes (rounded up to 256).  Returns 0 for invalid sizes.
+ */
+size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int N, int D);
+
+/*
+ * Backward of L = sum(dO * O) through the forward above.  Writes dq [B,Hq,N,D], dk and dv
+ * [B,Hkv,N,D] (bf16), fully overwritten; dk/dv hold the sum over the G = Hq/Hkv query heads that
+ * share each kv head.
+ *   q, k, v, o, dO, lse : device inputs; o and lse must be the forward's outputs for (q, k, v).
+ *   workspace           : device scratch of at least swa_attn_bwd_workspace_bytes(B,Hq,N,D) bytes,
+ *                         16-byte aligned; contents on entry are ignored and left undefined.
+ * Three kernels run in order on `stream`: Delta = rowsum(dO * O), the dK/dV kernel (each key block
+ * walks only the query blocks inside its window, over every query head of its group) and the dQ
+ * kernel (each query block walks only the key blocks inside its window).  The window bookkeeping
+ * follows Lab 28's patch ("Method and disclosure"): blocks wholly outside the window are skipped,
+ * edge tiles are masked, dQ starts at each query tile's first visited key tile, and dK/dV of key
+ * tiles that no query visits are written as zeros.
+ */
+swa_status swa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                        const float* lse, void* dq, void* dk, void* dv,
+                        int B, int Hq, int Hkv, int N, int D, int window, float scale,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* swa_strerror(swa_status status);
+
+/*
+ * Synchronizes `stream`, then reads and clears the current device's error word, which a kernel
+ * sets when one of its bounded waits runs out.  Returns SWA_ERR_DEVICE_TIMEOUT if it was set,
+ * SWA_ERR_CUDA if the synchronize failed, else SWA_OK.
+ */
+swa_status swa_check_device(cudaStream_t stream);
+
+/* Library ABI version (major*100 + minor). */
+int swa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_ATTN_H */

@@ -1,0 +1,224 @@
+"""Python binding of libswa.so: causal sliding-window attention with grouped-query heads for
+training, forward and backward, hand-written for GB300 (sm_103a).
+
+The binding only marshals arguments: torch tensors become device pointers and the current CUDA
+stream becomes ``cudaStream_t``; every step of the computation runs in the library's kernels.
+PyTorch owns all device memory (outputs and the backward workspace are allocated here with torch).
+There is no fallback: if libswa.so is missing or the device is not sm_103, the calls raise.
+
+    o, lse = swa_attn_fwd(q, k, v, window, scale)
+    dq, dk, dv = swa_attn_bwd(q, k, v, o, do, lse, window, scale)
+    out = SlidingWindowAttention.apply(q, k, v, window, scale)   # autograd wrapper
+
+Layout: q, o, do, dq [B, Hq, N, D]; k, v, dk, dv [B, Hkv, N, D], all contiguous bf16;
+lse [B, Hq, N] fp32.  D in {64, 128}; Hq % Hkv == 0.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+__all__ = [
+    "load",
+    "library_path",
+    "SwaError",
+    "swa_attn_fwd",
+    "swa_attn_bwd",
+    "swa_attn_bwd_workspace_bytes",
+    "swa_check_device",
+    "SlidingWindowAttention",
+    "STATUS",
+]
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libswa.so"
+_lib: Optional[ctypes.CDLL] = None
+
+STATUS = {
+    0: "SWA_OK",
+    1: "SWA_ERR_INVALID_ARG",
+    2: "SWA_ERR_UNSUPPORTED",
+    3: "SWA_ERR_MISALIGNED",
+    4: "SWA_ERR_CUDA",
+    5: "SWA_ERR_DEVICE_TIMEOUT",
+    6: "SWA_ERR_WORKSPACE",
+}
+
+# Every symbol include/swa_attn.h declares, with its ctypes signature.
+_c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+SIGNATURES = {
+    "swa_attn_fwd": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _vp]),
+    "swa_attn_bwd_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
+    "swa_attn_bwd": (
+        _c_int,
+        [_vp] * 9 + [_c_int] * 6 + [_c_float, _vp, ctypes.c_size_t, _vp],
+    ),
+    "swa_strerror": (ctypes.c_char_p, [_c_int]),
+    "swa_check_device": (_c_int, [_vp]),
+    "swa_version": (_c_int, []),
+}
+
+
+class SwaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = STATUS.get(code, f"status {code}")
+        if _lib is not None:
+            msg = _lib.swa_strerror(code).decode()
+        super().__init__(f"{where}: {msg}")
+
+
+def library_path() -> str:
+    return os.path.join(_PKG_DIR, _LIB_NAME)
+
+
+def load() -> ctypes.CDLL:
+    """Load libswa.so (built in-tree by ``sliding_window_flash_gb300.build``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} not found: build it with `python -m sliding_window_flash_gb300.build` "
+            "(there is no CPU or PyTorch fallback)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _stream_handle(device) -> int:
+    import torch
+
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check_tensor(t, name, shape, dtype):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _dims(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be 4-D [B, H, N, D]")
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    return B, Hq, Hkv, N, D
+
+
+def _scale(scale, D):
+    return float(scale) if scale is not None else 1.0 / math.sqrt(D)
+
+
+def swa_attn_fwd(q, k, v, window: int, scale: Optional[float] = None, out=None, lse=None):
+    """Forward: returns (o [B,Hq,N,D] bf16, lse [B,Hq,N] fp32)."""
+    import torch
+
+    lib = load()
+    B, Hq, Hkv, N, D = _dims(q, k)
+    _check_tensor(q, "q", (B, Hq, N, D), torch.bfloat16)
+    _check_tensor(k, "k", (B, Hkv, N, D), torch.bfloat16)
+    _check_tensor(v, "v", (B, Hkv, N, D), torch.bfloat16)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    _check_tensor(out, "out", (B, Hq, N, D), torch.bfloat16)
+    _check_tensor(lse, "lse", (B, Hq, N), torch.float32)
+    rc = lib.swa_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                          B, Hq, Hkv, N, D, int(window), _scale(scale, D), _stream_handle(q.device))
+    if rc != 0:
+        raise SwaError(rc, "swa_attn_fwd")
+    return out, lse
+
+
+def swa_attn_bwd_workspace_bytes(B: int, Hq: int, N: int, D: int) -> int:
+    return int(load().swa_attn_bwd_workspace_bytes(B, Hq, N, D))
+
+
+def swa_attn_bwd(q, k, v, o, do, lse, window: int, scale: Optional[float] = None,
+                 dq=None, dk=None, dv=None, workspace=None) -> Tuple:
+    """Backward of sum(do * o): returns (dq, dk, dv), bf16, dk/dv summed over each kv group."""
+    import torch
+
+    lib = load()
+    B, Hq, Hkv, N, D = _dims(q, k)
+    for t, name, hs in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq)):
+        _check_tensor(t, name, (B, hs, N, D), torch.bfloat16)
+    _check_tensor(lse, "lse", (B, Hq, N), torch.float32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, name, hs in ((dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
+        _check_tensor(t, name, (B, hs, N, D), torch.bfloat16)
+    ws_bytes = int(lib.swa_attn_bwd_workspace_bytes(B, Hq, N, D))
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    rc = lib.swa_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                          B, Hq, Hkv, N, D, int(window), _scale(scale, D),
+                          workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                          _stream_handle(q.device))
+    if rc != 0:
+        raise SwaError(rc, "swa_attn_bwd")
+    return dq, dk, dv
+
+
+def swa_check_device(device=None) -> None:
+    """Synchronize the current stream and raise if a kernel's bounded wait ran out."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    rc = load().swa_check_device(_stream_handle(dev))
+    if rc != 0:
+        raise SwaError(rc, "swa_check_device")
+
+
+def _make_autograd():
+    import torch
+
+    class SlidingWindowAttention(torch.autograd.Function):
+        """o = attention(q, k, v) with a causal window; saves only (o, lse) for the backward."""
+
+        @staticmethod
+        def forward(ctx, q, k, v, window: int, scale: Optional[float] = None):
+            o, lse = swa_attn_fwd(q, k, v, window, scale)
+            ctx.save_for_backward(q, k, v, o, lse)
+            ctx.window, ctx.scale = window, scale
+            return o
+
+        @staticmethod
+        def backward(ctx, do):
+            q, k, v, o, lse = ctx.saved_tensors
+            dq, dk, dv = swa_attn_bwd(q, k, v, o, do.contiguous(), lse, ctx.window, ctx.scale)
+            return dq, dk, dv, None, None
+
+    return SlidingWindowAttention
+
+
+class _LazyAutograd:
+    _cls = None
+
+    def __getattr__(self, name):
+        if _LazyAutograd._cls is None:
+            _LazyAutograd._cls = _make_autograd()
+        return getattr(_LazyAutograd._cls, name)
+
+
+SlidingWindowAttention = _LazyAutograd()

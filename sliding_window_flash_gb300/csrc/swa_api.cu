@@ -1,0 +1,161 @@
+// swa_api.cu — the C ABI of libswa.so (declared in include/swa_attn.h): argument checks, the
+// per-device error word, and the launch sequence of the forward and the backward.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "swa_attn.h"
+#include "swa_kernels.h"
+
+namespace {
+
+// Set by a kernel whose bounded wait ran out; one copy per device.
+__device__ unsigned g_swa_error_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool probed = false;
+  bool supported = false;
+  unsigned* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Capability check and error-word address of the current device (cached).
+swa_status current_device(unsigned** err) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SWA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SWA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.probed) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    // The kernels are built for sm_103a only (tcgen05, TMEM, TMA).
+    st.supported = (major == 10 && minor == 3);
+    if (st.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_swa_error_word) != cudaSuccess) return SWA_ERR_CUDA;
+      st.err = static_cast<unsigned*>(p);
+    }
+    st.probed = true;
+  }
+  if (!st.supported) return SWA_ERR_UNSUPPORTED;
+  *err = st.err;
+  return SWA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+swa_status check_sizes(int B, int Hq, int Hkv, int N, int D, int window, float scale) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || window < 1) return SWA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return SWA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return SWA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return SWA_ERR_UNSUPPORTED;
+  // Index arithmetic: row indices bh*N + i in 32 bits, grid in 31 bits.
+  const long long rows = static_cast<long long>(B) * Hq * N;
+  const long long tiles = static_cast<long long>(B) * Hq * ((N + swa::kBlockM - 1) / swa::kBlockM);
+  if (rows >= (1ll << 31) || tiles >= (1ll << 31)) return SWA_ERR_INVALID_ARG;
+  return SWA_OK;
+}
+
+swa::Problem make_problem(int B, int Hq, int Hkv, int N, int D, int window, float scale,
+                          unsigned* err) {
+  swa::Problem pb;
+  pb.B = B;
+  pb.Hq = Hq;
+  pb.Hkv = Hkv;
+  pb.N = N;
+  pb.D = D;
+  pb.W = window < N ? window : N;  // a window that covers the sequence is plain causal
+  pb.scale = scale;
+  pb.err = err;
+  return pb;
+}
+
+}  // namespace
+
+extern "C" {
+
+swa_status swa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Hq, int Hkv, int N, int D, int window, float scale,
+                        cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
+  if (st != SWA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return SWA_ERR_MISALIGNED;
+  unsigned* err = nullptr;
+  if ((st = current_device(&err)) != SWA_OK) return st;
+  const swa::Problem pb = make_problem(B, Hq, Hkv, N, D, window, scale, err);
+  if (swa::launch_fwd(pb, q, k, v, o, lse, stream) != cudaSuccess) return SWA_ERR_CUDA;
+  return SWA_OK;
+}
+
+size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int N, int D) {
+  if (B < 1 || Hq < 1 || N < 1 || (D != 64 && D != 128)) return 0;
+  const size_t bytes = static_cast<size_t>(B) * Hq * N * sizeof(float);
+  return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+swa_status swa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                        const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                        int N, int D, int window, float scale, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
+  if (st != SWA_OK) return st;
+  if (!workspace || workspace_bytes < swa_attn_bwd_workspace_bytes(B, Hq, N, D))
+    return SWA_ERR_WORKSPACE;
+  const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return SWA_ERR_MISALIGNED;
+  unsigned* err = nullptr;
+  if ((st = current_device(&err)) != SWA_OK) return st;
+  const swa::Problem pb = make_problem(B, Hq, Hkv, N, D, window, scale, err);
+  float* delta = static_cast<float*>(workspace);
+  if (swa::launch_bwd_delta(pb, o, dO, delta, stream) != cudaSuccess) return SWA_ERR_CUDA;
+  if (swa::launch_bwd_dkdv(pb, q, k, v, dO, lse, delta, dk, dv, stream) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (swa::launch_bwd_dq(pb, q, k, v, dO, lse, delta, dq, stream) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  return SWA_OK;
+}
+
+const char* swa_strerror(swa_status status) {
+  switch (status) {
+    case SWA_OK: return "SWA_OK";
+    case SWA_ERR_INVALID_ARG: return "SWA_ERR_INVALID_ARG: size, window, scale or pointer invalid";
+    case SWA_ERR_UNSUPPORTED: return "SWA_ERR_UNSUPPORTED: head dim not in {64,128} or device not sm_103";
+    case SWA_ERR_MISALIGNED: return "SWA_ERR_MISALIGNED: pointer not 16-byte aligned";
+    case SWA_ERR_CUDA: return "SWA_ERR_CUDA: CUDA call or kernel launch failed";
+    case SWA_ERR_DEVICE_TIMEOUT: return "SWA_ERR_DEVICE_TIMEOUT: a kernel's bounded wait ran out";
+    case SWA_ERR_WORKSPACE: return "SWA_ERR_WORKSPACE: workspace null or too small";
+  }
+  return "SWA_ERR_UNKNOWN";
+}
+
+swa_status swa_check_device(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SWA_ERR_CUDA;
+  unsigned* err = nullptr;
+  swa_status st = current_device(&err);
+  if (st != SWA_OK) return st;
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_swa_error_word, sizeof(word)) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (word != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_swa_error_word, &zero, sizeof(zero)) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    return SWA_ERR_DEVICE_TIMEOUT;
+  }
+  return SWA_OK;
+}
+
+int swa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,354 @@
+// swa_bwd_dq.cu — dQ of causal sliding-window attention on sm_103a.
+//
+// One CTA computes dQ for one 128-row query tile of one (batch, query head), walking only the key
+// blocks inside the tile's window (the same walk as the forward), and recomputing per block
+//   S = Q K_j^T,  P = exp(scale S - LSE) (window-masked),  dP = dO V_j^T,  dS = P (dP - Delta),
+//   dQ += dS K_j,
+// with a final dQ *= scale.  dQ accumulates in TMEM (fp32) and is initialised by the first visited
+// key block rather than block zero ("Off NVIDIA, you fix the platform yourself", Lab 28, "Method and
+// disclosure": dQ is initialized on each query tile's first visited key tile).  One bf16 rounding
+// at the store; S and dP stay fp32 in TMEM and only dS is rounded to bf16 as an MMA operand (the
+// lab's fp32-score-tile experiment showed the error of bf16 score scratch).
+//
+// Warp roles (192 threads): warps 0-3 compute (thread r = query row q0 + r = TMEM lane r),
+// warp 4 TMA producer (Q and dO once, K_j / V_j through a ring of stages), warp 5 MMA issuer and
+// TMEM owner.  TMEM columns: [0,128) S, [128,256) dP, [256, 256+D) dQ.
+#include "swa_kernels.h"
+#include "swa_ptx.cuh"
+#include "swa_tmap.h"
+
+namespace swa {
+namespace {
+
+template <int D>
+struct DqCfg {
+  static constexpr int kTileBytes = kBlockM * D * 2;
+  static constexpr int kChunkBytes = kBlockM * 128;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kDSBytes = kBlockM * kBlockN * 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kOffQ + kTileBytes;
+  static constexpr int kOffK = kOffDO + kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffDS = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffDS + kDSBytes;
+  static constexpr int kQDFull = 0;
+  static constexpr int kKFull = 1;
+  static constexpr int kVFull = kKFull + kStages;
+  static constexpr int kKVEmpty = kVFull + kStages;
+  static constexpr int kSFull = kKVEmpty + kStages;
+  static constexpr int kSEmpty = kSFull + 1;
+  static constexpr int kDPFull = kSEmpty + 1;
+  static constexpr int kDPEmpty = kDPFull + 1;
+  static constexpr int kDSFull = kDPEmpty + 1;
+  static constexpr int kDQDone = kDSFull + 1;
+  static constexpr int kDrain = kDQDone + 1;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  static constexpr int kThreads = 192;
+};
+
+struct DqArgs {
+  const float* lse;
+  const float* delta;
+  __nv_bfloat16* dq;
+  int BH, Hq, Hkv, G, N, W, nqb;
+  float scale, scale_log2;
+  unsigned* err;
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    swa_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const DqArgs a) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  __shared__ int abort_flag;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t sQ = smem_u32(smem + C::kOffQ);
+  const uint32_t sDO = smem_u32(smem + C::kOffDO);
+  const uint32_t sK0 = smem_u32(smem + C::kOffK);
+  const uint32_t sV0 = smem_u32(smem + C::kOffV);
+  const uint32_t sDS = smem_u32(smem + C::kOffDS);
+
+  const int qb = a.nqb - 1 - static_cast<int>(blockIdx.x) / a.BH;
+  const int bh = static_cast<int>(blockIdx.x) % a.BH;
+  const int hq = bh % a.Hq;
+  const int bhk = (bh / a.Hq) * a.Hkv + hq / a.G;
+  const int q0 = qb * kBlockM;
+  const int kb_lo = fwd_first_kblock(q0, a.W);
+  const int kb_hi = fwd_last_kblock(q0, a.N);
+  const int nkv = kb_hi - kb_lo + 1;
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(bar(C::kQDFull), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kKFull + s), 1);
+      mbar_init(bar(C::kVFull + s), 1);
+      mbar_init(bar(C::kKVEmpty + s), 1);
+    }
+    mbar_init(bar(C::kSFull), 1);
+    mbar_init(bar(C::kSEmpty), 128);
+    mbar_init(bar(C::kDPFull), 1);
+    mbar_init(bar(C::kDPEmpty), 128);
+    mbar_init(bar(C::kDSFull), 128);
+    mbar_init(bar(C::kDQDone), 1);
+    mbar_init(bar(C::kDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar(C::kQDFull), 2 * C::kTileBytes);
+      for (int h = 0; h < C::kChunks; ++h) {
+        tma_load_3d(sQ + h * C::kChunkBytes, &tm_q, bar(C::kQDFull), 64 * h, q0, bh);
+        tma_load_3d(sDO + h * C::kChunkBytes, &tm_do, bar(C::kQDFull), 64 * h, q0, bh);
+      }
+      int last_fill[C::kStages];
+      for (int s = 0; s < C::kStages; ++s) last_fill[s] = -1;
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % C::kStages, n = j / C::kStages;
+        if (j >= C::kStages && !mbar_wait(bar(C::kKVEmpty + s), (n - 1) & 1, &abort_flag, a.err))
+          break;
+        const int k0 = (kb_lo + j) * kBlockN;
+        const uint32_t sK = sK0 + s * C::kTileBytes, sV = sV0 + s * C::kTileBytes;
+        mbar_arrive_expect_tx(bar(C::kKFull + s), C::kTileBytes);
+        for (int h = 0; h < C::kChunks; ++h)
+          tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKFull + s), 64 * h, k0, bhk);
+        mbar_arrive_expect_tx(bar(C::kVFull + s), C::kTileBytes);
+        for (int h = 0; h < C::kChunks; ++h)
+          tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kVFull + s), 64 * h, k0, bhk);
+        last_fill[s] = j;
+      }
+      drain_wait(bar(C::kQDFull), 0, a.err);
+      for (int s = 0; s < C::kStages; ++s) {
+        if (last_fill[s] >= 0) {
+          drain_wait(bar(C::kKFull + s), (last_fill[s] / C::kStages) & 1, a.err);
+          drain_wait(bar(C::kVFull + s), (last_fill[s] / C::kStages) & 1, a.err);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdSq = idesc_bf16(kBlockM, kBlockN, false, false);  // S, dP
+      constexpr uint32_t kIdDq = idesc_bf16(kBlockM, D, false, true);         // dQ += dS K
+      auto issue_s = [&](int j) -> bool {  // S = Q K_j^T
+        const int s = j % C::kStages, n = j / C::kStages;
+        if (!mbar_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
+        if (j >= 1 && !mbar_wait(bar(C::kSEmpty), (j - 1) & 1, &abort_flag, a.err)) return false;
+        tc_fence_after();
+        const uint32_t sK = sK0 + s * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+          umma_ss(tmem + C::kColS, smem_desc_sw128(sQ + off, 16, 1024),
+                  smem_desc_sw128(sK + off, 16, 1024), kIdSq, ks > 0);
+        }
+        umma_commit(bar(C::kSFull));
+        return true;
+      };
+      auto issue_dp = [&](int j) -> bool {  // dP = dO V_j^T
+        const int s = j % C::kStages, n = j / C::kStages;
+        if (!mbar_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
+        if (j >= 1 && !mbar_wait(bar(C::kDPEmpty), (j - 1) & 1, &abort_flag, a.err)) return false;
+        tc_fence_after();
+        const uint32_t sV = sV0 + s * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+          umma_ss(tmem + C::kColDP, smem_desc_sw128(sDO + off, 16, 1024),
+                  smem_desc_sw128(sV + off, 16, 1024), kIdSq, ks > 0);
+        }
+        umma_commit(bar(C::kDPFull));
+        return true;
+      };
+      auto issue_dq = [&](int j) -> bool {  // dQ += dS K_j  (K_j as the MN-major B operand)
+        const int s = j % C::kStages;
+        if (!mbar_wait(bar(C::kDSFull), j & 1, &abort_flag, a.err)) return false;
+        tc_fence_after();
+        const uint32_t sK = sK0 + s * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kBlockN / 16; ++ks) {
+          const uint32_t aoff = (ks >> 2) * (kBlockM * 128) + (ks & 3) * 32;
+          umma_ss(tmem + C::kColDQ, smem_desc_sw128(sDS + aoff, 16, 1024),
+                  smem_desc_sw128(sK + ks * 16 * 128, C::kChunkBytes, 1024), kIdDq,
+                  (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(C::kDQDone));
+        umma_commit(bar(C::kKVEmpty + s));
+        return true;
+      };
+      bool ok = mbar_wait(bar(C::kQDFull), 0, &abort_flag, a.err);
+      if (ok) ok = issue_s(0);
+      if (ok) ok = issue_dp(0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        if (j + 1 < nkv) {
+          ok = issue_s(j + 1);
+          if (ok) ok = issue_dp(j + 1);
+        }
+        if (ok) ok = issue_dq(j);
+      }
+      umma_commit(bar(C::kDrain));
+      drain_wait(bar(C::kDrain), 0, a.err);
+    }
+  } else {
+    // ------------------------------------------------------------------ compute (warps 0-3)
+    const int r = static_cast<int>(threadIdx.x);
+    const int row = q0 + r;
+    const bool in_range = row < a.N;
+    const size_t grow = static_cast<size_t>(bh) * a.N + row;
+    const uint32_t lane_base = (warp * 32u) << 16;
+    // Rows past the end see P = 0 (their LSE is taken as +inf), so they add nothing.
+    const float lse2 = in_range ? a.lse[grow] * kLog2e : SWA_POS_INF;
+    const float dlt = in_range ? a.delta[grow] : 0.f;
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int k0 = (kb_lo + j) * kBlockN;
+      if (!(ok = warp_wait(bar(C::kSFull), j & 1, &abort_flag, a.err))) break;
+      tc_fence_after();
+      float p[kBlockN];
+#pragma unroll
+      for (int c4 = 0; c4 < kBlockN / 32; ++c4) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + C::kColS + 32u * c4, rr);
+        tmem_wait_ld(rr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) p[32 * c4 + i] = __uint_as_float(rr[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::kSEmpty));
+#pragma unroll
+      for (int c = 0; c < kBlockN; ++c) p[c] = ex2(fmaf(p[c], sl2, -lse2));
+      const bool interior = (k0 + kBlockN - 1 <= q0) && (q0 + kBlockM - 1 - k0 < a.W);
+      if (!interior) {
+        const int lo = row - a.W + 1 - k0, hi = row - k0;
+#pragma unroll
+        for (int c = 0; c < kBlockN; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
+      }
+
+      if (!(ok = warp_wait(bar(C::kDPFull), j & 1, &abort_flag, a.err))) break;
+      tc_fence_after();
+      uint32_t pk[kBlockN / 2];
+#pragma unroll
+      for (int c4 = 0; c4 < kBlockN / 32; ++c4) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + C::kColDP + 32u * c4, rr);
+        tmem_wait_ld(rr);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = 32 * c4 + 2 * i;
+          const float d0 = p[c] * (__uint_as_float(rr[2 * i]) - dlt);
+          const float d1 = p[c + 1] * (__uint_as_float(rr[2 * i + 1]) - dlt);
+          pk[c >> 1] = pack_bf16x2(d0, d1);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::kDPEmpty));
+      // dS K_{j-1} must have consumed the dS buffer before it is overwritten.
+      if (j > 0 && !(ok = warp_wait(bar(C::kDQDone), (j - 1) & 1, &abort_flag, a.err))) break;
+      store_row_sw128_128(sDS, r, pk);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::kDSFull));
+    }
+    if (ok && warp_wait(bar(C::kDQDone), (nkv - 1) & 1, &abort_flag, a.err)) {
+      tc_fence_after();
+      __nv_bfloat16* dst_row = a.dq + grow * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + C::kColDQ + c0, rr);
+        tmem_wait_ld(rr);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * a.scale,
+                              __uint_as_float(rr[2 * i + 1]) * a.scale);
+        if (in_range) {
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_dq_d(const Problem& pb, const void* q, const void* k, const void* v,
+                        const void* dO, const float* lse, const float* delta, void* dq,
+                        cudaStream_t stream) {
+  using C = DqCfg<D>;
+  CUtensorMap tq, tdo, tk, tv;
+  const uint64_t bhq = static_cast<uint64_t>(pb.B) * pb.Hq, bhk = static_cast<uint64_t>(pb.B) * pb.Hkv;
+  if (!make_tmap_bf16_3d(&tq, q, bhq, pb.N, D, kBlockM) ||
+      !make_tmap_bf16_3d(&tdo, dO, bhq, pb.N, D, kBlockM) ||
+      !make_tmap_bf16_3d(&tk, k, bhk, pb.N, D, kBlockN) ||
+      !make_tmap_bf16_3d(&tv, v, bhk, pb.N, D, kBlockN))
+    return cudaErrorInvalidValue;
+  auto kern = swa_dq_kernel<D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  DqArgs a;
+  a.lse = lse;
+  a.delta = delta;
+  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.BH = pb.B * pb.Hq;
+  a.Hq = pb.Hq;
+  a.Hkv = pb.Hkv;
+  a.G = pb.Hq / pb.Hkv;
+  a.N = pb.N;
+  a.W = pb.W;
+  a.nqb = (pb.N + kBlockM - 1) / kBlockM;
+  a.scale = pb.scale;
+  a.scale_log2 = pb.scale * kLog2e;
+  a.err = pb.err;
+  const unsigned grid = static_cast<unsigned>(a.nqb) * static_cast<unsigned>(a.BH);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tdo, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq(const Problem& pb, const void* q, const void* k, const void* v,
+                          const void* dO, const float* lse, const float* delta, void* dq,
+                          cudaStream_t stream) {
+  if (pb.D == 64) return launch_dq_d<64>(pb, q, k, v, dO, lse, delta, dq, stream);
+  if (pb.D == 128) return launch_dq_d<128>(pb, q, k, v, dO, lse, delta, dq, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace swa

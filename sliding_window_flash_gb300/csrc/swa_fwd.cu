@@ -1,0 +1,359 @@
+// swa_fwd.cu — forward of causal sliding-window attention on sm_103a.
+//
+// One CTA computes one 128-row query tile of one (batch, query head):
+//   O[q0:q0+128] = softmax(scale * Q K^T, window mask) V,  LSE = natural-log row log-sum-exp,
+// walking only the key blocks kb_lo..kb_hi that the window reaches ("Off NVIDIA, you fix the
+// platform yourself", Lab 28, "What did fixing it take?": skip blocks wholly outside the window,
+// mask the cells at its edge; the first block a query tile visits is no longer block zero).
+// Only O and LSE are written (mlx-train-perf README, flash-attention section: the saved state is
+// the output and the log-sum-exp).
+//
+// Warp roles (192 threads):
+//   warps 0-3  softmax: thread r owns query row q0 + r = TMEM lane r.  Reads S from TMEM, masks,
+//              keeps the running max m and sum l in registers, writes bf16 P to shared memory,
+//              rescales its O row in TMEM when its max grows by more than 2^8, and finally writes
+//              O / l and LSE.
+//   warp 4     TMA producer: Q once, then K_j / V_j through a ring of shared-memory stages.
+//   warp 5     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one of two TMEM S buffers,
+//              O += P_j V_j into the TMEM O accumulator.  S_{j+1} is issued before O += P_j V_j so
+//              the tensor core computes the next scores while the softmax warps work on this block.
+// TMEM columns: [0,128) S buffer 0, [128,256) S buffer 1, [256, 256+D) O.
+#include "swa_kernels.h"
+#include "swa_ptx.cuh"
+#include "swa_tmap.h"
+
+namespace swa {
+namespace {
+
+// Running max is only moved (and O rescaled) when it grows by more than this many powers of 2;
+// otherwise P is computed against the stale max, with values up to 2^8 (exact softmax either way).
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kTileBytes = kBlockM * D * 2;  // one 128 x D bf16 tile
+  static constexpr int kChunkBytes = kBlockM * 128;   // 128 rows x 64 columns (128-byte rows)
+  static constexpr int kChunks = D / 64;
+  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kPBytes = kBlockM * kBlockN * 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffP = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffP + kPBytes;
+  // barrier indices
+  static constexpr int kQFull = 0;
+  static constexpr int kKFull = 1;
+  static constexpr int kVFull = kKFull + kStages;
+  static constexpr int kKVEmpty = kVFull + kStages;
+  static constexpr int kSFull = kKVEmpty + kStages;  // 2
+  static constexpr int kSEmpty = kSFull + 2;         // 2
+  static constexpr int kPFull = kSEmpty + 2;
+  static constexpr int kODone = kPFull + 1;
+  static constexpr int kDrain = kODone + 1;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM slot + align
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;  // buffer b at kColS + 128 b
+  static constexpr uint32_t kColO = 256;
+  static constexpr int kThreads = 192;
+};
+
+struct FwdArgs {
+  __nv_bfloat16* o;
+  float* lse;
+  int BH;  // B * Hq
+  int Hq, Hkv, G, N, W, nqb;
+  float scale_log2;  // scale * log2(e)
+  unsigned* err;
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    swa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  __shared__ int abort_flag;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t sQ = smem_u32(smem + C::kOffQ);
+  const uint32_t sK0 = smem_u32(smem + C::kOffK);
+  const uint32_t sV0 = smem_u32(smem + C::kOffV);
+  const uint32_t sP = smem_u32(smem + C::kOffP);
+
+  // Heaviest query blocks first (the causal case gives later blocks more key blocks).
+  const int qb = a.nqb - 1 - static_cast<int>(blockIdx.x) / a.BH;
+  const int bh = static_cast<int>(blockIdx.x) % a.BH;
+  const int hq = bh % a.Hq;
+  const int bhk = (bh / a.Hq) * a.Hkv + hq / a.G;
+  const int q0 = qb * kBlockM;
+  const int kb_lo = fwd_first_kblock(q0, a.W);
+  const int kb_hi = fwd_last_kblock(q0, a.N);
+  const int nkv = kb_hi - kb_lo + 1;
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(bar(C::kQFull), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kKFull + s), 1);
+      mbar_init(bar(C::kVFull + s), 1);
+      mbar_init(bar(C::kKVEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::kSFull + b), 1);
+      mbar_init(bar(C::kSEmpty + b), 128);
+    }
+    mbar_init(bar(C::kPFull), 128);
+    mbar_init(bar(C::kODone), 1);
+    mbar_init(bar(C::kDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar(C::kQFull), C::kTileBytes);
+      for (int h = 0; h < C::kChunks; ++h)
+        tma_load_3d(sQ + h * C::kChunkBytes, &tm_q, bar(C::kQFull), 64 * h, q0, bh);
+      int last_fill[C::kStages];
+      for (int s = 0; s < C::kStages; ++s) last_fill[s] = -1;
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % C::kStages, n = j / C::kStages;
+        if (j >= C::kStages && !mbar_wait(bar(C::kKVEmpty + s), (n - 1) & 1, &abort_flag, a.err))
+          break;
+        const int k0 = (kb_lo + j) * kBlockN;
+        const uint32_t sK = sK0 + s * C::kTileBytes, sV = sV0 + s * C::kTileBytes;
+        mbar_arrive_expect_tx(bar(C::kKFull + s), C::kTileBytes);
+        for (int h = 0; h < C::kChunks; ++h)
+          tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKFull + s), 64 * h, k0, bhk);
+        mbar_arrive_expect_tx(bar(C::kVFull + s), C::kTileBytes);
+        for (int h = 0; h < C::kChunks; ++h)
+          tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kVFull + s), 64 * h, k0, bhk);
+        last_fill[s] = j;
+      }
+      // Never leave a copy in flight: wait for the last fill of every stage.
+      drain_wait(bar(C::kQFull), 0, a.err);
+      for (int s = 0; s < C::kStages; ++s) {
+        if (last_fill[s] >= 0) {
+          drain_wait(bar(C::kKFull + s), (last_fill[s] / C::kStages) & 1, a.err);
+          drain_wait(bar(C::kVFull + s), (last_fill[s] / C::kStages) & 1, a.err);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(kBlockM, kBlockN, false, false);
+      constexpr uint32_t kIdO = idesc_bf16(kBlockM, D, false, true);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % C::kStages, n = j / C::kStages, sb = j & 1;
+        if (!mbar_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
+        if (j >= 2 && !mbar_wait(bar(C::kSEmpty + sb), ((j - 2) >> 1) & 1, &abort_flag, a.err))
+          return false;
+        tc_fence_after();
+        const uint32_t sK = sK0 + s * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+          umma_ss(tmem + C::kColS + 128u * sb, smem_desc_sw128(sQ + off, 16, 1024),
+                  smem_desc_sw128(sK + off, 16, 1024), kIdS, ks > 0);
+        }
+        umma_commit(bar(C::kSFull + sb));
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int s = j % C::kStages, n = j / C::kStages;
+        if (!mbar_wait(bar(C::kPFull), j & 1, &abort_flag, a.err)) return false;
+        if (!mbar_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
+        tc_fence_after();
+        const uint32_t sV = sV0 + s * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kBlockN / 16; ++ks) {
+          const uint32_t aoff = (ks >> 2) * (kBlockM * 128) + (ks & 3) * 32;
+          umma_ss(tmem + C::kColO, smem_desc_sw128(sP + aoff, 16, 1024),
+                  smem_desc_sw128(sV + ks * 16 * 128, C::kChunkBytes, 1024), kIdO,
+                  (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(C::kODone));
+        umma_commit(bar(C::kKVEmpty + s));
+        return true;
+      };
+      bool ok = mbar_wait(bar(C::kQFull), 0, &abort_flag, a.err);
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        if (j + 1 < nkv) ok = issue_s(j + 1);
+        if (ok) ok = issue_pv(j);
+      }
+      // Every issued MMA completes before TMEM is released.
+      umma_commit(bar(C::kDrain));
+      drain_wait(bar(C::kDrain), 0, a.err);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax (warps 0-3)
+    const int r = static_cast<int>(threadIdx.x);  // row within the tile == TMEM lane
+    const int row = q0 + r;
+    const uint32_t lane_base = (warp * 32u) << 16;
+    const float sl2 = a.scale_log2;
+    float m_ref = SWA_NEG_INF;  // reference max (log2 domain) that P and l are taken against
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int k0 = (kb_lo + j) * kBlockN;
+      const int sb = j & 1;
+      if (!(ok = warp_wait(bar(C::kSFull + sb), (j >> 1) & 1, &abort_flag, a.err))) break;
+      tc_fence_after();
+      float x[kBlockN];
+#pragma unroll
+      for (int c4 = 0; c4 < kBlockN / 32; ++c4) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + C::kColS + 128u * sb + 32u * c4, rr);
+        tmem_wait_ld(rr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[32 * c4 + i] = __uint_as_float(rr[i]) * sl2;
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::kSEmpty + sb));
+
+      // Window mask: the cells of this block visible to row `row` are keys in [row-W+1, row].
+      const bool interior = (k0 + kBlockN - 1 <= q0) && (q0 + kBlockM - 1 - k0 < a.W);
+      if (!interior) {
+        const int lo = row - a.W + 1 - k0, hi = row - k0;
+#pragma unroll
+        for (int c = 0; c < kBlockN; ++c) x[c] = (c >= lo && c <= hi) ? x[c] : SWA_NEG_INF;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int c = 1; c < kBlockN; ++c) mx = fmaxf(mx, x[c]);
+      const float m_new = fmaxf(m_ref, mx);
+      const bool resc = m_new > m_ref + kRescaleThreshold;
+      float factor = 1.f;
+      if (resc) {
+        factor = ex2(m_ref - m_new);  // 0 when m_ref is -inf
+        l *= factor;
+        m_ref = m_new;
+      }
+      const float m_use = (m_ref == SWA_NEG_INF) ? 0.f : m_ref;
+      uint32_t pk[kBlockN / 2];
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBlockN / 2; ++c) {
+        const float p0 = ex2(x[2 * c] - m_use), p1 = ex2(x[2 * c + 1] - m_use);
+        rs += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      l += rs;
+
+      // P_{j-1} V_{j-1} must be done before P is overwritten and before O is rescaled.
+      if (j > 0) {
+        if (!(ok = warp_wait(bar(C::kODone), (j - 1) & 1, &abort_flag, a.err))) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tmem + lane_base + C::kColO + c0, rr);
+            tmem_wait_ld(rr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * factor);
+            tmem_st32(tmem + lane_base + C::kColO + c0, rr);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P row -> shared memory, K-major with 128-byte swizzle (two 64-key chunks).
+      store_row_sw128_128(sP, r, pk);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::kPFull));
+    }
+    if (ok && warp_wait(bar(C::kODone), (nkv - 1) & 1, &abort_flag, a.err)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const float m_use = (m_ref == SWA_NEG_INF) ? 0.f : m_ref;
+      const bool in_range = row < a.N;
+      const size_t grow = static_cast<size_t>(bh) * a.N + row;
+      if (in_range) a.lse[grow] = (m_use + log2f(l)) * kLn2;
+      __nv_bfloat16* orow = a.o + grow * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + C::kColO + c0, rr);
+        tmem_wait_ld(rr);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
+                              __uint_as_float(rr[2 * i + 1]) * inv_l);
+        if (in_range) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const Problem& pb, const void* q, const void* k, const void* v, void* o,
+                         float* lse, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bf16_3d(&tq, q, static_cast<uint64_t>(pb.B) * pb.Hq, pb.N, D, kBlockM) ||
+      !make_tmap_bf16_3d(&tk, k, static_cast<uint64_t>(pb.B) * pb.Hkv, pb.N, D, kBlockN) ||
+      !make_tmap_bf16_3d(&tv, v, static_cast<uint64_t>(pb.B) * pb.Hkv, pb.N, D, kBlockN))
+    return cudaErrorInvalidValue;
+  auto kern = swa_fwd_kernel<D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  FwdArgs a;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.BH = pb.B * pb.Hq;
+  a.Hq = pb.Hq;
+  a.Hkv = pb.Hkv;
+  a.G = pb.Hq / pb.Hkv;
+  a.N = pb.N;
+  a.W = pb.W;
+  a.nqb = (pb.N + kBlockM - 1) / kBlockM;
+  a.scale_log2 = pb.scale * kLog2e;
+  a.err = pb.err;
+  const unsigned grid = static_cast<unsigned>(a.nqb) * static_cast<unsigned>(a.BH);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const Problem& pb, const void* q, const void* k, const void* v, void* o,
+                       float* lse, cudaStream_t stream) {
+  if (pb.D == 64) return launch_fwd_d<64>(pb, q, k, v, o, lse, stream);
+  if (pb.D == 128) return launch_fwd_d<128>(pb, q, k, v, o, lse, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace swa

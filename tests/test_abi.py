@@ -1,0 +1,106 @@
+"""Host-only checks of the C ABI: the library builds, loads, exports every symbol that
+include/swa_attn.h declares, and rejects bad arguments before launching anything (these calls
+return from the argument checks, so they need no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "swa_attn.h")
+
+FAKE = 0x10000  # 16-byte-aligned fake device address; never dereferenced by these calls
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import sliding_window_flash_gb300 as swa
+    from sliding_window_flash_gb300 import build as swa_build
+
+    if not os.path.exists(swa.library_path()):
+        swa_build.build()
+    return swa.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(swa_[a-z_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for required in ("swa_attn_fwd", "swa_attn_bwd", "swa_attn_bwd_workspace_bytes", "swa_strerror"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import sliding_window_flash_gb300 as swa
+
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert name in swa.SIGNATURES, f"binding has no signature for {name}"
+
+
+def test_version_and_strerror(lib):
+    assert lib.swa_version() >= 100
+    for code in range(7):
+        assert lib.swa_strerror(code)
+    assert b"UNKNOWN" in lib.swa_strerror(99)
+
+
+def _fwd(lib, B=1, Hq=2, Hkv=1, N=16, D=64, W=4, scale=0.125, ptrs=None):
+    p = ptrs or [FAKE] * 5
+    return lib.swa_attn_fwd(*p, B, Hq, Hkv, N, D, W, scale, None)
+
+
+def _bwd(lib, B=1, Hq=2, Hkv=1, N=16, D=64, W=4, scale=0.125, ptrs=None, ws=FAKE, ws_bytes=1 << 20):
+    p = ptrs or [FAKE] * 9
+    return lib.swa_attn_bwd(*p, B, Hq, Hkv, N, D, W, scale, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=0), 1), (dict(B=0), 1), (dict(Hq=0), 1), (dict(Hkv=0), 1), (dict(W=0), 1),
+    (dict(W=-3), 1), (dict(Hq=3, Hkv=2), 1), (dict(scale=0.0), 1), (dict(scale=-1.0), 1),
+    (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
+    (dict(D=96), 2), (dict(D=256), 2), (dict(D=32), 2),
+])
+def test_fwd_rejects_bad_sizes(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+    assert _bwd(lib, **kw) == code
+
+
+def test_null_and_misaligned_pointers(lib):
+    assert _fwd(lib, ptrs=[FAKE, 0, FAKE, FAKE, FAKE]) == 1
+    assert _fwd(lib, ptrs=[FAKE, FAKE, FAKE + 8, FAKE, FAKE]) == 3
+    assert _fwd(lib, ptrs=[FAKE, FAKE, FAKE, FAKE, FAKE + 4]) == 3
+    assert _bwd(lib, ptrs=[FAKE] * 8 + [0]) == 1
+    assert _bwd(lib, ptrs=[FAKE] * 8 + [FAKE + 2]) == 3
+
+
+def test_workspace_checks(lib):
+    need = lib.swa_attn_bwd_workspace_bytes(2, 4, 100, 128)
+    assert need == ((2 * 4 * 100 * 4 + 255) // 256) * 256
+    assert lib.swa_attn_bwd_workspace_bytes(0, 4, 100, 128) == 0
+    assert lib.swa_attn_bwd_workspace_bytes(1, 4, 100, 80) == 0
+    assert _bwd(lib, ws=0) == 6
+    assert _bwd(lib, ws_bytes=lib.swa_attn_bwd_workspace_bytes(1, 2, 16, 64) - 1) == 6
+    assert _bwd(lib, ws=FAKE + 8) == 3
+
+
+def test_index_range_limits(lib):
+    # B*Hq*N rows must stay below 2^31.
+    assert _fwd(lib, B=1 << 12, Hq=1 << 10, Hkv=1, N=1 << 10) == 1
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+
+    import sliding_window_flash_gb300 as swa
+
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        swa.swa_attn_fwd(q, k, k, 4)
