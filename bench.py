@@ -1,0 +1,572 @@
+"""Benchmark of the sliding-window attention hot path on GB300: one step = forward + backward
+(Delta preprocess, dK/dV, dQ) of one long-context sliding-window layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (default): B=1, Hq=32, Hkv=16, N=32768, D=128, window 1024, bf16 Q/K/V ~ N(0,1),
+dO ~ N(0, 1e-2), seeded synthetic data.  Metric: window-effective TFLOP/s of forward + backward,
+counting only visible (query, key) pairs: forward 4*D, backward 10*D flops per pair and head.
+
+Printed as one JSON line (rank 0).  `value` is device-timed with inputs resident in HBM; `e2e` is
+the same metric with the host->device copy of the step's inputs and the device->host copy of its
+outputs inside the timed region; `roofline` reports the dominant kernel against the measured peak;
+`cpu_baseline` times the fp64 oracle on a bounded sample of the same workload on the host cores.
+With --gpus N > 1 (launched under torchrun) every rank runs its own independent layer (weak
+scaling, no data-path collective); the barrier and max-over-ranks timing use torch.distributed.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import swa_inputs as si  # noqa: E402
+
+METRIC = "SWA fwd+bwd window-effective TFLOP/s & peak GB at N=32768, W=1024 (1×GB300)"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ------------------------------------------------------------------------------------------------
+# Flop and byte accounting (window-effective: visible pairs only)
+# ------------------------------------------------------------------------------------------------
+
+def visible_pairs(N: int, W: int) -> int:
+    """(query, key) pairs with 0 <= i - j < W in one head of length N."""
+    W = min(W, N)
+    return N * W - W * (W - 1) // 2
+
+
+def step_flops(case: si.Case) -> dict:
+    pairs = visible_pairs(case.N, case.W) * case.B * case.Hq
+    return {
+        "fwd": 4 * case.D * pairs,
+        "bwd": 10 * case.D * pairs,
+        # algorithmic share of each backward kernel: dK/dV does the S, dP, dV and dK contractions
+        # of the backward's five, dQ adds the fifth (its own S and dP are recomputation)
+        "dkdv": 8 * case.D * pairs,
+        "dq": 2 * case.D * pairs,
+        "pairs": pairs,
+    }
+
+
+def delta_bytes(case: si.Case) -> int:
+    rows = case.B * case.Hq * case.N
+    return rows * case.D * 2 * 2 + rows * 4
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ------------------------------------------------------------------------------------------------
+
+_CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={_CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# Distributed plumbing (barrier and max-over-ranks only)
+# ------------------------------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, device):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    backend = "nccl" if device.type == "cuda" else "gloo"
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device):
+    if dist is not None:
+        if device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------------
+# The CPU oracle on a bounded sample
+# ------------------------------------------------------------------------------------------------
+
+def _blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def oracle_sample(case: si.Case, rows_per_sample: int, samples: int, seed: int = 0) -> dict:
+    """Time the fp64 oracle (forward + backward) on `samples` blocks of `rows_per_sample` query rows
+    of head (0, 0) of the workload, mid-sequence; returns window-effective TFLOP/s of that work."""
+    from oracle import swa_oracle as orc
+
+    import numpy as np
+
+    N, D, W = case.N, case.D, case.W
+    one_head = si.Case(B=1, Hq=1, Hkv=1, N=N, D=D, W=W, do_std=case.do_std, seed=seed)
+    inp = si.make_inputs(one_head)
+    qh, kh, vh, doh = (inp[k_][0, 0].double().numpy() for k_ in ("q", "k", "v", "do"))
+
+    flops = 0
+    t0 = time.perf_counter()
+    for s in range(samples):
+        r0 = min(N - rows_per_sample, N // 2 + s * rows_per_sample) if N > rows_per_sample else 0
+        rows = np.arange(r0, min(N, r0 + rows_per_sample))
+        orc.rows_backward(qh, kh, vh, doh, rows, W, case.softmax_scale)
+        vis = int(np.sum(np.minimum(rows + 1, W)))
+        flops += 14 * D * vis
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "seconds": dt, "flops": flops,
+            "rows": rows_per_sample * samples}
+
+
+# ------------------------------------------------------------------------------------------------
+# Our arm
+# ------------------------------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import sliding_window_flash_gb300 as swa
+
+    swa.load()  # fails loudly when libswa.so is missing: there is no fallback
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = dist_init(world, device)
+    case = si.long_swa_case(32768)
+    case = si.Case(**{**case.__dict__, "seed": rank})
+    fl = step_flops(case)
+    peaks = load_peaks()
+
+    inp = si.make_inputs(case, device=str(device))
+    q, k, v, do = inp["q"], inp["k"], inp["v"], inp["do"]
+    o = torch.empty_like(q)
+    lse = torch.empty(case.B, case.Hq, case.N, dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty(case.B, case.Hq, case.N, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    n_ev = 5  # fwd | delta | dkdv | dq boundaries
+    def one_step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        swa.swa_attn_fwd(q, k, v, case.W, case.softmax_scale, out=o, lse=lse)
+        marks = None
+        if evs is not None:
+            marks = lambda i: evs[i + 1].record(stream)
+        swa.swa_attn_bwd_phases(q, k, v, o, do, lse, case.W, case.softmax_scale,
+                                dq=dq, dk=dk, dv=dv, delta=delta, between=marks)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize(device)
+    swa.swa_check_device(device)
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(dist, device)
+        torch.cuda.synchronize(device)
+        start.record(stream)
+        for s in range(args.steps):
+            one_step(events[s])
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+    swa.swa_check_device(device)
+    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(dist, total_ms, device)
+    ms_step = total_ms / args.steps
+    per = {"fwd": [], "delta": [], "dkdv": [], "dq": []}
+    for evs in events:
+        per["fwd"].append(evs[0].elapsed_time(evs[1]))
+        per["delta"].append(evs[1].elapsed_time(evs[2]))
+        per["dkdv"].append(evs[2].elapsed_time(evs[3]))
+        per["dq"].append(evs[3].elapsed_time(evs[4]))
+    avg = {key: sum(vals) / len(vals) for key, vals in per.items()}
+    step_total = fl["fwd"] + fl["bwd"]
+    value = world * step_total * args.steps / (total_ms * 1e-3) / 1e12
+
+    kern_tflops = {
+        "fwd": fl["fwd"] / (avg["fwd"] * 1e-3) / 1e12,
+        "dkdv": fl["dkdv"] / (avg["dkdv"] * 1e-3) / 1e12,
+        "dq": fl["dq"] / (avg["dq"] * 1e-3) / 1e12,
+        "bwd": fl["bwd"] / ((avg["delta"] + avg["dkdv"] + avg["dq"]) * 1e-3) / 1e12,
+    }
+    dominant = max(("fwd", "dkdv", "dq"), key=lambda k_: avg[k_])
+    peak_tf = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+    traffic = _profiled_traffic(dominant)
+    roofline = {
+        "kernel": {"fwd": "swa_fwd_kernel<128>", "dkdv": "swa_dkdv_kernel<128>",
+                   "dq": "swa_dq_kernel<128>"}[dominant],
+        "bound": "tensor",
+        "achieved": kern_tflops[dominant],
+        "peak": peak_tf,
+        "unit": "TFLOP/s",
+        "frac": kern_tflops[dominant] / peak_tf,
+        "traffic": traffic,
+        "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a repeated step)",
+    }
+    delta_gbs = delta_bytes(case) / (avg["delta"] * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "long-context sliding-window layer: B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, "
+                        "fwd + bwd (Delta, dK/dV, dQ)",
+            "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "N": case.N, "D": case.D, "W": case.W,
+            "global_batch": case.B * world,
+            "seq_len": case.N,
+            "parallelism": f"independent layer per rank x{world}" if world > 1 else "single GPU",
+            "l2": "no flush: each step reads Q/dO (268 MB each) and K/V (134 MB each), all larger "
+                  "than the 129 MB L2",
+            "flops_per_step": {"fwd": fl["fwd"], "bwd": fl["bwd"]},
+        },
+        "gpu_launches": 4 * args.steps,
+        "kernels_ms": avg,
+        "kernels_tflops": kern_tflops,
+        "fwd_tflops": kern_tflops["fwd"],
+        "bwd_tflops": kern_tflops["bwd"],
+        "delta_gbs": delta_gbs,
+        "roofline": roofline,
+        "clocks": clk.summary(),
+    }
+    del events
+
+    if rank == 0 and not args.no_memory:
+        result["memory"] = measure_memory(swa, device)
+        result["peak_gb"] = result["memory"]["peak_gb_total"][-1]
+    if not args.no_e2e:
+        result["e2e"] = measure_e2e(swa, case, device, dist, args, world)
+    if rank == 0 and not args.no_extra:
+        result["other_workloads"] = measure_other_workloads(swa, device)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        smp = oracle_sample(case, rows_per_sample=1024, samples=args.cpu_samples)
+        result["cpu_baseline"] = {
+            "value": smp["value"], "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"fp64 NumPy oracle fwd+bwd of {smp['rows']} query rows (blocks of 1024, "
+                      f"mid-sequence) of one head of the N=32768 W=1024 layer, {smp['seconds']:.1f} s; "
+                      "BLAS matmuls threaded, elementwise ops single-threaded",
+            "seconds": smp["seconds"],
+        }
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it covers this kernel build."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(kernel)
+        if ent and ent.get("valid", False):
+            return ent.get("bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def measure_memory(swa, device) -> dict:
+    """Peak device memory of one layer's fwd + bwd versus N (inputs Q, K, V, dO excluded)."""
+    out = {"N": [], "peak_gb_total": [], "peak_gb_above_inputs": []}
+    for N in (8192, 16384, 32768):
+        case = si.long_swa_case(N)
+        torch.cuda.synchronize(device)
+        torch.cuda.empty_cache()
+        inp = si.make_inputs(case, device=str(device))
+        torch.cuda.synchronize(device)
+        torch.cuda.reset_peak_memory_stats(device)
+        base = torch.cuda.memory_allocated(device)
+        o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale)
+        dq, dk, dv = swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
+                                      case.softmax_scale)
+        torch.cuda.synchronize(device)
+        peak = torch.cuda.max_memory_allocated(device)
+        out["N"].append(N)
+        out["peak_gb_total"].append(peak / 1e9)
+        out["peak_gb_above_inputs"].append((peak - base) / 1e9)
+        del inp, o, lse, dq, dk, dv
+    a = out["peak_gb_above_inputs"]
+    out["ratio_per_doubling"] = [a[i + 1] / a[i] for i in range(len(a) - 1)]
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_e2e(swa, case, device, dist, args, world) -> dict:
+    """Same metric through the public API with host buffers: each step copies Q, K, V, dO from pinned
+    host memory, runs fwd + bwd, and copies O, LSE, dQ, dK, dV back to pinned host memory."""
+    host = {k_: v_.cpu().pin_memory() for k_, v_ in si.make_inputs(case, device=str(device)).items()}
+    dev = {k_: torch.empty(v_.shape, dtype=v_.dtype, device=device) for k_, v_ in host.items()}
+    o = torch.empty_like(dev["q"])
+    lse = torch.empty(case.B, case.Hq, case.N, dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(dev["q"]), torch.empty_like(dev["k"]), torch.empty_like(dev["v"])
+    ws = torch.empty(swa.swa_attn_bwd_workspace_bytes(case.B, case.Hq, case.N, case.D),
+                     dtype=torch.uint8, device=device)
+    outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    host_out = {k_: torch.empty(v_.shape, dtype=v_.dtype).pin_memory() for k_, v_ in outs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def step():
+        for k_ in host:
+            dev[k_].copy_(host[k_], non_blocking=True)
+        swa.swa_attn_fwd(dev["q"], dev["k"], dev["v"], case.W, case.softmax_scale, out=o, lse=lse)
+        swa.swa_attn_bwd(dev["q"], dev["k"], dev["v"], o, dev["do"], lse, case.W, case.softmax_scale,
+                         dq=dq, dk=dk, dv=dv, workspace=ws)
+        for k_ in outs:
+            host_out[k_].copy_(outs[k_], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(device)
+    stream = torch.cuda.current_stream(device)
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(1, min(args.steps, 10))
+    barrier(dist, device)
+    s_ev.record(stream)
+    for _ in range(steps):
+        step()
+    e_ev.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    ms = max_over_ranks(dist, s_ev.elapsed_time(e_ev), device)
+    fl = step_flops(case)
+    val = world * (fl["fwd"] + fl["bwd"]) * steps / (ms * 1e-3) / 1e12
+    swa.swa_check_device(device)
+    return {"value": val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms / steps, "steps": steps}
+
+
+def measure_other_workloads(swa, device) -> dict:
+    """Full-causal GQA layer (fwd and bwd timed separately) and the 12-layer mixed step."""
+    res = {}
+    case = si.gqa_causal_case()
+    inp = si.make_inputs(case, device=str(device))
+    fl = step_flops(case)
+    stream = torch.cuda.current_stream(device)
+
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) / reps
+
+    o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale)
+    f_ms = timed(lambda: swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
+                                          out=o, lse=lse))
+    b_ms = timed(lambda: swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
+                                          case.softmax_scale))
+    res["gqa_causal_8k"] = {
+        "workload": "B=1 Hq=32 Hkv=8 N=8192 D=128 full causal",
+        "fwd_ms": f_ms, "bwd_ms": b_ms,
+        "fwd_tflops": fl["fwd"] / (f_ms * 1e-3) / 1e12,
+        "bwd_tflops": fl["bwd"] / (b_ms * 1e-3) / 1e12,
+    }
+    del inp, o, lse
+    torch.cuda.empty_cache()
+
+    layers = si.mixed_layer_cases()
+    data = [si.make_inputs(c, device=str(device)) for c in layers]
+    outs = [None] * len(layers)
+
+    def mixed_step():
+        for i, c in enumerate(layers):
+            outs[i] = swa.swa_attn_fwd(data[i]["q"], data[i]["k"], data[i]["v"], c.W, c.softmax_scale)
+        for i in reversed(range(len(layers))):
+            c = layers[i]
+            swa.swa_attn_bwd(data[i]["q"], data[i]["k"], data[i]["v"], outs[i][0], data[i]["do"],
+                             outs[i][1], c.W, c.softmax_scale)
+
+    m_ms = timed(mixed_step, reps=3)
+    tot = sum(step_flops(c)["fwd"] + step_flops(c)["bwd"] for c in layers)
+    res["mixed_12_layers"] = {
+        "workload": "12 layers (W=1024 except layers 5 and 11 full causal), B=1 Hq=32 Hkv=16 "
+                    "N=30553 D=128, fwd all then bwd 11..0",
+        "step_ms": m_ms,
+        "tflops": tot / (m_ms * 1e-3) / 1e12,
+    }
+    del data, outs
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------------------------------------------
+# Reference arm: the fp64 oracle on the host cores
+# ------------------------------------------------------------------------------------------------
+
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return
+    case = si.long_swa_case(32768)
+    for _ in range(args.warmup):
+        oracle_sample(case, rows_per_sample=256, samples=1)
+    t0 = time.perf_counter()
+    smp = oracle_sample(case, rows_per_sample=256, samples=args.steps)
+    dt = time.perf_counter() - t0
+    val = smp["value"]
+    result = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": val,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {
+            "workload": "long-context sliding-window layer: B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, "
+                        "fwd + bwd; each step = 256 query rows of one head on the CPU oracle",
+        },
+        "cpu_baseline": {
+            "value": val, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{args.steps} steps x 256 query rows (mid-sequence) of one head, fp64 NumPy "
+                      "oracle fwd+bwd",
+        },
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(result), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-memory", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-samples", type=int, default=8)
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -89,6 +89,27 @@ swa_status swa_attn_bwd(const void* q, const void* k, const void* v, const void*
                         int B, int Hq, int Hkv, int N, int D, int window, float scale,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * The three phases swa_attn_bwd runs, callable one by one (same arguments, same checks, same
+ * kernels), e.g. to time each kernel or to run the dK/dV and dQ phases on two streams once the
+ * preprocess has finished.  `delta` is the workspace of swa_attn_bwd (fp32 [B,Hq,N]).
+ *   swa_attn_bwd_preprocess : delta = rowsum(dO * O) per query row.
+ *   swa_attn_bwd_dkdv       : dk, dv, walking for each key block only the query blocks inside its
+ *                             window, summed over the query heads of its kv group; needs delta.
+ *   swa_attn_bwd_dq         : dq, walking for each query block only the key blocks inside its
+ *                             window; needs delta.
+ */
+swa_status swa_attn_bwd_preprocess(const void* o, const void* dO, float* delta,
+                                   int B, int Hq, int N, int D, cudaStream_t stream);
+swa_status swa_attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO,
+                             const float* lse, const float* delta, void* dk, void* dv,
+                             int B, int Hq, int Hkv, int N, int D, int window, float scale,
+                             cudaStream_t stream);
+swa_status swa_attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
+                           const float* lse, const float* delta, void* dq,
+                           int B, int Hq, int Hkv, int N, int D, int window, float scale,
+                           cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* swa_strerror(swa_status status);
 

@@ -51,6 +51,7 @@ __all__ = [
     "kv_head_of",
     "head_forward",
     "head_backward",
+    "rows_backward",
     "oracle_forward",
     "oracle_backward",
     "group_backward",
@@ -142,21 +143,38 @@ def head_backward(qh, kh, vh, doh, W: int, scale: float, row_block: int = 1024) 
         "dv": np.zeros((N, vh.shape[1])),
     }
     for rows in _row_blocks(N, row_block):
-        s = _scores(qh, kh, rows, W, scale)
-        l_r = _logsumexp_rows(s)
-        p = np.exp(s - l_r[:, None])
-        o_r = p @ vh
-        do_r = doh[rows]
-        dp = do_r @ vh.T
-        delta = np.sum(do_r * o_r, axis=1)
-        ds = p * (dp - delta[:, None])
-        out["o"][rows] = o_r
-        out["lse"][rows] = l_r
-        out["delta"][rows] = delta
-        out["dq"][rows] = scale * (ds @ kh)
-        out["dk"] += scale * (ds.T @ qh[rows])
-        out["dv"] += p.T @ do_r
+        r = rows_backward(qh, kh, vh, doh, rows, W, scale)
+        for key in ("o", "lse", "delta", "dq"):
+            out[key][rows] = r[key]
+        out["dk"] += r["dk"]
+        out["dv"] += r["dv"]
     return out
+
+
+def rows_backward(qh, kh, vh, doh, rows, W: int, scale: float) -> Dict[str, np.ndarray]:
+    """Forward and backward restricted to the query rows `rows` of one head.
+
+    Returns o, lse, delta, dq for those rows and dk, dv [N, D] = those rows' contribution to the kv
+    head's gradients (dK[j] and dV[j] are sums over query rows i).
+    """
+    qh, kh, vh, doh = _as64(qh), _as64(kh), _as64(vh), _as64(doh)
+    rows = np.asarray(rows, dtype=np.int64)
+    s = _scores(qh, kh, rows, W, scale)
+    lse = _logsumexp_rows(s)
+    p = np.exp(s - lse[:, None])
+    o_r = p @ vh
+    do_r = doh[rows]
+    dp = do_r @ vh.T
+    delta = np.sum(do_r * o_r, axis=1)
+    ds = p * (dp - delta[:, None])
+    return {
+        "o": o_r,
+        "lse": lse,
+        "delta": delta,
+        "dq": scale * (ds @ kh),
+        "dk": scale * (ds.T @ qh[rows]),
+        "dv": p.T @ do_r,
+    }
 
 
 def oracle_forward(q, k, v, window: int, scale: float, row_block: int = 1024):

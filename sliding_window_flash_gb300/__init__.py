@@ -27,6 +27,7 @@ __all__ = [
     "swa_attn_fwd",
     "swa_attn_bwd",
     "swa_attn_bwd_workspace_bytes",
+    "swa_attn_bwd_phases",
     "swa_check_device",
     "SlidingWindowAttention",
     "STATUS",
@@ -55,6 +56,9 @@ SIGNATURES = {
         _c_int,
         [_vp] * 9 + [_c_int] * 6 + [_c_float, _vp, ctypes.c_size_t, _vp],
     ),
+    "swa_attn_bwd_preprocess": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_vp]),
+    "swa_attn_bwd_dkdv": (_c_int, [_vp] * 8 + [_c_int] * 6 + [_c_float, _vp]),
+    "swa_attn_bwd_dq": (_c_int, [_vp] * 7 + [_c_int] * 6 + [_c_float, _vp]),
     "swa_strerror": (ctypes.c_char_p, [_c_int]),
     "swa_check_device": (_c_int, [_vp]),
     "swa_version": (_c_int, []),
@@ -177,6 +181,49 @@ def swa_attn_bwd(q, k, v, o, do, lse, window: int, scale: Optional[float] = None
                           _stream_handle(q.device))
     if rc != 0:
         raise SwaError(rc, "swa_attn_bwd")
+    return dq, dk, dv
+
+
+def swa_attn_bwd_phases(q, k, v, o, do, lse, window: int, scale: Optional[float] = None,
+                        dq=None, dk=None, dv=None, delta=None, between=None) -> Tuple:
+    """The backward as its three C-ABI phases (preprocess, dK/dV, dQ) on the current stream.
+
+    Same kernels and results as swa_attn_bwd.  ``between(i)`` (optional) is called before phase i
+    and after the last one (i = 0..3), e.g. to record CUDA events around each kernel.
+    """
+    import torch
+
+    lib = load()
+    B, Hq, Hkv, N, D = _dims(q, k)
+    sc = _scale(scale, D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if delta is None:
+        delta = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    for t, name, hs in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq),
+                        (dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
+        _check_tensor(t, name, (B, hs, N, D), torch.bfloat16)
+    _check_tensor(lse, "lse", (B, Hq, N), torch.float32)
+    _check_tensor(delta, "delta", (B, Hq, N), torch.float32)
+    st = _stream_handle(q.device)
+    mark = between or (lambda i: None)
+    mark(0)
+    rc = lib.swa_attn_bwd_preprocess(o.data_ptr(), do.data_ptr(), delta.data_ptr(), B, Hq, N, D, st)
+    if rc != 0:
+        raise SwaError(rc, "swa_attn_bwd_preprocess")
+    mark(1)
+    rc = lib.swa_attn_bwd_dkdv(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                               delta.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, D,
+                               int(window), sc, st)
+    if rc != 0:
+        raise SwaError(rc, "swa_attn_bwd_dkdv")
+    mark(2)
+    rc = lib.swa_attn_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                             delta.data_ptr(), dq.data_ptr(), B, Hq, Hkv, N, D, int(window), sc, st)
+    if rc != 0:
+        raise SwaError(rc, "swa_attn_bwd_dq")
+    mark(3)
     return dq, dk, dv
 
 

@@ -126,6 +126,52 @@ swa_status swa_attn_bwd(const void* q, const void* k, const void* v, const void*
   return SWA_OK;
 }
 
+swa_status swa_attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int Hq,
+                                   int N, int D, cudaStream_t stream) {
+  if (!o || !dO || !delta) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_sizes(B, Hq, Hq, N, D, 1, 1.f);
+  if (st != SWA_OK) return st;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(delta)) return SWA_ERR_MISALIGNED;
+  unsigned* err = nullptr;
+  if ((st = current_device(&err)) != SWA_OK) return st;
+  const swa::Problem pb = make_problem(B, Hq, Hq, N, D, 1, 1.f, err);
+  return swa::launch_bwd_delta(pb, o, dO, delta, stream) == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+swa_status swa_attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO,
+                             const float* lse, const float* delta, void* dk, void* dv, int B,
+                             int Hq, int Hkv, int N, int D, int window, float scale,
+                             cudaStream_t stream) {
+  if (!q || !k || !v || !dO || !lse || !delta || !dk || !dv) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
+  if (st != SWA_OK) return st;
+  const void* ptrs[] = {q, k, v, dO, lse, delta, dk, dv};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return SWA_ERR_MISALIGNED;
+  unsigned* err = nullptr;
+  if ((st = current_device(&err)) != SWA_OK) return st;
+  const swa::Problem pb = make_problem(B, Hq, Hkv, N, D, window, scale, err);
+  return swa::launch_bwd_dkdv(pb, q, k, v, dO, lse, delta, dk, dv, stream) == cudaSuccess
+             ? SWA_OK
+             : SWA_ERR_CUDA;
+}
+
+swa_status swa_attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
+                           const float* lse, const float* delta, void* dq, int B, int Hq, int Hkv,
+                           int N, int D, int window, float scale, cudaStream_t stream) {
+  if (!q || !k || !v || !dO || !lse || !delta || !dq) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
+  if (st != SWA_OK) return st;
+  const void* ptrs[] = {q, k, v, dO, lse, delta, dq};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return SWA_ERR_MISALIGNED;
+  unsigned* err = nullptr;
+  if ((st = current_device(&err)) != SWA_OK) return st;
+  const swa::Problem pb = make_problem(B, Hq, Hkv, N, D, window, scale, err);
+  return swa::launch_bwd_dq(pb, q, k, v, dO, lse, delta, dq, stream) == cudaSuccess ? SWA_OK
+                                                                                    : SWA_ERR_CUDA;
+}
+
 const char* swa_strerror(swa_status status) {
   switch (status) {
     case SWA_OK: return "SWA_OK";
