@@ -110,6 +110,34 @@ swa_status swa_attn_bwd_dq(const void* q, const void* k, const void* v, const vo
                            int B, int Hq, int Hkv, int N, int D, int window, float scale,
                            cudaStream_t stream);
 
+/*
+ * Backward without any caller-provided workspace and without allocating: the same computation and
+ * kernels as swa_attn_bwd, but the per-row Delta scratch lives in a fixed array of device memory
+ * that is part of the library image (SWA_NOALLOC_MAX_ROWS fp32 values, 16 MiB; every GPU that loads
+ * the library keeps that array until the process exits).  The pages this library follows have no
+ * counterpart of this entry point.
+ *
+ * It is for callers that cannot obtain scratch device memory: code whose device memory is owned
+ * and planned by a host framework's allocator (which a side cudaMalloc would bypass), code that
+ * must not allocate once its steady state has begun (an allocation can synchronize the device or
+ * fail under memory pressure mid-run), and plain C callers that only hold the tensors' pointers.
+ * The caller still passes every input and output buffer.
+ *
+ *   Limit: B*Hq*N <= SWA_NOALLOC_MAX_ROWS, else SWA_ERR_WORKSPACE and nothing is launched.
+ *   Set-up: the first call on each device, with that device current, looks up the array's device
+ *           address (no allocation); make that first call before any stream capture.
+ *   Sharing: every call on a device uses the same array, and it keeps the last call's contents.
+ *           Each call fully rewrites the rows it reads before reading them, so nothing has to start
+ *           at zero; but calls whose kernels overlap on the GPU (other streams, other threads) race
+ *           on the array and give wrong results.  Serialize them.
+ * Other arguments, checks and errors are those of swa_attn_bwd.
+ */
+#define SWA_NOALLOC_MAX_ROWS (1 << 22)
+swa_status swa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                                const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                                int B, int Hq, int Hkv, int N, int D, int window, float scale,
+                                cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* swa_strerror(swa_status status);
 

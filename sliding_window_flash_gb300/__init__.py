@@ -59,6 +59,7 @@ SIGNATURES = {
     "swa_attn_bwd_preprocess": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_vp]),
     "swa_attn_bwd_dkdv": (_c_int, [_vp] * 8 + [_c_int] * 6 + [_c_float, _vp]),
     "swa_attn_bwd_dq": (_c_int, [_vp] * 7 + [_c_int] * 6 + [_c_float, _vp]),
+    "swa_attn_bwd_noalloc": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_c_float, _vp]),
     "swa_strerror": (ctypes.c_char_p, [_c_int]),
     "swa_check_device": (_c_int, [_vp]),
     "swa_version": (_c_int, []),

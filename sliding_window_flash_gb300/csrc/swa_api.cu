@@ -205,3 +205,58 @@ swa_status swa_check_device(cudaStream_t stream) {
 int swa_version(void) { return 100; }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// Backward without caller workspace: the Delta scratch is a fixed device array of this file.
+// ------------------------------------------------------------------------------------------------
+namespace {
+
+// Delta scratch of swa_attn_bwd_noalloc (one fp32 per query row), shared by every call on a device.
+static __device__ __align__(256) float g_swa_noalloc_delta[SWA_NOALLOC_MAX_ROWS];
+
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code the array's name is
+// only a host-side stand-in, so the address is looked up once per device (no allocation).
+swa_status noalloc_scratch(float** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SWA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SWA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_swa_noalloc_delta) != cudaSuccess || p == nullptr)
+      return SWA_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return SWA_OK;
+}
+
+}  // namespace
+
+extern "C" swa_status swa_attn_bwd_noalloc(const void* q, const void* k, const void* v,
+                                           const void* o, const void* dO, const float* lse,
+                                           void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                                           int N, int D, int window, float scale,
+                                           cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
+  if (st != SWA_OK) return st;
+  if (static_cast<long long>(B) * Hq * N > SWA_NOALLOC_MAX_ROWS) return SWA_ERR_WORKSPACE;
+  const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return SWA_ERR_MISALIGNED;
+  unsigned* err = nullptr;
+  if ((st = current_device(&err)) != SWA_OK) return st;
+  float* delta = nullptr;
+  if ((st = noalloc_scratch(&delta)) != SWA_OK) return st;
+  const swa::Problem pb = make_problem(B, Hq, Hkv, N, D, window, scale, err);
+  if (swa::launch_bwd_delta(pb, o, dO, delta, stream) != cudaSuccess) return SWA_ERR_CUDA;
+  if (swa::launch_bwd_dkdv(pb, q, k, v, dO, lse, delta, dk, dv, stream) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (swa::launch_bwd_dq(pb, q, k, v, dO, lse, delta, dq, stream) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  return SWA_OK;
+}
