@@ -12,9 +12,10 @@
 // a key tile that no query visits are still written (as zeros).
 //
 // Warp roles (192 threads): warps 0-3 compute (thread r = key row k0 + r = TMEM lane r),
-// warp 4 TMA producer (K and V once; Q_t, dO_t through two slots), warp 5 MMA issuer and TMEM
-// owner.  P^T and dS^T share one bf16 operand tile in shared memory.  TMEM columns: [0,128) S^T,
-// [128,256) dP^T, [256, 256+D) dK, [256+D, 256+2D) dV.
+// warp 4 TMA producer (K and V once; Q_t and dO_t through two shared-memory rings), warp 5 MMA
+// issuer and TMEM owner.  P^T and dS^T go back to TMEM (bf16 pairs, over the columns of S^T and
+// dP^T they came from) and are the A operands of dV += P^T dO and dK += dS^T Q.  TMEM columns:
+// [0,128) S^T / P^T, [128,256) dP^T / dS^T, [256, 256+D) dK, [256+D, 256+2D) dV.
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 #include "swa_tmap.h"
@@ -27,30 +28,29 @@ struct DkdvCfg {
   static constexpr int kTileBytes = kBlockM * D * 2;
   static constexpr int kChunkBytes = kBlockM * 128;
   static constexpr int kChunks = D / 64;
-  static constexpr int kOpBytes = kBlockN * kBlockM * 2;  // P^T / dS^T operand tile
+  static constexpr int kQStages = (D == 128) ? 2 : 4;
+  static constexpr int kDOStages = (D == 128) ? 2 : 4;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffQ = kOffV + kTileBytes;          // 2 slots
-  static constexpr int kOffDO = kOffQ + 2 * kTileBytes;     // 2 slots
-  static constexpr int kOffOp = kOffDO + 2 * kTileBytes;
-  static constexpr int kOffRow = kOffOp + kOpBytes;         // lse2[128], delta[128]
+  static constexpr int kOffQ = kOffV + kTileBytes;
+  static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
+  static constexpr int kOffRow = kOffDO + kDOStages * kTileBytes;  // lse2[128], delta[128]
   static constexpr int kOffBar = kOffRow + 2 * kBlockM * 4;
   static constexpr int kKVFull = 0;
-  static constexpr int kQFull = 1;       // 2
-  static constexpr int kDOFull = 3;      // 2
-  static constexpr int kPairEmpty = 5;   // 2
-  static constexpr int kSFull = 7;
-  static constexpr int kSEmpty = 8;
-  static constexpr int kDPFull = 9;
-  static constexpr int kDPEmpty = 10;
-  static constexpr int kPFull = 11;
-  static constexpr int kDSFull = 12;
-  static constexpr int kDVDone = 13;
-  static constexpr int kDKDone = 14;
-  static constexpr int kDrain = 15;
-  static constexpr int kNumBars = 16;
+  static constexpr int kQFull = 1;
+  static constexpr int kQEmpty = kQFull + kQStages;
+  static constexpr int kDOFull = kQEmpty + kQStages;
+  static constexpr int kDOEmpty = kDOFull + kDOStages;
+  static constexpr int kSFull = kDOEmpty + kDOStages;
+  static constexpr int kDPFull = kSFull + 1;
+  static constexpr int kPFull = kDPFull + 1;
+  static constexpr int kDSFull = kPFull + 1;
+  static constexpr int kDone = kDSFull + 1;
+  static constexpr int kDrain = kDone + 1;
+  static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
+  // P^T is written over the first 64 columns of S^T, dS^T over the first 64 of dP^T.
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 256 + D;
   static constexpr int kThreads = 192;
 };
@@ -84,7 +84,6 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sV = smem_u32(smem + C::kOffV);
   const uint32_t sQ0 = smem_u32(smem + C::kOffQ);
   const uint32_t sDO0 = smem_u32(smem + C::kOffDO);
-  const uint32_t sOp = smem_u32(smem + C::kOffOp);
 
   // Key blocks with the longest walks (lowest index under a full causal window) go first.
   const int kb = static_cast<int>(blockIdx.x) / a.BHK;
@@ -102,19 +101,19 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(bar(C::kKVFull), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(bar(C::kQFull + s), 1);
+      mbar_init(bar(C::kQEmpty + s), 1);
+    }
+    for (int s = 0; s < C::kDOStages; ++s) {
       mbar_init(bar(C::kDOFull + s), 1);
-      mbar_init(bar(C::kPairEmpty + s), 1);
+      mbar_init(bar(C::kDOEmpty + s), 1);
     }
     mbar_init(bar(C::kSFull), 1);
-    mbar_init(bar(C::kSEmpty), 128);
     mbar_init(bar(C::kDPFull), 1);
-    mbar_init(bar(C::kDPEmpty), 128);
     mbar_init(bar(C::kPFull), 128);
     mbar_init(bar(C::kDSFull), 128);
-    mbar_init(bar(C::kDVDone), 1);
-    mbar_init(bar(C::kDKDone), 1);
+    mbar_init(bar(C::kDone), 1);
     mbar_init(bar(C::kDrain), 1);
     fence_barrier_init();
   }
@@ -139,37 +138,47 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKVFull), 64 * h, k0, bhk);
         tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kKVFull), 64 * h, k0, bhk);
       }
-      int last_fill[2] = {-1, -1};
+      int last_q[C::kQStages], last_do[C::kDOStages];
+      for (int s = 0; s < C::kQStages; ++s) last_q[s] = -1;
+      for (int s = 0; s < C::kDOStages; ++s) last_do[s] = -1;
       for (int t = 0; t < T; ++t) {
-        const int s = t & 1, n = t >> 1;
-        if (t >= 2 && !mbar_wait(bar(C::kPairEmpty + s), (n - 1) & 1, &abort_flag, a.err)) break;
         const int q0 = tile_q0(t), bhq = tile_bhq(t);
-        const uint32_t sQ = sQ0 + s * C::kTileBytes, sDO = sDO0 + s * C::kTileBytes;
-        mbar_arrive_expect_tx(bar(C::kQFull + s), C::kTileBytes);
+        const int sq = t % C::kQStages, nqs = t / C::kQStages;
+        if (t >= C::kQStages && !mbar_wait(bar(C::kQEmpty + sq), (nqs - 1) & 1, &abort_flag, a.err))
+          break;
+        const uint32_t sQ = sQ0 + sq * C::kTileBytes;
+        mbar_arrive_expect_tx(bar(C::kQFull + sq), C::kTileBytes);
         for (int h = 0; h < C::kChunks; ++h)
-          tma_load_3d(sQ + h * C::kChunkBytes, &tm_q, bar(C::kQFull + s), 64 * h, q0, bhq);
-        mbar_arrive_expect_tx(bar(C::kDOFull + s), C::kTileBytes);
+          tma_load_3d(sQ + h * C::kChunkBytes, &tm_q, bar(C::kQFull + sq), 64 * h, q0, bhq);
+        last_q[sq] = t;
+        const int sd = t % C::kDOStages, nds = t / C::kDOStages;
+        if (t >= C::kDOStages &&
+            !mbar_wait(bar(C::kDOEmpty + sd), (nds - 1) & 1, &abort_flag, a.err))
+          break;
+        const uint32_t sDO = sDO0 + sd * C::kTileBytes;
+        mbar_arrive_expect_tx(bar(C::kDOFull + sd), C::kTileBytes);
         for (int h = 0; h < C::kChunks; ++h)
-          tma_load_3d(sDO + h * C::kChunkBytes, &tm_do, bar(C::kDOFull + s), 64 * h, q0, bhq);
-        last_fill[s] = t;
+          tma_load_3d(sDO + h * C::kChunkBytes, &tm_do, bar(C::kDOFull + sd), 64 * h, q0, bhq);
+        last_do[sd] = t;
       }
       drain_wait(bar(C::kKVFull), 0, a.err);
-      for (int s = 0; s < 2; ++s) {
-        if (last_fill[s] >= 0) {
-          drain_wait(bar(C::kQFull + s), (last_fill[s] >> 1) & 1, a.err);
-          drain_wait(bar(C::kDOFull + s), (last_fill[s] >> 1) & 1, a.err);
-        }
-      }
+      for (int s = 0; s < C::kQStages; ++s)
+        if (last_q[s] >= 0) drain_wait(bar(C::kQFull + s), (last_q[s] / C::kQStages) & 1, a.err);
+      for (int s = 0; s < C::kDOStages; ++s)
+        if (last_do[s] >= 0)
+          drain_wait(bar(C::kDOFull + s), (last_do[s] / C::kDOStages) & 1, a.err);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer
+    // Issue order: S_0, dP_0, then per tile t: dV += P_t^T dO_t, S_{t+1}, dK += dS_t^T Q_t, dP_{t+1}.
+    // The MMAs run in that order, so S_{t+1} overwrites the S^T / P^T columns only after dV_t has
+    // read P_t^T, and dP_{t+1} overwrites dP^T / dS^T only after dK_t has read dS_t^T.
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(kBlockN, kBlockM, false, false);  // S^T, dP^T
       constexpr uint32_t kIdAcc = idesc_bf16(kBlockN, D, false, true);       // dV, dK
       auto issue_s = [&](int t) -> bool {  // S^T = K Q_t^T
-        const int s = t & 1;
-        if (!mbar_wait(bar(C::kQFull + s), (t >> 1) & 1, &abort_flag, a.err)) return false;
-        if (t >= 1 && !mbar_wait(bar(C::kSEmpty), (t - 1) & 1, &abort_flag, a.err)) return false;
+        const int s = t % C::kQStages;
+        if (!mbar_wait(bar(C::kQFull + s), (t / C::kQStages) & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sQ = sQ0 + s * C::kTileBytes;
 #pragma unroll
@@ -182,9 +191,9 @@ __global__ void __launch_bounds__(192, 1)
         return true;
       };
       auto issue_dp = [&](int t) -> bool {  // dP^T = V dO_t^T
-        const int s = t & 1;
-        if (!mbar_wait(bar(C::kDOFull + s), (t >> 1) & 1, &abort_flag, a.err)) return false;
-        if (t >= 1 && !mbar_wait(bar(C::kDPEmpty), (t - 1) & 1, &abort_flag, a.err)) return false;
+        const int s = t % C::kDOStages;
+        if (!mbar_wait(bar(C::kDOFull + s), (t / C::kDOStages) & 1, &abort_flag, a.err))
+          return false;
         tc_fence_after();
         const uint32_t sDO = sDO0 + s * C::kTileBytes;
 #pragma unroll
@@ -196,32 +205,34 @@ __global__ void __launch_bounds__(192, 1)
         umma_commit(bar(C::kDPFull));
         return true;
       };
-      auto issue_acc = [&](int t, int wait_bar, uint32_t b_tile, uint32_t col, int done_bar) -> bool {
+      // acc += X^T B_t with X^T (bf16 pairs) in TMEM at column a_col and B_t = dO_t or Q_t (MN-major)
+      auto issue_acc = [&](int t, int wait_bar, uint32_t a_col, uint32_t b_tile,
+                           uint32_t d_col) -> bool {
         if (!mbar_wait(bar(wait_bar), t & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kBlockM / 16; ++ks) {
-          const uint32_t aoff = (ks >> 2) * (kBlockN * 128) + (ks & 3) * 32;
-          umma_ss(tmem + col, smem_desc_sw128(sOp + aoff, 16, 1024),
+          umma_ts(tmem + d_col, tmem + a_col + 8u * ks,
                   smem_desc_sw128(b_tile + ks * 16 * 128, C::kChunkBytes, 1024), kIdAcc,
                   (t > 0 || ks > 0) ? 1u : 0u);
         }
-        umma_commit(bar(done_bar));
         return true;
       };
       bool ok = mbar_wait(bar(C::kKVFull), 0, &abort_flag, a.err);
       if (ok) ok = issue_s(0);
       if (ok) ok = issue_dp(0);
       for (int t = 0; ok && t < T; ++t) {
-        const int s = t & 1;
-        // dV += P^T dO_t
-        ok = issue_acc(t, C::kPFull, sDO0 + s * C::kTileBytes, C::kColDV, C::kDVDone);
-        if (ok && t + 1 < T) ok = issue_s(t + 1);
-        // dK += dS^T Q_t, then release the (Q_t, dO_t) slot
-        if (ok) ok = issue_acc(t, C::kDSFull, sQ0 + s * C::kTileBytes, C::kColDK, C::kDKDone);
-        if (ok) umma_commit(bar(C::kPairEmpty + s));
-        if (ok && t + 1 < T) ok = issue_dp(t + 1);
+        const int sq = t % C::kQStages, sd = t % C::kDOStages;
+        ok = issue_acc(t, C::kPFull, C::kColS, sDO0 + sd * C::kTileBytes, C::kColDV);  // dV
+        if (!ok) break;
+        umma_commit(bar(C::kDOEmpty + sd));
+        if (t + 1 < T && !(ok = issue_s(t + 1))) break;
+        ok = issue_acc(t, C::kDSFull, C::kColDP, sQ0 + sq * C::kTileBytes, C::kColDK);  // dK
+        if (!ok) break;
+        umma_commit(bar(C::kQEmpty + sq));
+        if (t + 1 < T) ok = issue_dp(t + 1);
       }
+      if (ok) umma_commit(bar(C::kDone));
       umma_commit(bar(C::kDrain));
       drain_wait(bar(C::kDrain), 0, a.err);
     }
@@ -257,16 +268,18 @@ __global__ void __launch_bounds__(192, 1)
       if (!(ok = warp_wait(bar(C::kSFull), t & 1, &abort_flag, a.err))) break;
       tc_fence_after();
       float p[kBlockM];
+      {
+        uint32_t rr[4][32];
 #pragma unroll
-      for (int c4 = 0; c4 < kBlockM / 32; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kColS + 32u * c4, rr);
-        tmem_wait_ld(rr);
+        for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tmem + lane_base + C::kColS + 32u * c4, rr[c4]);
+        tmem_wait_ld_all();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) p[32 * c4 + i] = __uint_as_float(rr[i]);
+        for (int c4 = 0; c4 < 4; ++c4) {
+          reg_fence(rr[c4]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) p[32 * c4 + i] = __uint_as_float(rr[c4][i]);
+        }
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::kSEmpty));
       const float4* l4 = reinterpret_cast<const float4*>(s_lse2);
 #pragma unroll
       for (int c4 = 0; c4 < kBlockM / 4; ++c4) {
@@ -283,13 +296,14 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int c = 0; c < kBlockM; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
       }
-      uint32_t pk[kBlockM / 2];
+      {
+        uint32_t pk[2][32];
 #pragma unroll
-      for (int c = 0; c < kBlockM / 2; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
-      // dK of the previous tile must have consumed the shared operand tile.
-      if (t > 0 && !(ok = warp_wait(bar(C::kDKDone), (t - 1) & 1, &abort_flag, a.err))) break;
-      store_row_sw128_128(sOp, r, pk);
-      fence_proxy_async_smem();
+        for (int c = 0; c < kBlockM / 2; ++c) pk[c >> 5][c & 31] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+        tmem_st32(tmem + lane_base + C::kColS, pk[0]);
+        tmem_st32(tmem + lane_base + C::kColS + 32u, pk[1]);
+      }
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kPFull));
 
@@ -297,30 +311,31 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const float4* d4 = reinterpret_cast<const float4*>(s_delta);
 #pragma unroll
-      for (int c4 = 0; c4 < kBlockM / 32; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kColDP + 32u * c4, rr);
-        tmem_wait_ld(rr);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t rr[2][32];
+        tmem_ld32(tmem + lane_base + C::kColDP + 64u * h, rr[0]);
+        tmem_ld32(tmem + lane_base + C::kColDP + 64u * h + 32u, rr[1]);
+        tmem_wait_ld_all();
+        reg_fence(rr[0]);
+        reg_fence(rr[1]);
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = 32 * c4 + 4 * i;
+        for (int i = 0; i < 16; ++i) {
+          const int c = 64 * h + 4 * i;
           const float4 dl = d4[c >> 2];
-          pk[c >> 1] = pack_bf16x2(p[c] * (__uint_as_float(rr[4 * i]) - dl.x),
-                                   p[c + 1] * (__uint_as_float(rr[4 * i + 1]) - dl.y));
-          pk[(c >> 1) + 1] = pack_bf16x2(p[c + 2] * (__uint_as_float(rr[4 * i + 2]) - dl.z),
-                                         p[c + 3] * (__uint_as_float(rr[4 * i + 3]) - dl.w));
+          const uint32_t* src = &rr[i >> 3][(4 * i) & 31];
+          pk[2 * i] = pack_bf16x2(p[c] * (__uint_as_float(src[0]) - dl.x),
+                                  p[c + 1] * (__uint_as_float(src[1]) - dl.y));
+          pk[2 * i + 1] = pack_bf16x2(p[c + 2] * (__uint_as_float(src[2]) - dl.z),
+                                      p[c + 3] * (__uint_as_float(src[3]) - dl.w));
         }
+        tmem_st32(tmem + lane_base + C::kColDP + 32u * h, pk);
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::kDPEmpty));
-      // dV of this tile must have consumed P^T before dS^T replaces it.
-      if (!(ok = warp_wait(bar(C::kDVDone), t & 1, &abort_flag, a.err))) break;
-      store_row_sw128_128(sOp, r, pk);
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kDSFull));
     }
-    if (ok && warp_wait(bar(C::kDKDone), (T - 1) & 1, &abort_flag, a.err)) {
+    if (ok && warp_wait(bar(C::kDone), 0, &abort_flag, a.err)) {
       tc_fence_after();
       const bool in_range = key < a.N;
       const size_t grow = static_cast<size_t>(bhk) * a.N + key;
@@ -329,18 +344,20 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t col = which == 0 ? C::kColDK : C::kColDV;
         const float mul = which == 0 ? a.scale : 1.f;
         __nv_bfloat16* dst_row = (which == 0 ? a.dk : a.dv) + grow * D;
+        uint32_t rr[D / 32][32];
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tmem + lane_base + col + c0, rr);
-          tmem_wait_ld(rr);
+        for (int c4 = 0; c4 < D / 32; ++c4) tmem_ld32(tmem + lane_base + col + 32u * c4, rr[c4]);
+        tmem_wait_ld_all();
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          reg_fence(rr[c4]);
           uint32_t o16[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            o16[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * mul,
-                                 __uint_as_float(rr[2 * i + 1]) * mul);
+            o16[i] = pack_bf16x2(__uint_as_float(rr[c4][2 * i]) * mul,
+                                 __uint_as_float(rr[c4][2 * i + 1]) * mul);
           if (in_range) {
-            uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c4);
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               dst[v] = make_uint4(o16[4 * v], o16[4 * v + 1], o16[4 * v + 2], o16[4 * v + 3]);

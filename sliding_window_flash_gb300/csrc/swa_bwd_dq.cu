@@ -11,8 +11,9 @@
 // lab's fp32-score-tile experiment showed the error of bf16 score scratch).
 //
 // Warp roles (192 threads): warps 0-3 compute (thread r = query row q0 + r = TMEM lane r),
-// warp 4 TMA producer (Q and dO once, K_j / V_j through a ring of stages), warp 5 MMA issuer and
-// TMEM owner.  TMEM columns: [0,128) S, [128,256) dP, [256, 256+D) dQ.
+// warp 4 TMA producer (Q and dO once, K_j and V_j through two shared-memory rings), warp 5 MMA
+// issuer and TMEM owner.  dS goes back to TMEM and is the A operand of dQ += dS K_j.
+// TMEM columns: [0,128) S, [128,256) dP, [256, 256+D) dQ, [256+D, 320+D) dS (bf16 pairs).
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 #include "swa_tmap.h"
@@ -25,29 +26,28 @@ struct DqCfg {
   static constexpr int kTileBytes = kBlockM * D * 2;
   static constexpr int kChunkBytes = kBlockM * 128;
   static constexpr int kChunks = D / 64;
-  static constexpr int kStages = (D == 128) ? 2 : 3;
-  static constexpr int kDSBytes = kBlockM * kBlockN * 2;
+  static constexpr int kKStages = (D == 128) ? 3 : 4;
+  static constexpr int kVStages = (D == 128) ? 2 : 4;
   static constexpr int kOffQ = 0;
   static constexpr int kOffDO = kOffQ + kTileBytes;
   static constexpr int kOffK = kOffDO + kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffDS = kOffV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffDS + kDSBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kQDFull = 0;
   static constexpr int kKFull = 1;
-  static constexpr int kVFull = kKFull + kStages;
-  static constexpr int kKVEmpty = kVFull + kStages;
-  static constexpr int kSFull = kKVEmpty + kStages;
+  static constexpr int kKEmpty = kKFull + kKStages;
+  static constexpr int kVFull = kKEmpty + kKStages;
+  static constexpr int kVEmpty = kVFull + kVStages;
+  static constexpr int kSFull = kVEmpty + kVStages;
   static constexpr int kSEmpty = kSFull + 1;
   static constexpr int kDPFull = kSEmpty + 1;
-  static constexpr int kDPEmpty = kDPFull + 1;
-  static constexpr int kDSFull = kDPEmpty + 1;
+  static constexpr int kDSFull = kDPFull + 1;
   static constexpr int kDQDone = kDSFull + 1;
   static constexpr int kDrain = kDQDone + 1;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
   static constexpr int kThreads = 192;
 };
 
@@ -76,7 +76,6 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sDO = smem_u32(smem + C::kOffDO);
   const uint32_t sK0 = smem_u32(smem + C::kOffK);
   const uint32_t sV0 = smem_u32(smem + C::kOffV);
-  const uint32_t sDS = smem_u32(smem + C::kOffDS);
 
   const int qb = a.nqb - 1 - static_cast<int>(blockIdx.x) / a.BH;
   const int bh = static_cast<int>(blockIdx.x) % a.BH;
@@ -91,15 +90,17 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(bar(C::kQDFull), 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bar(C::kKFull + s), 1);
+      mbar_init(bar(C::kKEmpty + s), 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(bar(C::kVFull + s), 1);
-      mbar_init(bar(C::kKVEmpty + s), 1);
+      mbar_init(bar(C::kVEmpty + s), 1);
     }
     mbar_init(bar(C::kSFull), 1);
     mbar_init(bar(C::kSEmpty), 128);
     mbar_init(bar(C::kDPFull), 1);
-    mbar_init(bar(C::kDPEmpty), 128);
     mbar_init(bar(C::kDSFull), 128);
     mbar_init(bar(C::kDQDone), 1);
     mbar_init(bar(C::kDrain), 1);
@@ -126,37 +127,44 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_3d(sQ + h * C::kChunkBytes, &tm_q, bar(C::kQDFull), 64 * h, q0, bh);
         tma_load_3d(sDO + h * C::kChunkBytes, &tm_do, bar(C::kQDFull), 64 * h, q0, bh);
       }
-      int last_fill[C::kStages];
-      for (int s = 0; s < C::kStages; ++s) last_fill[s] = -1;
+      int last_k[C::kKStages], last_v[C::kVStages];
+      for (int s = 0; s < C::kKStages; ++s) last_k[s] = -1;
+      for (int s = 0; s < C::kVStages; ++s) last_v[s] = -1;
       for (int j = 0; j < nkv; ++j) {
-        const int s = j % C::kStages, n = j / C::kStages;
-        if (j >= C::kStages && !mbar_wait(bar(C::kKVEmpty + s), (n - 1) & 1, &abort_flag, a.err))
-          break;
         const int k0 = (kb_lo + j) * kBlockN;
-        const uint32_t sK = sK0 + s * C::kTileBytes, sV = sV0 + s * C::kTileBytes;
-        mbar_arrive_expect_tx(bar(C::kKFull + s), C::kTileBytes);
+        const int sk = j % C::kKStages, nk = j / C::kKStages;
+        if (j >= C::kKStages && !mbar_wait(bar(C::kKEmpty + sk), (nk - 1) & 1, &abort_flag, a.err))
+          break;
+        const uint32_t sK = sK0 + sk * C::kTileBytes;
+        mbar_arrive_expect_tx(bar(C::kKFull + sk), C::kTileBytes);
         for (int h = 0; h < C::kChunks; ++h)
-          tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKFull + s), 64 * h, k0, bhk);
-        mbar_arrive_expect_tx(bar(C::kVFull + s), C::kTileBytes);
+          tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKFull + sk), 64 * h, k0, bhk);
+        last_k[sk] = j;
+        const int sv = j % C::kVStages, nv = j / C::kVStages;
+        if (j >= C::kVStages && !mbar_wait(bar(C::kVEmpty + sv), (nv - 1) & 1, &abort_flag, a.err))
+          break;
+        const uint32_t sV = sV0 + sv * C::kTileBytes;
+        mbar_arrive_expect_tx(bar(C::kVFull + sv), C::kTileBytes);
         for (int h = 0; h < C::kChunks; ++h)
-          tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kVFull + s), 64 * h, k0, bhk);
-        last_fill[s] = j;
+          tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kVFull + sv), 64 * h, k0, bhk);
+        last_v[sv] = j;
       }
       drain_wait(bar(C::kQDFull), 0, a.err);
-      for (int s = 0; s < C::kStages; ++s) {
-        if (last_fill[s] >= 0) {
-          drain_wait(bar(C::kKFull + s), (last_fill[s] / C::kStages) & 1, a.err);
-          drain_wait(bar(C::kVFull + s), (last_fill[s] / C::kStages) & 1, a.err);
-        }
-      }
+      for (int s = 0; s < C::kKStages; ++s)
+        if (last_k[s] >= 0) drain_wait(bar(C::kKFull + s), (last_k[s] / C::kKStages) & 1, a.err);
+      for (int s = 0; s < C::kVStages; ++s)
+        if (last_v[s] >= 0) drain_wait(bar(C::kVFull + s), (last_v[s] / C::kVStages) & 1, a.err);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer
+    // Issue order S_0, dP_0, then per block j: S_{j+1}, dQ += dS_j K_j, dP_{j+1}.  The MMAs run in
+    // that order, so dP_{j+1} lands only after dQ_j has read dS_j: when the compute warps see
+    // dP_{j+1} they may overwrite the single TMEM dS buffer.
     if (lane == 0) {
       constexpr uint32_t kIdSq = idesc_bf16(kBlockM, kBlockN, false, false);  // S, dP
       constexpr uint32_t kIdDq = idesc_bf16(kBlockM, D, false, true);         // dQ += dS K
       auto issue_s = [&](int j) -> bool {  // S = Q K_j^T
-        const int s = j % C::kStages, n = j / C::kStages;
+        const int s = j % C::kKStages, n = j / C::kKStages;
         if (!mbar_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
         if (j >= 1 && !mbar_wait(bar(C::kSEmpty), (j - 1) & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
@@ -170,10 +178,9 @@ __global__ void __launch_bounds__(192, 1)
         umma_commit(bar(C::kSFull));
         return true;
       };
-      auto issue_dp = [&](int j) -> bool {  // dP = dO V_j^T
-        const int s = j % C::kStages, n = j / C::kStages;
+      auto issue_dp = [&](int j) -> bool {  // dP = dO V_j^T (dP_{j-1} was read before dS_{j-1})
+        const int s = j % C::kVStages, n = j / C::kVStages;
         if (!mbar_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
-        if (j >= 1 && !mbar_wait(bar(C::kDPEmpty), (j - 1) & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sV = sV0 + s * C::kTileBytes;
 #pragma unroll
@@ -183,33 +190,31 @@ __global__ void __launch_bounds__(192, 1)
                   smem_desc_sw128(sV + off, 16, 1024), kIdSq, ks > 0);
         }
         umma_commit(bar(C::kDPFull));
+        umma_commit(bar(C::kVEmpty + s));
         return true;
       };
-      auto issue_dq = [&](int j) -> bool {  // dQ += dS K_j  (K_j as the MN-major B operand)
-        const int s = j % C::kStages;
+      auto issue_dq = [&](int j) -> bool {  // dQ += dS K_j  (dS from TMEM, K_j as MN-major B)
+        const int s = j % C::kKStages;
         if (!mbar_wait(bar(C::kDSFull), j & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sK = sK0 + s * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < kBlockN / 16; ++ks) {
-          const uint32_t aoff = (ks >> 2) * (kBlockM * 128) + (ks & 3) * 32;
-          umma_ss(tmem + C::kColDQ, smem_desc_sw128(sDS + aoff, 16, 1024),
+          umma_ts(tmem + C::kColDQ, tmem + C::kColDS + 8u * ks,
                   smem_desc_sw128(sK + ks * 16 * 128, C::kChunkBytes, 1024), kIdDq,
                   (j > 0 || ks > 0) ? 1u : 0u);
         }
-        umma_commit(bar(C::kDQDone));
-        umma_commit(bar(C::kKVEmpty + s));
+        umma_commit(bar(C::kKEmpty + s));
+        if (j == nkv - 1) umma_commit(bar(C::kDQDone));
         return true;
       };
       bool ok = mbar_wait(bar(C::kQDFull), 0, &abort_flag, a.err);
       if (ok) ok = issue_s(0);
       if (ok) ok = issue_dp(0);
       for (int j = 0; ok && j < nkv; ++j) {
-        if (j + 1 < nkv) {
-          ok = issue_s(j + 1);
-          if (ok) ok = issue_dp(j + 1);
-        }
+        if (j + 1 < nkv) ok = issue_s(j + 1);
         if (ok) ok = issue_dq(j);
+        if (ok && j + 1 < nkv) ok = issue_dp(j + 1);
       }
       umma_commit(bar(C::kDrain));
       drain_wait(bar(C::kDrain), 0, a.err);
@@ -231,13 +236,17 @@ __global__ void __launch_bounds__(192, 1)
       if (!(ok = warp_wait(bar(C::kSFull), j & 1, &abort_flag, a.err))) break;
       tc_fence_after();
       float p[kBlockN];
+      {
+        uint32_t rr[4][32];
 #pragma unroll
-      for (int c4 = 0; c4 < kBlockN / 32; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kColS + 32u * c4, rr);
-        tmem_wait_ld(rr);
+        for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tmem + lane_base + C::kColS + 32u * c4, rr[c4]);
+        tmem_wait_ld_all();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) p[32 * c4 + i] = __uint_as_float(rr[i]);
+        for (int c4 = 0; c4 < 4; ++c4) {
+          reg_fence(rr[c4]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) p[32 * c4 + i] = __uint_as_float(rr[c4][i]);
+        }
       }
       tc_fence_before();
       mbar_arrive(bar(C::kSEmpty));
@@ -250,46 +259,48 @@ __global__ void __launch_bounds__(192, 1)
         for (int c = 0; c < kBlockN; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
       }
 
+      // dP_j landing also means dQ_{j-1} has finished reading the TMEM dS buffer.
       if (!(ok = warp_wait(bar(C::kDPFull), j & 1, &abort_flag, a.err))) break;
       tc_fence_after();
-      uint32_t pk[kBlockN / 2];
 #pragma unroll
-      for (int c4 = 0; c4 < kBlockN / 32; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kColDP + 32u * c4, rr);
-        tmem_wait_ld(rr);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t rr[2][32];
+        tmem_ld32(tmem + lane_base + C::kColDP + 64u * h, rr[0]);
+        tmem_ld32(tmem + lane_base + C::kColDP + 64u * h + 32u, rr[1]);
+        tmem_wait_ld_all();
+        reg_fence(rr[0]);
+        reg_fence(rr[1]);
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = 32 * c4 + 2 * i;
-          const float d0 = p[c] * (__uint_as_float(rr[2 * i]) - dlt);
-          const float d1 = p[c + 1] * (__uint_as_float(rr[2 * i + 1]) - dlt);
-          pk[c >> 1] = pack_bf16x2(d0, d1);
+        for (int i = 0; i < 32; ++i) {
+          const int c = 64 * h + 2 * i;
+          const uint32_t d0 = rr[i >> 4][(2 * i) & 31], d1 = rr[i >> 4][(2 * i + 1) & 31];
+          pk[i] = pack_bf16x2(p[c] * (__uint_as_float(d0) - dlt),
+                              p[c + 1] * (__uint_as_float(d1) - dlt));
         }
+        tmem_st32(tmem + lane_base + C::kColDS + 32u * h, pk);
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::kDPEmpty));
-      // dS K_{j-1} must have consumed the dS buffer before it is overwritten.
-      if (j > 0 && !(ok = warp_wait(bar(C::kDQDone), (j - 1) & 1, &abort_flag, a.err))) break;
-      store_row_sw128_128(sDS, r, pk);
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kDSFull));
     }
-    if (ok && warp_wait(bar(C::kDQDone), (nkv - 1) & 1, &abort_flag, a.err)) {
+    if (ok && warp_wait(bar(C::kDQDone), 0, &abort_flag, a.err)) {
       tc_fence_after();
       __nv_bfloat16* dst_row = a.dq + grow * D;
+      uint32_t rr[D / 32][32];
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kColDQ + c0, rr);
-        tmem_wait_ld(rr);
+      for (int c4 = 0; c4 < D / 32; ++c4) tmem_ld32(tmem + lane_base + C::kColDQ + 32u * c4, rr[c4]);
+      tmem_wait_ld_all();
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        reg_fence(rr[c4]);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * a.scale,
-                              __uint_as_float(rr[2 * i + 1]) * a.scale);
+          pk[i] = pack_bf16x2(__uint_as_float(rr[c4][2 * i]) * a.scale,
+                              __uint_as_float(rr[c4][2 * i + 1]) * a.scale);
         if (in_range) {
-          uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c4);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);

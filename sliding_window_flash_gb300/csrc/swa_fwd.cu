@@ -10,14 +10,18 @@
 //
 // Warp roles (192 threads):
 //   warps 0-3  softmax: thread r owns query row q0 + r = TMEM lane r.  Reads S from TMEM, masks,
-//              keeps the running max m and sum l in registers, writes bf16 P to shared memory,
-//              rescales its O row in TMEM when its max grows by more than 2^8, and finally writes
-//              O / l and LSE.
-//   warp 4     TMA producer: Q once, then K_j / V_j through a ring of shared-memory stages.
-//   warp 5     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one of two TMEM S buffers,
-//              O += P_j V_j into the TMEM O accumulator.  S_{j+1} is issued before O += P_j V_j so
-//              the tensor core computes the next scores while the softmax warps work on this block.
-// TMEM columns: [0,128) S buffer 0, [128,256) S buffer 1, [256, 256+D) O.
+//              keeps the running max m and sum l in registers, writes bf16 P back to TMEM (packed
+//              pairs), rescales its O row in TMEM when its max grows by more than 2^8, and finally
+//              writes O / l and LSE.
+//   warp 4     TMA producer: Q once, then K_j and V_j through two independent shared-memory rings
+//              (K is released as soon as S_j is computed, V after P_j V_j).
+//   warp 5     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one of two TMEM S buffers
+//              (A and B from shared memory); O += P_j V_j with P_j read from TMEM (A operand) and V_j
+//              from shared memory.  S_{j+1} is issued before O += P_j V_j so the tensor core computes
+//              the next scores while the softmax warps work on this block.  tcgen05.mma operations of
+//              one thread run in issue order, which orders every TMEM reuse below.
+// TMEM columns: [0,128) S buffer 0, [128,256) S buffer 1, [256, 256+D) O, then two 64-column
+// P buffers (128 bf16 per row, two per column).
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 #include "swa_tmap.h"
@@ -34,28 +38,28 @@ struct FwdCfg {
   static constexpr int kTileBytes = kBlockM * D * 2;  // one 128 x D bf16 tile
   static constexpr int kChunkBytes = kBlockM * 128;   // 128 rows x 64 columns (128-byte rows)
   static constexpr int kChunks = D / 64;
-  static constexpr int kStages = (D == 128) ? 2 : 3;
-  static constexpr int kPBytes = kBlockM * kBlockN * 2;
+  static constexpr int kKStages = (D == 128) ? 3 : 4;
+  static constexpr int kVStages = (D == 128) ? 3 : 4;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   // barrier indices
   static constexpr int kQFull = 0;
   static constexpr int kKFull = 1;
-  static constexpr int kVFull = kKFull + kStages;
-  static constexpr int kKVEmpty = kVFull + kStages;
-  static constexpr int kSFull = kKVEmpty + kStages;  // 2
-  static constexpr int kSEmpty = kSFull + 2;         // 2
-  static constexpr int kPFull = kSEmpty + 2;
-  static constexpr int kODone = kPFull + 1;
-  static constexpr int kDrain = kODone + 1;
+  static constexpr int kKEmpty = kKFull + kKStages;
+  static constexpr int kVFull = kKEmpty + kKStages;
+  static constexpr int kVEmpty = kVFull + kVStages;
+  static constexpr int kSFull = kVEmpty + kVStages;  // 2
+  static constexpr int kPFull = kSFull + 2;          // 2
+  static constexpr int kPVDone = kPFull + 2;         // 2
+  static constexpr int kDrain = kPVDone + 2;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM slot + align
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;  // buffer b at kColS + 128 b
   static constexpr uint32_t kColO = 256;
+  static constexpr uint32_t kColP = 256 + D;  // buffer b at kColP + 64 b
   static constexpr int kThreads = 192;
 };
 
@@ -82,7 +86,6 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sQ = smem_u32(smem + C::kOffQ);
   const uint32_t sK0 = smem_u32(smem + C::kOffK);
   const uint32_t sV0 = smem_u32(smem + C::kOffV);
-  const uint32_t sP = smem_u32(smem + C::kOffP);
 
   // Heaviest query blocks first (the causal case gives later blocks more key blocks).
   const int qb = a.nqb - 1 - static_cast<int>(blockIdx.x) / a.BH;
@@ -98,17 +101,19 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(bar(C::kQFull), 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bar(C::kKFull + s), 1);
+      mbar_init(bar(C::kKEmpty + s), 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(bar(C::kVFull + s), 1);
-      mbar_init(bar(C::kKVEmpty + s), 1);
+      mbar_init(bar(C::kVEmpty + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::kSFull + b), 1);
-      mbar_init(bar(C::kSEmpty + b), 128);
+      mbar_init(bar(C::kPFull + b), 128);
+      mbar_init(bar(C::kPVDone + b), 1);
     }
-    mbar_init(bar(C::kPFull), 128);
-    mbar_init(bar(C::kODone), 1);
     mbar_init(bar(C::kDrain), 1);
     fence_barrier_init();
   }
@@ -130,30 +135,34 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive_expect_tx(bar(C::kQFull), C::kTileBytes);
       for (int h = 0; h < C::kChunks; ++h)
         tma_load_3d(sQ + h * C::kChunkBytes, &tm_q, bar(C::kQFull), 64 * h, q0, bh);
-      int last_fill[C::kStages];
-      for (int s = 0; s < C::kStages; ++s) last_fill[s] = -1;
+      int last_k[C::kKStages], last_v[C::kVStages];
+      for (int s = 0; s < C::kKStages; ++s) last_k[s] = -1;
+      for (int s = 0; s < C::kVStages; ++s) last_v[s] = -1;
       for (int j = 0; j < nkv; ++j) {
-        const int s = j % C::kStages, n = j / C::kStages;
-        if (j >= C::kStages && !mbar_wait(bar(C::kKVEmpty + s), (n - 1) & 1, &abort_flag, a.err))
-          break;
         const int k0 = (kb_lo + j) * kBlockN;
-        const uint32_t sK = sK0 + s * C::kTileBytes, sV = sV0 + s * C::kTileBytes;
-        mbar_arrive_expect_tx(bar(C::kKFull + s), C::kTileBytes);
+        const int sk = j % C::kKStages, nk = j / C::kKStages;
+        if (j >= C::kKStages && !mbar_wait(bar(C::kKEmpty + sk), (nk - 1) & 1, &abort_flag, a.err))
+          break;
+        const uint32_t sK = sK0 + sk * C::kTileBytes;
+        mbar_arrive_expect_tx(bar(C::kKFull + sk), C::kTileBytes);
         for (int h = 0; h < C::kChunks; ++h)
-          tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKFull + s), 64 * h, k0, bhk);
-        mbar_arrive_expect_tx(bar(C::kVFull + s), C::kTileBytes);
+          tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKFull + sk), 64 * h, k0, bhk);
+        last_k[sk] = j;
+        const int sv = j % C::kVStages, nv = j / C::kVStages;
+        if (j >= C::kVStages && !mbar_wait(bar(C::kVEmpty + sv), (nv - 1) & 1, &abort_flag, a.err))
+          break;
+        const uint32_t sV = sV0 + sv * C::kTileBytes;
+        mbar_arrive_expect_tx(bar(C::kVFull + sv), C::kTileBytes);
         for (int h = 0; h < C::kChunks; ++h)
-          tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kVFull + s), 64 * h, k0, bhk);
-        last_fill[s] = j;
+          tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kVFull + sv), 64 * h, k0, bhk);
+        last_v[sv] = j;
       }
       // Never leave a copy in flight: wait for the last fill of every stage.
       drain_wait(bar(C::kQFull), 0, a.err);
-      for (int s = 0; s < C::kStages; ++s) {
-        if (last_fill[s] >= 0) {
-          drain_wait(bar(C::kKFull + s), (last_fill[s] / C::kStages) & 1, a.err);
-          drain_wait(bar(C::kVFull + s), (last_fill[s] / C::kStages) & 1, a.err);
-        }
-      }
+      for (int s = 0; s < C::kKStages; ++s)
+        if (last_k[s] >= 0) drain_wait(bar(C::kKFull + s), (last_k[s] / C::kKStages) & 1, a.err);
+      for (int s = 0; s < C::kVStages; ++s)
+        if (last_v[s] >= 0) drain_wait(bar(C::kVFull + s), (last_v[s] / C::kVStages) & 1, a.err);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer
@@ -161,10 +170,10 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t kIdS = idesc_bf16(kBlockM, kBlockN, false, false);
       constexpr uint32_t kIdO = idesc_bf16(kBlockM, D, false, true);
       auto issue_s = [&](int j) -> bool {
-        const int s = j % C::kStages, n = j / C::kStages, sb = j & 1;
+        // S buffer (j & 1) was last read by the softmax warps for block j-2; P_FULL of j-2, which
+        // issue_pv(j-2) waited for, already implies that.
+        const int s = j % C::kKStages, n = j / C::kKStages, sb = j & 1;
         if (!mbar_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
-        if (j >= 2 && !mbar_wait(bar(C::kSEmpty + sb), ((j - 2) >> 1) & 1, &abort_flag, a.err))
-          return false;
         tc_fence_after();
         const uint32_t sK = sK0 + s * C::kTileBytes;
 #pragma unroll
@@ -174,23 +183,23 @@ __global__ void __launch_bounds__(192, 1)
                   smem_desc_sw128(sK + off, 16, 1024), kIdS, ks > 0);
         }
         umma_commit(bar(C::kSFull + sb));
+        umma_commit(bar(C::kKEmpty + s));
         return true;
       };
       auto issue_pv = [&](int j) -> bool {
-        const int s = j % C::kStages, n = j / C::kStages;
-        if (!mbar_wait(bar(C::kPFull), j & 1, &abort_flag, a.err)) return false;
+        const int s = j % C::kVStages, n = j / C::kVStages, pb = j & 1;
+        if (!mbar_wait(bar(C::kPFull + pb), (j >> 1) & 1, &abort_flag, a.err)) return false;
         if (!mbar_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sV = sV0 + s * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < kBlockN / 16; ++ks) {
-          const uint32_t aoff = (ks >> 2) * (kBlockM * 128) + (ks & 3) * 32;
-          umma_ss(tmem + C::kColO, smem_desc_sw128(sP + aoff, 16, 1024),
+          umma_ts(tmem + C::kColO, tmem + C::kColP + 64u * pb + 8u * ks,
                   smem_desc_sw128(sV + ks * 16 * 128, C::kChunkBytes, 1024), kIdO,
                   (j > 0 || ks > 0) ? 1u : 0u);
         }
-        umma_commit(bar(C::kODone));
-        umma_commit(bar(C::kKVEmpty + s));
+        umma_commit(bar(C::kPVDone + pb));
+        umma_commit(bar(C::kVEmpty + s));
         return true;
       };
       bool ok = mbar_wait(bar(C::kQFull), 0, &abort_flag, a.err);
@@ -218,16 +227,19 @@ __global__ void __launch_bounds__(192, 1)
       if (!(ok = warp_wait(bar(C::kSFull + sb), (j >> 1) & 1, &abort_flag, a.err))) break;
       tc_fence_after();
       float x[kBlockN];
+      {
+        uint32_t rr[4][32];
 #pragma unroll
-      for (int c4 = 0; c4 < kBlockN / 32; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kColS + 128u * sb + 32u * c4, rr);
-        tmem_wait_ld(rr);
+        for (int c4 = 0; c4 < 4; ++c4)
+          tmem_ld32(tmem + lane_base + C::kColS + 128u * sb + 32u * c4, rr[c4]);
+        tmem_wait_ld_all();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[32 * c4 + i] = __uint_as_float(rr[i]) * sl2;
+        for (int c4 = 0; c4 < 4; ++c4) {
+          reg_fence(rr[c4]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[32 * c4 + i] = __uint_as_float(rr[c4][i]) * sl2;
+        }
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::kSEmpty + sb));
 
       // Window mask: the cells of this block visible to row `row` are keys in [row-W+1, row].
       const bool interior = (k0 + kBlockN - 1 <= q0) && (q0 + kBlockM - 1 - k0 < a.W);
@@ -248,40 +260,44 @@ __global__ void __launch_bounds__(192, 1)
         m_ref = m_new;
       }
       const float m_use = (m_ref == SWA_NEG_INF) ? 0.f : m_ref;
-      uint32_t pk[kBlockN / 2];
+      uint32_t pk[2][32];
       float rs = 0.f;
 #pragma unroll
       for (int c = 0; c < kBlockN / 2; ++c) {
         const float p0 = ex2(x[2 * c] - m_use), p1 = ex2(x[2 * c + 1] - m_use);
         rs += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+        pk[c >> 5][c & 31] = pack_bf16x2(p0, p1);
       }
       l += rs;
 
-      // P_{j-1} V_{j-1} must be done before P is overwritten and before O is rescaled.
-      if (j > 0) {
-        if (!(ok = warp_wait(bar(C::kODone), (j - 1) & 1, &abort_flag, a.err))) break;
+      // P buffer (j & 1) was last read by P_{j-2} V_{j-2}.
+      if (j >= 2 && !(ok = warp_wait(bar(C::kPVDone + sb), ((j - 2) >> 1) & 1, &abort_flag, a.err)))
+        break;
+      // Rescaling O needs P_{j-1} V_{j-1} (and so every earlier one) to have landed.
+      if (j >= 1 && __any_sync(0xffffffffu, resc)) {
+        if (!(ok = warp_wait(bar(C::kPVDone + (sb ^ 1)), ((j - 1) >> 1) & 1, &abort_flag, a.err)))
+          break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t rr[32];
-            tmem_ld32(tmem + lane_base + C::kColO + c0, rr);
-            tmem_wait_ld(rr);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_base + C::kColO + c0, rr);
+          tmem_wait_ld(rr);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * factor);
-            tmem_st32(tmem + lane_base + C::kColO + c0, rr);
-          }
-          tmem_wait_st();
+          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * factor);
+          tmem_st32(tmem + lane_base + C::kColO + c0, rr);
         }
+      } else {
+        tc_fence_after();
       }
-      // P row -> shared memory, K-major with 128-byte swizzle (two 64-key chunks).
-      store_row_sw128_128(sP, r, pk);
-      fence_proxy_async_smem();
+      tmem_st32(tmem + lane_base + C::kColP + 64u * sb, pk[0]);
+      tmem_st32(tmem + lane_base + C::kColP + 64u * sb + 32u, pk[1]);
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(C::kPFull));
+      mbar_arrive(bar(C::kPFull + sb));
     }
-    if (ok && warp_wait(bar(C::kODone), (nkv - 1) & 1, &abort_flag, a.err)) {
+    const int last = nkv - 1;
+    if (ok && warp_wait(bar(C::kPVDone + (last & 1)), (last >> 1) & 1, &abort_flag, a.err)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const float m_use = (m_ref == SWA_NEG_INF) ? 0.f : m_ref;
@@ -289,18 +305,20 @@ __global__ void __launch_bounds__(192, 1)
       const size_t grow = static_cast<size_t>(bh) * a.N + row;
       if (in_range) a.lse[grow] = (m_use + log2f(l)) * kLn2;
       __nv_bfloat16* orow = a.o + grow * D;
+      uint32_t rr[D / 32][32];
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kColO + c0, rr);
-        tmem_wait_ld(rr);
+      for (int c4 = 0; c4 < D / 32; ++c4) tmem_ld32(tmem + lane_base + C::kColO + 32u * c4, rr[c4]);
+      tmem_wait_ld_all();
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        reg_fence(rr[c4]);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
-                              __uint_as_float(rr[2 * i + 1]) * inv_l);
+          pk[i] = pack_bf16x2(__uint_as_float(rr[c4][2 * i]) * inv_l,
+                              __uint_as_float(rr[c4][2 * i + 1]) * inv_l);
         if (in_range) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c4);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);

@@ -239,6 +239,18 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
   for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
 }
 
+// Waits for all of this thread's outstanding TMEM loads (use reg_fence on every loaded array
+// afterwards, so that no use of those registers is scheduled above the wait).
+__device__ __forceinline__ void tmem_wait_ld_all() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
