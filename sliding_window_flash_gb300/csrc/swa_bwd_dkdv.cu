@@ -11,11 +11,12 @@
 // disclosure": tiles wholly outside the window are skipped, edge tiles are masked, and dK / dV of
 // a key tile that no query visits are still written (as zeros).
 //
-// Warp roles (192 threads): warps 0-3 compute (thread r = key row k0 + r = TMEM lane r),
-// warp 4 TMA producer (K and V once; Q_t and dO_t through two shared-memory rings), warp 5 MMA
-// issuer and TMEM owner.  P^T and dS^T go back to TMEM (bf16 pairs, over the columns of S^T and
-// dP^T they came from) and are the A operands of dV += P^T dO and dK += dS^T Q.  TMEM columns:
-// [0,128) S^T / P^T, [128,256) dP^T / dS^T, [256, 256+D) dK, [256+D, 256+2D) dV.
+// Warp roles (320 threads): warps 0-7 compute — warp w handles TMEM lanes 32(w%4)..+31 (key rows)
+// and query columns [64 h, 64 h + 64) of every tile, h = w / 4; warp 8 TMA producer (K and V once;
+// Q_t and dO_t through two shared-memory rings); warp 9 MMA issuer and TMEM owner.  P^T and dS^T go
+// back to TMEM as bf16 pairs, each half over the first 32 of the 64 S^T / dP^T columns it read, and
+// are the A operands of dV += P^T dO and dK += dS^T Q.  TMEM columns: [0,128) S^T / P^T,
+// [128,256) dP^T / dS^T, [256, 256+D) dK, [256+D, 256+2D) dV.
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 #include "swa_tmap.h"
@@ -34,8 +35,9 @@ struct DkdvCfg {
   static constexpr int kOffV = kOffK + kTileBytes;
   static constexpr int kOffQ = kOffV + kTileBytes;
   static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
-  static constexpr int kOffRow = kOffDO + kDOStages * kTileBytes;  // lse2[128], delta[128]
-  static constexpr int kOffBar = kOffRow + 2 * kBlockM * 4;
+  // two slots of the per-query vectors {lse2[128], delta[128]}
+  static constexpr int kOffRow = kOffDO + kDOStages * kTileBytes;
+  static constexpr int kOffBar = kOffRow + 2 * 2 * kBlockM * 4;
   static constexpr int kKVFull = 0;
   static constexpr int kQFull = 1;
   static constexpr int kQEmpty = kQFull + kQStages;
@@ -45,14 +47,16 @@ struct DkdvCfg {
   static constexpr int kDPFull = kSFull + 1;
   static constexpr int kPFull = kDPFull + 1;
   static constexpr int kDSFull = kPFull + 1;
-  static constexpr int kDone = kDSFull + 1;
+  static constexpr int kVecFull = kDSFull + 1;  // 2 slots
+  static constexpr int kDone = kVecFull + 2;
   static constexpr int kDrain = kDone + 1;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
   // P^T is written over the first 64 columns of S^T, dS^T over the first 64 of dP^T.
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 256 + D;
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 320;
+  static constexpr int kComputeThreads = 256;
 };
 
 struct DkdvArgs {
@@ -66,7 +70,7 @@ struct DkdvArgs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     swa_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -76,8 +80,7 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
-  float* s_lse2 = reinterpret_cast<float*>(smem + C::kOffRow);
-  float* s_delta = s_lse2 + kBlockM;
+  float* s_rows = reinterpret_cast<float*>(smem + C::kOffRow);  // [slot][lse2 | delta][128]
   __shared__ int abort_flag;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t sK = smem_u32(smem + C::kOffK);
@@ -111,13 +114,15 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(bar(C::kSFull), 1);
     mbar_init(bar(C::kDPFull), 1);
-    mbar_init(bar(C::kPFull), 128);
-    mbar_init(bar(C::kDSFull), 128);
+    mbar_init(bar(C::kPFull), C::kComputeThreads);
+    mbar_init(bar(C::kDSFull), C::kComputeThreads);
+    mbar_init(bar(C::kVecFull + 0), C::kComputeThreads / 32);
+    mbar_init(bar(C::kVecFull + 1), C::kComputeThreads / 32);
     mbar_init(bar(C::kDone), 1);
     mbar_init(bar(C::kDrain), 1);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -126,7 +131,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -168,140 +173,146 @@ __global__ void __launch_bounds__(192, 1)
         if (last_do[s] >= 0)
           drain_wait(bar(C::kDOFull + s), (last_do[s] / C::kDOStages) & 1, a.err);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
     // Issue order: S_0, dP_0, then per tile t: dV += P_t^T dO_t, S_{t+1}, dK += dS_t^T Q_t, dP_{t+1}.
     // The MMAs run in that order, so S_{t+1} overwrites the S^T / P^T columns only after dV_t has
     // read P_t^T, and dP_{t+1} overwrites dP^T / dS^T only after dK_t has read dS_t^T.
-    if (lane == 0) {
+    {  // the whole warp, converged; one elected lane issues
       constexpr uint32_t kIdS = idesc_bf16(kBlockN, kBlockM, false, false);  // S^T, dP^T
       constexpr uint32_t kIdAcc = idesc_bf16(kBlockN, D, false, true);       // dV, dK
       auto issue_s = [&](int t) -> bool {  // S^T = K Q_t^T
         const int s = t % C::kQStages;
-        if (!mbar_wait(bar(C::kQFull + s), (t / C::kQStages) & 1, &abort_flag, a.err)) return false;
+        if (!warp_wait(bar(C::kQFull + s), (t / C::kQStages) & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sQ = sQ0 + s * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          umma_ss(tmem + C::kColS, smem_desc_sw128(sK + off, 16, 1024),
+          umma_ss_w(tmem + C::kColS, smem_desc_sw128(sK + off, 16, 1024),
                   smem_desc_sw128(sQ + off, 16, 1024), kIdS, ks > 0);
         }
-        umma_commit(bar(C::kSFull));
+        umma_commit_w(bar(C::kSFull));
         return true;
       };
       auto issue_dp = [&](int t) -> bool {  // dP^T = V dO_t^T
         const int s = t % C::kDOStages;
-        if (!mbar_wait(bar(C::kDOFull + s), (t / C::kDOStages) & 1, &abort_flag, a.err))
+        if (!warp_wait(bar(C::kDOFull + s), (t / C::kDOStages) & 1, &abort_flag, a.err))
           return false;
         tc_fence_after();
         const uint32_t sDO = sDO0 + s * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          umma_ss(tmem + C::kColDP, smem_desc_sw128(sV + off, 16, 1024),
+          umma_ss_w(tmem + C::kColDP, smem_desc_sw128(sV + off, 16, 1024),
                   smem_desc_sw128(sDO + off, 16, 1024), kIdS, ks > 0);
         }
-        umma_commit(bar(C::kDPFull));
+        umma_commit_w(bar(C::kDPFull));
         return true;
       };
       // acc += X^T B_t with X^T (bf16 pairs) in TMEM at column a_col and B_t = dO_t or Q_t (MN-major)
       auto issue_acc = [&](int t, int wait_bar, uint32_t a_col, uint32_t b_tile,
                            uint32_t d_col) -> bool {
-        if (!mbar_wait(bar(wait_bar), t & 1, &abort_flag, a.err)) return false;
+        if (!warp_wait(bar(wait_bar), t & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kBlockM / 16; ++ks) {
-          umma_ts(tmem + d_col, tmem + a_col + 8u * ks,
+          // query columns 16 ks .. 16 ks + 15 sit at packed column 8 ks + 32 (ks / 4)
+          umma_ts_w(tmem + d_col, tmem + a_col + 8u * ks + 32u * (ks >> 2),
                   smem_desc_sw128(b_tile + ks * 16 * 128, C::kChunkBytes, 1024), kIdAcc,
                   (t > 0 || ks > 0) ? 1u : 0u);
         }
         return true;
       };
-      bool ok = mbar_wait(bar(C::kKVFull), 0, &abort_flag, a.err);
+      bool ok = warp_wait(bar(C::kKVFull), 0, &abort_flag, a.err);
       if (ok) ok = issue_s(0);
       if (ok) ok = issue_dp(0);
       for (int t = 0; ok && t < T; ++t) {
         const int sq = t % C::kQStages, sd = t % C::kDOStages;
         ok = issue_acc(t, C::kPFull, C::kColS, sDO0 + sd * C::kTileBytes, C::kColDV);  // dV
         if (!ok) break;
-        umma_commit(bar(C::kDOEmpty + sd));
+        umma_commit_w(bar(C::kDOEmpty + sd));
         if (t + 1 < T && !(ok = issue_s(t + 1))) break;
         ok = issue_acc(t, C::kDSFull, C::kColDP, sQ0 + sq * C::kTileBytes, C::kColDK);  // dK
         if (!ok) break;
-        umma_commit(bar(C::kQEmpty + sq));
+        umma_commit_w(bar(C::kQEmpty + sq));
         if (t + 1 < T) ok = issue_dp(t + 1);
       }
-      if (ok) umma_commit(bar(C::kDone));
-      umma_commit(bar(C::kDrain));
-      drain_wait(bar(C::kDrain), 0, a.err);
+      if (ok) umma_commit_w(bar(C::kDone));
+      umma_commit_w(bar(C::kDrain));
+      warp_drain_wait(bar(C::kDrain), 0, a.err);
     }
   } else {
-    // ------------------------------------------------------------------ compute (warps 0-3)
-    const int r = static_cast<int>(threadIdx.x);
+    // ------------------------------------------------------------------ compute (warps 0-7)
+    const int r = static_cast<int>(threadIdx.x & 127);  // key row within the block = TMEM lane
+    const uint32_t h = warp >> 2;                          // query-column half of every tile
     const int key = k0 + r;
-    const uint32_t lane_base = (warp * 32u) << 16;
+    const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
     const float sl2 = a.scale_log2;
-    // This thread's share of the per-query vectors of the next tile (query q0 + r).
-    float nxt_lse2 = 0.f, nxt_delta = 0.f;
+    // Per-query vectors of the next tile: the h = 0 threads fetch LSE, the h = 1 threads Delta,
+    // for query q0 + r.  The raw value is kept until it is stored, so the load's latency hides
+    // behind a whole tile.
+    float nxt = 0.f;
     auto fetch_row = [&](int t) {
       const int q = tile_q0(t) + r;
       if (q < a.N) {
         const size_t gi = static_cast<size_t>(tile_bhq(t)) * a.N + q;
-        nxt_lse2 = a.lse[gi] * kLog2e;
-        nxt_delta = a.delta[gi];
+        nxt = h == 0 ? a.lse[gi] : a.delta[gi];
       } else {  // queries past the end contribute P = 0
-        nxt_lse2 = SWA_POS_INF;
-        nxt_delta = 0.f;
+        nxt = h == 0 ? SWA_POS_INF : 0.f;
       }
     };
     fetch_row(0);
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int q0 = tile_q0(t);
-      named_barrier_sync(1, 128);  // every thread is done with the previous tile's vectors
-      s_lse2[r] = nxt_lse2;
-      s_delta[r] = nxt_delta;
-      named_barrier_sync(1, 128);
+      // Slot t & 1 was last read in tile t - 2; every compute thread has finished that tile
+      // (dK_{t-2}, which needed all of them, precedes dP_{t-1}, which this thread has seen).
+      float* s_lse2 = s_rows + (t & 1) * 2 * kBlockM;
+      float* s_delta = s_lse2 + kBlockM;
+      if (h == 0)
+        s_lse2[r] = nxt * kLog2e;
+      else
+        s_delta[r] = nxt;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kVecFull + (t & 1)));
+      if (!(ok = warp_wait(bar(C::kVecFull + (t & 1)), (t >> 1) & 1, &abort_flag, a.err))) break;
       if (t + 1 < T) fetch_row(t + 1);
 
       if (!(ok = warp_wait(bar(C::kSFull), t & 1, &abort_flag, a.err))) break;
       tc_fence_after();
-      float p[kBlockM];
+      float p[64];
       {
-        uint32_t rr[4][32];
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tmem + lane_base + C::kColS + 32u * c4, rr[c4]);
+        uint32_t rr[2][32];
+        tmem_ld32(tmem + lane_base + C::kColS + 64u * h, rr[0]);
+        tmem_ld32(tmem + lane_base + C::kColS + 64u * h + 32u, rr[1]);
         tmem_wait_ld_all();
+        reg_fence(rr[0]);
+        reg_fence(rr[1]);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          reg_fence(rr[c4]);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) p[32 * c4 + i] = __uint_as_float(rr[c4][i]);
-        }
+        for (int i = 0; i < 64; ++i) p[i] = __uint_as_float(rr[i >> 5][i & 31]);
       }
-      const float4* l4 = reinterpret_cast<const float4*>(s_lse2);
+      const float4* l4 = reinterpret_cast<const float4*>(s_lse2 + 64 * h);
 #pragma unroll
-      for (int c4 = 0; c4 < kBlockM / 4; ++c4) {
+      for (int c4 = 0; c4 < 16; ++c4) {
         const float4 l = l4[c4];
         p[4 * c4 + 0] = ex2(fmaf(p[4 * c4 + 0], sl2, -l.x));
         p[4 * c4 + 1] = ex2(fmaf(p[4 * c4 + 1], sl2, -l.y));
         p[4 * c4 + 2] = ex2(fmaf(p[4 * c4 + 2], sl2, -l.z));
         p[4 * c4 + 3] = ex2(fmaf(p[4 * c4 + 3], sl2, -l.w));
       }
-      // Query q0 + c sees this key iff 0 <= q0 + c - key < W.
+      // Query q0 + 64h + c sees this key iff 0 <= q0 + 64h + c - key < W.
       const bool interior = (q0 >= k0 + kBlockN - 1) && (q0 + kBlockM - 1 - k0 < a.W);
       if (!interior) {
-        const int lo = key - q0, hi = key - q0 + a.W - 1;
+        const int lo = key - q0 - 64 * static_cast<int>(h), hi = lo + a.W - 1;
 #pragma unroll
-        for (int c = 0; c < kBlockM; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
+        for (int c = 0; c < 64; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
       }
       {
-        uint32_t pk[2][32];
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < kBlockM / 2; ++c) pk[c >> 5][c & 31] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
-        tmem_st32(tmem + lane_base + C::kColS, pk[0]);
-        tmem_st32(tmem + lane_base + C::kColS + 32u, pk[1]);
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+        tmem_st32(tmem + lane_base + C::kColS + 64u * h, pk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -309,9 +320,8 @@ __global__ void __launch_bounds__(192, 1)
 
       if (!(ok = warp_wait(bar(C::kDPFull), t & 1, &abort_flag, a.err))) break;
       tc_fence_after();
-      const float4* d4 = reinterpret_cast<const float4*>(s_delta);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      {
+        const float4* d4 = reinterpret_cast<const float4*>(s_delta + 64 * h);
         uint32_t rr[2][32];
         tmem_ld32(tmem + lane_base + C::kColDP + 64u * h, rr[0]);
         tmem_ld32(tmem + lane_base + C::kColDP + 64u * h + 32u, rr[1]);
@@ -321,15 +331,15 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int c = 64 * h + 4 * i;
-          const float4 dl = d4[c >> 2];
+          const int c = 4 * i;
+          const float4 dl = d4[i];
           const uint32_t* src = &rr[i >> 3][(4 * i) & 31];
           pk[2 * i] = pack_bf16x2(p[c] * (__uint_as_float(src[0]) - dl.x),
                                   p[c + 1] * (__uint_as_float(src[1]) - dl.y));
           pk[2 * i + 1] = pack_bf16x2(p[c + 2] * (__uint_as_float(src[2]) - dl.z),
                                       p[c + 3] * (__uint_as_float(src[3]) - dl.w));
         }
-        tmem_st32(tmem + lane_base + C::kColDP + 32u * h, pk);
+        tmem_st32(tmem + lane_base + C::kColDP + 64u * h, pk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -337,19 +347,20 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (ok && warp_wait(bar(C::kDone), 0, &abort_flag, a.err)) {
       tc_fence_after();
+      constexpr int kHalf = D / 2;
       const bool in_range = key < a.N;
       const size_t grow = static_cast<size_t>(bhk) * a.N + key;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? C::kColDK : C::kColDV;
+        const uint32_t col = (which == 0 ? C::kColDK : C::kColDV) + kHalf * h;
         const float mul = which == 0 ? a.scale : 1.f;
-        __nv_bfloat16* dst_row = (which == 0 ? a.dk : a.dv) + grow * D;
-        uint32_t rr[D / 32][32];
+        __nv_bfloat16* dst_row = (which == 0 ? a.dk : a.dv) + grow * D + kHalf * h;
+        uint32_t rr[kHalf / 32][32];
 #pragma unroll
-        for (int c4 = 0; c4 < D / 32; ++c4) tmem_ld32(tmem + lane_base + col + 32u * c4, rr[c4]);
+        for (int c4 = 0; c4 < kHalf / 32; ++c4) tmem_ld32(tmem + lane_base + col + 32u * c4, rr[c4]);
         tmem_wait_ld_all();
 #pragma unroll
-        for (int c4 = 0; c4 < D / 32; ++c4) {
+        for (int c4 = 0; c4 < kHalf / 32; ++c4) {
           reg_fence(rr[c4]);
           uint32_t o16[16];
 #pragma unroll
@@ -369,7 +380,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

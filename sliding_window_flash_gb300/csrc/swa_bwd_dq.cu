@@ -10,9 +10,10 @@
 // at the store; S and dP stay fp32 in TMEM and only dS is rounded to bf16 as an MMA operand (the
 // lab's fp32-score-tile experiment showed the error of bf16 score scratch).
 //
-// Warp roles (192 threads): warps 0-3 compute (thread r = query row q0 + r = TMEM lane r),
-// warp 4 TMA producer (Q and dO once, K_j and V_j through two shared-memory rings), warp 5 MMA
-// issuer and TMEM owner.  dS goes back to TMEM and is the A operand of dQ += dS K_j.
+// Warp roles (320 threads): warps 0-7 compute — warp w handles TMEM lanes 32(w%4)..+31 (query
+// rows) and columns [64 h, 64 h + 64) of every 128-column tile, h = w / 4, so each score row is
+// split over two threads; warp 8 TMA producer (Q and dO once, K_j and V_j through two
+// shared-memory rings); warp 9 MMA issuer and TMEM owner.  dS goes back to TMEM and is the A operand of dQ += dS K_j.
 // TMEM columns: [0,128) S, [128,256) dP, [256, 256+D) dQ, [256+D, 320+D) dS (bf16 pairs).
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
@@ -48,7 +49,8 @@ struct DqCfg {
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 320;
+  static constexpr int kComputeThreads = 256;
 };
 
 struct DqArgs {
@@ -61,7 +63,7 @@ struct DqArgs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     swa_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DqArgs a) {
@@ -99,14 +101,14 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(bar(C::kVEmpty + s), 1);
     }
     mbar_init(bar(C::kSFull), 1);
-    mbar_init(bar(C::kSEmpty), 128);
+    mbar_init(bar(C::kSEmpty), C::kComputeThreads);
     mbar_init(bar(C::kDPFull), 1);
-    mbar_init(bar(C::kDSFull), 128);
+    mbar_init(bar(C::kDSFull), C::kComputeThreads);
     mbar_init(bar(C::kDQDone), 1);
     mbar_init(bar(C::kDrain), 1);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -155,60 +157,60 @@ __global__ void __launch_bounds__(192, 1)
       for (int s = 0; s < C::kVStages; ++s)
         if (last_v[s] >= 0) drain_wait(bar(C::kVFull + s), (last_v[s] / C::kVStages) & 1, a.err);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
     // Issue order S_0, dP_0, then per block j: S_{j+1}, dQ += dS_j K_j, dP_{j+1}.  The MMAs run in
     // that order, so dP_{j+1} lands only after dQ_j has read dS_j: when the compute warps see
     // dP_{j+1} they may overwrite the single TMEM dS buffer.
-    if (lane == 0) {
+    {  // the whole warp, converged; one elected lane issues
       constexpr uint32_t kIdSq = idesc_bf16(kBlockM, kBlockN, false, false);  // S, dP
       constexpr uint32_t kIdDq = idesc_bf16(kBlockM, D, false, true);         // dQ += dS K
       auto issue_s = [&](int j) -> bool {  // S = Q K_j^T
         const int s = j % C::kKStages, n = j / C::kKStages;
-        if (!mbar_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
-        if (j >= 1 && !mbar_wait(bar(C::kSEmpty), (j - 1) & 1, &abort_flag, a.err)) return false;
+        if (!warp_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
+        if (j >= 1 && !warp_wait(bar(C::kSEmpty), (j - 1) & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sK = sK0 + s * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          umma_ss(tmem + C::kColS, smem_desc_sw128(sQ + off, 16, 1024),
+          umma_ss_w(tmem + C::kColS, smem_desc_sw128(sQ + off, 16, 1024),
                   smem_desc_sw128(sK + off, 16, 1024), kIdSq, ks > 0);
         }
-        umma_commit(bar(C::kSFull));
+        umma_commit_w(bar(C::kSFull));
         return true;
       };
       auto issue_dp = [&](int j) -> bool {  // dP = dO V_j^T (dP_{j-1} was read before dS_{j-1})
         const int s = j % C::kVStages, n = j / C::kVStages;
-        if (!mbar_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
+        if (!warp_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sV = sV0 + s * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          umma_ss(tmem + C::kColDP, smem_desc_sw128(sDO + off, 16, 1024),
+          umma_ss_w(tmem + C::kColDP, smem_desc_sw128(sDO + off, 16, 1024),
                   smem_desc_sw128(sV + off, 16, 1024), kIdSq, ks > 0);
         }
-        umma_commit(bar(C::kDPFull));
-        umma_commit(bar(C::kVEmpty + s));
+        umma_commit_w(bar(C::kDPFull));
+        umma_commit_w(bar(C::kVEmpty + s));
         return true;
       };
       auto issue_dq = [&](int j) -> bool {  // dQ += dS K_j  (dS from TMEM, K_j as MN-major B)
         const int s = j % C::kKStages;
-        if (!mbar_wait(bar(C::kDSFull), j & 1, &abort_flag, a.err)) return false;
+        if (!warp_wait(bar(C::kDSFull), j & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sK = sK0 + s * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < kBlockN / 16; ++ks) {
-          umma_ts(tmem + C::kColDQ, tmem + C::kColDS + 8u * ks,
+          umma_ts_w(tmem + C::kColDQ, tmem + C::kColDS + 8u * ks,
                   smem_desc_sw128(sK + ks * 16 * 128, C::kChunkBytes, 1024), kIdDq,
                   (j > 0 || ks > 0) ? 1u : 0u);
         }
-        umma_commit(bar(C::kKEmpty + s));
-        if (j == nkv - 1) umma_commit(bar(C::kDQDone));
+        umma_commit_w(bar(C::kKEmpty + s));
+        if (j == nkv - 1) umma_commit_w(bar(C::kDQDone));
         return true;
       };
-      bool ok = mbar_wait(bar(C::kQDFull), 0, &abort_flag, a.err);
+      bool ok = warp_wait(bar(C::kQDFull), 0, &abort_flag, a.err);
       if (ok) ok = issue_s(0);
       if (ok) ok = issue_dp(0);
       for (int j = 0; ok && j < nkv; ++j) {
@@ -216,16 +218,17 @@ __global__ void __launch_bounds__(192, 1)
         if (ok) ok = issue_dq(j);
         if (ok && j + 1 < nkv) ok = issue_dp(j + 1);
       }
-      umma_commit(bar(C::kDrain));
-      drain_wait(bar(C::kDrain), 0, a.err);
+      umma_commit_w(bar(C::kDrain));
+      warp_drain_wait(bar(C::kDrain), 0, a.err);
     }
   } else {
-    // ------------------------------------------------------------------ compute (warps 0-3)
-    const int r = static_cast<int>(threadIdx.x);
+    // ------------------------------------------------------------------ compute (warps 0-7)
+    const int r = static_cast<int>(threadIdx.x & 127);  // query row within the tile = TMEM lane
+    const uint32_t h = warp >> 2;                          // column half of every tile
     const int row = q0 + r;
     const bool in_range = row < a.N;
     const size_t grow = static_cast<size_t>(bh) * a.N + row;
-    const uint32_t lane_base = (warp * 32u) << 16;
+    const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
     // Rows past the end see P = 0 (their LSE is taken as +inf), so they add nothing.
     const float lse2 = in_range ? a.lse[grow] * kLog2e : SWA_POS_INF;
     const float dlt = in_range ? a.delta[grow] : 0.f;
@@ -235,35 +238,33 @@ __global__ void __launch_bounds__(192, 1)
       const int k0 = (kb_lo + j) * kBlockN;
       if (!(ok = warp_wait(bar(C::kSFull), j & 1, &abort_flag, a.err))) break;
       tc_fence_after();
-      float p[kBlockN];
+      float p[64];
       {
-        uint32_t rr[4][32];
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tmem + lane_base + C::kColS + 32u * c4, rr[c4]);
+        uint32_t rr[2][32];
+        tmem_ld32(tmem + lane_base + C::kColS + 64u * h, rr[0]);
+        tmem_ld32(tmem + lane_base + C::kColS + 64u * h + 32u, rr[1]);
         tmem_wait_ld_all();
+        reg_fence(rr[0]);
+        reg_fence(rr[1]);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          reg_fence(rr[c4]);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) p[32 * c4 + i] = __uint_as_float(rr[c4][i]);
-        }
+        for (int i = 0; i < 64; ++i) p[i] = __uint_as_float(rr[i >> 5][i & 31]);
       }
       tc_fence_before();
       mbar_arrive(bar(C::kSEmpty));
 #pragma unroll
-      for (int c = 0; c < kBlockN; ++c) p[c] = ex2(fmaf(p[c], sl2, -lse2));
+      for (int c = 0; c < 64; ++c) p[c] = ex2(fmaf(p[c], sl2, -lse2));
       const bool interior = (k0 + kBlockN - 1 <= q0) && (q0 + kBlockM - 1 - k0 < a.W);
       if (!interior) {
-        const int lo = row - a.W + 1 - k0, hi = row - k0;
+        const int lo = row - a.W + 1 - k0 - 64 * static_cast<int>(h);
+        const int hi = row - k0 - 64 * static_cast<int>(h);
 #pragma unroll
-        for (int c = 0; c < kBlockN; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
+        for (int c = 0; c < 64; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
       }
 
       // dP_j landing also means dQ_{j-1} has finished reading the TMEM dS buffer.
       if (!(ok = warp_wait(bar(C::kDPFull), j & 1, &abort_flag, a.err))) break;
       tc_fence_after();
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      {
         uint32_t rr[2][32];
         tmem_ld32(tmem + lane_base + C::kColDP + 64u * h, rr[0]);
         tmem_ld32(tmem + lane_base + C::kColDP + 64u * h + 32u, rr[1]);
@@ -273,11 +274,11 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int c = 64 * h + 2 * i;
           const uint32_t d0 = rr[i >> 4][(2 * i) & 31], d1 = rr[i >> 4][(2 * i + 1) & 31];
-          pk[i] = pack_bf16x2(p[c] * (__uint_as_float(d0) - dlt),
-                              p[c + 1] * (__uint_as_float(d1) - dlt));
+          pk[i] = pack_bf16x2(p[2 * i] * (__uint_as_float(d0) - dlt),
+                              p[2 * i + 1] * (__uint_as_float(d1) - dlt));
         }
+        // dS columns [64h, 64h+64) -> packed TMEM columns [32h, 32h+32) of the dS buffer.
         tmem_st32(tmem + lane_base + C::kColDS + 32u * h, pk);
       }
       tmem_wait_st();
@@ -286,13 +287,15 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (ok && warp_wait(bar(C::kDQDone), 0, &abort_flag, a.err)) {
       tc_fence_after();
-      __nv_bfloat16* dst_row = a.dq + grow * D;
-      uint32_t rr[D / 32][32];
+      constexpr int kHalf = D / 2;
+      __nv_bfloat16* dst_row = a.dq + grow * D + kHalf * h;
+      uint32_t rr[kHalf / 32][32];
 #pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) tmem_ld32(tmem + lane_base + C::kColDQ + 32u * c4, rr[c4]);
+      for (int c4 = 0; c4 < kHalf / 32; ++c4)
+        tmem_ld32(tmem + lane_base + C::kColDQ + kHalf * h + 32u * c4, rr[c4]);
       tmem_wait_ld_all();
 #pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
+      for (int c4 = 0; c4 < kHalf / 32; ++c4) {
         reg_fence(rr[c4]);
         uint32_t pk[16];
 #pragma unroll
@@ -311,7 +314,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

@@ -8,14 +8,16 @@
 // Only O and LSE are written (mlx-train-perf README, flash-attention section: the saved state is
 // the output and the log-sum-exp).
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread r owns query row q0 + r = TMEM lane r.  Reads S from TMEM, masks,
-//              keeps the running max m and sum l in registers, writes bf16 P back to TMEM (packed
-//              pairs), rescales its O row in TMEM when its max grows by more than 2^8, and finally
-//              writes O / l and LSE.
-//   warp 4     TMA producer: Q once, then K_j and V_j through two independent shared-memory rings
+// Warp roles (320 threads):
+//   warps 0-7  softmax: warp w owns TMEM lanes 32(w%4)..+31 (query rows) and columns
+//              [64 h, 64 h + 64) of every score tile, h = w / 4, so each row is split over two
+//              threads that swap their partial row max through shared memory every block.  Each
+//              masks its half, keeps the running max m and its partial sum l in registers, writes
+//              bf16 P back to TMEM (packed pairs), rescales its half of the O row in TMEM when the
+//              max grows by more than 2^8, and finally writes its half of O / l (and LSE).
+//   warp 8     TMA producer: Q once, then K_j and V_j through two independent shared-memory rings
 //              (K is released as soon as S_j is computed, V after P_j V_j).
-//   warp 5     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one of two TMEM S buffers
+//   warp 9     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one of two TMEM S buffers
 //              (A and B from shared memory); O += P_j V_j with P_j read from TMEM (A operand) and V_j
 //              from shared memory.  S_{j+1} is issued before O += P_j V_j so the tensor core computes
 //              the next scores while the softmax warps work on this block.  tcgen05.mma operations of
@@ -39,11 +41,12 @@ struct FwdCfg {
   static constexpr int kChunkBytes = kBlockM * 128;   // 128 rows x 64 columns (128-byte rows)
   static constexpr int kChunks = D / 64;
   static constexpr int kKStages = (D == 128) ? 3 : 4;
-  static constexpr int kVStages = (D == 128) ? 3 : 4;
+  static constexpr int kVStages = (D == 128) ? 2 : 4;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+  static constexpr int kOffRed = kOffV + kVStages * kTileBytes;  // [2 slots][2 halves][128] fp32
+  static constexpr int kOffBar = kOffRed + 2 * 2 * kBlockM * 4;
   // barrier indices
   static constexpr int kQFull = 0;
   static constexpr int kKFull = 1;
@@ -53,14 +56,16 @@ struct FwdCfg {
   static constexpr int kSFull = kVEmpty + kVStages;  // 2
   static constexpr int kPFull = kSFull + 2;          // 2
   static constexpr int kPVDone = kPFull + 2;         // 2
-  static constexpr int kDrain = kPVDone + 2;
+  static constexpr int kXch = kPVDone + 2;           // [4 lane quarters][2 slots]
+  static constexpr int kDrain = kXch + 8;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM slot + align
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;  // buffer b at kColS + 128 b
   static constexpr uint32_t kColO = 256;
   static constexpr uint32_t kColP = 256 + D;  // buffer b at kColP + 64 b
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 320;
+  static constexpr int kComputeThreads = 256;
 };
 
 struct FwdArgs {
@@ -73,7 +78,7 @@ struct FwdArgs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     swa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
   using C = FwdCfg<D>;
@@ -86,6 +91,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sQ = smem_u32(smem + C::kOffQ);
   const uint32_t sK0 = smem_u32(smem + C::kOffK);
   const uint32_t sV0 = smem_u32(smem + C::kOffV);
+  float* s_red = reinterpret_cast<float*>(smem + C::kOffRed);
 
   // Heaviest query blocks first (the causal case gives later blocks more key blocks).
   const int qb = a.nqb - 1 - static_cast<int>(blockIdx.x) / a.BH;
@@ -111,13 +117,14 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::kSFull + b), 1);
-      mbar_init(bar(C::kPFull + b), 128);
+      mbar_init(bar(C::kPFull + b), C::kComputeThreads);
       mbar_init(bar(C::kPVDone + b), 1);
     }
+    for (int x = 0; x < 8; ++x) mbar_init(bar(C::kXch + x), 2);  // the two warps of a lane quarter
     mbar_init(bar(C::kDrain), 1);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -126,7 +133,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -164,93 +171,109 @@ __global__ void __launch_bounds__(192, 1)
       for (int s = 0; s < C::kVStages; ++s)
         if (last_v[s] >= 0) drain_wait(bar(C::kVFull + s), (last_v[s] / C::kVStages) & 1, a.err);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {  // the whole warp, converged; one elected lane issues
       constexpr uint32_t kIdS = idesc_bf16(kBlockM, kBlockN, false, false);
       constexpr uint32_t kIdO = idesc_bf16(kBlockM, D, false, true);
       auto issue_s = [&](int j) -> bool {
         // S buffer (j & 1) was last read by the softmax warps for block j-2; P_FULL of j-2, which
         // issue_pv(j-2) waited for, already implies that.
         const int s = j % C::kKStages, n = j / C::kKStages, sb = j & 1;
-        if (!mbar_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
+        if (!warp_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sK = sK0 + s * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          umma_ss(tmem + C::kColS + 128u * sb, smem_desc_sw128(sQ + off, 16, 1024),
+          umma_ss_w(tmem + C::kColS + 128u * sb, smem_desc_sw128(sQ + off, 16, 1024),
                   smem_desc_sw128(sK + off, 16, 1024), kIdS, ks > 0);
         }
-        umma_commit(bar(C::kSFull + sb));
-        umma_commit(bar(C::kKEmpty + s));
+        umma_commit_w(bar(C::kSFull + sb));
+        umma_commit_w(bar(C::kKEmpty + s));
         return true;
       };
       auto issue_pv = [&](int j) -> bool {
         const int s = j % C::kVStages, n = j / C::kVStages, pb = j & 1;
-        if (!mbar_wait(bar(C::kPFull + pb), (j >> 1) & 1, &abort_flag, a.err)) return false;
-        if (!mbar_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
+        if (!warp_wait(bar(C::kPFull + pb), (j >> 1) & 1, &abort_flag, a.err)) return false;
+        if (!warp_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sV = sV0 + s * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < kBlockN / 16; ++ks) {
-          umma_ts(tmem + C::kColO, tmem + C::kColP + 64u * pb + 8u * ks,
+          umma_ts_w(tmem + C::kColO, tmem + C::kColP + 64u * pb + 8u * ks,
                   smem_desc_sw128(sV + ks * 16 * 128, C::kChunkBytes, 1024), kIdO,
                   (j > 0 || ks > 0) ? 1u : 0u);
         }
-        umma_commit(bar(C::kPVDone + pb));
-        umma_commit(bar(C::kVEmpty + s));
+        umma_commit_w(bar(C::kPVDone + pb));
+        umma_commit_w(bar(C::kVEmpty + s));
         return true;
       };
-      bool ok = mbar_wait(bar(C::kQFull), 0, &abort_flag, a.err);
+      bool ok = warp_wait(bar(C::kQFull), 0, &abort_flag, a.err);
       if (ok) ok = issue_s(0);
       for (int j = 0; ok && j < nkv; ++j) {
         if (j + 1 < nkv) ok = issue_s(j + 1);
         if (ok) ok = issue_pv(j);
       }
       // Every issued MMA completes before TMEM is released.
-      umma_commit(bar(C::kDrain));
-      drain_wait(bar(C::kDrain), 0, a.err);
+      umma_commit_w(bar(C::kDrain));
+      warp_drain_wait(bar(C::kDrain), 0, a.err);
     }
   } else {
-    // ------------------------------------------------------------------ softmax (warps 0-3)
-    const int r = static_cast<int>(threadIdx.x);  // row within the tile == TMEM lane
+    // ------------------------------------------------------------------ softmax (warps 0-7)
+    const int r = static_cast<int>(threadIdx.x & 127);  // row within the tile == TMEM lane
+    const uint32_t h = warp >> 2;                          // column half of every tile
+    const uint32_t quarter = warp & 3u;
     const int row = q0 + r;
-    const uint32_t lane_base = (warp * 32u) << 16;
+    const uint32_t lane_base = (quarter * 32u) << 16;
     const float sl2 = a.scale_log2;
     float m_ref = SWA_NEG_INF;  // reference max (log2 domain) that P and l are taken against
-    float l = 0.f;
+    float l = 0.f;              // partial row sum over this thread's half of the columns
     bool ok = true;
+    // Swap a per-row value with the thread that owns the other half of the row.  Slot `n & 1`
+    // was last used two exchanges ago, and the partner arrived at the exchange in between only
+    // after reading it.
+    auto exchange = [&](int n, float v, float* other) -> bool {
+      float* red = s_red + (n & 1) * 2 * kBlockM;
+      red[h * kBlockM + r] = v;
+      __syncwarp();
+      const uint32_t xb = bar(C::kXch + quarter * 2 + (n & 1));
+      if (lane == 0) mbar_arrive(xb);
+      if (!warp_wait(xb, (n >> 1) & 1, &abort_flag, a.err)) return false;
+      *other = red[(h ^ 1u) * kBlockM + r];
+      return true;
+    };
     for (int j = 0; j < nkv; ++j) {
       const int k0 = (kb_lo + j) * kBlockN;
       const int sb = j & 1;
       if (!(ok = warp_wait(bar(C::kSFull + sb), (j >> 1) & 1, &abort_flag, a.err))) break;
       tc_fence_after();
-      float x[kBlockN];
+      float x[64];
       {
-        uint32_t rr[4][32];
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-          tmem_ld32(tmem + lane_base + C::kColS + 128u * sb + 32u * c4, rr[c4]);
+        uint32_t rr[2][32];
+        tmem_ld32(tmem + lane_base + C::kColS + 128u * sb + 64u * h, rr[0]);
+        tmem_ld32(tmem + lane_base + C::kColS + 128u * sb + 64u * h + 32u, rr[1]);
         tmem_wait_ld_all();
+        reg_fence(rr[0]);
+        reg_fence(rr[1]);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          reg_fence(rr[c4]);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[32 * c4 + i] = __uint_as_float(rr[c4][i]) * sl2;
-        }
+        for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(rr[i >> 5][i & 31]) * sl2;
       }
 
       // Window mask: the cells of this block visible to row `row` are keys in [row-W+1, row].
       const bool interior = (k0 + kBlockN - 1 <= q0) && (q0 + kBlockM - 1 - k0 < a.W);
       if (!interior) {
-        const int lo = row - a.W + 1 - k0, hi = row - k0;
+        const int hi = row - k0 - 64 * static_cast<int>(h), lo = hi - a.W + 1;
 #pragma unroll
-        for (int c = 0; c < kBlockN; ++c) x[c] = (c >= lo && c <= hi) ? x[c] : SWA_NEG_INF;
+        for (int c = 0; c < 64; ++c) x[c] = (c >= lo && c <= hi) ? x[c] : SWA_NEG_INF;
       }
       float mx = x[0];
 #pragma unroll
-      for (int c = 1; c < kBlockN; ++c) mx = fmaxf(mx, x[c]);
+      for (int c = 1; c < 64; ++c) mx = fmaxf(mx, x[c]);
+      float mx_other;
+      if (!(ok = exchange(j, mx, &mx_other))) break;
+      mx = fmaxf(mx, mx_other);
+      // Both halves of a row see the same maxima, so they take the same decisions below.
       const float m_new = fmaxf(m_ref, mx);
       const bool resc = m_new > m_ref + kRescaleThreshold;
       float factor = 1.f;
@@ -260,13 +283,13 @@ __global__ void __launch_bounds__(192, 1)
         m_ref = m_new;
       }
       const float m_use = (m_ref == SWA_NEG_INF) ? 0.f : m_ref;
-      uint32_t pk[2][32];
+      uint32_t pk[32];
       float rs = 0.f;
 #pragma unroll
-      for (int c = 0; c < kBlockN / 2; ++c) {
+      for (int c = 0; c < 32; ++c) {
         const float p0 = ex2(x[2 * c] - m_use), p1 = ex2(x[2 * c + 1] - m_use);
         rs += p0 + p1;
-        pk[c >> 5][c & 31] = pack_bf16x2(p0, p1);
+        pk[c] = pack_bf16x2(p0, p1);
       }
       l += rs;
 
@@ -279,38 +302,44 @@ __global__ void __launch_bounds__(192, 1)
           break;
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          const uint32_t oc = tmem + lane_base + C::kColO + (D / 2) * h + c0;
           uint32_t rr[32];
-          tmem_ld32(tmem + lane_base + C::kColO + c0, rr);
+          tmem_ld32(oc, rr);
           tmem_wait_ld(rr);
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * factor);
-          tmem_st32(tmem + lane_base + C::kColO + c0, rr);
+          tmem_st32(oc, rr);
         }
       } else {
         tc_fence_after();
       }
-      tmem_st32(tmem + lane_base + C::kColP + 64u * sb, pk[0]);
-      tmem_st32(tmem + lane_base + C::kColP + 64u * sb + 32u, pk[1]);
+      // keys [64h, 64h+64) -> packed P columns [32h, 32h+32)
+      tmem_st32(tmem + lane_base + C::kColP + 64u * sb + 32u * h, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kPFull + sb));
     }
+    float l_other = 0.f;
+    if (ok) ok = exchange(nkv, l, &l_other);
     const int last = nkv - 1;
     if (ok && warp_wait(bar(C::kPVDone + (last & 1)), (last >> 1) & 1, &abort_flag, a.err)) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float l_row = l + l_other;
+      const float inv_l = 1.f / l_row;
       const float m_use = (m_ref == SWA_NEG_INF) ? 0.f : m_ref;
       const bool in_range = row < a.N;
       const size_t grow = static_cast<size_t>(bh) * a.N + row;
-      if (in_range) a.lse[grow] = (m_use + log2f(l)) * kLn2;
-      __nv_bfloat16* orow = a.o + grow * D;
-      uint32_t rr[D / 32][32];
+      if (in_range && h == 0) a.lse[grow] = (m_use + log2f(l_row)) * kLn2;
+      constexpr int kHalf = D / 2;
+      __nv_bfloat16* orow = a.o + grow * D + kHalf * h;
+      uint32_t rr[kHalf / 32][32];
 #pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) tmem_ld32(tmem + lane_base + C::kColO + 32u * c4, rr[c4]);
+      for (int c4 = 0; c4 < kHalf / 32; ++c4)
+        tmem_ld32(tmem + lane_base + C::kColO + kHalf * h + 32u * c4, rr[c4]);
       tmem_wait_ld_all();
 #pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
+      for (int c4 = 0; c4 < kHalf / 32; ++c4) {
         reg_fence(rr[c4]);
         uint32_t pk[16];
 #pragma unroll
@@ -329,7 +358,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

@@ -211,6 +211,40 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       : "memory");
 }
 
+// Warp-converged forms: every lane of the issuing warp executes these, one elected lane issues.
+// Keeping the MMA warp converged (rather than running its loop on one lane) keeps the tensor pipe
+// fed: branches inside a single-lane region stall the issue of the next MMA.
+__device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
+}
+
 // ------------------------------------------------------------------------------------------------
 // tcgen05: TMEM <-> registers, 32 lanes x 32 columns of 32 bits (one lane per thread of the warp).
 // A warp may only touch the 32-lane quarter (warp_id % 4) of TMEM.
@@ -314,6 +348,13 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned* err) {
   int never = 0;
   mbar_wait(bar, parity, &never, err);
+}
+
+// drain_wait for all 32 lanes of a warp.
+__device__ __forceinline__ void warp_drain_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+  int never = 0;
+  const bool ok = mbar_wait(bar, parity, &never, err);
+  __all_sync(0xffffffffu, ok);
 }
 
 // All 32 lanes wait; the result is uniform across the warp.
