@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(320, 1)
       const int sb = j & 1;
       if (!(ok = warp_wait(bar(C::kSFull + sb), (j >> 1) & 1, &abort_flag, a.err))) break;
       tc_fence_after();
-      float x[64];
+      float x[64];  // raw scores S (the scale is applied inside the exponent below)
       {
         uint32_t rr[2][32];
         tmem_ld32(tmem + lane_base + C::kColS + 128u * sb + 64u * h, rr[0]);
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(320, 1)
         reg_fence(rr[0]);
         reg_fence(rr[1]);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(rr[i >> 5][i & 31]) * sl2;
+        for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(rr[i >> 5][i & 31]);
       }
 
       // Window mask: the cells of this block visible to row `row` are keys in [row-W+1, row].
@@ -267,9 +267,14 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) x[c] = (c >= lo && c <= hi) ? x[c] : SWA_NEG_INF;
       }
-      float mx = x[0];
+      // Row max of this half as a tree (eight independent chains), in the log2 domain.
+      float m8[8];
 #pragma unroll
-      for (int c = 1; c < 64; ++c) mx = fmaxf(mx, x[c]);
+      for (int i = 0; i < 8; ++i) m8[i] = x[i];
+#pragma unroll
+      for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
       float mx_other;
       if (!(ok = exchange(j, mx, &mx_other))) break;
       mx = fmaxf(mx, mx_other);
@@ -284,14 +289,15 @@ __global__ void __launch_bounds__(320, 1)
       }
       const float m_use = (m_ref == SWA_NEG_INF) ? 0.f : m_ref;
       uint32_t pk[32];
-      float rs = 0.f;
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(x[2 * c] - m_use), p1 = ex2(x[2 * c + 1] - m_use);
-        rs += p0 + p1;
+        // p = 2^(scale log2(e) S - m): one FFMA and one MUFU.EX2 per score
+        const float p0 = ex2(fmaf(x[2 * c], sl2, -m_use)), p1 = ex2(fmaf(x[2 * c + 1], sl2, -m_use));
+        rs8[c & 7] += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
-      l += rs;
+      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
 
       // P buffer (j & 1) was last read by P_{j-2} V_{j-2}.
       if (j >= 2 && !(ok = warp_wait(bar(C::kPVDone + sb), ((j - 2) >> 1) & 1, &abort_flag, a.err)))
