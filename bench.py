@@ -66,6 +66,12 @@ def delta_bytes(case: si.Case) -> int:
     return rows * case.D * 2 * 2 + rows * 4
 
 
+def aggregate_tflops(world: int, flops_per_step_per_rank: int, steps: int, ms_max: float) -> float:
+    """Whole-job window-effective TFLOP/s: every rank ran `steps` steps of the same workload
+    (weak scaling); the job took the slowest rank's time."""
+    return world * flops_per_step_per_rank * steps / (ms_max * 1e-3) / 1e12
+
+
 def load_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -280,7 +286,7 @@ def run_ours(args, world, rank, local):
         per["dq"].append(evs[3].elapsed_time(evs[4]))
     avg = {key: sum(vals) / len(vals) for key, vals in per.items()}
     step_total = fl["fwd"] + fl["bwd"]
-    value = world * step_total * args.steps / (total_ms * 1e-3) / 1e12
+    value = aggregate_tflops(world, step_total, args.steps, total_ms)
 
     kern_tflops = {
         "fwd": fl["fwd"] / (avg["fwd"] * 1e-3) / 1e12,
@@ -442,7 +448,7 @@ def measure_e2e(swa, case, device, dist, args, world) -> dict:
     barrier(dist, device)
     ms = max_over_ranks(dist, s_ev.elapsed_time(e_ev), device)
     fl = step_flops(case)
-    val = world * (fl["fwd"] + fl["bwd"]) * steps / (ms * 1e-3) / 1e12
+    val = aggregate_tflops(world, fl["fwd"] + fl["bwd"], steps, ms)
     swa.swa_check_device(device)
     return {"value": val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms / steps, "steps": steps}

@@ -1,0 +1,118 @@
+"""GPU parity at the full workload sizes, in the launch configuration bench.py times.
+
+The dense fp64 oracle cannot evaluate every output at N = 32,768 in seconds, so it evaluates
+sampled outputs one by one: O / LSE / dQ rows of sampled (head, row) pairs need only those rows'
+scores; dK / dV rows of sampled keys need the full forward (LSE, O, Delta) of their kv group's query
+heads, which the oracle runs densely.  Each comparison is norm-wise relative error <= 1e-2 over the
+sampled values (|LSE difference| <= 1e-3).
+"""
+import numpy as np
+import pytest
+import torch
+
+import swa_inputs as si
+from oracle import swa_oracle as orc
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+REL_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(np.asarray(a) - np.asarray(b)) / np.linalg.norm(np.asarray(b)))
+
+
+def _np(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def _run(swa, case, inp):
+    dev = torch.device("cuda:0")
+    g = {k: v.to(dev) for k, v in inp.items()}
+    o, lse = swa.swa_attn_fwd(g["q"], g["k"], g["v"], case.W, case.softmax_scale)
+    dq, dk, dv = swa.swa_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, case.W, case.softmax_scale)
+    swa.swa_check_device()
+    return {"o": o.cpu(), "lse": lse.cpu(), "dq": dq.cpu(), "dk": dk.cpu(), "dv": dv.cpu()}
+
+
+def _check_sampled(case, inp, gpu, heads, rows, kv_heads, keys):
+    """Compare sampled rows of O, LSE, dQ (query heads `heads`) and sampled keys of dK, dV."""
+    q, k, v, do = inp["q"], inp["k"], inp["v"], inp["do"]
+    W, sc = case.W, case.softmax_scale
+    o_ref, o_gpu, l_ref, l_gpu, dq_ref, dq_gpu = [], [], [], [], [], []
+    for hq in heads:
+        hk = orc.kv_head_of(hq, case.Hq, case.Hkv)
+        o_r, l_r = orc.forward_rows(q[0, hq], k[0, hk], v[0, hk], rows, W, sc)
+        o_ref.append(o_r)
+        l_ref.append(l_r)
+        o_gpu.append(_np(gpu["o"][0, hq, rows]))
+        l_gpu.append(_np(gpu["lse"][0, hq, rows]))
+        dq_ref.append(orc.dq_rows(q[0, hq], k[0, hk], v[0, hk], do[0, hq], rows, W, sc))
+        dq_gpu.append(_np(gpu["dq"][0, hq, rows]))
+    assert _rel(np.concatenate(o_gpu), np.concatenate(o_ref)) <= REL_TOL
+    assert np.max(np.abs(np.concatenate(l_gpu) - np.concatenate(l_ref))) <= LSE_TOL
+    assert _rel(np.concatenate(dq_gpu), np.concatenate(dq_ref)) <= REL_TOL
+    dk_ref, dk_gpu, dv_ref, dv_gpu = [], [], [], []
+    for hk in kv_heads:
+        group = [hq for hq in range(case.Hq) if orc.kv_head_of(hq, case.Hq, case.Hkv) == hk]
+        dk_r, dv_r = orc.dkdv_rows([q[0, hq] for hq in group], k[0, hk], v[0, hk],
+                                   [do[0, hq] for hq in group], keys, W, sc)
+        dk_ref.append(dk_r)
+        dv_ref.append(dv_r)
+        dk_gpu.append(_np(gpu["dk"][0, hk, keys]))
+        dv_gpu.append(_np(gpu["dv"][0, hk, keys]))
+    if kv_heads:
+        assert _rel(np.concatenate(dk_gpu), np.concatenate(dk_ref)) <= REL_TOL
+        assert _rel(np.concatenate(dv_gpu), np.concatenate(dv_ref)) <= REL_TOL
+
+
+def _sample(rng, N, n, must=()):
+    s = set(int(x) for x in rng.choice(N, size=min(n, N), replace=False))
+    s.update(int(m) for m in must if 0 <= m < N)
+    return np.array(sorted(s))
+
+
+def test_long_swa_layer_n32768(swa):
+    case = si.long_swa_case(32768)
+    inp = si.make_inputs(case)
+    gpu = _run(swa, case, inp)
+    for key, t in gpu.items():
+        assert torch.isfinite(t.float()).all(), key
+    rng = np.random.default_rng(1)
+    N = case.N
+    # first rows (window not yet full), block boundaries, the last row
+    rows = _sample(rng, N, 24, must=(0, 1, 127, 128, 1023, 1024, 1151, N - 1))
+    keys = _sample(rng, N, 24, must=(0, 127, 128, N - 129, N - 128, N - 1))
+    _check_sampled(case, inp, gpu, heads=[0, 1, 17, 31], rows=rows, kv_heads=[0, 15], keys=keys)
+
+
+def test_gqa_full_causal_n8192_group(swa):
+    """Full causal, 4 query heads per kv head: one whole kv group exactly, plus sampled rows."""
+    case = si.gqa_causal_case()
+    inp = si.make_inputs(case)
+    gpu = _run(swa, case, inp)
+    ref = orc.group_backward(inp["q"], inp["k"], inp["v"], inp["do"], 0, 3, case.W, case.softmax_scale,
+                             row_block=512)
+    hq = ref["hq"]
+    assert _rel(_np(gpu["o"][0, hq]), ref["o"]) <= REL_TOL
+    assert np.max(np.abs(_np(gpu["lse"][0, hq]) - ref["lse"])) <= LSE_TOL
+    assert _rel(_np(gpu["dq"][0, hq]), ref["dq"]) <= REL_TOL
+    assert _rel(_np(gpu["dk"][0, 3]), ref["dk"]) <= REL_TOL
+    assert _rel(_np(gpu["dv"][0, 3]), ref["dv"]) <= REL_TOL
+    rng = np.random.default_rng(2)
+    rows = _sample(rng, case.N, 16, must=(0, case.N - 1))
+    _check_sampled(case, inp, gpu, heads=[5, 30], rows=rows, kv_heads=[], keys=[])
+
+
+@pytest.mark.parametrize("layer", [0, 5])
+def test_mixed_step_layers_n30553(swa, layer):
+    """Layers of the mixed step (N = 30,553, not a tile multiple): a sliding and a full layer."""
+    case = si.mixed_layer_cases()[layer]
+    inp = si.make_inputs(case)
+    gpu = _run(swa, case, inp)
+    rng = np.random.default_rng(3 + layer)
+    N = case.N
+    rows = _sample(rng, N, 16, must=(0, N - 89, N - 1))
+    keys = _sample(rng, N, 16, must=(N - 89, N - 1))
+    _check_sampled(case, inp, gpu, heads=[0, 31], rows=rows, kv_heads=[15], keys=keys)
