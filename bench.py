@@ -297,6 +297,14 @@ def run_ours(args, world, rank, local):
     dominant = max(("fwd", "dkdv", "dq"), key=lambda k_: avg[k_])
     peak_tf = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
     traffic = _profiled_traffic(dominant)
+    algorithmic_bytes = {  # each kernel's compulsory DRAM traffic per launch
+        "fwd": 2 * (case.B * case.Hq * case.N * case.D * 2) + 2 * (case.B * case.Hkv * case.N * case.D * 2)
+               + case.B * case.Hq * case.N * 4,
+        "dkdv": 2 * (case.B * case.Hq * case.N * case.D * 2) + 4 * (case.B * case.Hkv * case.N * case.D * 2)
+                + 2 * case.B * case.Hq * case.N * 4,
+        "dq": 3 * (case.B * case.Hq * case.N * case.D * 2) + 2 * (case.B * case.Hkv * case.N * case.D * 2)
+              + 2 * case.B * case.Hq * case.N * 4,
+    }
     roofline = {
         "kernel": {"fwd": "swa_fwd_kernel<128>", "dkdv": "swa_dkdv_kernel<128>",
                    "dq": "swa_dq_kernel<128>"}[dominant],
@@ -306,6 +314,7 @@ def run_ours(args, world, rank, local):
         "unit": "TFLOP/s",
         "frac": kern_tflops[dominant] / peak_tf,
         "traffic": traffic,
+        "algorithmic_bytes": algorithmic_bytes[dominant],
         "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a repeated step)",
     }
     delta_gbs = delta_bytes(case) / (avg["delta"] * 1e-3) / 1e9
@@ -368,19 +377,27 @@ def run_ours(args, world, rank, local):
 
 
 def _profiled_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it covers this kernel build."""
+    """DRAM bytes per launch from the committed ncu capture, or None when the kernel's sources
+    have changed since the counters were taken."""
+    import hashlib
+
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
         with open(path) as f:
-            d = json.load(f)
-        ent = d.get(kernel)
-        if ent and ent.get("valid", False):
-            return ent.get("bytes_per_launch")
-    except Exception:
-        pass
-    return None
+            ent = json.load(f).get(kernel)
+        if not ent:
+            return None
+        h = hashlib.sha256()
+        for name in ent["sources"]:
+            with open(os.path.join(ROOT, "sliding_window_flash_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != ent["source_sha256"]:
+            return None
+        return ent["bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def measure_memory(swa, device) -> dict:
