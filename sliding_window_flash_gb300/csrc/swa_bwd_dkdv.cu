@@ -49,7 +49,8 @@ struct DkdvCfg {
   static constexpr int kDSFull = kPFull + 1;
   static constexpr int kVecFull = kDSFull + 1;  // 2 slots
   static constexpr int kDone = kVecFull + 2;
-  static constexpr int kDrain = kDone + 1;
+  static constexpr int kOutFull = kDone + 1;  // staged dK / dV tiles complete (one arrival per warp)
+  static constexpr int kDrain = kOutFull + 1;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
@@ -74,7 +75,9 @@ __global__ void __launch_bounds__(320, 1)
     swa_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const DkdvArgs a) {
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv, const DkdvArgs a) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -119,6 +122,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar(C::kVecFull + 0), C::kComputeThreads / 32);
     mbar_init(bar(C::kVecFull + 1), C::kComputeThreads / 32);
     mbar_init(bar(C::kDone), 1);
+    mbar_init(bar(C::kOutFull), C::kComputeThreads / 32);
     mbar_init(bar(C::kDrain), 1);
     fence_barrier_init();
   }
@@ -347,14 +351,14 @@ __global__ void __launch_bounds__(320, 1)
     }
     if (ok && warp_wait(bar(C::kDone), 0, &abort_flag, a.err)) {
       tc_fence_after();
+      // dK * scale and dV -> bf16, staged in the two Q slots (free: every MMA has completed) and
+      // written with tensor stores, one per 64-column chunk (rows past N are not written).
       constexpr int kHalf = D / 2;
-      const bool in_range = key < a.N;
-      const size_t grow = static_cast<size_t>(bhk) * a.N + key;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = (which == 0 ? C::kColDK : C::kColDV) + kHalf * h;
         const float mul = which == 0 ? a.scale : 1.f;
-        __nv_bfloat16* dst_row = (which == 0 ? a.dk : a.dv) + grow * D + kHalf * h;
+        const uint32_t stage = sQ0 + which * C::kTileBytes;
         uint32_t rr[kHalf / 32][32];
 #pragma unroll
         for (int c4 = 0; c4 < kHalf / 32; ++c4) tmem_ld32(tmem + lane_base + col + 32u * c4, rr[c4]);
@@ -367,13 +371,19 @@ __global__ void __launch_bounds__(320, 1)
           for (int i = 0; i < 16; ++i)
             o16[i] = pack_bf16x2(__uint_as_float(rr[c4][2 * i]) * mul,
                                  __uint_as_float(rr[c4][2 * i + 1]) * mul);
-          if (in_range) {
-            uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c4);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(o16[4 * v], o16[4 * v + 1], o16[4 * v + 2], o16[4 * v + 3]);
-          }
+          stage_row32_sw128(stage, r, kHalf * h + 32u * c4, o16);
         }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kOutFull));
+      if (warp == 0 && warp_wait(bar(C::kOutFull), 0, &abort_flag, a.err) && lane == 0) {
+        for (int hh = 0; hh < C::kChunks; ++hh) {
+          tma_store_3d(&tm_dk, sQ0 + hh * C::kChunkBytes, 64 * hh, k0, bhk);
+          tma_store_3d(&tm_dv, sQ0 + C::kTileBytes + hh * C::kChunkBytes, 64 * hh, k0, bhk);
+        }
+        bulk_commit_group();
+        bulk_wait_group_read0();
       }
     }
   }
@@ -391,12 +401,14 @@ cudaError_t launch_dkdv_d(const Problem& pb, const void* q, const void* k, const
                           const void* dO, const float* lse, const float* delta, void* dk, void* dv,
                           cudaStream_t stream) {
   using C = DkdvCfg<D>;
-  CUtensorMap tq, tdo, tk, tv;
+  CUtensorMap tq, tdo, tk, tv, tdk, tdv;
   const uint64_t bhq = static_cast<uint64_t>(pb.B) * pb.Hq, bhk = static_cast<uint64_t>(pb.B) * pb.Hkv;
   if (!make_tmap_bf16_3d(&tq, q, bhq, pb.N, D, kBlockM) ||
       !make_tmap_bf16_3d(&tdo, dO, bhq, pb.N, D, kBlockM) ||
       !make_tmap_bf16_3d(&tk, k, bhk, pb.N, D, kBlockN) ||
-      !make_tmap_bf16_3d(&tv, v, bhk, pb.N, D, kBlockN))
+      !make_tmap_bf16_3d(&tv, v, bhk, pb.N, D, kBlockN) ||
+      !make_tmap_bf16_3d(&tdk, dk, bhk, pb.N, D, kBlockN) ||
+      !make_tmap_bf16_3d(&tdv, dv, bhk, pb.N, D, kBlockN))
     return cudaErrorInvalidValue;
   auto kern = swa_dkdv_kernel<D>;
   cudaError_t e =
@@ -418,7 +430,7 @@ cudaError_t launch_dkdv_d(const Problem& pb, const void* q, const void* k, const
   a.scale_log2 = pb.scale * kLog2e;
   a.err = pb.err;
   const unsigned grid = static_cast<unsigned>(a.nkb) * static_cast<unsigned>(a.BHK);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tdo, tk, tv, a);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tdo, tk, tv, tdk, tdv, a);
   return cudaGetLastError();
 }
 

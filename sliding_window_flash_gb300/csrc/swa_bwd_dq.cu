@@ -44,7 +44,8 @@ struct DqCfg {
   static constexpr int kDPFull = kSEmpty + 1;
   static constexpr int kDSFull = kDPFull + 1;
   static constexpr int kDQDone = kDSFull + 1;
-  static constexpr int kDrain = kDQDone + 1;
+  static constexpr int kOutFull = kDQDone + 1;  // staged dQ tile complete (one arrival per warp)
+  static constexpr int kDrain = kOutFull + 1;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
@@ -66,7 +67,7 @@ template <int D>
 __global__ void __launch_bounds__(320, 1)
     swa_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const DqArgs a) {
+                  const __grid_constant__ CUtensorMap tm_dq, const DqArgs a) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -105,6 +106,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar(C::kDPFull), 1);
     mbar_init(bar(C::kDSFull), C::kComputeThreads);
     mbar_init(bar(C::kDQDone), 1);
+    mbar_init(bar(C::kOutFull), C::kComputeThreads / 32);
     mbar_init(bar(C::kDrain), 1);
     fence_barrier_init();
   }
@@ -287,8 +289,9 @@ __global__ void __launch_bounds__(320, 1)
     }
     if (ok && warp_wait(bar(C::kDQDone), 0, &abort_flag, a.err)) {
       tc_fence_after();
+      // dQ * scale -> bf16, staged in the Q tile (free: every MMA has completed) and written with
+      // one tensor store per 64-column chunk (rows past N are not written).
       constexpr int kHalf = D / 2;
-      __nv_bfloat16* dst_row = a.dq + grow * D + kHalf * h;
       uint32_t rr[kHalf / 32][32];
 #pragma unroll
       for (int c4 = 0; c4 < kHalf / 32; ++c4)
@@ -302,12 +305,16 @@ __global__ void __launch_bounds__(320, 1)
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(rr[c4][2 * i]) * a.scale,
                               __uint_as_float(rr[c4][2 * i + 1]) * a.scale);
-        if (in_range) {
-          uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c4);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-        }
+        stage_row32_sw128(sQ, r, kHalf * h + 32u * c4, pk);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kOutFull));
+      if (warp == 0 && warp_wait(bar(C::kOutFull), 0, &abort_flag, a.err) && lane == 0) {
+        for (int hh = 0; hh < C::kChunks; ++hh)
+          tma_store_3d(&tm_dq, sQ + hh * C::kChunkBytes, 64 * hh, q0, bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();
       }
     }
   }
@@ -325,12 +332,13 @@ cudaError_t launch_dq_d(const Problem& pb, const void* q, const void* k, const v
                         const void* dO, const float* lse, const float* delta, void* dq,
                         cudaStream_t stream) {
   using C = DqCfg<D>;
-  CUtensorMap tq, tdo, tk, tv;
+  CUtensorMap tq, tdo, tk, tv, tdq;
   const uint64_t bhq = static_cast<uint64_t>(pb.B) * pb.Hq, bhk = static_cast<uint64_t>(pb.B) * pb.Hkv;
   if (!make_tmap_bf16_3d(&tq, q, bhq, pb.N, D, kBlockM) ||
       !make_tmap_bf16_3d(&tdo, dO, bhq, pb.N, D, kBlockM) ||
       !make_tmap_bf16_3d(&tk, k, bhk, pb.N, D, kBlockN) ||
-      !make_tmap_bf16_3d(&tv, v, bhk, pb.N, D, kBlockN))
+      !make_tmap_bf16_3d(&tv, v, bhk, pb.N, D, kBlockN) ||
+      !make_tmap_bf16_3d(&tdq, dq, bhq, pb.N, D, kBlockM))
     return cudaErrorInvalidValue;
   auto kern = swa_dq_kernel<D>;
   cudaError_t e =
@@ -351,7 +359,7 @@ cudaError_t launch_dq_d(const Problem& pb, const void* q, const void* k, const v
   a.scale_log2 = pb.scale * kLog2e;
   a.err = pb.err;
   const unsigned grid = static_cast<unsigned>(a.nqb) * static_cast<unsigned>(a.BH);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tdo, tk, tv, a);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tdo, tk, tv, tdq, a);
   return cudaGetLastError();
 }
 

@@ -57,7 +57,8 @@ struct FwdCfg {
   static constexpr int kPFull = kSFull + 2;          // 2
   static constexpr int kPVDone = kPFull + 2;         // 2
   static constexpr int kXch = kPVDone + 2;           // [4 lane quarters][2 slots]
-  static constexpr int kDrain = kXch + 8;
+  static constexpr int kOutFull = kXch + 8;  // staged output tile complete (one arrival per warp)
+  static constexpr int kDrain = kOutFull + 1;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM slot + align
   static constexpr uint32_t kTmemCols = 512;
@@ -80,7 +81,8 @@ struct FwdArgs {
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     swa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const FwdArgs a) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -121,6 +123,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar(C::kPVDone + b), 1);
     }
     for (int x = 0; x < 8; ++x) mbar_init(bar(C::kXch + x), 2);  // the two warps of a lane quarter
+    mbar_init(bar(C::kOutFull), C::kComputeThreads / 32);
     mbar_init(bar(C::kDrain), 1);
     fence_barrier_init();
   }
@@ -337,8 +340,10 @@ __global__ void __launch_bounds__(320, 1)
       const bool in_range = row < a.N;
       const size_t grow = static_cast<size_t>(bh) * a.N + row;
       if (in_range && h == 0) a.lse[grow] = (m_use + log2f(l_row)) * kLn2;
+      // O / l -> bf16, staged in the Q tile (free: every S MMA has completed) in the swizzled layout
+      // of the TMA map, then written with one tensor store per 64-column chunk (rows past N are
+      // not written).
       constexpr int kHalf = D / 2;
-      __nv_bfloat16* orow = a.o + grow * D + kHalf * h;
       uint32_t rr[kHalf / 32][32];
 #pragma unroll
       for (int c4 = 0; c4 < kHalf / 32; ++c4)
@@ -352,12 +357,15 @@ __global__ void __launch_bounds__(320, 1)
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(rr[c4][2 * i]) * inv_l,
                               __uint_as_float(rr[c4][2 * i + 1]) * inv_l);
-        if (in_range) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c4);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-        }
+        stage_row32_sw128(sQ, r, kHalf * h + 32u * c4, pk);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kOutFull));
+      if (warp == 0 && warp_wait(bar(C::kOutFull), 0, &abort_flag, a.err) && lane == 0) {
+        for (int hh = 0; hh < C::kChunks; ++hh) tma_store_3d(&tm_o, sQ + hh * C::kChunkBytes, 64 * hh, q0, bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();
       }
     }
   }
@@ -374,8 +382,9 @@ template <int D>
 cudaError_t launch_fwd_d(const Problem& pb, const void* q, const void* k, const void* v, void* o,
                          float* lse, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!make_tmap_bf16_3d(&tq, q, static_cast<uint64_t>(pb.B) * pb.Hq, pb.N, D, kBlockM) ||
+      !make_tmap_bf16_3d(&to, o, static_cast<uint64_t>(pb.B) * pb.Hq, pb.N, D, kBlockM) ||
       !make_tmap_bf16_3d(&tk, k, static_cast<uint64_t>(pb.B) * pb.Hkv, pb.N, D, kBlockN) ||
       !make_tmap_bf16_3d(&tv, v, static_cast<uint64_t>(pb.B) * pb.Hkv, pb.N, D, kBlockN))
     return cudaErrorInvalidValue;
@@ -396,7 +405,7 @@ cudaError_t launch_fwd_d(const Problem& pb, const void* q, const void* k, const 
   a.scale_log2 = pb.scale * kLog2e;
   a.err = pb.err;
   const unsigned grid = static_cast<unsigned>(a.nqb) * static_cast<unsigned>(a.BH);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 

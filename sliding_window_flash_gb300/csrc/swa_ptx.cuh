@@ -118,6 +118,26 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 3-D tile store from shared memory (same box and swizzle as the loads).  Elements outside the
+// tensor are not written.  Completion is tracked with the bulk async-group of the issuing thread.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until every committed bulk store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------------------
 // tcgen05: TMEM allocation
 // ------------------------------------------------------------------------------------------------
@@ -362,6 +382,28 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
                                           unsigned* err) {
   const bool ok = mbar_wait(bar, parity, abort_flag, err);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Stores 32 packed bf16 pairs (64 columns, one 128-byte row of a 64-column chunk) of row `row`
+// into a 128B-swizzled chunk at `chunk`, the layout a 3-D TMA store with 64 x 128 boxes reads.
+__device__ __forceinline__ void store_half_row_sw128(uint32_t chunk, uint32_t row,
+                                                     const uint32_t (&pk)[32]) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    st_shared_v4(chunk + sw128_offset(row, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                 pk[4 * u + 3]);
+}
+
+// Stages 16 packed bf16 pairs = columns [c0, c0 + 32) of row `row` of a 128-row tile whose
+// 64-column chunks (128 rows x 128 bytes, 128B-swizzled) start at `tile` + chunk * 16 KB.
+__device__ __forceinline__ void stage_row32_sw128(uint32_t tile, uint32_t row, uint32_t c0,
+                                                  const uint32_t (&pk)[16]) {
+  const uint32_t chunk = tile + (c0 >> 6) * (128u * 128u);
+  const uint32_t unit0 = (c0 & 63u) >> 3;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    st_shared_v4(chunk + sw128_offset(row, unit0 + u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                 pk[4 * u + 3]);
 }
 
 // Stores one thread's row of 128 bf16 values (64 packed pairs) into a 128 x 128 K-major operand
