@@ -117,8 +117,8 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(bar(C::kSFull), 1);
     mbar_init(bar(C::kDPFull), 1);
-    mbar_init(bar(C::kPFull), C::kComputeThreads);
-    mbar_init(bar(C::kDSFull), C::kComputeThreads);
+    mbar_init(bar(C::kPFull), C::kComputeThreads / 32);
+    mbar_init(bar(C::kDSFull), C::kComputeThreads / 32);
     mbar_init(bar(C::kVecFull + 0), C::kComputeThreads / 32);
     mbar_init(bar(C::kVecFull + 1), C::kComputeThreads / 32);
     mbar_init(bar(C::kDone), 1);
@@ -287,6 +287,12 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       float p[64];
       {
+        // The per-query log-sum-exp values are read from shared memory while the TMEM load of S^T
+        // is in flight (the loads are issued before the wait, so their latencies overlap).
+        const float4* l4 = reinterpret_cast<const float4*>(s_lse2 + 64 * h);
+        float4 lv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) lv[i] = l4[i];
         uint32_t rr[2][32];
         tmem_ld32(tmem + lane_base + C::kColS + 64u * h, rr[0]);
         tmem_ld32(tmem + lane_base + C::kColS + 64u * h + 32u, rr[1]);
@@ -294,16 +300,13 @@ __global__ void __launch_bounds__(320, 1)
         reg_fence(rr[0]);
         reg_fence(rr[1]);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) p[i] = __uint_as_float(rr[i >> 5][i & 31]);
-      }
-      const float4* l4 = reinterpret_cast<const float4*>(s_lse2 + 64 * h);
-#pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l = l4[c4];
-        p[4 * c4 + 0] = ex2(fmaf(p[4 * c4 + 0], sl2, -l.x));
-        p[4 * c4 + 1] = ex2(fmaf(p[4 * c4 + 1], sl2, -l.y));
-        p[4 * c4 + 2] = ex2(fmaf(p[4 * c4 + 2], sl2, -l.z));
-        p[4 * c4 + 3] = ex2(fmaf(p[4 * c4 + 3], sl2, -l.w));
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t* src = &rr[i >> 3][(4 * i) & 31];
+          p[4 * i + 0] = ex2(fmaf(__uint_as_float(src[0]), sl2, -lv[i].x));
+          p[4 * i + 1] = ex2(fmaf(__uint_as_float(src[1]), sl2, -lv[i].y));
+          p[4 * i + 2] = ex2(fmaf(__uint_as_float(src[2]), sl2, -lv[i].z));
+          p[4 * i + 3] = ex2(fmaf(__uint_as_float(src[3]), sl2, -lv[i].w));
+        }
       }
       // Query q0 + 64h + c sees this key iff 0 <= q0 + 64h + c - key < W.
       const bool interior = (q0 >= k0 + kBlockN - 1) && (q0 + kBlockM - 1 - k0 < a.W);
@@ -319,13 +322,15 @@ __global__ void __launch_bounds__(320, 1)
         tmem_st32(tmem + lane_base + C::kColS + 64u * h, pk);
       }
       tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::kPFull));
+      warp_arrive(bar(C::kPFull));
 
       if (!(ok = warp_wait(bar(C::kDPFull), t & 1, &abort_flag, a.err))) break;
       tc_fence_after();
       {
         const float4* d4 = reinterpret_cast<const float4*>(s_delta + 64 * h);
+        float4 dv4[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dv4[i] = d4[i];
         uint32_t rr[2][32];
         tmem_ld32(tmem + lane_base + C::kColDP + 64u * h, rr[0]);
         tmem_ld32(tmem + lane_base + C::kColDP + 64u * h + 32u, rr[1]);
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = 4 * i;
-          const float4 dl = d4[i];
+          const float4 dl = dv4[i];
           const uint32_t* src = &rr[i >> 3][(4 * i) & 31];
           pk[2 * i] = pack_bf16x2(p[c] * (__uint_as_float(src[0]) - dl.x),
                                   p[c + 1] * (__uint_as_float(src[1]) - dl.y));
@@ -346,8 +351,7 @@ __global__ void __launch_bounds__(320, 1)
         tmem_st32(tmem + lane_base + C::kColDP + 64u * h, pk);
       }
       tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::kDSFull));
+      warp_arrive(bar(C::kDSFull));
     }
     if (ok && warp_wait(bar(C::kDone), 0, &abort_flag, a.err)) {
       tc_fence_after();

@@ -13,8 +13,9 @@
 // Warp roles (320 threads): warps 0-7 compute — warp w handles TMEM lanes 32(w%4)..+31 (query
 // rows) and columns [64 h, 64 h + 64) of every 128-column tile, h = w / 4, so each score row is
 // split over two threads; warp 8 TMA producer (Q and dO once, K_j and V_j through two
-// shared-memory rings); warp 9 MMA issuer and TMEM owner.  dS goes back to TMEM and is the A operand of dQ += dS K_j.
-// TMEM columns: [0,128) S, [128,256) dP, [256, 256+D) dQ, [256+D, 320+D) dS (bf16 pairs).
+// shared-memory rings); warp 9 MMA issuer and TMEM owner.  dS goes back to TMEM (two buffers)
+// and is the A operand of dQ += dS K_j.
+// TMEM columns: [0,128) S, [128,256) dP, [256, 256+D) dQ, [256+D, 384+D) dS x 2 (bf16 pairs).
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 #include "swa_tmap.h"
@@ -42,8 +43,9 @@ struct DqCfg {
   static constexpr int kSFull = kVEmpty + kVStages;
   static constexpr int kSEmpty = kSFull + 1;
   static constexpr int kDPFull = kSEmpty + 1;
-  static constexpr int kDSFull = kDPFull + 1;
-  static constexpr int kDQDone = kDSFull + 1;
+  static constexpr int kDPEmpty = kDPFull + 1;
+  static constexpr int kDSFull = kDPEmpty + 1;  // 2 (one per dS buffer)
+  static constexpr int kDQDone = kDSFull + 2;
   static constexpr int kOutFull = kDQDone + 1;  // staged dQ tile complete (one arrival per warp)
   static constexpr int kDrain = kOutFull + 1;
   static constexpr int kNumBars = kDrain + 1;
@@ -102,9 +104,11 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar(C::kVEmpty + s), 1);
     }
     mbar_init(bar(C::kSFull), 1);
-    mbar_init(bar(C::kSEmpty), C::kComputeThreads);
+    mbar_init(bar(C::kSEmpty), C::kComputeThreads / 32);
     mbar_init(bar(C::kDPFull), 1);
-    mbar_init(bar(C::kDSFull), C::kComputeThreads);
+    mbar_init(bar(C::kDPEmpty), C::kComputeThreads / 32);
+    mbar_init(bar(C::kDSFull + 0), C::kComputeThreads / 32);
+    mbar_init(bar(C::kDSFull + 1), C::kComputeThreads / 32);
     mbar_init(bar(C::kDQDone), 1);
     mbar_init(bar(C::kOutFull), C::kComputeThreads / 32);
     mbar_init(bar(C::kDrain), 1);
@@ -161,9 +165,10 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
-    // Issue order S_0, dP_0, then per block j: S_{j+1}, dQ += dS_j K_j, dP_{j+1}.  The MMAs run in
-    // that order, so dP_{j+1} lands only after dQ_j has read dS_j: when the compute warps see
-    // dP_{j+1} they may overwrite the single TMEM dS buffer.
+    // Issue order S_0, dP_0, then per block j: S_{j+1}, dP_{j+1}, dQ += dS_j K_j.  The next block's
+    // S and dP are computed as soon as the compute warps have read this block's, so they never wait
+    // on dQ_j.  dS alternates between two TMEM buffers: dP_{j+2} runs after dQ_j, so when the
+    // compute warps see dP_{j+2} the buffer of dS_j is free again.
     {  // the whole warp, converged; one elected lane issues
       constexpr uint32_t kIdSq = idesc_bf16(kBlockM, kBlockN, false, false);  // S, dP
       constexpr uint32_t kIdDq = idesc_bf16(kBlockM, D, false, true);         // dQ += dS K
@@ -182,9 +187,10 @@ __global__ void __launch_bounds__(320, 1)
         umma_commit_w(bar(C::kSFull));
         return true;
       };
-      auto issue_dp = [&](int j) -> bool {  // dP = dO V_j^T (dP_{j-1} was read before dS_{j-1})
+      auto issue_dp = [&](int j) -> bool {  // dP = dO V_j^T once dP_{j-1} has been read
         const int s = j % C::kVStages, n = j / C::kVStages;
         if (!warp_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
+        if (j >= 1 && !warp_wait(bar(C::kDPEmpty), (j - 1) & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sV = sV0 + s * C::kTileBytes;
 #pragma unroll
@@ -198,13 +204,13 @@ __global__ void __launch_bounds__(320, 1)
         return true;
       };
       auto issue_dq = [&](int j) -> bool {  // dQ += dS K_j  (dS from TMEM, K_j as MN-major B)
-        const int s = j % C::kKStages;
-        if (!warp_wait(bar(C::kDSFull), j & 1, &abort_flag, a.err)) return false;
+        const int s = j % C::kKStages, db = j & 1;
+        if (!warp_wait(bar(C::kDSFull + db), (j >> 1) & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sK = sK0 + s * C::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < kBlockN / 16; ++ks) {
-          umma_ts_w(tmem + C::kColDQ, tmem + C::kColDS + 8u * ks,
+          umma_ts_w(tmem + C::kColDQ, tmem + C::kColDS + 64u * db + 8u * ks,
                   smem_desc_sw128(sK + ks * 16 * 128, C::kChunkBytes, 1024), kIdDq,
                   (j > 0 || ks > 0) ? 1u : 0u);
         }
@@ -216,9 +222,11 @@ __global__ void __launch_bounds__(320, 1)
       if (ok) ok = issue_s(0);
       if (ok) ok = issue_dp(0);
       for (int j = 0; ok && j < nkv; ++j) {
-        if (j + 1 < nkv) ok = issue_s(j + 1);
+        if (j + 1 < nkv) {
+          ok = issue_s(j + 1);
+          if (ok) ok = issue_dp(j + 1);
+        }
         if (ok) ok = issue_dq(j);
-        if (ok && j + 1 < nkv) ok = issue_dp(j + 1);
       }
       umma_commit_w(bar(C::kDrain));
       warp_drain_wait(bar(C::kDrain), 0, a.err);
@@ -251,8 +259,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) p[i] = __uint_as_float(rr[i >> 5][i & 31]);
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::kSEmpty));
+      warp_arrive(bar(C::kSEmpty));
 #pragma unroll
       for (int c = 0; c < 64; ++c) p[c] = ex2(fmaf(p[c], sl2, -lse2));
       const bool interior = (k0 + kBlockN - 1 <= q0) && (q0 + kBlockM - 1 - k0 < a.W);
@@ -263,7 +270,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < 64; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
       }
 
-      // dP_j landing also means dQ_{j-1} has finished reading the TMEM dS buffer.
+      // dP_j landing also means dQ_{j-2} has finished reading dS buffer (j & 1).
       if (!(ok = warp_wait(bar(C::kDPFull), j & 1, &abort_flag, a.err))) break;
       tc_fence_after();
       {
@@ -273,6 +280,7 @@ __global__ void __launch_bounds__(320, 1)
         tmem_wait_ld_all();
         reg_fence(rr[0]);
         reg_fence(rr[1]);
+        warp_arrive(bar(C::kDPEmpty));
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -280,12 +288,11 @@ __global__ void __launch_bounds__(320, 1)
           pk[i] = pack_bf16x2(p[2 * i] * (__uint_as_float(d0) - dlt),
                               p[2 * i + 1] * (__uint_as_float(d1) - dlt));
         }
-        // dS columns [64h, 64h+64) -> packed TMEM columns [32h, 32h+32) of the dS buffer.
-        tmem_st32(tmem + lane_base + C::kColDS + 32u * h, pk);
+        // dS columns [64h, 64h+64) -> packed TMEM columns [32h, 32h+32) of dS buffer (j & 1).
+        tmem_st32(tmem + lane_base + C::kColDS + 64u * (j & 1) + 32u * h, pk);
       }
       tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::kDSFull));
+      warp_arrive(bar(C::kDSFull + (j & 1)));
     }
     if (ok && warp_wait(bar(C::kDQDone), 0, &abort_flag, a.err)) {
       tc_fence_after();

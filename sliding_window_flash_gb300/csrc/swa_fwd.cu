@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::kSFull + b), 1);
-      mbar_init(bar(C::kPFull + b), C::kComputeThreads);
+      mbar_init(bar(C::kPFull + b), C::kComputeThreads / 32);
       mbar_init(bar(C::kPVDone + b), 1);
     }
     for (int x = 0; x < 8; ++x) mbar_init(bar(C::kXch + x), 2);  // the two warps of a lane quarter
@@ -326,8 +326,7 @@ __global__ void __launch_bounds__(320, 1)
       // keys [64h, 64h+64) -> packed P columns [32h, 32h+32)
       tmem_st32(tmem + lane_base + C::kColP + 64u * sb + 32u * h, pk);
       tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::kPFull + sb));
+      warp_arrive(bar(C::kPFull + sb));
     }
     float l_other = 0.f;
     if (ok) ok = exchange(nkv, l, &l_other);

@@ -67,12 +67,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Waits until the phase with the given parity has completed.  Bounded: returns false (and raises
-// the CTA's abort flag and the device error word) when the wait runs out, or returns false at once
-// when another role of the CTA has already raised the abort flag.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* err_word) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of the waits below: keeps polling until the phase completes, the abort flag rises, or
+// the bound runs out (then raises the abort flag and the device error word).  Kept out of line so
+// that a wait whose phase has already completed costs one try_wait.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                            unsigned* err_word) {
   const long long t0 = clock64();
   for (unsigned it = 0; it < kWaitPollLimit; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -84,6 +83,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   *abort_flag = 1;
   atomicOr(err_word, kErrWaitTimeout);
   return false;
+}
+
+// Waits until the phase with the given parity has completed.  Bounded: returns false (and raises
+// the CTA's abort flag and the device error word) when the wait runs out, or returns false at once
+// when another role of the CTA has already raised the abort flag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* err_word) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err_word);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -377,10 +385,22 @@ __device__ __forceinline__ void warp_drain_wait(uint32_t bar, uint32_t parity, u
   __all_sync(0xffffffffu, ok);
 }
 
-// All 32 lanes wait; the result is uniform across the warp.
+// One arrival per warp: every lane has finished its own tcgen05 loads/stores (wait::ld / wait::st)
+// and shared-memory writes before this; the before_thread_sync fence and __syncwarp order them
+// ahead of lane 0's release-arrive.  Barriers fed this way count warps, not threads, which keeps
+// the shared-memory atomics per phase at one per warp.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31u) == 0u) mbar_arrive(bar);
+}
+
+// All 32 lanes wait; the result is uniform across the warp.  Fast path: one try_wait per lane and
+// one vote.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned* err) {
-  const bool ok = mbar_wait(bar, parity, abort_flag, err);
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const bool ok = mbar_wait_slow(bar, parity, abort_flag, err);
   return __all_sync(0xffffffffu, ok);
 }
 
