@@ -190,12 +190,8 @@ __global__ void __launch_bounds__(320, 1)
         if (!warp_wait(bar(C::kQFull + s), (t / C::kQStages) & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sQ = sQ0 + s * C::kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          umma_ss_w(tmem + C::kColS, smem_desc_sw128(sK + off, 16, 1024),
-                  smem_desc_sw128(sQ + off, 16, 1024), kIdS, ks > 0);
-        }
+        umma_ss_kmajor_d<D>(tmem + C::kColS, smem_desc_sw128(sK, 16, 1024),
+                            smem_desc_sw128(sQ, 16, 1024), kIdS, 0u);
         umma_commit_w(bar(C::kSFull));
         return true;
       };
@@ -205,12 +201,8 @@ __global__ void __launch_bounds__(320, 1)
           return false;
         tc_fence_after();
         const uint32_t sDO = sDO0 + s * C::kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          umma_ss_w(tmem + C::kColDP, smem_desc_sw128(sV + off, 16, 1024),
-                  smem_desc_sw128(sDO + off, 16, 1024), kIdS, ks > 0);
-        }
+        umma_ss_kmajor_d<D>(tmem + C::kColDP, smem_desc_sw128(sV, 16, 1024),
+                            smem_desc_sw128(sDO, 16, 1024), kIdS, 0u);
         umma_commit_w(bar(C::kDPFull));
         return true;
       };
@@ -219,13 +211,10 @@ __global__ void __launch_bounds__(320, 1)
                            uint32_t d_col) -> bool {
         if (!warp_wait(bar(wait_bar), t & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < kBlockM / 16; ++ks) {
-          // query columns 16 ks .. 16 ks + 15 sit at packed column 8 ks + 32 (ks / 4)
-          umma_ts_w(tmem + d_col, tmem + a_col + 8u * ks + 32u * (ks >> 2),
-                  smem_desc_sw128(b_tile + ks * 16 * 128, C::kChunkBytes, 1024), kIdAcc,
-                  (t > 0 || ks > 0) ? 1u : 0u);
-        }
+        // query columns 16 ks .. 16 ks + 15 sit at packed column 8 ks + 32 (ks / 4)
+        umma_ts_mnmajor_x8_split(tmem + d_col, tmem + a_col,
+                                 smem_desc_sw128(b_tile, C::kChunkBytes, 1024), kIdAcc,
+                                 t > 0 ? 1u : 0u);
         return true;
       };
       bool ok = warp_wait(bar(C::kKVFull), 0, &abort_flag, a.err);

@@ -178,12 +178,8 @@ __global__ void __launch_bounds__(320, 1)
         if (j >= 1 && !warp_wait(bar(C::kSEmpty), (j - 1) & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sK = sK0 + s * C::kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          umma_ss_w(tmem + C::kColS, smem_desc_sw128(sQ + off, 16, 1024),
-                  smem_desc_sw128(sK + off, 16, 1024), kIdSq, ks > 0);
-        }
+        umma_ss_kmajor_d<D>(tmem + C::kColS, smem_desc_sw128(sQ, 16, 1024),
+                            smem_desc_sw128(sK, 16, 1024), kIdSq, 0u);
         umma_commit_w(bar(C::kSFull));
         return true;
       };
@@ -193,12 +189,8 @@ __global__ void __launch_bounds__(320, 1)
         if (j >= 1 && !warp_wait(bar(C::kDPEmpty), (j - 1) & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sV = sV0 + s * C::kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          umma_ss_w(tmem + C::kColDP, smem_desc_sw128(sDO + off, 16, 1024),
-                  smem_desc_sw128(sV + off, 16, 1024), kIdSq, ks > 0);
-        }
+        umma_ss_kmajor_d<D>(tmem + C::kColDP, smem_desc_sw128(sDO, 16, 1024),
+                            smem_desc_sw128(sV, 16, 1024), kIdSq, 0u);
         umma_commit_w(bar(C::kDPFull));
         umma_commit_w(bar(C::kVEmpty + s));
         return true;
@@ -208,12 +200,8 @@ __global__ void __launch_bounds__(320, 1)
         if (!warp_wait(bar(C::kDSFull + db), (j >> 1) & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sK = sK0 + s * C::kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < kBlockN / 16; ++ks) {
-          umma_ts_w(tmem + C::kColDQ, tmem + C::kColDS + 64u * db + 8u * ks,
-                  smem_desc_sw128(sK + ks * 16 * 128, C::kChunkBytes, 1024), kIdDq,
-                  (j > 0 || ks > 0) ? 1u : 0u);
-        }
+        umma_ts_mnmajor_x8(tmem + C::kColDQ, tmem + C::kColDS + 64u * db,
+                           smem_desc_sw128(sK, C::kChunkBytes, 1024), kIdDq, j > 0 ? 1u : 0u);
         umma_commit_w(bar(C::kKEmpty + s));
         if (j == nkv - 1) umma_commit_w(bar(C::kDQDone));
         return true;

@@ -186,12 +186,8 @@ __global__ void __launch_bounds__(320, 1)
         if (!warp_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sK = sK0 + s * C::kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          umma_ss_w(tmem + C::kColS + 128u * sb, smem_desc_sw128(sQ + off, 16, 1024),
-                  smem_desc_sw128(sK + off, 16, 1024), kIdS, ks > 0);
-        }
+        umma_ss_kmajor_d<D>(tmem + C::kColS + 128u * sb, smem_desc_sw128(sQ, 16, 1024),
+                            smem_desc_sw128(sK, 16, 1024), kIdS, 0u);
         umma_commit_w(bar(C::kSFull + sb));
         umma_commit_w(bar(C::kKEmpty + s));
         return true;
@@ -202,12 +198,8 @@ __global__ void __launch_bounds__(320, 1)
         if (!warp_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sV = sV0 + s * C::kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < kBlockN / 16; ++ks) {
-          umma_ts_w(tmem + C::kColO, tmem + C::kColP + 64u * pb + 8u * ks,
-                  smem_desc_sw128(sV + ks * 16 * 128, C::kChunkBytes, 1024), kIdO,
-                  (j > 0 || ks > 0) ? 1u : 0u);
-        }
+        umma_ts_mnmajor_x8(tmem + C::kColO, tmem + C::kColP + 64u * pb,
+                           smem_desc_sw128(sV, C::kChunkBytes, 1024), kIdO, j > 0 ? 1u : 0u);
         umma_commit_w(bar(C::kPVDone + pb));
         umma_commit_w(bar(C::kVEmpty + s));
         return true;

@@ -273,6 +273,124 @@ __device__ __forceinline__ void umma_commit_w(uint32_t bar) {
       : "memory");
 }
 
+// 8 MMAs along K (16 each) with A and B both K-major, 128B-swizzled, 128-row tiles in shared
+// memory: K-step ks starts 32 bytes further inside a 64-column chunk, and every fourth step moves
+// to the next 16 KB chunk.  One elect.sync for the whole group; descriptor offsets (16-byte units)
+// are immediate adds.  The first MMA accumulates iff `accumulate`, the others always do.
+__device__ __forceinline__ void umma_ss_kmajor_x8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b64 ra, rb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %3, %3;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 1024;\n\tadd.s64 rb, %2, 1024;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 1026;\n\tadd.s64 rb, %2, 1026;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 1028;\n\tadd.s64 rb, %2, 1028;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 1030;\n\tadd.s64 rb, %2, 1030;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "}" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 4 MMAs along K (16 each) with A and B both K-major, 128B-swizzled, 128-row tiles in shared
+// memory: K-step ks starts 32 bytes further inside a 64-column chunk, and every fourth step moves
+// to the next 16 KB chunk.  One elect.sync for the whole group; descriptor offsets (16-byte units)
+// are immediate adds.  The first MMA accumulates iff `accumulate`, the others always do.
+__device__ __forceinline__ void umma_ss_kmajor_x4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b64 ra, rb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %3, %3;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "}" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// S-type product over the head dimension D (64 or 128): D / 16 MMAs.
+template <int D>
+__device__ __forceinline__ void umma_ss_kmajor_d(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  static_assert(D == 64 || D == 128, "head dim");
+  if constexpr (D == 128)
+    umma_ss_kmajor_x8(d_tmem, a_desc, b_desc, idesc, accumulate);
+  else
+    umma_ss_kmajor_x4(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+
+// 8 MMAs along K = 128 with A (bf16 pairs) in TMEM and B MN-major, 128B-swizzled in shared memory
+// (one 128-byte row per K index, so K-step ks starts 2048 bytes further).  A's K-step ks sits at
+// column 8 ks (contiguous packing) or 8 ks + 32 (ks / 4) (two 32-column halves 64 columns apart).
+__device__ __forceinline__ void umma_ts_mnmajor_x8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 ra;\n\t.reg .b64 rb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %3, %3;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.u32 ra, %1, 8;\n\tadd.s64 rb, %2, 128;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.u32 ra, %1, 16;\n\tadd.s64 rb, %2, 256;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.u32 ra, %1, 24;\n\tadd.s64 rb, %2, 384;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.u32 ra, %1, 32;\n\tadd.s64 rb, %2, 512;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.u32 ra, %1, 40;\n\tadd.s64 rb, %2, 640;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.u32 ra, %1, 48;\n\tadd.s64 rb, %2, 768;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.u32 ra, %1, 56;\n\tadd.s64 rb, %2, 896;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "}" ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_mnmajor_x8_split(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 ra;\n\t.reg .b64 rb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %3, %3;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.u32 ra, %1, 8;\n\tadd.s64 rb, %2, 128;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.u32 ra, %1, 16;\n\tadd.s64 rb, %2, 256;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.u32 ra, %1, 24;\n\tadd.s64 rb, %2, 384;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.u32 ra, %1, 64;\n\tadd.s64 rb, %2, 512;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.u32 ra, %1, 72;\n\tadd.s64 rb, %2, 640;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.u32 ra, %1, 80;\n\tadd.s64 rb, %2, 768;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.u32 ra, %1, 88;\n\tadd.s64 rb, %2, 896;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "}" ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // ------------------------------------------------------------------------------------------------
 // tcgen05: TMEM <-> registers, 32 lanes x 32 columns of 32 bits (one lane per thread of the warp).
 // A warp may only touch the 32-lane quarter (warp_id % 4) of TMEM.
