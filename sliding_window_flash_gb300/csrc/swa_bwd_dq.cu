@@ -1,7 +1,7 @@
 // swa_bwd_dq.cu — dQ of causal sliding-window attention on sm_103a.
 //
-// One CTA computes dQ for one 128-row query tile of one (batch, query head), walking only the key
-// blocks inside the tile's window (the same walk as the forward), and recomputing per block
+// A tile is one 128-row query block of one (batch, query head).  dQ for it walks only the key
+// blocks inside the tile's window (the same walk as the forward), recomputing per block
 //   S = Q K_j^T,  P = exp(scale S - LSE) (window-masked),  dP = dO V_j^T,  dS = P (dP - Delta),
 //   dQ += dS K_j,
 // with a final dQ *= scale.  dQ accumulates in TMEM (fp32) and is initialised by the first visited
@@ -10,9 +10,13 @@
 // at the store; S and dP stay fp32 in TMEM and only dS is rounded to bf16 as an MMA operand (the
 // lab's fp32-score-tile experiment showed the error of bf16 score scratch).
 //
+// The kernel is persistent: one CTA per SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// (heaviest first).  A tile's Q and dO are released as soon as its last dP has been computed, so
+// the next tile's Q, dO and first key blocks load while the current tile finishes.
+//
 // Warp roles (320 threads): warps 0-7 compute — warp w handles TMEM lanes 32(w%4)..+31 (query
 // rows) and columns [64 h, 64 h + 64) of every 128-column tile, h = w / 4, so each score row is
-// split over two threads; warp 8 TMA producer (Q and dO once, K_j and V_j through two
+// split over two threads; warp 8 TMA producer (Q and dO per tile, K_j and V_j through two
 // shared-memory rings); warp 9 MMA issuer and TMEM owner.  dS goes back to TMEM (two buffers)
 // and is the A operand of dQ += dS K_j.
 // TMEM columns: [0,128) S, [128,256) dP, [256, 256+D) dQ, [256+D, 384+D) dS x 2 (bf16 pairs).
@@ -36,7 +40,8 @@ struct DqCfg {
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kQDFull = 0;
-  static constexpr int kKFull = 1;
+  static constexpr int kQDEmpty = 1;
+  static constexpr int kKFull = 2;
   static constexpr int kKEmpty = kKFull + kKStages;
   static constexpr int kVFull = kKEmpty + kKStages;
   static constexpr int kVEmpty = kVFull + kVStages;
@@ -45,9 +50,9 @@ struct DqCfg {
   static constexpr int kDPFull = kSEmpty + 1;
   static constexpr int kDPEmpty = kDPFull + 1;
   static constexpr int kDSFull = kDPEmpty + 1;  // 2 (one per dS buffer)
-  static constexpr int kDQDone = kDSFull + 2;
-  static constexpr int kOutFull = kDQDone + 1;  // staged dQ tile complete (one arrival per warp)
-  static constexpr int kDrain = kOutFull + 1;
+  static constexpr int kDQDone = kDSFull + 2;   // a tile's last dQ MMA has completed
+  static constexpr int kDQEmpty = kDQDone + 1;  // the epilogue has read the dQ accumulator
+  static constexpr int kDrain = kDQEmpty + 1;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
@@ -60,16 +65,32 @@ struct DqArgs {
   const float* lse;
   const float* delta;
   __nv_bfloat16* dq;
-  int BH, Hq, Hkv, G, N, W, nqb;
+  int BH, Hq, Hkv, G, N, W, nqb, ntiles;
   float scale, scale_log2;
   unsigned* err;
 };
+
+struct DqTile {
+  int bh, bhk, q0, kb_lo, nkv;
+};
+
+// Tile t: heaviest query blocks first (the causal case gives later blocks more key blocks).
+__device__ __forceinline__ DqTile dq_tile(int t, const DqArgs& a) {
+  DqTile f;
+  const int qb = a.nqb - 1 - t / a.BH;
+  f.bh = t % a.BH;
+  f.bhk = (f.bh / a.Hq) * a.Hkv + (f.bh % a.Hq) / a.G;
+  f.q0 = qb * kBlockM;
+  f.kb_lo = fwd_first_kblock(f.q0, a.W);
+  f.nkv = fwd_last_kblock(f.q0, a.N) - f.kb_lo + 1;
+  return f;
+}
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     swa_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_dq, const DqArgs a) {
+                  const DqArgs a) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -81,20 +102,13 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t sDO = smem_u32(smem + C::kOffDO);
   const uint32_t sK0 = smem_u32(smem + C::kOffK);
   const uint32_t sV0 = smem_u32(smem + C::kOffV);
-
-  const int qb = a.nqb - 1 - static_cast<int>(blockIdx.x) / a.BH;
-  const int bh = static_cast<int>(blockIdx.x) % a.BH;
-  const int hq = bh % a.Hq;
-  const int bhk = (bh / a.Hq) * a.Hkv + hq / a.G;
-  const int q0 = qb * kBlockM;
-  const int kb_lo = fwd_first_kblock(q0, a.W);
-  const int kb_hi = fwd_last_kblock(q0, a.N);
-  const int nkv = kb_hi - kb_lo + 1;
+  const int tile_step = static_cast<int>(gridDim.x);
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(bar(C::kQDFull), 1);
+    mbar_init(bar(C::kQDEmpty), 1);
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bar(C::kKFull + s), 1);
       mbar_init(bar(C::kKEmpty + s), 1);
@@ -110,7 +124,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar(C::kDSFull + 0), C::kComputeThreads / 32);
     mbar_init(bar(C::kDSFull + 1), C::kComputeThreads / 32);
     mbar_init(bar(C::kDQDone), 1);
-    mbar_init(bar(C::kOutFull), C::kComputeThreads / 32);
+    mbar_init(bar(C::kDQEmpty), C::kComputeThreads / 32);
     mbar_init(bar(C::kDrain), 1);
     fence_barrier_init();
   }
@@ -130,34 +144,45 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tm_do);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar(C::kQDFull), 2 * C::kTileBytes);
-      for (int h = 0; h < C::kChunks; ++h) {
-        tma_load_3d(sQ + h * C::kChunkBytes, &tm_q, bar(C::kQDFull), 64 * h, q0, bh);
-        tma_load_3d(sDO + h * C::kChunkBytes, &tm_do, bar(C::kQDFull), 64 * h, q0, bh);
-      }
+      int last_qd = -1;
       int last_k[C::kKStages], last_v[C::kVStages];
       for (int s = 0; s < C::kKStages; ++s) last_k[s] = -1;
       for (int s = 0; s < C::kVStages; ++s) last_v[s] = -1;
-      for (int j = 0; j < nkv; ++j) {
-        const int k0 = (kb_lo + j) * kBlockN;
-        const int sk = j % C::kKStages, nk = j / C::kKStages;
-        if (j >= C::kKStages && !mbar_wait(bar(C::kKEmpty + sk), (nk - 1) & 1, &abort_flag, a.err))
-          break;
-        const uint32_t sK = sK0 + sk * C::kTileBytes;
-        mbar_arrive_expect_tx(bar(C::kKFull + sk), C::kTileBytes);
-        for (int h = 0; h < C::kChunks; ++h)
-          tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKFull + sk), 64 * h, k0, bhk);
-        last_k[sk] = j;
-        const int sv = j % C::kVStages, nv = j / C::kVStages;
-        if (j >= C::kVStages && !mbar_wait(bar(C::kVEmpty + sv), (nv - 1) & 1, &abort_flag, a.err))
-          break;
-        const uint32_t sV = sV0 + sv * C::kTileBytes;
-        mbar_arrive_expect_tx(bar(C::kVFull + sv), C::kTileBytes);
-        for (int h = 0; h < C::kChunks; ++h)
-          tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kVFull + sv), 64 * h, k0, bhk);
-        last_v[sv] = j;
+      int g = 0;  // key blocks loaded so far by this CTA
+      bool ok = true;
+      for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
+        const DqTile f = dq_tile(t, a);
+        // Q / dO of the previous tile are free once its last dP has been computed.
+        if (it >= 1 && !mbar_wait(bar(C::kQDEmpty), (it - 1) & 1, &abort_flag, a.err)) break;
+        mbar_arrive_expect_tx(bar(C::kQDFull), 2 * C::kTileBytes);
+        for (int h = 0; h < C::kChunks; ++h) {
+          tma_load_3d(sQ + h * C::kChunkBytes, &tm_q, bar(C::kQDFull), 64 * h, f.q0, f.bh);
+          tma_load_3d(sDO + h * C::kChunkBytes, &tm_do, bar(C::kQDFull), 64 * h, f.q0, f.bh);
+        }
+        last_qd = it;
+        for (int j = 0; j < f.nkv; ++j, ++g) {
+          const int k0 = (f.kb_lo + j) * kBlockN;
+          const int sk = g % C::kKStages, nk = g / C::kKStages;
+          if (g >= C::kKStages &&
+              !(ok = mbar_wait(bar(C::kKEmpty + sk), (nk - 1) & 1, &abort_flag, a.err)))
+            break;
+          const uint32_t sK = sK0 + sk * C::kTileBytes;
+          mbar_arrive_expect_tx(bar(C::kKFull + sk), C::kTileBytes);
+          for (int h = 0; h < C::kChunks; ++h)
+            tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKFull + sk), 64 * h, k0, f.bhk);
+          last_k[sk] = g;
+          const int sv = g % C::kVStages, nv = g / C::kVStages;
+          if (g >= C::kVStages &&
+              !(ok = mbar_wait(bar(C::kVEmpty + sv), (nv - 1) & 1, &abort_flag, a.err)))
+            break;
+          const uint32_t sV = sV0 + sv * C::kTileBytes;
+          mbar_arrive_expect_tx(bar(C::kVFull + sv), C::kTileBytes);
+          for (int h = 0; h < C::kChunks; ++h)
+            tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kVFull + sv), 64 * h, k0, f.bhk);
+          last_v[sv] = g;
+        }
       }
-      drain_wait(bar(C::kQDFull), 0, a.err);
+      if (last_qd >= 0) drain_wait(bar(C::kQDFull), last_qd & 1, a.err);
       for (int s = 0; s < C::kKStages; ++s)
         if (last_k[s] >= 0) drain_wait(bar(C::kKFull + s), (last_k[s] / C::kKStages) & 1, a.err);
       for (int s = 0; s < C::kVStages; ++s)
@@ -165,127 +190,142 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
-    // Issue order S_0, dP_0, then per block j: S_{j+1}, dP_{j+1}, dQ += dS_j K_j.  The next block's
-    // S and dP are computed as soon as the compute warps have read this block's, so they never wait
-    // on dQ_j.  dS alternates between two TMEM buffers: dP_{j+2} runs after dQ_j, so when the
-    // compute warps see dP_{j+2} the buffer of dS_j is free again.
-    {  // the whole warp, converged; one elected lane issues
-      constexpr uint32_t kIdSq = idesc_bf16(kBlockM, kBlockN, false, false);  // S, dP
-      constexpr uint32_t kIdDq = idesc_bf16(kBlockM, D, false, true);         // dQ += dS K
-      auto issue_s = [&](int j) -> bool {  // S = Q K_j^T
-        const int s = j % C::kKStages, n = j / C::kKStages;
-        if (!warp_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
-        if (j >= 1 && !warp_wait(bar(C::kSEmpty), (j - 1) & 1, &abort_flag, a.err)) return false;
-        tc_fence_after();
-        const uint32_t sK = sK0 + s * C::kTileBytes;
-        umma_ss_kmajor_d<D>(tmem + C::kColS, smem_desc_sw128(sQ, 16, 1024),
-                            smem_desc_sw128(sK, 16, 1024), kIdSq, 0u);
-        umma_commit_w(bar(C::kSFull));
-        return true;
-      };
-      auto issue_dp = [&](int j) -> bool {  // dP = dO V_j^T once dP_{j-1} has been read
-        const int s = j % C::kVStages, n = j / C::kVStages;
-        if (!warp_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
-        if (j >= 1 && !warp_wait(bar(C::kDPEmpty), (j - 1) & 1, &abort_flag, a.err)) return false;
-        tc_fence_after();
-        const uint32_t sV = sV0 + s * C::kTileBytes;
-        umma_ss_kmajor_d<D>(tmem + C::kColDP, smem_desc_sw128(sDO, 16, 1024),
-                            smem_desc_sw128(sV, 16, 1024), kIdSq, 0u);
-        umma_commit_w(bar(C::kDPFull));
-        umma_commit_w(bar(C::kVEmpty + s));
-        return true;
-      };
-      auto issue_dq = [&](int j) -> bool {  // dQ += dS K_j  (dS from TMEM, K_j as MN-major B)
-        const int s = j % C::kKStages, db = j & 1;
-        if (!warp_wait(bar(C::kDSFull + db), (j >> 1) & 1, &abort_flag, a.err)) return false;
-        tc_fence_after();
-        const uint32_t sK = sK0 + s * C::kTileBytes;
-        umma_ts_mnmajor_x8(tmem + C::kColDQ, tmem + C::kColDS + 64u * db,
-                           smem_desc_sw128(sK, C::kChunkBytes, 1024), kIdDq, j > 0 ? 1u : 0u);
-        umma_commit_w(bar(C::kKEmpty + s));
-        if (j == nkv - 1) umma_commit_w(bar(C::kDQDone));
-        return true;
-      };
-      bool ok = warp_wait(bar(C::kQDFull), 0, &abort_flag, a.err);
-      if (ok) ok = issue_s(0);
-      if (ok) ok = issue_dp(0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        if (j + 1 < nkv) {
-          ok = issue_s(j + 1);
-          if (ok) ok = issue_dp(j + 1);
+    // Per tile: S_0, dP_0, then per block j: S_{j+1}, dP_{j+1}, dQ += dS_j K_j.  The next block's
+    // S and dP are computed as soon as the compute warps have read this block's, so they never
+    // wait on dQ_j.  dS alternates between two TMEM buffers: dP_{g+2} runs after dQ_g, so when the
+    // compute warps see dP_{g+2} the buffer of dS_g is free again.  Block counters run across tiles.
+    constexpr uint32_t kIdSq = idesc_bf16(kBlockM, kBlockN, false, false);  // S, dP
+    constexpr uint32_t kIdDq = idesc_bf16(kBlockM, D, false, true);         // dQ += dS K
+    auto issue_s = [&](int gg) -> bool {  // S = Q K_gg^T once S_{gg-1} has been read
+      const int s = gg % C::kKStages, n = gg / C::kKStages;
+      if (!warp_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
+      if (gg >= 1 && !warp_wait(bar(C::kSEmpty), (gg - 1) & 1, &abort_flag, a.err)) return false;
+      tc_fence_after();
+      umma_ss_kmajor_d<D>(tmem + C::kColS, smem_desc_sw128(sQ, 16, 1024),
+                          smem_desc_sw128(sK0 + s * C::kTileBytes, 16, 1024), kIdSq, 0u);
+      umma_commit_w(bar(C::kSFull));
+      return true;
+    };
+    auto issue_dp = [&](int gg, bool tile_last) -> bool {  // dP = dO V_gg^T once dP_{gg-1} read
+      const int s = gg % C::kVStages, n = gg / C::kVStages;
+      if (!warp_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
+      if (gg >= 1 && !warp_wait(bar(C::kDPEmpty), (gg - 1) & 1, &abort_flag, a.err)) return false;
+      tc_fence_after();
+      umma_ss_kmajor_d<D>(tmem + C::kColDP, smem_desc_sw128(sDO, 16, 1024),
+                          smem_desc_sw128(sV0 + s * C::kTileBytes, 16, 1024), kIdSq, 0u);
+      umma_commit_w(bar(C::kDPFull));
+      umma_commit_w(bar(C::kVEmpty + s));
+      if (tile_last) umma_commit_w(bar(C::kQDEmpty));  // every S and dP of the tile is issued
+      return true;
+    };
+    auto issue_dq = [&](int gg, bool first, bool tile_last) -> bool {  // dQ += dS K_gg
+      const int s = gg % C::kKStages, db = gg & 1;
+      if (!warp_wait(bar(C::kDSFull + db), (gg >> 1) & 1, &abort_flag, a.err)) return false;
+      tc_fence_after();
+      umma_ts_mnmajor_x8(tmem + C::kColDQ, tmem + C::kColDS + 64u * db,
+                         smem_desc_sw128(sK0 + s * C::kTileBytes, C::kChunkBytes, 1024), kIdDq,
+                         first ? 0u : 1u);
+      umma_commit_w(bar(C::kKEmpty + s));
+      if (tile_last) umma_commit_w(bar(C::kDQDone));
+      return true;
+    };
+    int g = 0;  // key blocks issued so far by this CTA
+    bool ok = true;
+    for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
+      const DqTile f = dq_tile(t, a);
+      const int n = f.nkv;
+      ok = warp_wait(bar(C::kQDFull), it & 1, &abort_flag, a.err);
+      if (ok) ok = issue_s(g);
+      if (ok) ok = issue_dp(g, n == 1);
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n) {
+          ok = issue_s(g + j + 1);
+          if (ok) ok = issue_dp(g + j + 1, j + 2 == n);
         }
-        if (ok) ok = issue_dq(j);
+        // The first dQ of a tile overwrites the accumulator: the previous tile's epilogue must
+        // have read it.
+        if (ok && j == 0 && it > 0)
+          ok = warp_wait(bar(C::kDQEmpty), (it - 1) & 1, &abort_flag, a.err);
+        if (ok) ok = issue_dq(g + j, j == 0, j + 1 == n);
       }
-      umma_commit_w(bar(C::kDrain));
-      warp_drain_wait(bar(C::kDrain), 0, a.err);
+      g += n;
     }
+    umma_commit_w(bar(C::kDrain));
+    warp_drain_wait(bar(C::kDrain), 0, a.err);
   } else {
     // ------------------------------------------------------------------ compute (warps 0-7)
     const int r = static_cast<int>(threadIdx.x & 127);  // query row within the tile = TMEM lane
     const uint32_t h = warp >> 2;                          // column half of every tile
-    const int row = q0 + r;
-    const bool in_range = row < a.N;
-    const size_t grow = static_cast<size_t>(bh) * a.N + row;
     const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
-    // Rows past the end see P = 0 (their LSE is taken as +inf), so they add nothing.
-    const float lse2 = in_range ? a.lse[grow] * kLog2e : SWA_POS_INF;
-    const float dlt = in_range ? a.delta[grow] : 0.f;
     const float sl2 = a.scale_log2;
+    int g = 0;  // key blocks consumed so far by this CTA
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int k0 = (kb_lo + j) * kBlockN;
-      if (!(ok = warp_wait(bar(C::kSFull), j & 1, &abort_flag, a.err))) break;
-      tc_fence_after();
-      float p[64];
-      {
-        uint32_t rr[2][32];
-        tmem_ld32(tmem + lane_base + C::kColS + 64u * h, rr[0]);
-        tmem_ld32(tmem + lane_base + C::kColS + 64u * h + 32u, rr[1]);
-        tmem_wait_ld_all();
-        reg_fence(rr[0]);
-        reg_fence(rr[1]);
+    for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
+      const DqTile f = dq_tile(t, a);
+      const int q0 = f.q0;
+      const int row = q0 + r;
+      const bool in_range = row < a.N;
+      const size_t grow = static_cast<size_t>(f.bh) * a.N + row;
+      // Rows past the end see P = 0 (their LSE is taken as +inf), so they add nothing.
+      const float lse2 = in_range ? a.lse[grow] * kLog2e : SWA_POS_INF;
+      const float dlt = in_range ? a.delta[grow] : 0.f;
+      for (int j = 0; j < f.nkv; ++j) {
+        const int gg = g + j;
+        const int k0 = (f.kb_lo + j) * kBlockN;
+        if (!(ok = warp_wait(bar(C::kSFull), gg & 1, &abort_flag, a.err))) break;
+        tc_fence_after();
+        float p[64];
+        {
+          uint32_t rr[2][32];
+          tmem_ld32(tmem + lane_base + C::kColS + 64u * h, rr[0]);
+          tmem_ld32(tmem + lane_base + C::kColS + 64u * h + 32u, rr[1]);
+          tmem_wait_ld_all();
+          reg_fence(rr[0]);
+          reg_fence(rr[1]);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) p[i] = __uint_as_float(rr[i >> 5][i & 31]);
-      }
-      warp_arrive(bar(C::kSEmpty));
-#pragma unroll
-      for (int c = 0; c < 64; ++c) p[c] = ex2(fmaf(p[c], sl2, -lse2));
-      const bool interior = (k0 + kBlockN - 1 <= q0) && (q0 + kBlockM - 1 - k0 < a.W);
-      if (!interior) {
-        const int lo = row - a.W + 1 - k0 - 64 * static_cast<int>(h);
-        const int hi = row - k0 - 64 * static_cast<int>(h);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
-      }
-
-      // dP_j landing also means dQ_{j-2} has finished reading dS buffer (j & 1).
-      if (!(ok = warp_wait(bar(C::kDPFull), j & 1, &abort_flag, a.err))) break;
-      tc_fence_after();
-      {
-        uint32_t rr[2][32];
-        tmem_ld32(tmem + lane_base + C::kColDP + 64u * h, rr[0]);
-        tmem_ld32(tmem + lane_base + C::kColDP + 64u * h + 32u, rr[1]);
-        tmem_wait_ld_all();
-        reg_fence(rr[0]);
-        reg_fence(rr[1]);
-        warp_arrive(bar(C::kDPEmpty));
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint32_t d0 = rr[i >> 4][(2 * i) & 31], d1 = rr[i >> 4][(2 * i + 1) & 31];
-          pk[i] = pack_bf16x2(p[2 * i] * (__uint_as_float(d0) - dlt),
-                              p[2 * i + 1] * (__uint_as_float(d1) - dlt));
+          for (int i = 0; i < 64; ++i) p[i] = __uint_as_float(rr[i >> 5][i & 31]);
         }
-        // dS columns [64h, 64h+64) -> packed TMEM columns [32h, 32h+32) of dS buffer (j & 1).
-        tmem_st32(tmem + lane_base + C::kColDS + 64u * (j & 1) + 32u * h, pk);
+        warp_arrive(bar(C::kSEmpty));
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p[c] = ex2(fmaf(p[c], sl2, -lse2));
+        const bool interior = (k0 + kBlockN - 1 <= q0) && (q0 + kBlockM - 1 - k0 < a.W);
+        if (!interior) {
+          const int lo = row - a.W + 1 - k0 - 64 * static_cast<int>(h);
+          const int hi = row - k0 - 64 * static_cast<int>(h);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
+        }
+
+        // dP_gg landing also means dQ_{gg-2} has finished reading dS buffer (gg & 1).
+        if (!(ok = warp_wait(bar(C::kDPFull), gg & 1, &abort_flag, a.err))) break;
+        tc_fence_after();
+        {
+          uint32_t rr[2][32];
+          tmem_ld32(tmem + lane_base + C::kColDP + 64u * h, rr[0]);
+          tmem_ld32(tmem + lane_base + C::kColDP + 64u * h + 32u, rr[1]);
+          tmem_wait_ld_all();
+          reg_fence(rr[0]);
+          reg_fence(rr[1]);
+          warp_arrive(bar(C::kDPEmpty));
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const uint32_t d0 = rr[i >> 4][(2 * i) & 31], d1 = rr[i >> 4][(2 * i + 1) & 31];
+            pk[i] = pack_bf16x2(p[2 * i] * (__uint_as_float(d0) - dlt),
+                                p[2 * i + 1] * (__uint_as_float(d1) - dlt));
+          }
+          // dS columns [64h, 64h+64) -> packed TMEM columns [32h, 32h+32) of dS buffer (gg & 1).
+          tmem_st32(tmem + lane_base + C::kColDS + 64u * (gg & 1) + 32u * h, pk);
+        }
+        tmem_wait_st();
+        warp_arrive(bar(C::kDSFull + (gg & 1)));
       }
-      tmem_wait_st();
-      warp_arrive(bar(C::kDSFull + (j & 1)));
-    }
-    if (ok && warp_wait(bar(C::kDQDone), 0, &abort_flag, a.err)) {
+      if (!ok) break;
+      g += f.nkv;
+
+      // ---------------------------------------------------------------- tile epilogue
+      if (!(ok = warp_wait(bar(C::kDQDone), it & 1, &abort_flag, a.err))) break;
       tc_fence_after();
-      // dQ * scale -> bf16, staged in the Q tile (free: every MMA has completed) and written with
-      // one tensor store per 64-column chunk (rows past N are not written).
       constexpr int kHalf = D / 2;
       uint32_t rr[kHalf / 32][32];
 #pragma unroll
@@ -293,23 +333,24 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32(tmem + lane_base + C::kColDQ + kHalf * h + 32u * c4, rr[c4]);
       tmem_wait_ld_all();
 #pragma unroll
-      for (int c4 = 0; c4 < kHalf / 32; ++c4) {
-        reg_fence(rr[c4]);
-        uint32_t pk[16];
+      for (int c4 = 0; c4 < kHalf / 32; ++c4) reg_fence(rr[c4]);
+      warp_arrive(bar(C::kDQEmpty));  // the next tile's first dQ may overwrite the accumulator
+      // dQ * scale -> bf16, written straight from registers: each thread owns 64 or 128
+      // contiguous bytes of its row; the stores drain while the next tile runs.
+      if (in_range) {
+        __nv_bfloat16* dst_row = a.dq + grow * D + kHalf * h;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(rr[c4][2 * i]) * a.scale,
-                              __uint_as_float(rr[c4][2 * i + 1]) * a.scale);
-        stage_row32_sw128(sQ, r, kHalf * h + 32u * c4, pk);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::kOutFull));
-      if (warp == 0 && warp_wait(bar(C::kOutFull), 0, &abort_flag, a.err) && lane == 0) {
-        for (int hh = 0; hh < C::kChunks; ++hh)
-          tma_store_3d(&tm_dq, sQ + hh * C::kChunkBytes, 64 * hh, q0, bh);
-        bulk_commit_group();
-        bulk_wait_group_read0();
+        for (int c4 = 0; c4 < kHalf / 32; ++c4) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(rr[c4][2 * i]) * a.scale,
+                                __uint_as_float(rr[c4][2 * i + 1]) * a.scale);
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c4);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
       }
     }
   }
@@ -327,13 +368,12 @@ cudaError_t launch_dq_d(const Problem& pb, const void* q, const void* k, const v
                         const void* dO, const float* lse, const float* delta, void* dq,
                         cudaStream_t stream) {
   using C = DqCfg<D>;
-  CUtensorMap tq, tdo, tk, tv, tdq;
+  CUtensorMap tq, tdo, tk, tv;
   const uint64_t bhq = static_cast<uint64_t>(pb.B) * pb.Hq, bhk = static_cast<uint64_t>(pb.B) * pb.Hkv;
   if (!make_tmap_bf16_3d(&tq, q, bhq, pb.N, D, kBlockM) ||
       !make_tmap_bf16_3d(&tdo, dO, bhq, pb.N, D, kBlockM) ||
       !make_tmap_bf16_3d(&tk, k, bhk, pb.N, D, kBlockN) ||
-      !make_tmap_bf16_3d(&tv, v, bhk, pb.N, D, kBlockN) ||
-      !make_tmap_bf16_3d(&tdq, dq, bhq, pb.N, D, kBlockM))
+      !make_tmap_bf16_3d(&tv, v, bhk, pb.N, D, kBlockN))
     return cudaErrorInvalidValue;
   auto kern = swa_dq_kernel<D>;
   cudaError_t e =
@@ -350,11 +390,12 @@ cudaError_t launch_dq_d(const Problem& pb, const void* q, const void* k, const v
   a.N = pb.N;
   a.W = pb.W;
   a.nqb = (pb.N + kBlockM - 1) / kBlockM;
+  a.ntiles = a.nqb * a.BH;
   a.scale = pb.scale;
   a.scale_log2 = pb.scale * kLog2e;
   a.err = pb.err;
-  const unsigned grid = static_cast<unsigned>(a.nqb) * static_cast<unsigned>(a.BH);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tdo, tk, tv, tdq, a);
+  const int grid = a.ntiles < sm_count() ? a.ntiles : sm_count();
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tdo, tk, tv, a);
   return cudaGetLastError();
 }
 

@@ -435,19 +435,6 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
-int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
 template <int D>
 cudaError_t launch_fwd_d(const Problem& pb, const void* q, const void* k, const void* v, void* o,
                          float* lse, cudaStream_t stream) {

@@ -35,6 +35,21 @@ __host__ __device__ inline int bwd_last_qblock(int k0, int N, int W) {
   return static_cast<int>((hi < N - 1 ? hi : N - 1) / kBlockM);
 }
 
+// Streaming multiprocessors of the current device (cached per device); persistent kernels launch
+// one CTA per SM.
+inline int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 // Launchers (each returns the launch's cudaError_t).
 cudaError_t launch_fwd(const Problem& pb, const void* q, const void* k, const void* v, void* o,
                        float* lse, cudaStream_t stream);
