@@ -48,7 +48,9 @@ typedef enum {
     SWA_ERR_MISALIGNED = 3,     /* a tensor pointer not 16-byte aligned                          */
     SWA_ERR_CUDA = 4,           /* a CUDA runtime / driver call or a launch failed               */
     SWA_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait ran out (reported by swa_check_device) */
-    SWA_ERR_WORKSPACE = 6       /* backward workspace null or smaller than required              */
+    SWA_ERR_WORKSPACE = 6,      /* backward workspace null or smaller than required              */
+    SWA_ERR_DEVICE_LAYOUT = 7   /* a kernel found its shared memory not 1024-byte aligned and did
+                                   no work (reported by swa_check_device)                        */
 } swa_status;
 
 /*
@@ -143,8 +145,10 @@ const char* swa_strerror(swa_status status);
 
 /*
  * Synchronizes `stream`, then reads and clears the current device's error word, which a kernel
- * sets when one of its bounded waits runs out.  Returns SWA_ERR_DEVICE_TIMEOUT if it was set,
- * SWA_ERR_CUDA if the synchronize failed, else SWA_OK.
+ * sets when one of its bounded waits runs out (or when it finds its dynamic shared memory not
+ * 1024-byte aligned, which the 128-byte-swizzled tiles need; it then returns without work).
+ * Returns SWA_ERR_DEVICE_LAYOUT or SWA_ERR_DEVICE_TIMEOUT if the word was set, SWA_ERR_CUDA if
+ * the synchronize failed, else SWA_OK.
  */
 swa_status swa_check_device(cudaStream_t stream);
 

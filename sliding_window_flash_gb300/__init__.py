@@ -45,6 +45,7 @@ STATUS = {
     4: "SWA_ERR_CUDA",
     5: "SWA_ERR_DEVICE_TIMEOUT",
     6: "SWA_ERR_WORKSPACE",
+    7: "SWA_ERR_DEVICE_LAYOUT",
 }
 
 # Every symbol include/swa_attn.h declares, with its ctypes signature.

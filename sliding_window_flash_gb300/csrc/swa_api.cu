@@ -181,6 +181,8 @@ const char* swa_strerror(swa_status status) {
     case SWA_ERR_CUDA: return "SWA_ERR_CUDA: CUDA call or kernel launch failed";
     case SWA_ERR_DEVICE_TIMEOUT: return "SWA_ERR_DEVICE_TIMEOUT: a kernel's bounded wait ran out";
     case SWA_ERR_WORKSPACE: return "SWA_ERR_WORKSPACE: workspace null or too small";
+    case SWA_ERR_DEVICE_LAYOUT:
+      return "SWA_ERR_DEVICE_LAYOUT: a kernel's shared memory was not 1024-byte aligned";
   }
   return "SWA_ERR_UNKNOWN";
 }
@@ -197,7 +199,7 @@ swa_status swa_check_device(cudaStream_t stream) {
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(g_swa_error_word, &zero, sizeof(zero)) != cudaSuccess)
       return SWA_ERR_CUDA;
-    return SWA_ERR_DEVICE_TIMEOUT;
+    return (word & swa::kErrSmemLayout) ? SWA_ERR_DEVICE_LAYOUT : SWA_ERR_DEVICE_TIMEOUT;
   }
   return SWA_OK;
 }

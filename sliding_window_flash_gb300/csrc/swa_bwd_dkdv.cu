@@ -11,9 +11,10 @@
 // disclosure": tiles wholly outside the window are skipped, edge tiles are masked, and dK / dV of
 // a key tile that no query visits are still written (as zeros).
 //
-// Warp roles (320 threads): warps 0-7 compute — warp w handles TMEM lanes 32(w%4)..+31 (key rows)
-// and query columns [64 h, 64 h + 64) of every tile, h = w / 4; warp 8 TMA producer (K and V once;
-// Q_t and dO_t through two shared-memory rings); warp 9 MMA issuer and TMEM owner.  P^T and dS^T go
+// Warp roles (352 threads): warps 0-7 compute — warp w handles TMEM lanes 32(w%4)..+31 (key rows)
+// and query columns [64 h, 64 h + 64) of every tile, h = w / 4; warp 8 TMA producer of K (once)
+// and of the Q_t ring, warp 10 of V (once) and of the dO_t ring — two issuing warps, because one
+// warp's TMA copies complete at only ~40 B/clk on this GPU; warp 9 MMA issuer and TMEM owner.  P^T and dS^T go
 // back to TMEM as bf16 pairs, each half over the first 32 of the 64 S^T / dP^T columns it read, and
 // are the A operands of dV += P^T dO and dK += dS^T Q.  TMEM columns: [0,128) S^T / P^T,
 // [128,256) dP^T / dS^T, [256, 256+D) dK, [256+D, 256+2D) dV.
@@ -29,7 +30,7 @@ struct DkdvCfg {
   static constexpr int kTileBytes = kBlockM * D * 2;
   static constexpr int kChunkBytes = kBlockM * 128;
   static constexpr int kChunks = D / 64;
-  static constexpr int kQStages = (D == 128) ? 2 : 4;
+  static constexpr int kQStages = (D == 128) ? 3 : 4;
   static constexpr int kDOStages = (D == 128) ? 2 : 4;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
@@ -52,11 +53,12 @@ struct DkdvCfg {
   static constexpr int kOutFull = kDone + 1;  // staged dK / dV tiles complete (one arrival per warp)
   static constexpr int kDrain = kOutFull + 1;
   static constexpr int kNumBars = kDrain + 1;
-  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;  // + TMEM address and abort flag
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
   // P^T is written over the first 64 columns of S^T, dS^T over the first 64 of dP^T.
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 256 + D;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
   static constexpr int kComputeThreads = 256;
 };
 
@@ -71,7 +73,7 @@ struct DkdvArgs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     swa_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -79,12 +81,13 @@ __global__ void __launch_bounds__(320, 1)
                     const __grid_constant__ CUtensorMap tm_dk,
                     const __grid_constant__ CUtensorMap tm_dv, const DkdvArgs a) {
   using C = DkdvCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (!smem_base_ok(smem, a.err)) return;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   float* s_rows = reinterpret_cast<float*>(smem + C::kOffRow);  // [slot][lse2 | delta][128]
-  __shared__ int abort_flag;
+  int& abort_flag = *reinterpret_cast<int*>(tmem_slot + 1);  // raised by a failed wait
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t sK = smem_u32(smem + C::kOffK);
   const uint32_t sV = smem_u32(smem + C::kOffV);
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    mbar_init(bar(C::kKVFull), 1);
+    mbar_init(bar(C::kKVFull), 2);  // one arrival per producer warp
     for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(bar(C::kQFull + s), 1);
       mbar_init(bar(C::kQEmpty + s), 1);
@@ -136,30 +139,41 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 8) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------------ TMA producer (K, Q ring)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_do);
       tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar(C::kKVFull), 2 * C::kTileBytes);
-      for (int h = 0; h < C::kChunks; ++h) {
+      mbar_arrive_expect_tx(bar(C::kKVFull), C::kTileBytes);
+      for (int h = 0; h < C::kChunks; ++h)
         tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKVFull), 64 * h, k0, bhk);
-        tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kKVFull), 64 * h, k0, bhk);
-      }
-      int last_q[C::kQStages], last_do[C::kDOStages];
+      int last_q[C::kQStages];
       for (int s = 0; s < C::kQStages; ++s) last_q[s] = -1;
-      for (int s = 0; s < C::kDOStages; ++s) last_do[s] = -1;
       for (int t = 0; t < T; ++t) {
-        const int q0 = tile_q0(t), bhq = tile_bhq(t);
         const int sq = t % C::kQStages, nqs = t / C::kQStages;
         if (t >= C::kQStages && !mbar_wait(bar(C::kQEmpty + sq), (nqs - 1) & 1, &abort_flag, a.err))
           break;
         const uint32_t sQ = sQ0 + sq * C::kTileBytes;
         mbar_arrive_expect_tx(bar(C::kQFull + sq), C::kTileBytes);
         for (int h = 0; h < C::kChunks; ++h)
-          tma_load_3d(sQ + h * C::kChunkBytes, &tm_q, bar(C::kQFull + sq), 64 * h, q0, bhq);
+          tma_load_3d(sQ + h * C::kChunkBytes, &tm_q, bar(C::kQFull + sq), 64 * h, tile_q0(t),
+                      tile_bhq(t));
         last_q[sq] = t;
+      }
+      drain_wait(bar(C::kKVFull), 0, a.err);
+      for (int s = 0; s < C::kQStages; ++s)
+        if (last_q[s] >= 0) drain_wait(bar(C::kQFull + s), (last_q[s] / C::kQStages) & 1, a.err);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------------ TMA producer (V, dO ring)
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar(C::kKVFull), C::kTileBytes);
+      for (int h = 0; h < C::kChunks; ++h)
+        tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kKVFull), 64 * h, k0, bhk);
+      int last_do[C::kDOStages];
+      for (int s = 0; s < C::kDOStages; ++s) last_do[s] = -1;
+      for (int t = 0; t < T; ++t) {
         const int sd = t % C::kDOStages, nds = t / C::kDOStages;
         if (t >= C::kDOStages &&
             !mbar_wait(bar(C::kDOEmpty + sd), (nds - 1) & 1, &abort_flag, a.err))
@@ -167,12 +181,11 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t sDO = sDO0 + sd * C::kTileBytes;
         mbar_arrive_expect_tx(bar(C::kDOFull + sd), C::kTileBytes);
         for (int h = 0; h < C::kChunks; ++h)
-          tma_load_3d(sDO + h * C::kChunkBytes, &tm_do, bar(C::kDOFull + sd), 64 * h, q0, bhq);
+          tma_load_3d(sDO + h * C::kChunkBytes, &tm_do, bar(C::kDOFull + sd), 64 * h, tile_q0(t),
+                      tile_bhq(t));
         last_do[sd] = t;
       }
       drain_wait(bar(C::kKVFull), 0, a.err);
-      for (int s = 0; s < C::kQStages; ++s)
-        if (last_q[s] >= 0) drain_wait(bar(C::kQFull + s), (last_q[s] / C::kQStages) & 1, a.err);
       for (int s = 0; s < C::kDOStages; ++s)
         if (last_do[s] >= 0)
           drain_wait(bar(C::kDOFull + s), (last_do[s] / C::kDOStages) & 1, a.err);

@@ -14,10 +14,12 @@
 // (heaviest first).  A tile's Q and dO are released as soon as its last dP has been computed, so
 // the next tile's Q, dO and first key blocks load while the current tile finishes.
 //
-// Warp roles (320 threads): warps 0-7 compute — warp w handles TMEM lanes 32(w%4)..+31 (query
+// Warp roles (352 threads): warps 0-7 compute — warp w handles TMEM lanes 32(w%4)..+31 (query
 // rows) and columns [64 h, 64 h + 64) of every 128-column tile, h = w / 4, so each score row is
-// split over two threads; warp 8 TMA producer (Q and dO per tile, K_j and V_j through two
-// shared-memory rings); warp 9 MMA issuer and TMEM owner.  dS goes back to TMEM (two buffers)
+// split over two threads; warp 8 TMA producer of Q and dO (per tile) and of the K ring; warp 10
+// TMA producer of the V ring; warp 9 MMA issuer and TMEM owner.  Loads are issued from two warps
+// because one warp's TMA copies complete at only ~40 B/clk on this GPU, less than one key block
+// (64 KB of K and V) per MMA period needs.  dS goes back to TMEM (two buffers)
 // and is the A operand of dQ += dS K_j.
 // TMEM columns: [0,128) S, [128,256) dP, [256, 256+D) dQ, [256+D, 384+D) dS x 2 (bf16 pairs).
 #include "swa_kernels.h"
@@ -54,10 +56,11 @@ struct DqCfg {
   static constexpr int kDQEmpty = kDQDone + 1;  // the epilogue has read the dQ accumulator
   static constexpr int kDrain = kDQEmpty + 1;
   static constexpr int kNumBars = kDrain + 1;
-  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;  // + TMEM address and abort flag
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
   static constexpr int kComputeThreads = 256;
 };
 
@@ -87,16 +90,17 @@ __device__ __forceinline__ DqTile dq_tile(int t, const DqArgs& a) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     swa_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DqArgs a) {
   using C = DqCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (!smem_base_ok(smem, a.err)) return;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
-  __shared__ int abort_flag;
+  int& abort_flag = *reinterpret_cast<int*>(tmem_slot + 1);  // raised by a failed wait
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t sQ = smem_u32(smem + C::kOffQ);
   const uint32_t sDO = smem_u32(smem + C::kOffDO);
@@ -143,11 +147,9 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
       tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       int last_qd = -1;
-      int last_k[C::kKStages], last_v[C::kVStages];
+      int last_k[C::kKStages];
       for (int s = 0; s < C::kKStages; ++s) last_k[s] = -1;
-      for (int s = 0; s < C::kVStages; ++s) last_v[s] = -1;
       int g = 0;  // key blocks loaded so far by this CTA
       bool ok = true;
       for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
@@ -171,6 +173,23 @@ __global__ void __launch_bounds__(320, 1)
           for (int h = 0; h < C::kChunks; ++h)
             tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKFull + sk), 64 * h, k0, f.bhk);
           last_k[sk] = g;
+        }
+      }
+      if (last_qd >= 0) drain_wait(bar(C::kQDFull), last_qd & 1, a.err);
+      for (int s = 0; s < C::kKStages; ++s)
+        if (last_k[s] >= 0) drain_wait(bar(C::kKFull + s), (last_k[s] / C::kKStages) & 1, a.err);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------------ TMA producer (V ring)
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_v);
+      int last_v[C::kVStages];
+      for (int s = 0; s < C::kVStages; ++s) last_v[s] = -1;
+      int g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < a.ntiles; t += tile_step) {
+        const DqTile f = dq_tile(t, a);
+        for (int j = 0; j < f.nkv; ++j, ++g) {
           const int sv = g % C::kVStages, nv = g / C::kVStages;
           if (g >= C::kVStages &&
               !(ok = mbar_wait(bar(C::kVEmpty + sv), (nv - 1) & 1, &abort_flag, a.err)))
@@ -178,13 +197,11 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t sV = sV0 + sv * C::kTileBytes;
           mbar_arrive_expect_tx(bar(C::kVFull + sv), C::kTileBytes);
           for (int h = 0; h < C::kChunks; ++h)
-            tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kVFull + sv), 64 * h, k0, f.bhk);
+            tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kVFull + sv), 64 * h,
+                        (f.kb_lo + j) * kBlockN, f.bhk);
           last_v[sv] = g;
         }
       }
-      if (last_qd >= 0) drain_wait(bar(C::kQDFull), last_qd & 1, a.err);
-      for (int s = 0; s < C::kKStages; ++s)
-        if (last_k[s] >= 0) drain_wait(bar(C::kKFull + s), (last_k[s] / C::kKStages) & 1, a.err);
       for (int s = 0; s < C::kVStages; ++s)
         if (last_v[s] >= 0) drain_wait(bar(C::kVFull + s), (last_v[s] / C::kVStages) & 1, a.err);
     }

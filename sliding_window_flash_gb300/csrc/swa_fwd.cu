@@ -12,7 +12,7 @@
 // (heaviest first).  Q is double-buffered, so the next tile's Q and first key blocks load, and its
 // first score tiles are computed, while the softmax warps finish the current tile.
 //
-// Warp roles (352 threads):
+// Warp roles (384 threads):
 //   warps 0-7  softmax: warp w owns TMEM lanes 32(w%4)..+31 (query rows) and columns
 //              [64 h, 64 h + 64) of every score tile, h = w / 4, so each row is split over two
 //              threads that swap their partial row max through shared memory every block.  Each
@@ -20,8 +20,11 @@
 //              bf16 P back to TMEM (packed pairs), rescales its half of the O row in TMEM when the
 //              max grows by more than 2^8, and at the end of a tile stages its half of O / l in
 //              the tile's Q buffer (and writes LSE).
-//   warp 8     TMA producer: Q per tile, then K_j and V_j through two shared-memory rings (K is
-//              released as soon as S_j is computed, V after P_j V_j).
+//   warp 8     TMA producer of Q (per tile) and of the K ring (K_j is released as soon as S_j is
+//              computed).
+//   warp 11    TMA producer of the V ring (V_j is released after P_j V_j).  Loads are issued
+//              from two warps because one warp's TMA copies complete at only ~40 B/clk on this
+//              GPU, less than one key block (64 KB of K and V) per MMA period needs.
 //   warp 9     MMA issuer and TMEM owner (converged warp, one elected lane issues): S_j = Q K_j^T
 //              into one of two TMEM S buffers; O += P_j V_j with P_j read from TMEM (A operand).
 //              S_{j+1} is issued before O += P_j V_j so the tensor core computes the next scores
@@ -46,7 +49,7 @@ struct FwdCfg {
   static constexpr int kTileBytes = kBlockM * D * 2;  // one 128 x D bf16 tile
   static constexpr int kChunkBytes = kBlockM * 128;   // 128 rows x 64 columns (128-byte rows)
   static constexpr int kChunks = D / 64;
-  static constexpr int kKStages = (D == 128) ? 2 : 4;
+  static constexpr int kKStages = (D == 128) ? 3 : 4;
   static constexpr int kVStages = (D == 128) ? 2 : 4;
   static constexpr int kOffQ = 0;  // 2 buffers
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
@@ -68,12 +71,13 @@ struct FwdCfg {
   static constexpr int kOutFull = kOEmpty + 1;       // 2: staged O tile complete, per Q buffer
   static constexpr int kDrain = kOutFull + 2;
   static constexpr int kNumBars = kDrain + 1;
-  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM slot + align
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;  // + TMEM address and abort flag
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;  // buffer b at kColS + 128 b
   static constexpr uint32_t kColO = 256;
   static constexpr uint32_t kColP = 256 + D;  // buffer b at kColP + 64 b
-  static constexpr int kThreads = 352;
+  static constexpr int kThreads = 384;
   static constexpr int kComputeThreads = 256;
 };
 
@@ -102,16 +106,17 @@ __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdArgs& a) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     swa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                    const FwdArgs a) {
   using C = FwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (!smem_base_ok(smem, a.err)) return;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
-  __shared__ int abort_flag;
+  int& abort_flag = *reinterpret_cast<int*>(tmem_slot + 1);  // raised by a failed wait
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t sQ0 = smem_u32(smem + C::kOffQ);
   const uint32_t sK0 = smem_u32(smem + C::kOffK);
@@ -157,11 +162,9 @@ __global__ void __launch_bounds__(352, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       int last_q[2] = {-1, -1};
-      int last_k[C::kKStages], last_v[C::kVStages];
+      int last_k[C::kKStages];
       for (int s = 0; s < C::kKStages; ++s) last_k[s] = -1;
-      for (int s = 0; s < C::kVStages; ++s) last_v[s] = -1;
       int g = 0;  // key blocks loaded so far by this CTA
       bool ok = true;
       for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
@@ -186,15 +189,6 @@ __global__ void __launch_bounds__(352, 1)
           for (int h = 0; h < C::kChunks; ++h)
             tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKFull + sk), 64 * h, k0, f.bhk);
           last_k[sk] = g;
-          const int sv = g % C::kVStages, nv = g / C::kVStages;
-          if (g >= C::kVStages &&
-              !(ok = mbar_wait(bar(C::kVEmpty + sv), (nv - 1) & 1, &abort_flag, a.err)))
-            break;
-          const uint32_t sV = sV0 + sv * C::kTileBytes;
-          mbar_arrive_expect_tx(bar(C::kVFull + sv), C::kTileBytes);
-          for (int h = 0; h < C::kChunks; ++h)
-            tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kVFull + sv), 64 * h, k0, f.bhk);
-          last_v[sv] = g;
         }
       }
       // Never leave a copy in flight: wait for the last fill of every buffer.
@@ -202,6 +196,30 @@ __global__ void __launch_bounds__(352, 1)
         if (last_q[b] >= 0) drain_wait(bar(C::kQFull + b), (last_q[b] >> 1) & 1, a.err);
       for (int s = 0; s < C::kKStages; ++s)
         if (last_k[s] >= 0) drain_wait(bar(C::kKFull + s), (last_k[s] / C::kKStages) & 1, a.err);
+    }
+  } else if (warp == 11) {
+    // ------------------------------------------------------------------ TMA producer (V ring)
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_v);
+      int last_v[C::kVStages];
+      for (int s = 0; s < C::kVStages; ++s) last_v[s] = -1;
+      int g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < a.ntiles; t += tile_step) {
+        const FwdTile f = fwd_tile(t, a);
+        for (int j = 0; j < f.nkv; ++j, ++g) {
+          const int sv = g % C::kVStages, nv = g / C::kVStages;
+          if (g >= C::kVStages &&
+              !(ok = mbar_wait(bar(C::kVEmpty + sv), (nv - 1) & 1, &abort_flag, a.err)))
+            break;
+          const uint32_t sV = sV0 + sv * C::kTileBytes;
+          mbar_arrive_expect_tx(bar(C::kVFull + sv), C::kTileBytes);
+          for (int h = 0; h < C::kChunks; ++h)
+            tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kVFull + sv), 64 * h,
+                        (f.kb_lo + j) * kBlockN, f.bhk);
+          last_v[sv] = g;
+        }
+      }
       for (int s = 0; s < C::kVStages; ++s)
         if (last_v[s] >= 0) drain_wait(bar(C::kVFull + s), (last_v[s] / C::kVStages) & 1, a.err);
     }

@@ -8,6 +8,11 @@
 
 namespace swa {
 
+// Bits of the per-device error word that kernels set (read and cleared by swa_check_device).
+constexpr unsigned kErrWaitTimeout = 1u;  // an mbarrier wait ran out
+constexpr unsigned kErrSmemLayout = 2u;   // dynamic shared memory not 1024-byte aligned; the
+                                          // kernel returned before any barrier or memory use
+
 constexpr int kBlockM = 128;  // query rows per tile
 constexpr int kBlockN = 128;  // key rows per tile
 

@@ -14,14 +14,14 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "swa_kernels.h"
+
 namespace swa {
 
 // ------------------------------------------------------------------------------------------------
 // Error reporting of bounded waits.
 // ------------------------------------------------------------------------------------------------
 
-// Bit set in the device error word when an mbarrier wait runs out.
-constexpr unsigned kErrWaitTimeout = 1u;
 // A wait gives up after this many SM clock cycles (~1 s at 2 GHz) or this many polls.
 constexpr long long kWaitCycleLimit = 2000000000ll;
 constexpr unsigned kWaitPollLimit = 1u << 30;
@@ -486,8 +486,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 #define SWA_NEG_INF (-__int_as_float(0x7f800000))
 #define SWA_POS_INF (__int_as_float(0x7f800000))
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+// True when the dynamic shared-memory window starts on a 1024-byte boundary, which the
+// 128-byte-swizzled tiles require.  Kernels declare no static shared memory and request exactly
+// their layout's size, so the window is aligned; a kernel that finds it is not raises
+// kErrSmemLayout and returns at once, before any barrier or tensor-memory use.
+__device__ __forceinline__ bool smem_base_ok(const uint8_t* smem, unsigned* err) {
+  if ((smem_u32(smem) & 1023u) == 0u) return true;
+  if (threadIdx.x == 0) atomicOr(err, kErrSmemLayout);
+  return false;
 }
 
 // Bounded wait that ignores the abort flag: used to drain a CTA's own copies before it exits.
