@@ -15,11 +15,14 @@
 // Warp roles (384 threads):
 //   warps 0-7  softmax: warp w owns TMEM lanes 32(w%4)..+31 (query rows) and columns
 //              [64 h, 64 h + 64) of every score tile, h = w / 4, so each row is split over two
-//              threads that swap their partial row max through shared memory every block.  Each
-//              masks its half, keeps the running max m and its partial sum l in registers, writes
-//              bf16 P back to TMEM (packed pairs), rescales its half of the O row in TMEM when the
-//              max grows by more than 2^8, and at the end of a tile stages its half of O / l in
-//              the tile's Q buffer (and writes LSE).
+//              threads.  Each masks its half and exponentiates it against the row's running
+//              reference max in one pass (packed fp32x2 arithmetic); the two halves swap their
+//              block sums through shared memory, and only a tile's first block or a block whose
+//              sum shows the max has risen far is redone exactly, with the halves' maxima
+//              swapped first.  Each keeps the running max m and its partial sum l in registers,
+//              writes bf16 P back to TMEM (packed pairs), rescales its half of the O row in TMEM
+//              when the max grows by more than 2^8, and at the end of a tile stages its half of
+//              O / l in the tile's Q buffer (and writes LSE).
 //   warp 8     TMA producer of Q (per tile) and of the K ring (K_j is released as soon as S_j is
 //              computed).
 //   warp 11    TMA producer of the V ring (V_j is released after P_j V_j).  Loads are issued
@@ -40,9 +43,12 @@
 namespace swa {
 namespace {
 
-// Running max is only moved (and O rescaled) when it grows by more than this many powers of 2;
-// otherwise P is computed against the stale max, with values up to 2^8 (exact softmax either way).
+// In the exact path the running max is only moved (and O rescaled) when it grows by more than
+// this many powers of 2; otherwise P is computed against the stale max (exact softmax either way).
 constexpr float kRescaleThreshold = 8.0f;
+// A block exponentiated against the running reference max stands when its row sum is at most
+// this (so every P <= 2^12); otherwise it is redone against the block's own max.
+constexpr float kFastSumLimit = 4096.0f;
 
 template <int D>
 struct FwdCfg {
@@ -340,38 +346,62 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int c = 0; c < 64; ++c) x[c] = (c >= lo && c <= hi) ? x[c] : SWA_NEG_INF;
         }
-        // Row max of this half as a tree (eight independent chains), in the log2 domain.
-        float m8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = x[i];
-#pragma unroll
-        for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
-        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
-        float mx_other;
-        if (!(ok = exchange(mx, &mx_other))) break;
-        mx = fmaxf(mx, mx_other);
-        // Both halves of a row see the same maxima, so they take the same decisions below.
-        const float m_new = fmaxf(m_ref, mx);
-        const bool resc = m_new > m_ref + kRescaleThreshold;
-        float factor = 1.f;
-        if (resc) {
-          factor = ex2(m_ref - m_new);  // 0 when m_ref is -inf
-          l *= factor;
-          m_ref = m_new;
-        }
-        const float m_use = (m_ref == SWA_NEG_INF) ? 0.f : m_ref;
+        // p = 2^(scale log2(e) S - m) for this half, two scores per step: one packed FFMA, two
+        // MUFU.EX2, one packed FADD into the row sum and one bf16 pack.  Returns the half's sum.
         uint32_t pk[32];
-        float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        auto exponentiate = [&](float m) -> float {
+          const float2 scale2 = make_float2(sl2, sl2), neg_m2 = make_float2(-m, -m);
+          float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          // p = 2^(scale log2(e) S - m): one FFMA and one MUFU.EX2 per score
-          const float p0 = ex2(fmaf(x[2 * c], sl2, -m_use));
-          const float p1 = ex2(fmaf(x[2 * c + 1], sl2, -m_use));
-          rs8[c & 7] += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
+          for (int c = 0; c < 32; ++c) {
+            const float2 tt = __ffma2_rn(make_float2(x[2 * c], x[2 * c + 1]), scale2, neg_m2);
+            const float2 e = make_float2(ex2(tt.x), ex2(tt.y));
+            rs2[c & 3] = __fadd2_rn(rs2[c & 3], e);
+            pk[c] = pack_bf16x2(e.x, e.y);
+          }
+          return ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) +
+                 ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
+        };
+        // Fast path: one pass against the reference max, taken when every row of the warp has a
+        // reference.  It stands unless some row's block sum exceeds 2^12; a sum within that bound
+        // keeps every P of the block <= 2^12, so the result is the exact softmax either way.  The
+        // two halves of a row swap their partial sums, so both take the same decision.
+        bool redo = true;
+        float bsum = 0.f;
+        if (__all_sync(0xffffffffu, m_ref != SWA_NEG_INF)) {
+          bsum = exponentiate(m_ref);
+          float other;
+          if (!(ok = exchange(bsum, &other))) break;
+          redo = __any_sync(0xffffffffu, !(bsum + other <= kFastSumLimit));
         }
-        l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+        bool resc = false;
+        float factor = 1.f;
+        if (redo) {
+          // Exact path (a tile's first block, or a large rise of the max): the row max first
+          // (a tree of eight chains per half, then swapped between the halves), then the
+          // exponentials against it.
+          float m8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = x[i];
+#pragma unroll
+          for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+          float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
+          float mx_other;
+          if (!(ok = exchange(mx, &mx_other))) break;
+          mx = fmaxf(mx, mx_other);
+          // Both halves of a row see the same maxima, so they take the same decisions below.
+          const float m_new = fmaxf(m_ref, mx);
+          resc = m_new > m_ref + kRescaleThreshold;
+          if (resc) {
+            factor = ex2(m_ref - m_new);  // 0 when m_ref is -inf
+            l *= factor;
+            m_ref = m_new;
+          }
+          bsum = exponentiate((m_ref == SWA_NEG_INF) ? 0.f : m_ref);
+        }
+        l += bsum;
 
         // P buffer (gg & 1) was last read by the P V of block gg - 2.
         if (gg >= 2 &&
