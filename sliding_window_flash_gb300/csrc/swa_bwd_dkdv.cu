@@ -274,12 +274,13 @@ __global__ void __launch_bounds__(352, 1)
       const int q0 = tile_q0(t);
       // Slot t & 1 was last read in tile t - 2; every compute thread has finished that tile
       // (dK_{t-2}, which needed all of them, precedes dP_{t-1}, which this thread has seen).
+      // Stored negated (-LSE log2(e) and -Delta), the addends of the packed FFMA / FADD below.
       float* s_lse2 = s_rows + (t & 1) * 2 * kBlockM;
       float* s_delta = s_lse2 + kBlockM;
       if (h == 0)
-        s_lse2[r] = nxt * kLog2e;
+        s_lse2[r] = -nxt * kLog2e;
       else
-        s_delta[r] = nxt;
+        s_delta[r] = -nxt;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::kVecFull + (t & 1)));
       if (!(ok = warp_wait(bar(C::kVecFull + (t & 1)), (t >> 1) & 1, &abort_flag, a.err))) break;
@@ -301,13 +302,19 @@ __global__ void __launch_bounds__(352, 1)
         tmem_wait_ld_all();
         reg_fence(rr[0]);
         reg_fence(rr[1]);
+        // P^T = 2^(scale log2(e) S^T - LSE log2(e)), two queries per packed FFMA.
+        const float2 scale2 = make_float2(sl2, sl2);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const uint32_t* src = &rr[i >> 3][(4 * i) & 31];
-          p[4 * i + 0] = ex2(fmaf(__uint_as_float(src[0]), sl2, -lv[i].x));
-          p[4 * i + 1] = ex2(fmaf(__uint_as_float(src[1]), sl2, -lv[i].y));
-          p[4 * i + 2] = ex2(fmaf(__uint_as_float(src[2]), sl2, -lv[i].z));
-          p[4 * i + 3] = ex2(fmaf(__uint_as_float(src[3]), sl2, -lv[i].w));
+          const float2 t0 = __ffma2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                       scale2, make_float2(lv[i].x, lv[i].y));
+          const float2 t1 = __ffma2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                       scale2, make_float2(lv[i].z, lv[i].w));
+          p[4 * i + 0] = ex2(t0.x);
+          p[4 * i + 1] = ex2(t0.y);
+          p[4 * i + 2] = ex2(t1.x);
+          p[4 * i + 3] = ex2(t1.y);
         }
       }
       // Query q0 + 64h + c sees this key iff 0 <= q0 + 64h + c - key < W.
@@ -339,16 +346,21 @@ __global__ void __launch_bounds__(352, 1)
         tmem_wait_ld_all();
         reg_fence(rr[0]);
         reg_fence(rr[1]);
+        // dS^T = P^T (dP^T - Delta), two queries per packed FADD / FMUL.
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = 4 * i;
-          const float4 dl = dv4[i];
+          const float4 nd = dv4[i];  // -Delta of queries c .. c + 3
           const uint32_t* src = &rr[i >> 3][(4 * i) & 31];
-          pk[2 * i] = pack_bf16x2(p[c] * (__uint_as_float(src[0]) - dl.x),
-                                  p[c + 1] * (__uint_as_float(src[1]) - dl.y));
-          pk[2 * i + 1] = pack_bf16x2(p[c + 2] * (__uint_as_float(src[2]) - dl.z),
-                                      p[c + 3] * (__uint_as_float(src[3]) - dl.w));
+          const float2 d0 = __fadd2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                       make_float2(nd.x, nd.y));
+          const float2 d1 = __fadd2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                       make_float2(nd.z, nd.w));
+          const float2 s0 = __fmul2_rn(make_float2(p[c], p[c + 1]), d0);
+          const float2 s1 = __fmul2_rn(make_float2(p[c + 2], p[c + 3]), d1);
+          pk[2 * i] = pack_bf16x2(s0.x, s0.y);
+          pk[2 * i + 1] = pack_bf16x2(s1.x, s1.y);
         }
         tmem_st32(tmem + lane_base + C::kColDP + 64u * h, pk);
       }

@@ -303,14 +303,23 @@ __global__ void __launch_bounds__(352, 1)
           for (int i = 0; i < 64; ++i) p[i] = __uint_as_float(rr[i >> 5][i & 31]);
         }
         warp_arrive(bar(C::kSEmpty));
-#pragma unroll
-        for (int c = 0; c < 64; ++c) p[c] = ex2(fmaf(p[c], sl2, -lse2));
+        // Masked cells get S = -inf, so P = 0 there.
         const bool interior = (k0 + kBlockN - 1 <= q0) && (q0 + kBlockM - 1 - k0 < a.W);
         if (!interior) {
           const int lo = row - a.W + 1 - k0 - 64 * static_cast<int>(h);
           const int hi = row - k0 - 64 * static_cast<int>(h);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
+          for (int c = 0; c < 64; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : SWA_NEG_INF;
+        }
+        // P = 2^(scale log2(e) S - LSE log2(e)), two scores per packed FFMA.
+        {
+          const float2 scale2 = make_float2(sl2, sl2), neg_l2 = make_float2(-lse2, -lse2);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 t = __ffma2_rn(make_float2(p[2 * c], p[2 * c + 1]), scale2, neg_l2);
+            p[2 * c] = ex2(t.x);
+            p[2 * c + 1] = ex2(t.y);
+          }
         }
 
         // dP_gg landing also means dQ_{gg-2} has finished reading dS buffer (gg & 1).
@@ -324,12 +333,17 @@ __global__ void __launch_bounds__(352, 1)
           reg_fence(rr[0]);
           reg_fence(rr[1]);
           warp_arrive(bar(C::kDPEmpty));
+          // dS = P (dP - Delta), two columns per packed FADD / FMUL.
           uint32_t pk[32];
+          const float2 neg_d2 = make_float2(-dlt, -dlt);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const uint32_t d0 = rr[i >> 4][(2 * i) & 31], d1 = rr[i >> 4][(2 * i + 1) & 31];
-            pk[i] = pack_bf16x2(p[2 * i] * (__uint_as_float(d0) - dlt),
-                                p[2 * i + 1] * (__uint_as_float(d1) - dlt));
+            const float2 ds = __fmul2_rn(make_float2(p[2 * i], p[2 * i + 1]),
+                                         __fadd2_rn(make_float2(__uint_as_float(d0),
+                                                                __uint_as_float(d1)),
+                                                    neg_d2));
+            pk[i] = pack_bf16x2(ds.x, ds.y);
           }
           // dS columns [64h, 64h+64) -> packed TMEM columns [32h, 32h+32) of dS buffer (gg & 1).
           tmem_st32(tmem + lane_base + C::kColDS + 64u * (gg & 1) + 32u * h, pk);
