@@ -44,10 +44,22 @@ def test_every_declared_symbol_is_exported(lib):
         assert name in swa.SIGNATURES, f"binding has no signature for {name}"
 
 
+def _declared_statuses():
+    """{value: name} of the swa_status enum in include/swa_attn.h."""
+    text = open(os.path.join(ROOT, "include", "swa_attn.h")).read()
+    return {int(v): n for n, v in re.findall(r"\b(SWA_(?:OK|ERR_[A-Z_]+))\s*=\s*(\d+)", text)}
+
+
 def test_version_and_strerror(lib):
+    import sliding_window_flash_gb300 as swa
+
     assert lib.swa_version() >= 100
-    for code in range(7):
-        assert lib.swa_strerror(code)
+    declared = _declared_statuses()
+    assert declared and sorted(declared) == list(range(len(declared)))
+    for code, name in declared.items():
+        msg = lib.swa_strerror(code)
+        assert msg.startswith(name.encode()), (code, msg)
+        assert swa.STATUS[code] == name
     assert b"UNKNOWN" in lib.swa_strerror(99)
 
 
