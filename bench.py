@@ -472,7 +472,8 @@ def measure_e2e(swa, case, device, dist, args, world) -> dict:
 
 
 def measure_other_workloads(swa, device) -> dict:
-    """Full-causal GQA layer (fwd and bwd timed separately) and the 12-layer mixed step."""
+    """Full-causal GQA layer (fwd and bwd timed separately), the headline layer in fp16, and the
+    12-layer mixed step."""
     res = {}
     case = si.gqa_causal_case()
     inp = si.make_inputs(case, device=str(device))
@@ -500,6 +501,25 @@ def measure_other_workloads(swa, device) -> dict:
         "fwd_ms": f_ms, "bwd_ms": b_ms,
         "fwd_tflops": fl["fwd"] / (f_ms * 1e-3) / 1e12,
         "bwd_tflops": fl["bwd"] / (b_ms * 1e-3) / 1e12,
+    }
+    del inp, o, lse
+    torch.cuda.empty_cache()
+
+    # The headline layer with fp16 tensors (swa_attn_fwd_f16 / swa_attn_bwd_f16).
+    case = si.long_swa_case(32768)
+    inp = si.make_inputs(case, device=str(device), dtype=torch.float16)
+    fl = step_flops(case)
+    o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale)
+    f_ms = timed(lambda: swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
+                                          out=o, lse=lse))
+    b_ms = timed(lambda: swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
+                                          case.softmax_scale))
+    res["long_swa_fp16"] = {
+        "workload": "B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, fp16 tensors",
+        "fwd_ms": f_ms, "bwd_ms": b_ms,
+        "fwd_tflops": fl["fwd"] / (f_ms * 1e-3) / 1e12,
+        "bwd_tflops": fl["bwd"] / (b_ms * 1e-3) / 1e12,
+        "fwd_bwd_tflops": (fl["fwd"] + fl["bwd"]) / ((f_ms + b_ms) * 1e-3) / 1e12,
     }
     del inp, o, lse
     torch.cuda.empty_cache()

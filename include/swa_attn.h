@@ -92,6 +92,22 @@ swa_status swa_attn_bwd(const void* q, const void* k, const void* v, const void*
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * fp16 forms of swa_attn_fwd and swa_attn_bwd: the same arguments, checks, kernels and outputs,
+ * with q, k, v, o, dO, dq, dk, dv holding IEEE fp16 instead of bf16 (lse and the workspace stay
+ * fp32).  P and dS are rounded to fp16 as tensor-core operands; scores and accumulators stay fp32.
+ * The pages' gradient sweep covers fp16 as well as bf16 inputs (Lab 28, "Gradient parity, small
+ * shapes").  The caller keeps the values in fp16's range: P is bounded by 2^12 inside the forward,
+ * so only the inputs themselves can overflow.
+ */
+swa_status swa_attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int N, int D, int window, float scale,
+                            cudaStream_t stream);
+swa_status swa_attn_bwd_f16(const void* q, const void* k, const void* v, const void* o,
+                            const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                            int B, int Hq, int Hkv, int N, int D, int window, float scale,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * The three phases swa_attn_bwd runs, callable one by one (same arguments, same checks, same
  * kernels), e.g. to time each kernel or to run the dK/dV and dQ phases on two streams once the
  * preprocess has finished.  `delta` is the workspace of swa_attn_bwd (fp32 [B,Hq,N]).

@@ -52,8 +52,13 @@ STATUS = {
 _c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
 SIGNATURES = {
     "swa_attn_fwd": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _vp]),
+    "swa_attn_fwd_f16": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _vp]),
     "swa_attn_bwd_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
     "swa_attn_bwd": (
+        _c_int,
+        [_vp] * 9 + [_c_int] * 6 + [_c_float, _vp, ctypes.c_size_t, _vp],
+    ),
+    "swa_attn_bwd_f16": (
         _c_int,
         [_vp] * 9 + [_c_int] * 6 + [_c_float, _vp, ctypes.c_size_t, _vp],
     ),
@@ -132,25 +137,37 @@ def _scale(scale, D):
     return float(scale) if scale is not None else 1.0 / math.sqrt(D)
 
 
+def _elem_dtype(q):
+    """Element type of a call: bf16, or fp16 (the *_f16 entry points), taken from q."""
+    import torch
+
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"q must be bfloat16 or float16, got {q.dtype}")
+    return q.dtype
+
+
 def swa_attn_fwd(q, k, v, window: int, scale: Optional[float] = None, out=None, lse=None):
-    """Forward: returns (o [B,Hq,N,D] bf16, lse [B,Hq,N] fp32)."""
+    """Forward: returns (o [B,Hq,N,D] in q's dtype (bf16 or fp16), lse [B,Hq,N] fp32)."""
     import torch
 
     lib = load()
     B, Hq, Hkv, N, D = _dims(q, k)
-    _check_tensor(q, "q", (B, Hq, N, D), torch.bfloat16)
-    _check_tensor(k, "k", (B, Hkv, N, D), torch.bfloat16)
-    _check_tensor(v, "v", (B, Hkv, N, D), torch.bfloat16)
+    dt = _elem_dtype(q)
+    _check_tensor(q, "q", (B, Hq, N, D), dt)
+    _check_tensor(k, "k", (B, Hkv, N, D), dt)
+    _check_tensor(v, "v", (B, Hkv, N, D), dt)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
-    _check_tensor(out, "out", (B, Hq, N, D), torch.bfloat16)
+    _check_tensor(out, "out", (B, Hq, N, D), dt)
     _check_tensor(lse, "lse", (B, Hq, N), torch.float32)
-    rc = lib.swa_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                          B, Hq, Hkv, N, D, int(window), _scale(scale, D), _stream_handle(q.device))
+    name = "swa_attn_fwd_f16" if dt == torch.float16 else "swa_attn_fwd"
+    rc = getattr(lib, name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr(), B, Hq, Hkv, N, D, int(window), _scale(scale, D),
+                            _stream_handle(q.device))
     if rc != 0:
-        raise SwaError(rc, "swa_attn_fwd")
+        raise SwaError(rc, name)
     return out, lse
 
 
@@ -160,29 +177,32 @@ def swa_attn_bwd_workspace_bytes(B: int, Hq: int, N: int, D: int) -> int:
 
 def swa_attn_bwd(q, k, v, o, do, lse, window: int, scale: Optional[float] = None,
                  dq=None, dk=None, dv=None, workspace=None) -> Tuple:
-    """Backward of sum(do * o): returns (dq, dk, dv), bf16, dk/dv summed over each kv group."""
+    """Backward of sum(do * o): returns (dq, dk, dv) in q's dtype (bf16 or fp16), dk/dv summed
+    over each kv group."""
     import torch
 
     lib = load()
     B, Hq, Hkv, N, D = _dims(q, k)
+    dt = _elem_dtype(q)
     for t, name, hs in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq)):
-        _check_tensor(t, name, (B, hs, N, D), torch.bfloat16)
+        _check_tensor(t, name, (B, hs, N, D), dt)
     _check_tensor(lse, "lse", (B, Hq, N), torch.float32)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     for t, name, hs in ((dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
-        _check_tensor(t, name, (B, hs, N, D), torch.bfloat16)
+        _check_tensor(t, name, (B, hs, N, D), dt)
     ws_bytes = int(lib.swa_attn_bwd_workspace_bytes(B, Hq, N, D))
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    rc = lib.swa_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                          B, Hq, Hkv, N, D, int(window), _scale(scale, D),
-                          workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                          _stream_handle(q.device))
+    name = "swa_attn_bwd_f16" if dt == torch.float16 else "swa_attn_bwd"
+    rc = getattr(lib, name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                            B, Hq, Hkv, N, D, int(window), _scale(scale, D),
+                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            _stream_handle(q.device))
     if rc != 0:
-        raise SwaError(rc, "swa_attn_bwd")
+        raise SwaError(rc, name)
     return dq, dk, dv
 
 

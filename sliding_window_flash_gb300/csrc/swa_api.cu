@@ -64,7 +64,7 @@ swa_status check_sizes(int B, int Hq, int Hkv, int N, int D, int window, float s
 }
 
 swa::Problem make_problem(int B, int Hq, int Hkv, int N, int D, int window, float scale,
-                          unsigned* err) {
+                          unsigned* err, int f16 = 0) {
   swa::Problem pb;
   pb.B = B;
   pb.Hq = Hq;
@@ -74,7 +74,48 @@ swa::Problem make_problem(int B, int Hq, int Hkv, int N, int D, int window, floa
   pb.W = window < N ? window : N;  // a window that covers the sequence is plain causal
   pb.scale = scale;
   pb.err = err;
+  pb.f16 = f16;
   return pb;
+}
+
+// Forward and backward for either element type (f16: 0 = bf16, 1 = fp16).
+swa_status fwd_impl(int f16, const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int Hq, int Hkv, int N, int D, int window, float scale,
+                    cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
+  if (st != SWA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return SWA_ERR_MISALIGNED;
+  unsigned* err = nullptr;
+  if ((st = current_device(&err)) != SWA_OK) return st;
+  const swa::Problem pb = make_problem(B, Hq, Hkv, N, D, window, scale, err, f16);
+  if (swa::launch_fwd(pb, q, k, v, o, lse, stream) != cudaSuccess) return SWA_ERR_CUDA;
+  return SWA_OK;
+}
+
+swa_status bwd_impl(int f16, const void* q, const void* k, const void* v, const void* o,
+                    const void* dO, const float* lse, void* dq, void* dk, void* dv, int B, int Hq,
+                    int Hkv, int N, int D, int window, float scale, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
+  if (st != SWA_OK) return st;
+  if (!workspace || workspace_bytes < swa_attn_bwd_workspace_bytes(B, Hq, N, D))
+    return SWA_ERR_WORKSPACE;
+  const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return SWA_ERR_MISALIGNED;
+  unsigned* err = nullptr;
+  if ((st = current_device(&err)) != SWA_OK) return st;
+  const swa::Problem pb = make_problem(B, Hq, Hkv, N, D, window, scale, err, f16);
+  float* delta = static_cast<float*>(workspace);
+  if (swa::launch_bwd_delta(pb, o, dO, delta, stream) != cudaSuccess) return SWA_ERR_CUDA;
+  if (swa::launch_bwd_dkdv(pb, q, k, v, dO, lse, delta, dk, dv, stream) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (swa::launch_bwd_dq(pb, q, k, v, dO, lse, delta, dq, stream) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  return SWA_OK;
 }
 
 }  // namespace
@@ -84,16 +125,13 @@ extern "C" {
 swa_status swa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int Hq, int Hkv, int N, int D, int window, float scale,
                         cudaStream_t stream) {
-  if (!q || !k || !v || !o || !lse) return SWA_ERR_INVALID_ARG;
-  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
-  if (st != SWA_OK) return st;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-    return SWA_ERR_MISALIGNED;
-  unsigned* err = nullptr;
-  if ((st = current_device(&err)) != SWA_OK) return st;
-  const swa::Problem pb = make_problem(B, Hq, Hkv, N, D, window, scale, err);
-  if (swa::launch_fwd(pb, q, k, v, o, lse, stream) != cudaSuccess) return SWA_ERR_CUDA;
-  return SWA_OK;
+  return fwd_impl(0, q, k, v, o, lse, B, Hq, Hkv, N, D, window, scale, stream);
+}
+
+swa_status swa_attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int N, int D, int window, float scale,
+                            cudaStream_t stream) {
+  return fwd_impl(1, q, k, v, o, lse, B, Hq, Hkv, N, D, window, scale, stream);
 }
 
 size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int N, int D) {
@@ -106,24 +144,16 @@ swa_status swa_attn_bwd(const void* q, const void* k, const void* v, const void*
                         const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
                         int N, int D, int window, float scale, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream) {
-  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return SWA_ERR_INVALID_ARG;
-  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
-  if (st != SWA_OK) return st;
-  if (!workspace || workspace_bytes < swa_attn_bwd_workspace_bytes(B, Hq, N, D))
-    return SWA_ERR_WORKSPACE;
-  const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv, workspace};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return SWA_ERR_MISALIGNED;
-  unsigned* err = nullptr;
-  if ((st = current_device(&err)) != SWA_OK) return st;
-  const swa::Problem pb = make_problem(B, Hq, Hkv, N, D, window, scale, err);
-  float* delta = static_cast<float*>(workspace);
-  if (swa::launch_bwd_delta(pb, o, dO, delta, stream) != cudaSuccess) return SWA_ERR_CUDA;
-  if (swa::launch_bwd_dkdv(pb, q, k, v, dO, lse, delta, dk, dv, stream) != cudaSuccess)
-    return SWA_ERR_CUDA;
-  if (swa::launch_bwd_dq(pb, q, k, v, dO, lse, delta, dq, stream) != cudaSuccess)
-    return SWA_ERR_CUDA;
-  return SWA_OK;
+  return bwd_impl(0, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, D, window, scale, workspace,
+                  workspace_bytes, stream);
+}
+
+swa_status swa_attn_bwd_f16(const void* q, const void* k, const void* v, const void* o,
+                            const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                            int Hq, int Hkv, int N, int D, int window, float scale,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return bwd_impl(1, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, D, window, scale, workspace,
+                  workspace_bytes, stream);
 }
 
 swa_status swa_attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int Hq,

@@ -3,18 +3,18 @@
 // into dS = P * (dP - Delta) in the dK/dV and dQ kernels.
 //
 // Bandwidth-bound: every row's O and dO are read once (2 * D * 2 bytes) and 4 bytes are written.
-// Each lane loads 16 bytes of O and of dO (8 bf16), D/8 lanes cover a row, and the partial sums
-// are combined with xor-shuffles inside those lanes.  The grid is a whole number of waves over
-// the 152 SMs and walks the rows with a grid stride.
+// Each lane loads 16 bytes of O and of dO (8 bf16 or fp16), D/8 lanes cover a row, and the partial
+// sums are combined with xor-shuffles inside those lanes.  The grid is a whole number of waves
+// over the 152 SMs and walks the rows with a grid stride.
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 
 namespace swa {
 namespace {
 
-template <int D>
-__global__ void __launch_bounds__(256) swa_delta_kernel(const __nv_bfloat16* __restrict__ o,
-                                                        const __nv_bfloat16* __restrict__ dO,
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) swa_delta_kernel(const uint16_t* __restrict__ o,
+                                                        const uint16_t* __restrict__ dO,
                                                         float* __restrict__ delta,
                                                         long long rows) {
   constexpr int kLanesPerRow = D / 8;
@@ -35,8 +35,8 @@ __global__ void __launch_bounds__(256) swa_delta_kernel(const __nv_bfloat16* __r
       const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[i]));
-        const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv[i]));
+        const float2 fa = Elem<F16>::unpack(av[i]);
+        const float2 fb = Elem<F16>::unpack(bv[i]);
         acc = fmaf(fa.x, fb.x, acc);
         acc = fmaf(fa.y, fb.y, acc);
       }
@@ -58,12 +58,17 @@ cudaError_t launch_bwd_delta(const Problem& pb, const void* o, const void* dO, f
   long long blocks = (rows + rows_per_block - 1) / rows_per_block;
   const long long cap = 152ll * 8 * 4;  // 4 waves of 8 resident 256-thread blocks per SM
   if (blocks > cap) blocks = cap;
-  const auto* po = static_cast<const __nv_bfloat16*>(o);
-  const auto* pd = static_cast<const __nv_bfloat16*>(dO);
-  if (pb.D == 64)
-    swa_delta_kernel<64><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(po, pd, delta, rows);
+  const auto* po = static_cast<const uint16_t*>(o);
+  const auto* pd = static_cast<const uint16_t*>(dO);
+  const dim3 grid(static_cast<unsigned>(blocks));
+  if (pb.D == 64 && !pb.f16)
+    swa_delta_kernel<64, false><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
+  else if (pb.D == 64)
+    swa_delta_kernel<64, true><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
+  else if (pb.D == 128 && !pb.f16)
+    swa_delta_kernel<128, false><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
   else if (pb.D == 128)
-    swa_delta_kernel<128><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(po, pd, delta, rows);
+    swa_delta_kernel<128, true><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

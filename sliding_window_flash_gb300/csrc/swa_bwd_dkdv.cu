@@ -65,14 +65,14 @@ struct DkdvCfg {
 struct DkdvArgs {
   const float* lse;
   const float* delta;
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
+  uint16_t* dk;  // bf16 or fp16 elements
+  uint16_t* dv;
   int BHK, Hq, Hkv, G, N, W, nkb;
   float scale, scale_log2;
   unsigned* err;
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(352, 1)
     swa_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_do,
@@ -196,8 +196,8 @@ __global__ void __launch_bounds__(352, 1)
     // The MMAs run in that order, so S_{t+1} overwrites the S^T / P^T columns only after dV_t has
     // read P_t^T, and dP_{t+1} overwrites dP^T / dS^T only after dK_t has read dS_t^T.
     {  // the whole warp, converged; one elected lane issues
-      constexpr uint32_t kIdS = idesc_bf16(kBlockN, kBlockM, false, false);  // S^T, dP^T
-      constexpr uint32_t kIdAcc = idesc_bf16(kBlockN, D, false, true);       // dV, dK
+      constexpr uint32_t kIdS = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockN, kBlockM, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdAcc = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockN, D, false, true);       // dV, dK
       auto issue_s = [&](int t) -> bool {  // S^T = K Q_t^T
         const int s = t % C::kQStages;
         if (!warp_wait(bar(C::kQFull + s), (t / C::kQStages) & 1, &abort_flag, a.err)) return false;
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(352, 1)
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+        for (int c = 0; c < 32; ++c) pk[c] = Elem<F16>::pack(p[2 * c], p[2 * c + 1]);
         tmem_st32(tmem + lane_base + C::kColS + 64u * h, pk);
       }
       tmem_wait_st();
@@ -359,8 +359,8 @@ __global__ void __launch_bounds__(352, 1)
                                        make_float2(nd.z, nd.w));
           const float2 s0 = __fmul2_rn(make_float2(p[c], p[c + 1]), d0);
           const float2 s1 = __fmul2_rn(make_float2(p[c + 2], p[c + 3]), d1);
-          pk[2 * i] = pack_bf16x2(s0.x, s0.y);
-          pk[2 * i + 1] = pack_bf16x2(s1.x, s1.y);
+          pk[2 * i] = Elem<F16>::pack(s0.x, s0.y);
+          pk[2 * i + 1] = Elem<F16>::pack(s1.x, s1.y);
         }
         tmem_st32(tmem + lane_base + C::kColDP + 64u * h, pk);
       }
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(352, 1)
           uint32_t o16[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            o16[i] = pack_bf16x2(__uint_as_float(rr[c4][2 * i]) * mul,
+            o16[i] = Elem<F16>::pack(__uint_as_float(rr[c4][2 * i]) * mul,
                                  __uint_as_float(rr[c4][2 * i + 1]) * mul);
           stage_row32_sw128(stage, r, kHalf * h + 32u * c4, o16);
         }
@@ -414,29 +414,29 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_dkdv_d(const Problem& pb, const void* q, const void* k, const void* v,
                           const void* dO, const float* lse, const float* delta, void* dk, void* dv,
                           cudaStream_t stream) {
   using C = DkdvCfg<D>;
   CUtensorMap tq, tdo, tk, tv, tdk, tdv;
   const uint64_t bhq = static_cast<uint64_t>(pb.B) * pb.Hq, bhk = static_cast<uint64_t>(pb.B) * pb.Hkv;
-  if (!make_tmap_bf16_3d(&tq, q, bhq, pb.N, D, kBlockM) ||
-      !make_tmap_bf16_3d(&tdo, dO, bhq, pb.N, D, kBlockM) ||
-      !make_tmap_bf16_3d(&tk, k, bhk, pb.N, D, kBlockN) ||
-      !make_tmap_bf16_3d(&tv, v, bhk, pb.N, D, kBlockN) ||
-      !make_tmap_bf16_3d(&tdk, dk, bhk, pb.N, D, kBlockN) ||
-      !make_tmap_bf16_3d(&tdv, dv, bhk, pb.N, D, kBlockN))
+  if (!make_tmap_3d(&tq, q, bhq, pb.N, D, kBlockM, F16) ||
+      !make_tmap_3d(&tdo, dO, bhq, pb.N, D, kBlockM, F16) ||
+      !make_tmap_3d(&tk, k, bhk, pb.N, D, kBlockN, F16) ||
+      !make_tmap_3d(&tv, v, bhk, pb.N, D, kBlockN, F16) ||
+      !make_tmap_3d(&tdk, dk, bhk, pb.N, D, kBlockN, F16) ||
+      !make_tmap_3d(&tdv, dv, bhk, pb.N, D, kBlockN, F16))
     return cudaErrorInvalidValue;
-  auto kern = swa_dkdv_kernel<D>;
+  auto kern = swa_dkdv_kernel<D, F16>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   DkdvArgs a;
   a.lse = lse;
   a.delta = delta;
-  a.dk = static_cast<__nv_bfloat16*>(dk);
-  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
   a.BHK = pb.B * pb.Hkv;
   a.Hq = pb.Hq;
   a.Hkv = pb.Hkv;
@@ -457,8 +457,12 @@ cudaError_t launch_dkdv_d(const Problem& pb, const void* q, const void* k, const
 cudaError_t launch_bwd_dkdv(const Problem& pb, const void* q, const void* k, const void* v,
                             const void* dO, const float* lse, const float* delta, void* dk,
                             void* dv, cudaStream_t stream) {
-  if (pb.D == 64) return launch_dkdv_d<64>(pb, q, k, v, dO, lse, delta, dk, dv, stream);
-  if (pb.D == 128) return launch_dkdv_d<128>(pb, q, k, v, dO, lse, delta, dk, dv, stream);
+  if (pb.D == 64)
+    return pb.f16 ? launch_dkdv_d<64, true>(pb, q, k, v, dO, lse, delta, dk, dv, stream)
+                  : launch_dkdv_d<64, false>(pb, q, k, v, dO, lse, delta, dk, dv, stream);
+  if (pb.D == 128)
+    return pb.f16 ? launch_dkdv_d<128, true>(pb, q, k, v, dO, lse, delta, dk, dv, stream)
+                  : launch_dkdv_d<128, false>(pb, q, k, v, dO, lse, delta, dk, dv, stream);
   return cudaErrorInvalidValue;
 }
 

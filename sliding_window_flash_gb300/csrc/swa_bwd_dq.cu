@@ -67,7 +67,7 @@ struct DqCfg {
 struct DqArgs {
   const float* lse;
   const float* delta;
-  __nv_bfloat16* dq;
+  uint16_t* dq;  // bf16 or fp16 elements
   int BH, Hq, Hkv, G, N, W, nqb, ntiles;
   float scale, scale_log2;
   unsigned* err;
@@ -89,7 +89,7 @@ __device__ __forceinline__ DqTile dq_tile(int t, const DqArgs& a) {
   return f;
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(352, 1)
     swa_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -211,8 +211,8 @@ __global__ void __launch_bounds__(352, 1)
     // S and dP are computed as soon as the compute warps have read this block's, so they never
     // wait on dQ_j.  dS alternates between two TMEM buffers: dP_{g+2} runs after dQ_g, so when the
     // compute warps see dP_{g+2} the buffer of dS_g is free again.  Block counters run across tiles.
-    constexpr uint32_t kIdSq = idesc_bf16(kBlockM, kBlockN, false, false);  // S, dP
-    constexpr uint32_t kIdDq = idesc_bf16(kBlockM, D, false, true);         // dQ += dS K
+    constexpr uint32_t kIdSq = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockM, kBlockN, false, false);  // S, dP
+    constexpr uint32_t kIdDq = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockM, D, false, true);         // dQ += dS K
     auto issue_s = [&](int gg) -> bool {  // S = Q K_gg^T once S_{gg-1} has been read
       const int s = gg % C::kKStages, n = gg / C::kKStages;
       if (!warp_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(352, 1)
                                          __fadd2_rn(make_float2(__uint_as_float(d0),
                                                                 __uint_as_float(d1)),
                                                     neg_d2));
-            pk[i] = pack_bf16x2(ds.x, ds.y);
+            pk[i] = Elem<F16>::pack(ds.x, ds.y);
           }
           // dS columns [64h, 64h+64) -> packed TMEM columns [32h, 32h+32) of dS buffer (gg & 1).
           tmem_st32(tmem + lane_base + C::kColDS + 64u * (gg & 1) + 32u * h, pk);
@@ -369,13 +369,13 @@ __global__ void __launch_bounds__(352, 1)
       // dQ * scale -> bf16, written straight from registers: each thread owns 64 or 128
       // contiguous bytes of its row; the stores drain while the next tile runs.
       if (in_range) {
-        __nv_bfloat16* dst_row = a.dq + grow * D + kHalf * h;
+        uint16_t* dst_row = a.dq + grow * D + kHalf * h;
 #pragma unroll
         for (int c4 = 0; c4 < kHalf / 32; ++c4) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(rr[c4][2 * i]) * a.scale,
+            pk[i] = Elem<F16>::pack(__uint_as_float(rr[c4][2 * i]) * a.scale,
                                 __uint_as_float(rr[c4][2 * i + 1]) * a.scale);
           uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c4);
 #pragma unroll
@@ -394,26 +394,26 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_dq_d(const Problem& pb, const void* q, const void* k, const void* v,
                         const void* dO, const float* lse, const float* delta, void* dq,
                         cudaStream_t stream) {
   using C = DqCfg<D>;
   CUtensorMap tq, tdo, tk, tv;
   const uint64_t bhq = static_cast<uint64_t>(pb.B) * pb.Hq, bhk = static_cast<uint64_t>(pb.B) * pb.Hkv;
-  if (!make_tmap_bf16_3d(&tq, q, bhq, pb.N, D, kBlockM) ||
-      !make_tmap_bf16_3d(&tdo, dO, bhq, pb.N, D, kBlockM) ||
-      !make_tmap_bf16_3d(&tk, k, bhk, pb.N, D, kBlockN) ||
-      !make_tmap_bf16_3d(&tv, v, bhk, pb.N, D, kBlockN))
+  if (!make_tmap_3d(&tq, q, bhq, pb.N, D, kBlockM, F16) ||
+      !make_tmap_3d(&tdo, dO, bhq, pb.N, D, kBlockM, F16) ||
+      !make_tmap_3d(&tk, k, bhk, pb.N, D, kBlockN, F16) ||
+      !make_tmap_3d(&tv, v, bhk, pb.N, D, kBlockN, F16))
     return cudaErrorInvalidValue;
-  auto kern = swa_dq_kernel<D>;
+  auto kern = swa_dq_kernel<D, F16>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   DqArgs a;
   a.lse = lse;
   a.delta = delta;
-  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.dq = static_cast<uint16_t*>(dq);
   a.BH = pb.B * pb.Hq;
   a.Hq = pb.Hq;
   a.Hkv = pb.Hkv;
@@ -435,8 +435,12 @@ cudaError_t launch_dq_d(const Problem& pb, const void* q, const void* k, const v
 cudaError_t launch_bwd_dq(const Problem& pb, const void* q, const void* k, const void* v,
                           const void* dO, const float* lse, const float* delta, void* dq,
                           cudaStream_t stream) {
-  if (pb.D == 64) return launch_dq_d<64>(pb, q, k, v, dO, lse, delta, dq, stream);
-  if (pb.D == 128) return launch_dq_d<128>(pb, q, k, v, dO, lse, delta, dq, stream);
+  if (pb.D == 64)
+    return pb.f16 ? launch_dq_d<64, true>(pb, q, k, v, dO, lse, delta, dq, stream)
+                  : launch_dq_d<64, false>(pb, q, k, v, dO, lse, delta, dq, stream);
+  if (pb.D == 128)
+    return pb.f16 ? launch_dq_d<128, true>(pb, q, k, v, dO, lse, delta, dq, stream)
+                  : launch_dq_d<128, false>(pb, q, k, v, dO, lse, delta, dq, stream);
   return cudaErrorInvalidValue;
 }
 

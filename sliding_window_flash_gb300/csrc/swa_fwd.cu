@@ -111,7 +111,7 @@ __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdArgs& a) {
   return f;
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(384, 1)
     swa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -231,8 +231,8 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdS = idesc_bf16(kBlockM, kBlockN, false, false);
-    constexpr uint32_t kIdO = idesc_bf16(kBlockM, D, false, true);
+    constexpr uint32_t kIdS = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockM, kBlockN, false, false);
+    constexpr uint32_t kIdO = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockM, D, false, true);
     // S_gg = Q K_gg^T into S buffer gg & 1.  That buffer was last read by the softmax warps for
     // block gg - 2, whose P_FULL the P V of gg - 2 (issued earlier) already waited for.
     auto issue_s = [&](int gg, uint32_t sQ) -> bool {
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(384, 1)
             const float2 tt = __ffma2_rn(make_float2(x[2 * c], x[2 * c + 1]), scale2, neg_m2);
             const float2 e = make_float2(ex2(tt.x), ex2(tt.y));
             rs2[c & 3] = __fadd2_rn(rs2[c & 3], e);
-            pk[c] = pack_bf16x2(e.x, e.y);
+            pk[c] = Elem<F16>::pack(e.x, e.y);
           }
           return ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) +
                  ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(rr[c4][2 * i]) * inv_l,
+          pk[i] = Elem<F16>::pack(__uint_as_float(rr[c4][2 * i]) * inv_l,
                               __uint_as_float(rr[c4][2 * i + 1]) * inv_l);
         stage_row32_sw128(sQ, r, kHalf * h + 32u * c4, pk);
       }
@@ -483,17 +483,17 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_fwd_d(const Problem& pb, const void* q, const void* k, const void* v, void* o,
                          float* lse, cudaStream_t stream) {
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv, to;
-  if (!make_tmap_bf16_3d(&tq, q, static_cast<uint64_t>(pb.B) * pb.Hq, pb.N, D, kBlockM) ||
-      !make_tmap_bf16_3d(&to, o, static_cast<uint64_t>(pb.B) * pb.Hq, pb.N, D, kBlockM) ||
-      !make_tmap_bf16_3d(&tk, k, static_cast<uint64_t>(pb.B) * pb.Hkv, pb.N, D, kBlockN) ||
-      !make_tmap_bf16_3d(&tv, v, static_cast<uint64_t>(pb.B) * pb.Hkv, pb.N, D, kBlockN))
+  if (!make_tmap_3d(&tq, q, static_cast<uint64_t>(pb.B) * pb.Hq, pb.N, D, kBlockM, F16) ||
+      !make_tmap_3d(&to, o, static_cast<uint64_t>(pb.B) * pb.Hq, pb.N, D, kBlockM, F16) ||
+      !make_tmap_3d(&tk, k, static_cast<uint64_t>(pb.B) * pb.Hkv, pb.N, D, kBlockN, F16) ||
+      !make_tmap_3d(&tv, v, static_cast<uint64_t>(pb.B) * pb.Hkv, pb.N, D, kBlockN, F16))
     return cudaErrorInvalidValue;
-  auto kern = swa_fwd_kernel<D>;
+  auto kern = swa_fwd_kernel<D, F16>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -518,8 +518,12 @@ cudaError_t launch_fwd_d(const Problem& pb, const void* q, const void* k, const 
 
 cudaError_t launch_fwd(const Problem& pb, const void* q, const void* k, const void* v, void* o,
                        float* lse, cudaStream_t stream) {
-  if (pb.D == 64) return launch_fwd_d<64>(pb, q, k, v, o, lse, stream);
-  if (pb.D == 128) return launch_fwd_d<128>(pb, q, k, v, o, lse, stream);
+  if (pb.D == 64)
+    return pb.f16 ? launch_fwd_d<64, true>(pb, q, k, v, o, lse, stream)
+                  : launch_fwd_d<64, false>(pb, q, k, v, o, lse, stream);
+  if (pb.D == 128)
+    return pb.f16 ? launch_fwd_d<128, true>(pb, q, k, v, o, lse, stream)
+                  : launch_fwd_d<128, false>(pb, q, k, v, o, lse, stream);
   return cudaErrorInvalidValue;
 }
 

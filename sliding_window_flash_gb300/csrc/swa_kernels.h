@@ -22,6 +22,7 @@ struct Problem {
   int W;          // window, already clamped to N (W >= N is plain causal)
   float scale;    // softmax scale
   unsigned* err;  // per-device error word (bounded-wait timeouts)
+  int f16 = 0;    // element type of every tensor but LSE / Delta: 0 = bf16, 1 = fp16
 };
 
 // First and last key block a query block visits, and the same for key blocks, so that the host

@@ -12,6 +12,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "swa_kernels.h"
@@ -200,10 +201,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 //   bits 4-5 D format (1 = f32)   bits 7-9 A format (1 = bf16)   bits 10-12 B format (1 = bf16)
 //   bit 15 A major (0 K, 1 MN)    bit 16 B major                  bits 17-22 N >> 3
 //   bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+// `fmt` is the A/B operand format of kind::f16: 0 = fp16, 1 = bf16 (both operands the same).
+__host__ __device__ constexpr uint32_t idesc_f16kind(uint32_t fmt, int M, int N, bool a_mn_major,
+                                                     bool b_mn_major) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return idesc_f16kind(1u, M, N, a_mn_major, b_mn_major);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -463,6 +469,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+
+// Element type of the attention tensors: bf16 (F16 = false) or fp16.  Both are kind::f16
+// tensor-core operands; P and dS are rounded to the element type (round to nearest even) and
+// every accumulator is fp32 either way.
+template <bool F16>
+struct Elem {
+  static constexpr uint32_t kMmaFmt = F16 ? 0u : 1u;  // A/B format field of the MMA descriptor
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    if constexpr (F16) {
+      __half2 h = __floats2half2_rn(lo, hi);
+      return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+      return pack_bf16x2(lo, hi);
+    }
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t v) {
+    if constexpr (F16)
+      return __half22float2(*reinterpret_cast<const __half2*>(&v));
+    else
+      return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+  }
+};
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {

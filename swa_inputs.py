@@ -50,17 +50,20 @@ class Case:
         return f"B{self.B}_Hq{self.Hq}_Hkv{self.Hkv}_N{self.N}_D{self.D}_W{self.W}_s{self.seed}"
 
 
-def _gaussian(shape, seed: int, std: float, device: str) -> torch.Tensor:
+def _gaussian(shape, seed: int, std: float, device: str,
+              dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     x = torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
     if std != 1.0:
         x.mul_(std)
-    return x.to(torch.bfloat16)
+    return x.to(dtype)
 
 
-def make_inputs(case: Case, device: str = "cpu", with_do: bool = True) -> Dict[str, torch.Tensor]:
-    """Return {'q','k','v'[, 'do']} as contiguous bf16 tensors in [B, H, N, D] layout.
+def make_inputs(case: Case, device: str = "cpu", with_do: bool = True,
+                dtype: torch.dtype = torch.bfloat16) -> Dict[str, torch.Tensor]:
+    """Return {'q','k','v'[, 'do']} as contiguous tensors in [B, H, N, D] layout, bf16 unless
+    `dtype` says fp16 (the same fp32 draws, rounded to the element type).
 
     The same (case, device) always gives the same values.  CPU and CUDA generators give
     different streams, so the tests draw on the CPU and copy to the GPU when the oracle is
@@ -68,12 +71,13 @@ def make_inputs(case: Case, device: str = "cpu", with_do: bool = True) -> Dict[s
     """
     base = case.seed * 16
     out = {
-        "q": _gaussian((case.B, case.Hq, case.N, case.D), base + _OFFSETS["q"], 1.0, device),
-        "k": _gaussian((case.B, case.Hkv, case.N, case.D), base + _OFFSETS["k"], 1.0, device),
-        "v": _gaussian((case.B, case.Hkv, case.N, case.D), base + _OFFSETS["v"], 1.0, device),
+        "q": _gaussian((case.B, case.Hq, case.N, case.D), base + _OFFSETS["q"], 1.0, device, dtype),
+        "k": _gaussian((case.B, case.Hkv, case.N, case.D), base + _OFFSETS["k"], 1.0, device, dtype),
+        "v": _gaussian((case.B, case.Hkv, case.N, case.D), base + _OFFSETS["v"], 1.0, device, dtype),
     }
     if with_do:
-        out["do"] = _gaussian((case.B, case.Hq, case.N, case.D), base + _OFFSETS["do"], case.do_std, device)
+        out["do"] = _gaussian((case.B, case.Hq, case.N, case.D), base + _OFFSETS["do"],
+                              case.do_std, device, dtype)
     return out
 
 

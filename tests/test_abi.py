@@ -63,14 +63,17 @@ def test_version_and_strerror(lib):
     assert b"UNKNOWN" in lib.swa_strerror(99)
 
 
-def _fwd(lib, B=1, Hq=2, Hkv=1, N=16, D=64, W=4, scale=0.125, ptrs=None):
+def _fwd(lib, B=1, Hq=2, Hkv=1, N=16, D=64, W=4, scale=0.125, ptrs=None, f16=False):
     p = ptrs or [FAKE] * 5
-    return lib.swa_attn_fwd(*p, B, Hq, Hkv, N, D, W, scale, None)
+    fn = lib.swa_attn_fwd_f16 if f16 else lib.swa_attn_fwd
+    return fn(*p, B, Hq, Hkv, N, D, W, scale, None)
 
 
-def _bwd(lib, B=1, Hq=2, Hkv=1, N=16, D=64, W=4, scale=0.125, ptrs=None, ws=FAKE, ws_bytes=1 << 20):
+def _bwd(lib, B=1, Hq=2, Hkv=1, N=16, D=64, W=4, scale=0.125, ptrs=None, ws=FAKE, ws_bytes=1 << 20,
+         f16=False):
     p = ptrs or [FAKE] * 9
-    return lib.swa_attn_bwd(*p, B, Hq, Hkv, N, D, W, scale, ws, ws_bytes, None)
+    fn = lib.swa_attn_bwd_f16 if f16 else lib.swa_attn_bwd
+    return fn(*p, B, Hq, Hkv, N, D, W, scale, ws, ws_bytes, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -79,17 +82,20 @@ def _bwd(lib, B=1, Hq=2, Hkv=1, N=16, D=64, W=4, scale=0.125, ptrs=None, ws=FAKE
     (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
     (dict(D=96), 2), (dict(D=256), 2), (dict(D=32), 2),
 ])
-def test_fwd_rejects_bad_sizes(lib, kw, code):
-    assert _fwd(lib, **kw) == code
-    assert _bwd(lib, **kw) == code
+@pytest.mark.parametrize("f16", [False, True], ids=["bf16", "fp16"])
+def test_fwd_rejects_bad_sizes(lib, kw, code, f16):
+    assert _fwd(lib, f16=f16, **kw) == code
+    assert _bwd(lib, f16=f16, **kw) == code
 
 
-def test_null_and_misaligned_pointers(lib):
-    assert _fwd(lib, ptrs=[FAKE, 0, FAKE, FAKE, FAKE]) == 1
-    assert _fwd(lib, ptrs=[FAKE, FAKE, FAKE + 8, FAKE, FAKE]) == 3
-    assert _fwd(lib, ptrs=[FAKE, FAKE, FAKE, FAKE, FAKE + 4]) == 3
-    assert _bwd(lib, ptrs=[FAKE] * 8 + [0]) == 1
-    assert _bwd(lib, ptrs=[FAKE] * 8 + [FAKE + 2]) == 3
+@pytest.mark.parametrize("f16", [False, True], ids=["bf16", "fp16"])
+def test_null_and_misaligned_pointers(lib, f16):
+    assert _fwd(lib, ptrs=[FAKE, 0, FAKE, FAKE, FAKE], f16=f16) == 1
+    assert _fwd(lib, ptrs=[FAKE, FAKE, FAKE + 8, FAKE, FAKE], f16=f16) == 3
+    assert _fwd(lib, ptrs=[FAKE, FAKE, FAKE, FAKE, FAKE + 4], f16=f16) == 3
+    assert _bwd(lib, ptrs=[FAKE] * 8 + [0], f16=f16) == 1
+    assert _bwd(lib, ptrs=[FAKE] * 8 + [FAKE + 2], f16=f16) == 3
+    assert _bwd(lib, ws=0, f16=f16) == 6
 
 
 def test_workspace_checks(lib):
@@ -116,3 +122,7 @@ def test_python_binding_refuses_cpu_tensors():
     k = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         swa.swa_attn_fwd(q, k, k, 4)
+    with pytest.raises(ValueError):
+        swa.swa_attn_fwd(q.half(), k.half(), k.half(), 4)
+    with pytest.raises(TypeError):
+        swa.swa_attn_fwd(q.float(), k.float(), k.float(), 4)
