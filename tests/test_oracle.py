@@ -11,6 +11,11 @@ Pins (what they fix and why a plausible mistake fails one of them):
   * structural invariants: softmax rows sum to 1, sum_j dS[i, j] = 0, dK/dV support in [i-W+1, i].
   * planted mistakes: an off-by-one window, a wrong GQA mapping, a dropped Delta, a transposed dS
     are each caught by the pins above.
+  * queries shorter than keys and non-causal windows: torch SDPA without a mask (non-causal, full
+    window) and with triu / tril-built masks (bottom-right causal band, two-sided band); the
+    short-query problem equals the suffix of the full-length one whose extra rows carry dO = 0;
+    reversal symmetry of the two-sided window; finite differences; brute-force loops; planted
+    top-left alignment and one-sided "non-causal" windows are rejected.
 """
 import math
 
@@ -238,12 +243,15 @@ def test_pins_accept_the_oracle():
 
 
 def test_pins_reject_off_by_one_window(monkeypatch):
-    monkeypatch.setattr(orc, "visible", lambda i, j, W: ((i - j) >= 0) & ((i - j) <= W))
+    monkeypatch.setattr(orc, "visible",
+                        lambda i, j, W, off=0, causal=True: ((i + off - j) >= 0) & ((i + off - j) <= W))
     assert not _pins_pass()
 
 
 def test_pins_reject_window_excluding_self(monkeypatch):
-    monkeypatch.setattr(orc, "visible", lambda i, j, W: ((i - j) > 0) & ((i - j) <= W) | ((i == 0) & (j == 0)))
+    monkeypatch.setattr(orc, "visible",
+                        lambda i, j, W, off=0, causal=True: ((i + off - j) > 0) & ((i + off - j) <= W)
+                        | ((i + off == 0) & (j == 0)))
     assert not _pins_pass()
 
 
@@ -255,8 +263,8 @@ def test_pins_reject_strided_gqa_mapping(monkeypatch):
 def test_pins_reject_dropped_delta(monkeypatch):
     real = orc.head_backward
 
-    def no_delta(qh, kh, vh, doh, W, scale, row_block=1024):
-        r = real(qh, kh, vh, np.asarray(doh), W, scale, row_block)
+    def no_delta(qh, kh, vh, doh, W, scale, row_block=1024, causal=True):
+        r = real(qh, kh, vh, np.asarray(doh), W, scale, row_block, causal)
         # Recompute dQ/dK as if Delta were zero.
         p = orc.probabilities(qh, kh, W, scale)
         ds = p * (np.asarray(doh) @ np.asarray(vh).T)
@@ -271,8 +279,8 @@ def test_pins_reject_dropped_delta(monkeypatch):
 def test_pins_reject_transposed_ds(monkeypatch):
     real = orc.head_backward
 
-    def transposed(qh, kh, vh, doh, W, scale, row_block=1024):
-        r = real(qh, kh, vh, doh, W, scale, row_block)
+    def transposed(qh, kh, vh, doh, W, scale, row_block=1024, causal=True):
+        r = real(qh, kh, vh, doh, W, scale, row_block, causal)
         p = orc.probabilities(qh, kh, W, scale)
         ds = p * (np.asarray(doh) @ np.asarray(vh).T - r["delta"][:, None])
         r["dk"] = scale * ds @ np.asarray(qh)  # should be ds.T @ q
@@ -293,3 +301,189 @@ def test_golden_fixture_reproduces():
     out = orc.oracle_backward(inp["q"], inp["k"], inp["v"], inp["do"], rec["window"], rec["scale"])
     for key, val in rec["outputs"].items():
         assert np.max(np.abs(out[key] - np.array(val))) < 1e-12, key
+
+
+# ---------------------------------------------------------------------------------------------
+# Queries shorter than keys (bottom-right alignment: query i at key position i + Lk - Lq) and
+# non-causal windows (|pos(i) - j| < W).
+# ---------------------------------------------------------------------------------------------
+
+def _torch_masked(q, k, v, do, mask, scale):
+    """torch SDPA (float64, CPU) with an explicit boolean mask [Lq, Lk] and autograd gradients."""
+    G = q.shape[1] // k.shape[1]
+    tq = torch.tensor(q, dtype=torch.float64, requires_grad=True)
+    tk = torch.tensor(k, dtype=torch.float64, requires_grad=True)
+    tv = torch.tensor(v, dtype=torch.float64, requires_grad=True)
+    o = F.scaled_dot_product_attention(tq, tk.repeat_interleave(G, dim=1),
+                                       tv.repeat_interleave(G, dim=1), attn_mask=mask, scale=scale)
+    (o * torch.tensor(do)).sum().backward()
+    return {"o": o.detach().numpy(), "dq": tq.grad.numpy(), "dk": tk.grad.numpy(), "dv": tv.grad.numpy()}
+
+
+def _lq_lk_inputs(B, Hq, Hkv, Lq, Lk, D, seed):
+    return (_rand((B, Hq, Lq, D), seed + 1), _rand((B, Hkv, Lk, D), seed + 2),
+            _rand((B, Hkv, Lk, D), seed + 3), _rand((B, Hq, Lq, D), seed + 4))
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 1, 9, 8), (2, 4, 2, 33, 16), (1, 3, 3, 1, 4)])
+def test_noncausal_full_window_is_plain_sdpa(shape):
+    B, Hq, Hkv, N, D = shape
+    q, k, v, do = _lq_lk_inputs(B, Hq, Hkv, N, N, D, 100)
+    scale = 1.0 / math.sqrt(D)
+    G = Hq // Hkv
+    tq = torch.tensor(q, requires_grad=True)
+    tk = torch.tensor(k, requires_grad=True)
+    tv = torch.tensor(v, requires_grad=True)
+    o = F.scaled_dot_product_attention(tq, tk.repeat_interleave(G, dim=1),
+                                       tv.repeat_interleave(G, dim=1), scale=scale)
+    (o * torch.tensor(do)).sum().backward()
+    ref = {"o": o.detach().numpy(), "dq": tq.grad.numpy(), "dk": tk.grad.numpy(), "dv": tv.grad.numpy()}
+    for W in (N, N + 3):
+        out = orc.oracle_backward(q, k, v, do, W, scale, causal=False)
+        for key in ref:
+            assert _rel(out[key], ref[key]) < 1e-12, (key, W)
+
+
+@pytest.mark.parametrize("Lq,Lk", [(1, 1), (5, 5), (7, 20), (20, 20), (13, 40)])
+@pytest.mark.parametrize("W", [1, 2, 6])
+@pytest.mark.parametrize("causal", [True, False])
+def test_windows_match_library_sdpa_with_masks(Lq, Lk, W, causal):
+    """Masks for torch's SDPA built from torch.triu / torch.tril diagonals: the band of a
+    bottom-right-aligned (Lk - Lq) causal window, or its two-sided form."""
+    B, Hq, Hkv, D = 1, 4, 2, 8
+    q, k, v, do = _lq_lk_inputs(B, Hq, Hkv, Lq, Lk, D, 110)
+    scale = 0.5
+    ones = torch.ones(Lq, Lk, dtype=torch.float64)
+    off = Lk - Lq
+    upper = torch.tril(ones, diagonal=off)  # keys at or before the query's position
+    lower = torch.triu(ones, diagonal=off - (W - 1))  # keys within W - 1 before it
+    if causal:
+        mask = (upper * lower) > 0.5
+    else:
+        mask = (torch.tril(ones, diagonal=off + (W - 1)) * lower) > 0.5
+    ref = _torch_masked(q, k, v, do, mask, scale)
+    out = orc.oracle_backward(q, k, v, do, W, scale, causal=causal)
+    for key in ref:
+        assert _rel(out[key], ref[key]) < 1e-12, key
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("W", [1, 4, 100])
+def test_shorter_queries_are_the_suffix_of_the_full_problem(causal, W):
+    """Lq < Lk equals the last Lq query rows of the Lq = Lk problem whose first Lk - Lq query rows
+    carry dO = 0 (those rows then add nothing to dK or dV)."""
+    B, Hq, Hkv, Lq, Lk, D = 1, 2, 1, 9, 25, 6
+    q, k, v, do = _lq_lk_inputs(B, Hq, Hkv, Lq, Lk, D, 120)
+    pre = _rand((B, Hq, Lk - Lq, D), 129)
+    q_full = np.concatenate([pre, q], axis=2)
+    do_full = np.concatenate([np.zeros_like(pre), do], axis=2)
+    scale = 0.7
+    short = orc.oracle_backward(q, k, v, do, W, scale, causal=causal)
+    full = orc.oracle_backward(q_full, k, v, do_full, W, scale, causal=causal)
+    for key in ("o", "lse", "delta", "dq"):
+        assert np.max(np.abs(short[key] - full[key][:, :, Lk - Lq:])) < 1e-12, key
+    for key in ("dk", "dv"):
+        assert np.max(np.abs(short[key] - full[key])) < 1e-12, key
+
+
+def test_noncausal_window_is_symmetric_under_reversal():
+    """Reversing the sequence maps a two-sided window onto itself."""
+    B, Hq, Hkv, N, D, W = 1, 2, 1, 17, 5, 4
+    q, k, v, do = _lq_lk_inputs(B, Hq, Hkv, N, N, D, 130)
+    scale = 0.6
+    a = orc.oracle_backward(q, k, v, do, W, scale, causal=False)
+    flip = lambda x: x[:, :, ::-1].copy()  # noqa: E731
+    b = orc.oracle_backward(flip(q), flip(k), flip(v), flip(do), W, scale, causal=False)
+    for key in ("o", "dq", "dk", "dv"):
+        assert np.max(np.abs(a[key] - flip(b[key]))) < 1e-12, key
+
+
+@pytest.mark.parametrize("Lq,Lk,W,causal", [(5, 9, 3, True), (6, 6, 3, False), (4, 10, 4, False)])
+def test_finite_differences_lq_lk(Lq, Lk, W, causal):
+    B, Hq, Hkv, D = 1, 2, 1, 3
+    q, k, v, do = _lq_lk_inputs(B, Hq, Hkv, Lq, Lk, D, 140)
+    scale = 0.8
+    out = orc.oracle_backward(q, k, v, do, W, scale, causal=causal)
+    h = 1e-6
+
+    def loss(qq, kk, vv):
+        o, _ = orc.oracle_forward(qq, kk, vv, W, scale, causal=causal)
+        return float(np.sum(do * o))
+
+    for name, arr, grad in (("q", q, out["dq"]), ("k", k, out["dk"]), ("v", v, out["dv"])):
+        fd = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = {"q": q, "k": k, "v": v}
+            args_p[name] = arr.copy()
+            args_m[name] = arr.copy()
+            args_p[name][idx] += h
+            args_m[name][idx] -= h
+            fd[idx] = (loss(args_p["q"], args_p["k"], args_p["v"])
+                       - loss(args_m["q"], args_m["k"], args_m["v"])) / (2 * h)
+        assert np.linalg.norm(fd - grad) / max(np.linalg.norm(fd), 1e-3) < 1e-6, name
+
+
+def _brute_force_forward_general(q, k, v, W, scale, causal):
+    """Loops with math.exp; query i at key position i + len(k) - len(q)."""
+    Lq, Lk, D = len(q), len(k), len(q[0])
+    off = Lk - Lq
+    o = [[0.0] * len(v[0]) for _ in range(Lq)]
+    lse = [0.0] * Lq
+    for i in range(Lq):
+        scores = []
+        for j in range(Lk):
+            d = i + off - j
+            if (0 <= d < W) if causal else (-W < d < W):
+                scores.append((j, scale * sum(q[i][c] * k[j][c] for c in range(D))))
+        m = max(sc for _, sc in scores)
+        lse[i] = m + math.log(sum(math.exp(sc - m) for _, sc in scores))
+        for j, sc in scores:
+            p = math.exp(sc - lse[i])
+            for c in range(len(v[0])):
+                o[i][c] += p * v[j][c]
+    return np.array(o), np.array(lse)
+
+
+@pytest.mark.parametrize("Lq,Lk,W,causal", [(3, 8, 2, True), (8, 8, 3, False), (2, 7, 9, False),
+                                            (1, 6, 1, True)])
+def test_brute_force_loops_lq_lk(Lq, Lk, W, causal):
+    D = 3
+    q, k, v = _rand((Lq, D), 150), _rand((Lk, D), 151), _rand((Lk, D), 152)
+    o, lse = orc.head_forward(q, k, v, W, 0.9, causal=causal)
+    o2, lse2 = _brute_force_forward_general(q.tolist(), k.tolist(), v.tolist(), W, 0.9, causal)
+    assert np.max(np.abs(o - o2)) < 1e-12
+    assert np.max(np.abs(lse - lse2)) < 1e-12
+
+
+def _lq_lk_pins_pass():
+    """The masked-SDPA pin on a short-query case, causal and not; True iff both agree."""
+    B, Hq, Hkv, Lq, Lk, D, W = 1, 2, 1, 6, 15, 4, 5
+    q, k, v, do = _lq_lk_inputs(B, Hq, Hkv, Lq, Lk, D, 160)
+    ones = torch.ones(Lq, Lk, dtype=torch.float64)
+    off = Lk - Lq
+    lower = torch.triu(ones, diagonal=off - (W - 1))
+    ok = True
+    for causal, upper in ((True, torch.tril(ones, diagonal=off)),
+                          (False, torch.tril(ones, diagonal=off + W - 1))):
+        ref = _torch_masked(q, k, v, do, (upper * lower) > 0.5, 0.5)
+        out = orc.oracle_backward(q, k, v, do, W, 0.5, causal=causal)
+        ok = ok and all(_rel(out[key], ref[key]) < 1e-12 for key in ref)
+    return ok
+
+
+def test_lq_lk_pins_accept_the_oracle():
+    assert _lq_lk_pins_pass()
+
+
+def test_lq_lk_pins_reject_top_left_alignment(monkeypatch):
+    monkeypatch.setattr(orc, "_offset", lambda qh, kh: 0)
+    assert not _lq_lk_pins_pass()
+
+
+def test_lq_lk_pins_reject_one_sided_noncausal_window(monkeypatch):
+    real = orc.visible
+    monkeypatch.setattr(orc, "visible", lambda i, j, W, off=0, causal=True: real(i, j, W, off, True))
+    assert not _lq_lk_pins_pass()
