@@ -108,6 +108,31 @@ swa_status swa_attn_bwd_f16(const void* q, const void* k, const void* v, const v
                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * General forms: queries shorter than keys, non-causal windows, either element type.
+ *   q, o, dO, dq : [B, Hq, Lq, D];  k, v, dk, dv : [B, Hkv, Lk, D];  lse : [B, Hq, Lq] fp32.
+ *   Lq <= Lk     : the queries are the last Lq positions of the key sequence (query i sits at key
+ *                  position i + Lk - Lq); Lq > Lk returns SWA_ERR_INVALID_ARG.
+ *   causal       : 1 -> key j visible to query i iff 0 <= i + Lk - Lq - j < window;
+ *                  0 -> iff |i + Lk - Lq - j| < window (window >= Lk: full attention).
+ *                  Other values return SWA_ERR_INVALID_ARG.
+ *   f16          : 0 -> bf16 tensors, 1 -> fp16 tensors; other values SWA_ERR_INVALID_ARG.
+ *   workspace    : at least swa_attn_bwd_workspace_bytes(B, Hq, Lq, D) bytes.
+ * Key blocks that no query sees (a short query suffix under a narrow window) get dk = dv = 0.
+ * The pages' gradient sweep covers "queries shorter than keys" and windows "causal and not"
+ * (Lab 28, numbers entry "Gradient parity, small shapes"); neither is defined there further, and
+ * the alignment and two-sided window above are this library's reading.  With Lq = Lk, causal = 1
+ * these are swa_attn_fwd / swa_attn_bwd (f16 = 1: the _f16 forms).
+ */
+swa_status swa_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal,
+                           float scale, int f16, cudaStream_t stream);
+swa_status swa_attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                           const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                           int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal,
+                           float scale, int f16, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/*
  * The three phases swa_attn_bwd runs, callable one by one (same arguments, same checks, same
  * kernels), e.g. to time each kernel or to run the dK/dV and dQ phases on two streams once the
  * preprocess has finished.  `delta` is the workspace of swa_attn_bwd (fp32 [B,Hq,N]).

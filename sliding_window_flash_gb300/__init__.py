@@ -53,6 +53,7 @@ _c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
 SIGNATURES = {
     "swa_attn_fwd": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _vp]),
     "swa_attn_fwd_f16": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _vp]),
+    "swa_attn_fwd_ex": (_c_int, [_vp] * 5 + [_c_int] * 8 + [_c_float, _c_int, _vp]),
     "swa_attn_bwd_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
     "swa_attn_bwd": (
         _c_int,
@@ -61,6 +62,10 @@ SIGNATURES = {
     "swa_attn_bwd_f16": (
         _c_int,
         [_vp] * 9 + [_c_int] * 6 + [_c_float, _vp, ctypes.c_size_t, _vp],
+    ),
+    "swa_attn_bwd_ex": (
+        _c_int,
+        [_vp] * 9 + [_c_int] * 8 + [_c_float, _c_int, _vp, ctypes.c_size_t, _vp],
     ),
     "swa_attn_bwd_preprocess": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_vp]),
     "swa_attn_bwd_dkdv": (_c_int, [_vp] * 8 + [_c_int] * 6 + [_c_float, _vp]),
@@ -126,11 +131,12 @@ def _check_tensor(t, name, shape, dtype):
 
 
 def _dims(q, k):
+    """(B, Hq, Hkv, Lq, Lk, D) of q [B, Hq, Lq, D] and k [B, Hkv, Lk, D]."""
     if q.dim() != 4 or k.dim() != 4:
-        raise ValueError("q and k must be 4-D [B, H, N, D]")
-    B, Hq, N, D = q.shape
-    Hkv = k.shape[1]
-    return B, Hq, Hkv, N, D
+        raise ValueError("q and k must be 4-D [B, H, L, D]")
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    return B, Hq, Hkv, Lq, Lk, D
 
 
 def _scale(scale, D):
@@ -146,26 +152,37 @@ def _elem_dtype(q):
     return q.dtype
 
 
-def swa_attn_fwd(q, k, v, window: int, scale: Optional[float] = None, out=None, lse=None):
-    """Forward: returns (o [B,Hq,N,D] in q's dtype (bf16 or fp16), lse [B,Hq,N] fp32)."""
+def swa_attn_fwd(q, k, v, window: int, scale: Optional[float] = None, out=None, lse=None,
+                 causal: bool = True):
+    """Forward: returns (o [B,Hq,Lq,D] in q's dtype (bf16 or fp16), lse [B,Hq,Lq] fp32).
+
+    q [B,Hq,Lq,D], k and v [B,Hkv,Lk,D] with Lq <= Lk: the queries are the last Lq positions of the
+    keys.  causal=False selects the two-sided window |pos - j| < window.
+    """
     import torch
 
     lib = load()
-    B, Hq, Hkv, N, D = _dims(q, k)
+    B, Hq, Hkv, Lq, Lk, D = _dims(q, k)
     dt = _elem_dtype(q)
-    _check_tensor(q, "q", (B, Hq, N, D), dt)
-    _check_tensor(k, "k", (B, Hkv, N, D), dt)
-    _check_tensor(v, "v", (B, Hkv, N, D), dt)
+    _check_tensor(q, "q", (B, Hq, Lq, D), dt)
+    _check_tensor(k, "k", (B, Hkv, Lk, D), dt)
+    _check_tensor(v, "v", (B, Hkv, Lk, D), dt)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
-        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
-    _check_tensor(out, "out", (B, Hq, N, D), dt)
-    _check_tensor(lse, "lse", (B, Hq, N), torch.float32)
-    name = "swa_attn_fwd_f16" if dt == torch.float16 else "swa_attn_fwd"
-    rc = getattr(lib, name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                            lse.data_ptr(), B, Hq, Hkv, N, D, int(window), _scale(scale, D),
-                            _stream_handle(q.device))
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    _check_tensor(out, "out", (B, Hq, Lq, D), dt)
+    _check_tensor(lse, "lse", (B, Hq, Lq), torch.float32)
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr())
+    f16 = dt == torch.float16
+    st = _stream_handle(q.device)
+    if Lq == Lk and causal:
+        name = "swa_attn_fwd_f16" if f16 else "swa_attn_fwd"
+        rc = getattr(lib, name)(*ptrs, B, Hq, Hkv, Lq, D, int(window), _scale(scale, D), st)
+    else:
+        name = "swa_attn_fwd_ex"
+        rc = lib.swa_attn_fwd_ex(*ptrs, B, Hq, Hkv, Lq, Lk, D, int(window), int(bool(causal)),
+                                 _scale(scale, D), int(f16), st)
     if rc != 0:
         raise SwaError(rc, name)
     return out, lse
@@ -176,31 +193,38 @@ def swa_attn_bwd_workspace_bytes(B: int, Hq: int, N: int, D: int) -> int:
 
 
 def swa_attn_bwd(q, k, v, o, do, lse, window: int, scale: Optional[float] = None,
-                 dq=None, dk=None, dv=None, workspace=None) -> Tuple:
+                 dq=None, dk=None, dv=None, workspace=None, causal: bool = True) -> Tuple:
     """Backward of sum(do * o): returns (dq, dk, dv) in q's dtype (bf16 or fp16), dk/dv summed
-    over each kv group."""
+    over each kv group.  Shapes and window as in swa_attn_fwd."""
     import torch
 
     lib = load()
-    B, Hq, Hkv, N, D = _dims(q, k)
+    B, Hq, Hkv, Lq, Lk, D = _dims(q, k)
     dt = _elem_dtype(q)
-    for t, name, hs in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq)):
-        _check_tensor(t, name, (B, hs, N, D), dt)
-    _check_tensor(lse, "lse", (B, Hq, N), torch.float32)
+    for t, name, hs, L in ((q, "q", Hq, Lq), (k, "k", Hkv, Lk), (v, "v", Hkv, Lk), (o, "o", Hq, Lq),
+                           (do, "do", Hq, Lq)):
+        _check_tensor(t, name, (B, hs, L, D), dt)
+    _check_tensor(lse, "lse", (B, Hq, Lq), torch.float32)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    for t, name, hs in ((dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
-        _check_tensor(t, name, (B, hs, N, D), dt)
-    ws_bytes = int(lib.swa_attn_bwd_workspace_bytes(B, Hq, N, D))
+    for t, name, hs, L in ((dq, "dq", Hq, Lq), (dk, "dk", Hkv, Lk), (dv, "dv", Hkv, Lk)):
+        _check_tensor(t, name, (B, hs, L, D), dt)
+    ws_bytes = int(lib.swa_attn_bwd_workspace_bytes(B, Hq, Lq, D))
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    name = "swa_attn_bwd_f16" if dt == torch.float16 else "swa_attn_bwd"
-    rc = getattr(lib, name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                            B, Hq, Hkv, N, D, int(window), _scale(scale, D),
-                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                            _stream_handle(q.device))
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
+    ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    f16 = dt == torch.float16
+    st = _stream_handle(q.device)
+    if Lq == Lk and causal:
+        name = "swa_attn_bwd_f16" if f16 else "swa_attn_bwd"
+        rc = getattr(lib, name)(*ptrs, B, Hq, Hkv, Lq, D, int(window), _scale(scale, D), *ws, st)
+    else:
+        name = "swa_attn_bwd_ex"
+        rc = lib.swa_attn_bwd_ex(*ptrs, B, Hq, Hkv, Lq, Lk, D, int(window), int(bool(causal)),
+                                 _scale(scale, D), int(f16), *ws, st)
     if rc != 0:
         raise SwaError(rc, name)
     return dq, dk, dv
@@ -216,7 +240,9 @@ def swa_attn_bwd_phases(q, k, v, o, do, lse, window: int, scale: Optional[float]
     import torch
 
     lib = load()
-    B, Hq, Hkv, N, D = _dims(q, k)
+    B, Hq, Hkv, N, Lk, D = _dims(q, k)
+    if Lk != N:
+        raise ValueError("the phase entry points take equal query and key lengths")
     sc = _scale(scale, D)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -263,20 +289,22 @@ def _make_autograd():
     import torch
 
     class SlidingWindowAttention(torch.autograd.Function):
-        """o = attention(q, k, v) with a causal window; saves only (o, lse) for the backward."""
+        """o = attention(q, k, v) under a sliding window (causal unless causal=False); saves only
+        (o, lse) for the backward."""
 
         @staticmethod
-        def forward(ctx, q, k, v, window: int, scale: Optional[float] = None):
-            o, lse = swa_attn_fwd(q, k, v, window, scale)
+        def forward(ctx, q, k, v, window: int, scale: Optional[float] = None, causal: bool = True):
+            o, lse = swa_attn_fwd(q, k, v, window, scale, causal=causal)
             ctx.save_for_backward(q, k, v, o, lse)
-            ctx.window, ctx.scale = window, scale
+            ctx.window, ctx.scale, ctx.causal = window, scale, causal
             return o
 
         @staticmethod
         def backward(ctx, do):
             q, k, v, o, lse = ctx.saved_tensors
-            dq, dk, dv = swa_attn_bwd(q, k, v, o, do.contiguous(), lse, ctx.window, ctx.scale)
-            return dq, dk, dv, None, None
+            dq, dk, dv = swa_attn_bwd(q, k, v, o, do.contiguous(), lse, ctx.window, ctx.scale,
+                                      causal=ctx.causal)
+            return dq, dk, dv, None, None, None
 
     return SlidingWindowAttention
 

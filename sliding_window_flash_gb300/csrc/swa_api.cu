@@ -51,64 +51,86 @@ swa_status current_device(unsigned** err) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-swa_status check_sizes(int B, int Hq, int Hkv, int N, int D, int window, float scale) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || window < 1) return SWA_ERR_INVALID_ARG;
+swa_status check_shape(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, float scale) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq || window < 1) return SWA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return SWA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return SWA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return SWA_ERR_UNSUPPORTED;
-  // Index arithmetic: row indices bh*N + i in 32 bits, grid in 31 bits.
-  const long long rows = static_cast<long long>(B) * Hq * N;
-  const long long tiles = static_cast<long long>(B) * Hq * ((N + swa::kBlockM - 1) / swa::kBlockM);
-  if (rows >= (1ll << 31) || tiles >= (1ll << 31)) return SWA_ERR_INVALID_ARG;
+  // Index arithmetic: row indices bh*L + i in 32 bits, grids in 31 bits.
+  const long long q_rows = static_cast<long long>(B) * Hq * Lq;
+  const long long k_rows = static_cast<long long>(B) * Hkv * Lk;
+  const long long q_tiles = static_cast<long long>(B) * Hq * ((Lq + swa::kBlockM - 1) / swa::kBlockM);
+  const long long k_tiles = static_cast<long long>(B) * Hkv * ((Lk + swa::kBlockN - 1) / swa::kBlockN);
+  if (q_rows >= (1ll << 31) || k_rows >= (1ll << 31) || q_tiles >= (1ll << 31) ||
+      k_tiles >= (1ll << 31))
+    return SWA_ERR_INVALID_ARG;
   return SWA_OK;
 }
 
-swa::Problem make_problem(int B, int Hq, int Hkv, int N, int D, int window, float scale,
-                          unsigned* err, int f16 = 0) {
+swa_status check_sizes(int B, int Hq, int Hkv, int N, int D, int window, float scale) {
+  return check_shape(B, Hq, Hkv, N, N, D, window, scale);
+}
+
+// Lq query rows as the last Lq positions of Lk keys; causal: 0 <= pos - j < W, else |pos - j| < W.
+swa::Problem make_problem_ex(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal,
+                             float scale, unsigned* err, int f16) {
   swa::Problem pb;
   pb.B = B;
   pb.Hq = Hq;
   pb.Hkv = Hkv;
-  pb.N = N;
   pb.D = D;
-  pb.W = window < N ? window : N;  // a window that covers the sequence is plain causal
+  // A window reaching past every key changes nothing; clamping keeps the offsets in range.
+  const int W = window < Lk ? window : Lk;
+  pb.span.Lq = Lq;
+  pb.span.Lk = Lk;
+  pb.span.off = Lk - Lq;
+  pb.span.dmin = causal ? 0 : -(W - 1);
+  pb.span.dmax = W - 1;
   pb.scale = scale;
   pb.err = err;
   pb.f16 = f16;
   return pb;
 }
 
-// Forward and backward for either element type (f16: 0 = bf16, 1 = fp16).
+swa::Problem make_problem(int B, int Hq, int Hkv, int N, int D, int window, float scale,
+                          unsigned* err, int f16 = 0) {
+  return make_problem_ex(B, Hq, Hkv, N, N, D, window, 1, scale, err, f16);
+}
+
+// Forward and backward for either element type (f16: 0 = bf16, 1 = fp16), any Lq <= Lk, causal
+// or not.
 swa_status fwd_impl(int f16, const void* q, const void* k, const void* v, void* o, float* lse,
-                    int B, int Hq, int Hkv, int N, int D, int window, float scale,
-                    cudaStream_t stream) {
+                    int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal,
+                    float scale, cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse) return SWA_ERR_INVALID_ARG;
-  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
+  if ((causal != 0 && causal != 1) || (f16 != 0 && f16 != 1)) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_shape(B, Hq, Hkv, Lq, Lk, D, window, scale);
   if (st != SWA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return SWA_ERR_MISALIGNED;
   unsigned* err = nullptr;
   if ((st = current_device(&err)) != SWA_OK) return st;
-  const swa::Problem pb = make_problem(B, Hq, Hkv, N, D, window, scale, err, f16);
+  const swa::Problem pb = make_problem_ex(B, Hq, Hkv, Lq, Lk, D, window, causal, scale, err, f16);
   if (swa::launch_fwd(pb, q, k, v, o, lse, stream) != cudaSuccess) return SWA_ERR_CUDA;
   return SWA_OK;
 }
 
 swa_status bwd_impl(int f16, const void* q, const void* k, const void* v, const void* o,
                     const void* dO, const float* lse, void* dq, void* dk, void* dv, int B, int Hq,
-                    int Hkv, int N, int D, int window, float scale, void* workspace,
-                    size_t workspace_bytes, cudaStream_t stream) {
+                    int Hkv, int Lq, int Lk, int D, int window, int causal, float scale,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return SWA_ERR_INVALID_ARG;
-  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
+  if ((causal != 0 && causal != 1) || (f16 != 0 && f16 != 1)) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_shape(B, Hq, Hkv, Lq, Lk, D, window, scale);
   if (st != SWA_OK) return st;
-  if (!workspace || workspace_bytes < swa_attn_bwd_workspace_bytes(B, Hq, N, D))
+  if (!workspace || workspace_bytes < swa_attn_bwd_workspace_bytes(B, Hq, Lq, D))
     return SWA_ERR_WORKSPACE;
   const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv, workspace};
   for (const void* p : ptrs)
     if (!aligned16(p)) return SWA_ERR_MISALIGNED;
   unsigned* err = nullptr;
   if ((st = current_device(&err)) != SWA_OK) return st;
-  const swa::Problem pb = make_problem(B, Hq, Hkv, N, D, window, scale, err, f16);
+  const swa::Problem pb = make_problem_ex(B, Hq, Hkv, Lq, Lk, D, window, causal, scale, err, f16);
   float* delta = static_cast<float*>(workspace);
   if (swa::launch_bwd_delta(pb, o, dO, delta, stream) != cudaSuccess) return SWA_ERR_CUDA;
   if (swa::launch_bwd_dkdv(pb, q, k, v, dO, lse, delta, dk, dv, stream) != cudaSuccess)
@@ -125,13 +147,19 @@ extern "C" {
 swa_status swa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int Hq, int Hkv, int N, int D, int window, float scale,
                         cudaStream_t stream) {
-  return fwd_impl(0, q, k, v, o, lse, B, Hq, Hkv, N, D, window, scale, stream);
+  return fwd_impl(0, q, k, v, o, lse, B, Hq, Hkv, N, N, D, window, 1, scale, stream);
 }
 
 swa_status swa_attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int Hq, int Hkv, int N, int D, int window, float scale,
                             cudaStream_t stream) {
-  return fwd_impl(1, q, k, v, o, lse, B, Hq, Hkv, N, D, window, scale, stream);
+  return fwd_impl(1, q, k, v, o, lse, B, Hq, Hkv, N, N, D, window, 1, scale, stream);
+}
+
+swa_status swa_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal,
+                           float scale, int f16, cudaStream_t stream) {
+  return fwd_impl(f16, q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, D, window, causal, scale, stream);
 }
 
 size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int N, int D) {
@@ -144,16 +172,25 @@ swa_status swa_attn_bwd(const void* q, const void* k, const void* v, const void*
                         const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
                         int N, int D, int window, float scale, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream) {
-  return bwd_impl(0, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, D, window, scale, workspace,
-                  workspace_bytes, stream);
+  return bwd_impl(0, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, N, D, window, 1, scale,
+                  workspace, workspace_bytes, stream);
 }
 
 swa_status swa_attn_bwd_f16(const void* q, const void* k, const void* v, const void* o,
                             const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
                             int Hq, int Hkv, int N, int D, int window, float scale,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  return bwd_impl(1, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, D, window, scale, workspace,
-                  workspace_bytes, stream);
+  return bwd_impl(1, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, N, D, window, 1, scale,
+                  workspace, workspace_bytes, stream);
+}
+
+swa_status swa_attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                           const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                           int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal,
+                           float scale, int f16, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  return bwd_impl(f16, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lk, D, window, causal,
+                  scale, workspace, workspace_bytes, stream);
 }
 
 swa_status swa_attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int Hq,

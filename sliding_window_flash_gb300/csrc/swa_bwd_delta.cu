@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(256) swa_delta_kernel(const uint16_t* __restri
 
 cudaError_t launch_bwd_delta(const Problem& pb, const void* o, const void* dO, float* delta,
                              cudaStream_t stream) {
-  const long long rows = static_cast<long long>(pb.B) * pb.Hq * pb.N;
+  const long long rows = static_cast<long long>(pb.B) * pb.Hq * pb.span.Lq;
   constexpr int kThreads = 256;
   const long long rows_per_block = (kThreads / 32) * (pb.D == 64 ? 4 : 2);
   long long blocks = (rows + rows_per_block - 1) / rows_per_block;

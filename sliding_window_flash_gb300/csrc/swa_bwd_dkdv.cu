@@ -67,7 +67,8 @@ struct DkdvArgs {
   const float* delta;
   uint16_t* dk;  // bf16 or fp16 elements
   uint16_t* dv;
-  int BHK, Hq, Hkv, G, N, W, nkb;
+  int BHK, Hq, Hkv, G, nkb;
+  Span span;
   float scale, scale_log2;
   unsigned* err;
 };
@@ -99,10 +100,19 @@ __global__ void __launch_bounds__(352, 1)
   const int bhk = static_cast<int>(blockIdx.x) % a.BHK;
   const int b = bhk / a.Hkv, hk = bhk % a.Hkv;
   const int k0 = kb * kBlockN;
-  const int qb_lo = bwd_first_qblock(k0);
-  const int qb_hi = bwd_last_qblock(k0, a.N, a.W);
-  const int nq = qb_hi - qb_lo + 1;  // >= 1: the diagonal block always sees the key block
-  const int T = a.G * nq;            // (query head, query block) tiles of the walk
+  const Span sp = a.span;  // window geometry, held in registers
+  const int qb_lo = sp.first_qblock(k0);
+  const int qb_hi = sp.last_qblock(k0);
+  // No query sees this key block when the queries are a short suffix of the keys: then nq <= 0,
+  // nothing is computed and dK = dV = 0 is written.
+  const int nq = qb_hi >= qb_lo ? qb_hi - qb_lo + 1 : 0;
+  const int T = a.G * nq;  // (query head, query block) tiles of the walk
+  // A query tile q0 needs no mask iff q_int_lo <= q0 <= q_int_hi (Span::interior for this key
+  // block, solved for q0 once).
+  const int q_int_lo = k0 + kBlockN - 1 + sp.dmin - sp.off;
+  const int q_int_hi = (k0 + kBlockN <= sp.Lk)
+                           ? min(k0 + sp.dmax - sp.off - (kBlockM - 1), sp.Lq - kBlockM)
+                           : -1;
   auto tile_q0 = [&](int t) { return (qb_lo + t % nq) * kBlockM; };
   auto tile_bhq = [&](int t) { return b * a.Hq + hk * a.G + t / nq; };
 
@@ -231,8 +241,8 @@ __global__ void __launch_bounds__(352, 1)
         return true;
       };
       bool ok = warp_wait(bar(C::kKVFull), 0, &abort_flag, a.err);
-      if (ok) ok = issue_s(0);
-      if (ok) ok = issue_dp(0);
+      if (ok && T > 0) ok = issue_s(0);
+      if (ok && T > 0) ok = issue_dp(0);
       for (int t = 0; ok && t < T; ++t) {
         const int sq = t % C::kQStages, sd = t % C::kDOStages;
         ok = issue_acc(t, C::kPFull, C::kColS, sDO0 + sd * C::kTileBytes, C::kColDV);  // dV
@@ -253,6 +263,7 @@ __global__ void __launch_bounds__(352, 1)
     const int r = static_cast<int>(threadIdx.x & 127);  // key row within the block = TMEM lane
     const uint32_t h = warp >> 2;                          // query-column half of every tile
     const int key = k0 + r;
+    const int vis_lo = key + sp.dmin - sp.off, vis_hi = key + sp.dmax - sp.off;  // visible queries
     const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
     const float sl2 = a.scale_log2;
     // Per-query vectors of the next tile: the h = 0 threads fetch LSE, the h = 1 threads Delta,
@@ -261,14 +272,14 @@ __global__ void __launch_bounds__(352, 1)
     float nxt = 0.f;
     auto fetch_row = [&](int t) {
       const int q = tile_q0(t) + r;
-      if (q < a.N) {
-        const size_t gi = static_cast<size_t>(tile_bhq(t)) * a.N + q;
+      if (q < sp.Lq) {
+        const size_t gi = static_cast<size_t>(tile_bhq(t)) * sp.Lq + q;
         nxt = h == 0 ? a.lse[gi] : a.delta[gi];
       } else {  // queries past the end contribute P = 0
         nxt = h == 0 ? SWA_POS_INF : 0.f;
       }
     };
-    fetch_row(0);
+    if (T > 0) fetch_row(0);
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int q0 = tile_q0(t);
@@ -317,10 +328,11 @@ __global__ void __launch_bounds__(352, 1)
           p[4 * i + 3] = ex2(t1.y);
         }
       }
-      // Query q0 + 64h + c sees this key iff 0 <= q0 + 64h + c - key < W.
-      const bool interior = (q0 >= k0 + kBlockN - 1) && (q0 + kBlockM - 1 - k0 < a.W);
-      if (!interior) {
-        const int lo = key - q0 - 64 * static_cast<int>(h), hi = lo + a.W - 1;
+      // Query q0 + 64h + c sees this key iff dmin <= q0 + 64h + c + off - key <= dmax, i.e.
+      // c in [vis_lo, vis_hi] - q0 - 64h (queries past the end already have P = 0).
+      if (!(q0 >= q_int_lo && q0 <= q_int_hi)) {
+        const int base = q0 + 64 * static_cast<int>(h);
+        const int lo = vis_lo - base, hi = vis_hi - base;
 #pragma unroll
         for (int c = 0; c < 64; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
       }
@@ -370,7 +382,7 @@ __global__ void __launch_bounds__(352, 1)
     if (ok && warp_wait(bar(C::kDone), 0, &abort_flag, a.err)) {
       tc_fence_after();
       // dK * scale and dV -> bf16, staged in the two Q slots (free: every MMA has completed) and
-      // written with tensor stores, one per 64-column chunk (rows past N are not written).
+      // written with tensor stores, one per 64-column chunk (rows past Lk are not written).
       constexpr int kHalf = D / 2;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
@@ -378,9 +390,16 @@ __global__ void __launch_bounds__(352, 1)
         const float mul = which == 0 ? a.scale : 1.f;
         const uint32_t stage = sQ0 + which * C::kTileBytes;
         uint32_t rr[kHalf / 32][32];
+        if (T > 0) {
 #pragma unroll
-        for (int c4 = 0; c4 < kHalf / 32; ++c4) tmem_ld32(tmem + lane_base + col + 32u * c4, rr[c4]);
-        tmem_wait_ld_all();
+          for (int c4 = 0; c4 < kHalf / 32; ++c4) tmem_ld32(tmem + lane_base + col + 32u * c4, rr[c4]);
+          tmem_wait_ld_all();
+        } else {  // no query visits this key block: its gradients are zero
+#pragma unroll
+          for (int c4 = 0; c4 < kHalf / 32; ++c4)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[c4][i] = 0u;
+        }
 #pragma unroll
         for (int c4 = 0; c4 < kHalf / 32; ++c4) {
           reg_fence(rr[c4]);
@@ -421,12 +440,12 @@ cudaError_t launch_dkdv_d(const Problem& pb, const void* q, const void* k, const
   using C = DkdvCfg<D>;
   CUtensorMap tq, tdo, tk, tv, tdk, tdv;
   const uint64_t bhq = static_cast<uint64_t>(pb.B) * pb.Hq, bhk = static_cast<uint64_t>(pb.B) * pb.Hkv;
-  if (!make_tmap_3d(&tq, q, bhq, pb.N, D, kBlockM, F16) ||
-      !make_tmap_3d(&tdo, dO, bhq, pb.N, D, kBlockM, F16) ||
-      !make_tmap_3d(&tk, k, bhk, pb.N, D, kBlockN, F16) ||
-      !make_tmap_3d(&tv, v, bhk, pb.N, D, kBlockN, F16) ||
-      !make_tmap_3d(&tdk, dk, bhk, pb.N, D, kBlockN, F16) ||
-      !make_tmap_3d(&tdv, dv, bhk, pb.N, D, kBlockN, F16))
+  if (!make_tmap_3d(&tq, q, bhq, pb.span.Lq, D, kBlockM, F16) ||
+      !make_tmap_3d(&tdo, dO, bhq, pb.span.Lq, D, kBlockM, F16) ||
+      !make_tmap_3d(&tk, k, bhk, pb.span.Lk, D, kBlockN, F16) ||
+      !make_tmap_3d(&tv, v, bhk, pb.span.Lk, D, kBlockN, F16) ||
+      !make_tmap_3d(&tdk, dk, bhk, pb.span.Lk, D, kBlockN, F16) ||
+      !make_tmap_3d(&tdv, dv, bhk, pb.span.Lk, D, kBlockN, F16))
     return cudaErrorInvalidValue;
   auto kern = swa_dkdv_kernel<D, F16>;
   cudaError_t e =
@@ -441,9 +460,8 @@ cudaError_t launch_dkdv_d(const Problem& pb, const void* q, const void* k, const
   a.Hq = pb.Hq;
   a.Hkv = pb.Hkv;
   a.G = pb.Hq / pb.Hkv;
-  a.N = pb.N;
-  a.W = pb.W;
-  a.nkb = (pb.N + kBlockN - 1) / kBlockN;
+  a.span = pb.span;
+  a.nkb = (pb.span.Lk + kBlockN - 1) / kBlockN;
   a.scale = pb.scale;
   a.scale_log2 = pb.scale * kLog2e;
   a.err = pb.err;

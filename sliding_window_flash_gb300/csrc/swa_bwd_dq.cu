@@ -68,7 +68,8 @@ struct DqArgs {
   const float* lse;
   const float* delta;
   uint16_t* dq;  // bf16 or fp16 elements
-  int BH, Hq, Hkv, G, N, W, nqb, ntiles;
+  int BH, Hq, Hkv, G, nqb, ntiles;
+  Span span;
   float scale, scale_log2;
   unsigned* err;
 };
@@ -78,14 +79,14 @@ struct DqTile {
 };
 
 // Tile t: heaviest query blocks first (the causal case gives later blocks more key blocks).
-__device__ __forceinline__ DqTile dq_tile(int t, const DqArgs& a) {
+__device__ __forceinline__ DqTile dq_tile(int t, const DqArgs& a, const Span sp) {
   DqTile f;
   const int qb = a.nqb - 1 - t / a.BH;
   f.bh = t % a.BH;
   f.bhk = (f.bh / a.Hq) * a.Hkv + (f.bh % a.Hq) / a.G;
   f.q0 = qb * kBlockM;
-  f.kb_lo = fwd_first_kblock(f.q0, a.W);
-  f.nkv = fwd_last_kblock(f.q0, a.N) - f.kb_lo + 1;
+  f.kb_lo = sp.first_kblock(f.q0);
+  f.nkv = sp.last_kblock(f.q0) - f.kb_lo + 1;
   return f;
 }
 
@@ -107,6 +108,7 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t sK0 = smem_u32(smem + C::kOffK);
   const uint32_t sV0 = smem_u32(smem + C::kOffV);
   const int tile_step = static_cast<int>(gridDim.x);
+  const Span sp = a.span;  // window geometry, held in registers
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(352, 1)
       int g = 0;  // key blocks loaded so far by this CTA
       bool ok = true;
       for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
-        const DqTile f = dq_tile(t, a);
+        const DqTile f = dq_tile(t, a, sp);
         // Q / dO of the previous tile are free once its last dP has been computed.
         if (it >= 1 && !mbar_wait(bar(C::kQDEmpty), (it - 1) & 1, &abort_flag, a.err)) break;
         mbar_arrive_expect_tx(bar(C::kQDFull), 2 * C::kTileBytes);
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(352, 1)
       int g = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < a.ntiles; t += tile_step) {
-        const DqTile f = dq_tile(t, a);
+        const DqTile f = dq_tile(t, a, sp);
         for (int j = 0; j < f.nkv; ++j, ++g) {
           const int sv = g % C::kVStages, nv = g / C::kVStages;
           if (g >= C::kVStages &&
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(352, 1)
     int g = 0;  // key blocks issued so far by this CTA
     bool ok = true;
     for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
-      const DqTile f = dq_tile(t, a);
+      const DqTile f = dq_tile(t, a, sp);
       const int n = f.nkv;
       ok = warp_wait(bar(C::kQDFull), it & 1, &abort_flag, a.err);
       if (ok) ok = issue_s(g);
@@ -278,11 +280,11 @@ __global__ void __launch_bounds__(352, 1)
     int g = 0;  // key blocks consumed so far by this CTA
     bool ok = true;
     for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
-      const DqTile f = dq_tile(t, a);
+      const DqTile f = dq_tile(t, a, sp);
       const int q0 = f.q0;
       const int row = q0 + r;
-      const bool in_range = row < a.N;
-      const size_t grow = static_cast<size_t>(f.bh) * a.N + row;
+      const bool in_range = row < sp.Lq;
+      const size_t grow = static_cast<size_t>(f.bh) * sp.Lq + row;
       // Rows past the end see P = 0 (their LSE is taken as +inf), so they add nothing.
       const float lse2 = in_range ? a.lse[grow] * kLog2e : SWA_POS_INF;
       const float dlt = in_range ? a.delta[grow] : 0.f;
@@ -304,10 +306,11 @@ __global__ void __launch_bounds__(352, 1)
         }
         warp_arrive(bar(C::kSEmpty));
         // Masked cells get S = -inf, so P = 0 there.
-        const bool interior = (k0 + kBlockN - 1 <= q0) && (q0 + kBlockM - 1 - k0 < a.W);
-        if (!interior) {
-          const int lo = row - a.W + 1 - k0 - 64 * static_cast<int>(h);
-          const int hi = row - k0 - 64 * static_cast<int>(h);
+        if (!sp.interior(q0, k0)) {
+          // Columns c (keys k0 + 64h + c) visible to row `row`, and inside the key sequence.
+          const int rel = row + sp.off - k0 - 64 * static_cast<int>(h);
+          const int lo = rel - sp.dmax;
+          const int hi = min(rel - sp.dmin, sp.Lk - 1 - k0 - 64 * static_cast<int>(h));
 #pragma unroll
           for (int c = 0; c < 64; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : SWA_NEG_INF;
         }
@@ -401,10 +404,10 @@ cudaError_t launch_dq_d(const Problem& pb, const void* q, const void* k, const v
   using C = DqCfg<D>;
   CUtensorMap tq, tdo, tk, tv;
   const uint64_t bhq = static_cast<uint64_t>(pb.B) * pb.Hq, bhk = static_cast<uint64_t>(pb.B) * pb.Hkv;
-  if (!make_tmap_3d(&tq, q, bhq, pb.N, D, kBlockM, F16) ||
-      !make_tmap_3d(&tdo, dO, bhq, pb.N, D, kBlockM, F16) ||
-      !make_tmap_3d(&tk, k, bhk, pb.N, D, kBlockN, F16) ||
-      !make_tmap_3d(&tv, v, bhk, pb.N, D, kBlockN, F16))
+  if (!make_tmap_3d(&tq, q, bhq, pb.span.Lq, D, kBlockM, F16) ||
+      !make_tmap_3d(&tdo, dO, bhq, pb.span.Lq, D, kBlockM, F16) ||
+      !make_tmap_3d(&tk, k, bhk, pb.span.Lk, D, kBlockN, F16) ||
+      !make_tmap_3d(&tv, v, bhk, pb.span.Lk, D, kBlockN, F16))
     return cudaErrorInvalidValue;
   auto kern = swa_dq_kernel<D, F16>;
   cudaError_t e =
@@ -418,9 +421,8 @@ cudaError_t launch_dq_d(const Problem& pb, const void* q, const void* k, const v
   a.Hq = pb.Hq;
   a.Hkv = pb.Hkv;
   a.G = pb.Hq / pb.Hkv;
-  a.N = pb.N;
-  a.W = pb.W;
-  a.nqb = (pb.N + kBlockM - 1) / kBlockM;
+  a.span = pb.span;
+  a.nqb = (pb.span.Lq + kBlockM - 1) / kBlockM;
   a.ntiles = a.nqb * a.BH;
   a.scale = pb.scale;
   a.scale_log2 = pb.scale * kLog2e;

@@ -90,7 +90,8 @@ struct FwdCfg {
 struct FwdArgs {
   float* lse;
   int BH;  // B * Hq
-  int Hq, Hkv, G, N, W, nqb, ntiles;
+  int Hq, Hkv, G, nqb, ntiles;
+  Span span;
   float scale_log2;  // scale * log2(e)
   unsigned* err;
 };
@@ -100,14 +101,14 @@ struct FwdTile {
 };
 
 // Tile t: heaviest query blocks first (the causal case gives later blocks more key blocks).
-__device__ __forceinline__ FwdTile fwd_tile(int t, const FwdArgs& a) {
+__device__ __forceinline__ FwdTile fwd_tile(int t, const FwdArgs& a, const Span sp) {
   FwdTile f;
   const int qb = a.nqb - 1 - t / a.BH;
   f.bh = t % a.BH;
   f.bhk = (f.bh / a.Hq) * a.Hkv + (f.bh % a.Hq) / a.G;
   f.q0 = qb * kBlockM;
-  f.kb_lo = fwd_first_kblock(f.q0, a.W);
-  f.nkv = fwd_last_kblock(f.q0, a.N) - f.kb_lo + 1;
+  f.kb_lo = sp.first_kblock(f.q0);
+  f.nkv = sp.last_kblock(f.q0) - f.kb_lo + 1;
   return f;
 }
 
@@ -129,6 +130,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sV0 = smem_u32(smem + C::kOffV);
   float* s_red = reinterpret_cast<float*>(smem + C::kOffRed);
   const int tile_step = static_cast<int>(gridDim.x);
+  const Span sp = a.span;  // window geometry, held in registers
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(384, 1)
       int g = 0;  // key blocks loaded so far by this CTA
       bool ok = true;
       for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
-        const FwdTile f = fwd_tile(t, a);
+        const FwdTile f = fwd_tile(t, a, sp);
         const int qbuf = it & 1;
         // The Q buffer was last the staging tile of tile it - 2's output.
         if (it >= 2 && !mbar_wait(bar(C::kQEmpty + qbuf), ((it - 2) >> 1) & 1, &abort_flag, a.err))
@@ -212,7 +214,7 @@ __global__ void __launch_bounds__(384, 1)
       int g = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < a.ntiles; t += tile_step) {
-        const FwdTile f = fwd_tile(t, a);
+        const FwdTile f = fwd_tile(t, a, sp);
         for (int j = 0; j < f.nkv; ++j, ++g) {
           const int sv = g % C::kVStages, nv = g / C::kVStages;
           if (g >= C::kVStages &&
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(384, 1)
     int g = 0;  // key blocks issued so far by this CTA
     bool ok = true;
     for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
-      const FwdTile f = fwd_tile(t, a);
+      const FwdTile f = fwd_tile(t, a, sp);
       const uint32_t sQ = sQ0 + (it & 1) * C::kTileBytes;
       ok = warp_wait(bar(C::kQFull + (it & 1)), (it >> 1) & 1, &abort_flag, a.err);
       if (ok) ok = issue_s(g, sQ);
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp == 10) {
     // ------------------------------------------------------------------ output stores
     for (int t = blockIdx.x, it = 0; t < a.ntiles; t += tile_step, ++it) {
-      const FwdTile f = fwd_tile(t, a);
+      const FwdTile f = fwd_tile(t, a, sp);
       const int b = it & 1;
       if (!warp_wait(bar(C::kOutFull + b), (it >> 1) & 1, &abort_flag, a.err)) break;
       if (lane == 0) {
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(384, 1)
     int g = 0;  // key blocks consumed so far by this CTA
     bool ok = true;
     for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
-      const FwdTile f = fwd_tile(t, a);
+      const FwdTile f = fwd_tile(t, a, sp);
       const int q0 = f.q0;
       const int row = q0 + r;
       float m_ref = SWA_NEG_INF;  // reference max (log2 domain) that P and l are taken against
@@ -339,10 +341,12 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(rr[i >> 5][i & 31]);
         }
-        // Window mask: the cells of this block visible to row `row` are keys in [row-W+1, row].
-        const bool interior = (k0 + kBlockN - 1 <= q0) && (q0 + kBlockM - 1 - k0 < a.W);
-        if (!interior) {
-          const int hi = row - k0 - 64 * static_cast<int>(h), lo = hi - a.W + 1;
+        // Window mask (the tile is not wholly visible): keep the cells row `row` sees.
+        if (!sp.interior(q0, k0)) {
+          // Columns c (keys k0 + 64h + c) visible to row `row`, and inside the key sequence.
+          const int rel = row + sp.off - k0 - 64 * static_cast<int>(h);
+          const int lo = rel - sp.dmax;
+          const int hi = min(rel - sp.dmin, sp.Lk - 1 - k0 - 64 * static_cast<int>(h));
 #pragma unroll
           for (int c = 0; c < 64; ++c) x[c] = (c >= lo && c <= hi) ? x[c] : SWA_NEG_INF;
         }
@@ -455,8 +459,8 @@ __global__ void __launch_bounds__(384, 1)
       const float l_row = l + l_other;
       const float inv_l = 1.f / l_row;
       const float m_use = (m_ref == SWA_NEG_INF) ? 0.f : m_ref;
-      if (row < a.N && h == 0)
-        a.lse[static_cast<size_t>(f.bh) * a.N + row] = (m_use + log2f(l_row)) * kLn2;
+      if (row < sp.Lq && h == 0)
+        a.lse[static_cast<size_t>(f.bh) * sp.Lq + row] = (m_use + log2f(l_row)) * kLn2;
       // O / l -> bf16, staged in this tile's Q buffer (free: every S MMA of the tile has
       // completed) in the swizzled layout of the TMA map; warp 10 stores it.
       const uint32_t sQ = sQ0 + (it & 1) * C::kTileBytes;
@@ -488,10 +492,11 @@ cudaError_t launch_fwd_d(const Problem& pb, const void* q, const void* k, const 
                          float* lse, cudaStream_t stream) {
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv, to;
-  if (!make_tmap_3d(&tq, q, static_cast<uint64_t>(pb.B) * pb.Hq, pb.N, D, kBlockM, F16) ||
-      !make_tmap_3d(&to, o, static_cast<uint64_t>(pb.B) * pb.Hq, pb.N, D, kBlockM, F16) ||
-      !make_tmap_3d(&tk, k, static_cast<uint64_t>(pb.B) * pb.Hkv, pb.N, D, kBlockN, F16) ||
-      !make_tmap_3d(&tv, v, static_cast<uint64_t>(pb.B) * pb.Hkv, pb.N, D, kBlockN, F16))
+  const uint64_t bhq = static_cast<uint64_t>(pb.B) * pb.Hq, bhk = static_cast<uint64_t>(pb.B) * pb.Hkv;
+  if (!make_tmap_3d(&tq, q, bhq, pb.span.Lq, D, kBlockM, F16) ||
+      !make_tmap_3d(&to, o, bhq, pb.span.Lq, D, kBlockM, F16) ||
+      !make_tmap_3d(&tk, k, bhk, pb.span.Lk, D, kBlockN, F16) ||
+      !make_tmap_3d(&tv, v, bhk, pb.span.Lk, D, kBlockN, F16))
     return cudaErrorInvalidValue;
   auto kern = swa_fwd_kernel<D, F16>;
   cudaError_t e =
@@ -503,9 +508,8 @@ cudaError_t launch_fwd_d(const Problem& pb, const void* q, const void* k, const 
   a.Hq = pb.Hq;
   a.Hkv = pb.Hkv;
   a.G = pb.Hq / pb.Hkv;
-  a.N = pb.N;
-  a.W = pb.W;
-  a.nqb = (pb.N + kBlockM - 1) / kBlockM;
+  a.span = pb.span;
+  a.nqb = (pb.span.Lq + kBlockM - 1) / kBlockM;
   a.ntiles = a.nqb * a.BH;
   a.scale_log2 = pb.scale * kLog2e;
   a.err = pb.err;

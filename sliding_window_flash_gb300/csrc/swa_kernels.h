@@ -16,30 +16,52 @@ constexpr unsigned kErrSmemLayout = 2u;   // dynamic shared memory not 1024-byte
 constexpr int kBlockM = 128;  // query rows per tile
 constexpr int kBlockN = 128;  // key rows per tile
 
-// Shape and window of one call.  All tensors are contiguous [B, H, N, D].
+// Window geometry.  Queries i in [0, Lq), keys j in [0, Lk), Lq <= Lk; query i sits at key
+// position i + off, off = Lk - Lq (the queries are the suffix of the key sequence).  Key j is
+// visible to query i iff dmin <= i + off - j <= dmax: [0, W - 1] for a causal sliding window (the
+// query itself included), [-(W - 1), W - 1] for a non-causal one.  Every query sees at least the
+// key at its own position.  The host and the kernels use these same functions for the block walks.
+struct Span {
+  int Lq, Lk, off, dmin, dmax;
+
+  // Key blocks a query block [q0, q0 + kBlockM) visits (never empty for q0 < Lq).
+  __host__ __device__ int first_kblock(int q0) const {
+    const int lo = q0 + off - dmax;
+    return lo > 0 ? lo / kBlockN : 0;
+  }
+  __host__ __device__ int last_kblock(int q0) const {
+    const int q_last = (q0 + kBlockM - 1 < Lq - 1) ? q0 + kBlockM - 1 : Lq - 1;
+    const int hi = q_last + off - dmin;
+    return (hi < Lk - 1 ? hi : Lk - 1) / kBlockN;
+  }
+  // Query blocks a key block [k0, k0 + kBlockN) is visited by; first > last when none is.
+  __host__ __device__ int first_qblock(int k0) const {
+    const int lo = k0 + dmin - off;
+    return lo > 0 ? lo / kBlockM : 0;
+  }
+  __host__ __device__ int last_qblock(int k0) const {
+    const long long k_last = (k0 + kBlockN - 1 < Lk - 1) ? k0 + kBlockN - 1 : Lk - 1;
+    const long long hi = k_last + dmax - off;
+    if (hi < 0) return -1;
+    return static_cast<int>((hi < Lq - 1 ? hi : Lq - 1) / kBlockM);
+  }
+  // True when every cell of the (query block q0, key block k0) tile is visible and inside both
+  // sequences, so the tile needs no mask.
+  __host__ __device__ bool interior(int q0, int k0) const {
+    return q0 + off - (k0 + kBlockN - 1) >= dmin && q0 + kBlockM - 1 + off - k0 <= dmax &&
+           k0 + kBlockN <= Lk && q0 + kBlockM <= Lq;
+  }
+};
+
+// Shape and window of one call.  Query tensors (q, o, dO, dq) are contiguous [B, Hq, Lq, D], key
+// tensors (k, v, dk, dv) [B, Hkv, Lk, D], LSE and Delta [B, Hq, Lq].
 struct Problem {
-  int B, Hq, Hkv, N, D;
-  int W;          // window, already clamped to N (W >= N is plain causal)
+  int B, Hq, Hkv, D;
+  Span span;
   float scale;    // softmax scale
   unsigned* err;  // per-device error word (bounded-wait timeouts)
   int f16 = 0;    // element type of every tensor but LSE / Delta: 0 = bf16, 1 = fp16
 };
-
-// First and last key block a query block visits, and the same for key blocks, so that the host
-// and the kernels agree on the walk.  Window rule: query i sees key j iff 0 <= i - j < W.
-__host__ __device__ inline int fwd_first_kblock(int q0, int W) {
-  const int lo = q0 - W + 1;
-  return lo > 0 ? lo / kBlockN : 0;
-}
-__host__ __device__ inline int fwd_last_kblock(int q0, int N) {
-  const int hi = q0 + kBlockM - 1;
-  return (hi < N - 1 ? hi : N - 1) / kBlockN;
-}
-__host__ __device__ inline int bwd_first_qblock(int k0) { return k0 / kBlockM; }
-__host__ __device__ inline int bwd_last_qblock(int k0, int N, int W) {
-  const long long hi = static_cast<long long>(k0) + kBlockN - 1 + W - 1;
-  return static_cast<int>((hi < N - 1 ? hi : N - 1) / kBlockM);
-}
 
 // Streaming multiprocessors of the current device (cached per device); persistent kernels launch
 // one CTA per SM.

@@ -98,6 +98,30 @@ def test_null_and_misaligned_pointers(lib, f16):
     assert _bwd(lib, ws=0, f16=f16) == 6
 
 
+def _fwd_ex(lib, B=1, Hq=2, Hkv=1, Lq=16, Lk=40, D=64, W=4, causal=1, scale=0.125, f16=0):
+    return lib.swa_attn_fwd_ex(*([FAKE] * 5), B, Hq, Hkv, Lq, Lk, D, W, causal, scale, f16, None)
+
+
+def _bwd_ex(lib, B=1, Hq=2, Hkv=1, Lq=16, Lk=40, D=64, W=4, causal=1, scale=0.125, f16=0,
+            ws_bytes=1 << 20):
+    return lib.swa_attn_bwd_ex(*([FAKE] * 9), B, Hq, Hkv, Lq, Lk, D, W, causal, scale, f16, FAKE,
+                               ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Lq=41), 1), (dict(Lq=0), 1), (dict(Lk=0), 1), (dict(causal=2), 1), (dict(causal=-1), 1),
+    (dict(f16=2), 1), (dict(W=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(D=256), 2),
+])
+def test_ex_entry_points_reject_bad_arguments(lib, kw, code):
+    assert _fwd_ex(lib, **kw) == code
+    assert _bwd_ex(lib, **kw) == code
+
+
+def test_ex_workspace_follows_the_query_length(lib):
+    need = lib.swa_attn_bwd_workspace_bytes(1, 2, 16, 64)
+    assert _bwd_ex(lib, ws_bytes=need - 1) == 6
+
+
 def test_workspace_checks(lib):
     need = lib.swa_attn_bwd_workspace_bytes(2, 4, 100, 128)
     assert need == ((2 * 4 * 100 * 4 + 255) // 256) * 256
