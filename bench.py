@@ -29,6 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import swa_inputs as si  # noqa: E402
@@ -46,6 +47,15 @@ def visible_pairs(N: int, W: int) -> int:
     """(query, key) pairs with 0 <= i - j < W in one head of length N."""
     W = min(W, N)
     return N * W - W * (W - 1) // 2
+
+
+def window_pairs(Lq: int, Lk: int, W: int, causal: bool) -> int:
+    """Visible (query, key) pairs in one head when query i sits at key position i + Lk - Lq and
+    sees keys j with 0 <= pos - j < W (causal) or |pos - j| < W (two-sided)."""
+    pos = np.arange(Lq, dtype=np.int64) + (Lk - Lq)
+    lo = np.maximum(pos - (W - 1), 0)
+    hi = pos if causal else np.minimum(pos + (W - 1), Lk - 1)
+    return int(np.sum(hi - lo + 1))
 
 
 def step_flops(case: si.Case) -> dict:
@@ -472,8 +482,8 @@ def measure_e2e(swa, case, device, dist, args, world) -> dict:
 
 
 def measure_other_workloads(swa, device) -> dict:
-    """Full-causal GQA layer (fwd and bwd timed separately), the headline layer in fp16, and the
-    12-layer mixed step."""
+    """Full-causal GQA layer (fwd and bwd timed separately), the headline layer in fp16, a query
+    suffix and a two-sided window over the headline keys, and the 12-layer mixed step."""
     res = {}
     case = si.gqa_causal_case()
     inp = si.make_inputs(case, device=str(device))
@@ -523,6 +533,34 @@ def measure_other_workloads(swa, device) -> dict:
     }
     del inp, o, lse
     torch.cuda.empty_cache()
+
+    # Queries shorter than keys and a two-sided window (swa_attn_fwd_ex / swa_attn_bwd_ex).
+    for name, Lq, causal, what in (
+            ("suffix_queries_8k_of_32k", 8192, True,
+             "B=1 Hq=32 Hkv=16 Lq=8192 Lk=32768 D=128 W=1024 causal, queries = the last 8192 "
+             "key positions"),
+            ("twosided_32k", 32768, False,
+             "B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024 two-sided (|i - j| < W)")):
+        case = si.long_swa_case(32768)
+        inp = si.make_inputs(case, device=str(device))
+        for key in ("q", "do"):
+            inp[key] = inp[key][:, :, case.N - Lq:].contiguous()
+        pairs = window_pairs(Lq, case.N, case.W, causal) * case.B * case.Hq
+        o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
+                                  causal=causal)
+        f_ms = timed(lambda: swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W,
+                                              case.softmax_scale, out=o, lse=lse, causal=causal))
+        b_ms = timed(lambda: swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse,
+                                              case.W, case.softmax_scale, causal=causal))
+        res[name] = {
+            "workload": what, "pairs_per_head": pairs // (case.B * case.Hq),
+            "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "fwd_tflops": 4 * case.D * pairs / (f_ms * 1e-3) / 1e12,
+            "bwd_tflops": 10 * case.D * pairs / (b_ms * 1e-3) / 1e12,
+            "fwd_bwd_tflops": 14 * case.D * pairs / ((f_ms + b_ms) * 1e-3) / 1e12,
+        }
+        del inp, o, lse
+        torch.cuda.empty_cache()
 
     layers = si.mixed_layer_cases()
     data = [si.make_inputs(c, device=str(device)) for c in layers]

@@ -27,28 +27,29 @@ def _np(t):
     return t.detach().float().cpu().double().numpy()
 
 
-def _run(swa, case, inp):
+def _run(swa, case, inp, causal=True):
     dev = torch.device("cuda:0")
     g = {k: v.to(dev) for k, v in inp.items()}
-    o, lse = swa.swa_attn_fwd(g["q"], g["k"], g["v"], case.W, case.softmax_scale)
-    dq, dk, dv = swa.swa_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, case.W, case.softmax_scale)
+    o, lse = swa.swa_attn_fwd(g["q"], g["k"], g["v"], case.W, case.softmax_scale, causal=causal)
+    dq, dk, dv = swa.swa_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, case.W, case.softmax_scale,
+                                  causal=causal)
     swa.swa_check_device()
     return {"o": o.cpu(), "lse": lse.cpu(), "dq": dq.cpu(), "dk": dk.cpu(), "dv": dv.cpu()}
 
 
-def _check_sampled(case, inp, gpu, heads, rows, kv_heads, keys):
+def _check_sampled(case, inp, gpu, heads, rows, kv_heads, keys, causal=True):
     """Compare sampled rows of O, LSE, dQ (query heads `heads`) and sampled keys of dK, dV."""
     q, k, v, do = inp["q"], inp["k"], inp["v"], inp["do"]
     W, sc = case.W, case.softmax_scale
     o_ref, o_gpu, l_ref, l_gpu, dq_ref, dq_gpu = [], [], [], [], [], []
     for hq in heads:
         hk = orc.kv_head_of(hq, case.Hq, case.Hkv)
-        o_r, l_r = orc.forward_rows(q[0, hq], k[0, hk], v[0, hk], rows, W, sc)
+        o_r, l_r = orc.forward_rows(q[0, hq], k[0, hk], v[0, hk], rows, W, sc, causal)
         o_ref.append(o_r)
         l_ref.append(l_r)
         o_gpu.append(_np(gpu["o"][0, hq, rows]))
         l_gpu.append(_np(gpu["lse"][0, hq, rows]))
-        dq_ref.append(orc.dq_rows(q[0, hq], k[0, hk], v[0, hk], do[0, hq], rows, W, sc))
+        dq_ref.append(orc.dq_rows(q[0, hq], k[0, hk], v[0, hk], do[0, hq], rows, W, sc, causal))
         dq_gpu.append(_np(gpu["dq"][0, hq, rows]))
     assert _rel(np.concatenate(o_gpu), np.concatenate(o_ref)) <= REL_TOL
     assert np.max(np.abs(np.concatenate(l_gpu) - np.concatenate(l_ref))) <= LSE_TOL
@@ -57,7 +58,7 @@ def _check_sampled(case, inp, gpu, heads, rows, kv_heads, keys):
     for hk in kv_heads:
         group = [hq for hq in range(case.Hq) if orc.kv_head_of(hq, case.Hq, case.Hkv) == hk]
         dk_r, dv_r = orc.dkdv_rows([q[0, hq] for hq in group], k[0, hk], v[0, hk],
-                                   [do[0, hq] for hq in group], keys, W, sc)
+                                   [do[0, hq] for hq in group], keys, W, sc, causal=causal)
         dk_ref.append(dk_r)
         dv_ref.append(dv_r)
         dk_gpu.append(_np(gpu["dk"][0, hk, keys]))
@@ -116,3 +117,38 @@ def test_mixed_step_layers_n30553(swa, layer):
     rows = _sample(rng, N, 16, must=(0, N - 89, N - 1))
     keys = _sample(rng, N, 16, must=(N - 89, N - 1))
     _check_sampled(case, inp, gpu, heads=[0, 31], rows=rows, kv_heads=[15], keys=keys)
+
+
+def test_two_sided_window_n32768(swa):
+    """The headline layer's shapes with a two-sided window (|i - j| < 1024), as bench.py times it."""
+    case = si.long_swa_case(32768)
+    inp = si.make_inputs(case)
+    gpu = _run(swa, case, inp, causal=False)
+    for key, t in gpu.items():
+        assert torch.isfinite(t.float()).all(), key
+    rng = np.random.default_rng(4)
+    N = case.N
+    rows = _sample(rng, N, 16, must=(0, 127, 128, 1023, N - 1024, N - 129, N - 1))
+    keys = _sample(rng, N, 16, must=(0, 1023, 1024, N - 1025, N - 1))
+    _check_sampled(case, inp, gpu, heads=[0, 31], rows=rows, kv_heads=[7], keys=keys,
+                   causal=False)
+
+
+def test_query_suffix_8192_of_32768(swa):
+    """8,192 queries at the last key positions of a 32,768-key layer (causal, W = 1024), as bench.py
+    times it: keys no query reaches get exact zeros, the rest match the oracle."""
+    case = si.long_swa_case(32768)
+    Lq = 8192
+    inp = si.make_inputs(case)
+    for key in ("q", "do"):
+        inp[key] = inp[key][:, :, case.N - Lq:].contiguous()
+    gpu = _run(swa, case, inp)
+    assert gpu["o"].shape[2] == Lq and gpu["dk"].shape[2] == case.N
+    first_seen = case.N - Lq - (case.W - 1)
+    assert torch.count_nonzero(gpu["dk"][:, :, :first_seen]) == 0
+    assert torch.count_nonzero(gpu["dv"][:, :, :first_seen]) == 0
+    rng = np.random.default_rng(5)
+    rows = _sample(rng, Lq, 16, must=(0, 127, 128, Lq - 1))
+    keys = _sample(rng, case.N - first_seen, 16, must=(0, 1023, 1024, case.N - first_seen - 1))
+    keys = keys + first_seen
+    _check_sampled(case, inp, gpu, heads=[3, 30], rows=rows, kv_heads=[1], keys=keys)

@@ -62,3 +62,17 @@ def test_visible_pairs_closed_form():
     for N, W in itertools.product((1, 5, 17, 128), (1, 2, 7, 128, 500)):
         brute = sum(1 for i in range(N) for j in range(N) if 0 <= i - j < W)
         assert bench.visible_pairs(N, W) == brute
+
+
+def test_window_pairs_counts_the_mask():
+    """The bench's pair count for Lq <= Lk and two-sided windows is the number of visible cells
+    (brute-force double loop over the offset window)."""
+    import itertools
+
+    for Lq, Lk, W, causal in itertools.product((1, 5, 17), (17, 40), (1, 3, 16, 100),
+                                              (True, False)):
+        off = Lk - Lq
+        brute = sum(1 for i in range(Lq) for j in range(Lk)
+                    if (0 <= i + off - j < W if causal else abs(i + off - j) < W))
+        assert bench.window_pairs(Lq, Lk, W, causal) == brute
+    assert bench.window_pairs(300, 300, 64, True) == bench.visible_pairs(300, 64)
