@@ -482,8 +482,9 @@ def measure_e2e(swa, case, device, dist, args, world) -> dict:
 
 
 def measure_other_workloads(swa, device) -> dict:
-    """Full-causal GQA layer (fwd and bwd timed separately), the headline layer in fp16, a query
-    suffix and a two-sided window over the headline keys, and the 12-layer mixed step."""
+    """Full-causal GQA layer (fwd and bwd timed separately), the headline layer in fp16 and in
+    fp32, a query suffix and a two-sided window over the headline keys, and the 12-layer mixed
+    step."""
     res = {}
     case = si.gqa_causal_case()
     inp = si.make_inputs(case, device=str(device))
@@ -532,6 +533,32 @@ def measure_other_workloads(swa, device) -> dict:
         "fwd_bwd_tflops": (fl["fwd"] + fl["bwd"]) / ((f_ms + b_ms) * 1e-3) / 1e12,
     }
     del inp, o, lse
+    torch.cuda.empty_cache()
+
+    # The headline layer with fp32 tensors (swa_attn_fwd_f32 / swa_attn_bwd_f32: rounding to bf16
+    # and widening of the results inside the timed calls).
+    case = si.long_swa_case(32768)
+    inp = si.make_inputs(case, device=str(device), dtype=torch.float32)
+    fl = step_flops(case)
+    ws = torch.empty(swa.swa_attn_f32_workspace_bytes(case.B, case.Hq, case.Hkv, case.N, case.N,
+                                                      case.D), dtype=torch.uint8, device=device)
+    o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
+                              workspace=ws)
+    grads = [torch.empty_like(inp[k_]) for k_ in ("q", "k", "v")]
+    f_ms = timed(lambda: swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
+                                          out=o, lse=lse, workspace=ws))
+    b_ms = timed(lambda: swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
+                                          case.softmax_scale, dq=grads[0], dk=grads[1],
+                                          dv=grads[2], workspace=ws))
+    res["long_swa_fp32"] = {
+        "workload": "B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, fp32 tensors (bf16 tensor-core "
+                    "operands)",
+        "fwd_ms": f_ms, "bwd_ms": b_ms,
+        "fwd_tflops": fl["fwd"] / (f_ms * 1e-3) / 1e12,
+        "bwd_tflops": fl["bwd"] / (b_ms * 1e-3) / 1e12,
+        "fwd_bwd_tflops": (fl["fwd"] + fl["bwd"]) / ((f_ms + b_ms) * 1e-3) / 1e12,
+    }
+    del inp, o, lse, ws, grads
     torch.cuda.empty_cache()
 
     # Queries shorter than keys and a two-sided window (swa_attn_fwd_ex / swa_attn_bwd_ex).

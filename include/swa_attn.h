@@ -133,6 +133,30 @@ swa_status swa_attn_bwd_ex(const void* q, const void* k, const void* v, const vo
                            cudaStream_t stream);
 
 /*
+ * fp32 tensors: the general forms above with q, k, v, o, dO, dq, dk, dv in IEEE fp32.
+ * The tensor cores take bf16 operands, so every input element is rounded once to the nearest bf16
+ * (ties to even) on the device; scores, accumulators, lse and Delta stay fp32, and the results are
+ * widened to fp32.  In the backward, Delta is formed from fp32 O and the bf16-rounded dO that the
+ * dP contraction sees.  The pages' gradient sweep runs fp32 inputs alongside the 16-bit ones
+ * (Lab 28, numbers entry "Gradient parity, small shapes").
+ *   workspace : device scratch of at least swa_attn_f32_workspace_bytes(B,Hq,Hkv,Lq,Lk,D) bytes,
+ *               16-byte aligned, owned by the caller (the bf16 copies and Delta live there; it
+ *               holds nothing between calls).  Too small or NULL: SWA_ERR_WORKSPACE.
+ * Shapes, windows, causal and errors as in the general forms; every pointer 16-byte aligned.
+ * A forward is three launches (round q, k, v; attention; widen o), a backward five.
+ */
+size_t swa_attn_f32_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D);
+swa_status swa_attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                            int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal,
+                            float scale, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+swa_status swa_attn_bwd_f32(const float* q, const float* k, const float* v, const float* o,
+                            const float* dO, const float* lse, float* dq, float* dk, float* dv,
+                            int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal,
+                            float scale, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+/*
  * The three phases swa_attn_bwd runs, callable one by one (same arguments, same checks, same
  * kernels), e.g. to time each kernel or to run the dK/dV and dQ phases on two streams once the
  * preprocess has finished.  `delta` is the workspace of swa_attn_bwd (fp32 [B,Hq,N]).

@@ -10,8 +10,9 @@ There is no fallback: if libswa.so is missing or the device is not sm_103, the c
     dq, dk, dv = swa_attn_bwd(q, k, v, o, do, lse, window, scale)
     out = SlidingWindowAttention.apply(q, k, v, window, scale)   # autograd wrapper
 
-Layout: q, o, do, dq [B, Hq, N, D]; k, v, dk, dv [B, Hkv, N, D], all contiguous bf16;
-lse [B, Hq, N] fp32.  D in {64, 128}; Hq % Hkv == 0.
+Layout: q, o, do, dq [B, Hq, Lq, D]; k, v, dk, dv [B, Hkv, Lk, D], all contiguous and of one
+dtype (bf16, fp16, or fp32 with bf16 tensor-core operands); lse [B, Hq, Lq] fp32.  D in {64, 128};
+Hq % Hkv == 0; Lq <= Lk (the queries are the last Lq key positions).
 """
 from __future__ import annotations
 
@@ -27,6 +28,7 @@ __all__ = [
     "swa_attn_fwd",
     "swa_attn_bwd",
     "swa_attn_bwd_workspace_bytes",
+    "swa_attn_f32_workspace_bytes",
     "swa_attn_bwd_phases",
     "swa_check_device",
     "SlidingWindowAttention",
@@ -67,6 +69,9 @@ SIGNATURES = {
         _c_int,
         [_vp] * 9 + [_c_int] * 8 + [_c_float, _c_int, _vp, ctypes.c_size_t, _vp],
     ),
+    "swa_attn_f32_workspace_bytes": (ctypes.c_size_t, [_c_int] * 6),
+    "swa_attn_fwd_f32": (_c_int, [_vp] * 5 + [_c_int] * 8 + [_c_float, _vp, ctypes.c_size_t, _vp]),
+    "swa_attn_bwd_f32": (_c_int, [_vp] * 9 + [_c_int] * 8 + [_c_float, _vp, ctypes.c_size_t, _vp]),
     "swa_attn_bwd_preprocess": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_vp]),
     "swa_attn_bwd_dkdv": (_c_int, [_vp] * 8 + [_c_int] * 6 + [_c_float, _vp]),
     "swa_attn_bwd_dq": (_c_int, [_vp] * 7 + [_c_int] * 6 + [_c_float, _vp]),
@@ -144,20 +149,35 @@ def _scale(scale, D):
 
 
 def _elem_dtype(q):
-    """Element type of a call: bf16, or fp16 (the *_f16 entry points), taken from q."""
+    """Element type of a call, taken from q: bf16, fp16 (the *_f16 entry points) or fp32 (the
+    *_f32 entry points: operands rounded to bf16 on the device, results widened to fp32)."""
     import torch
 
-    if q.dtype not in (torch.bfloat16, torch.float16):
-        raise TypeError(f"q must be bfloat16 or float16, got {q.dtype}")
+    if q.dtype not in (torch.bfloat16, torch.float16, torch.float32):
+        raise TypeError(f"q must be bfloat16, float16 or float32, got {q.dtype}")
     return q.dtype
 
 
+def swa_attn_f32_workspace_bytes(B: int, Hq: int, Hkv: int, Lq: int, Lk: int, D: int) -> int:
+    return int(load().swa_attn_f32_workspace_bytes(B, Hq, Hkv, Lq, Lk, D))
+
+
+def _f32_workspace(workspace, B, Hq, Hkv, Lq, Lk, D, device):
+    import torch
+
+    n = swa_attn_f32_workspace_bytes(B, Hq, Hkv, Lq, Lk, D)
+    if workspace is None:
+        workspace = torch.empty(n, dtype=torch.uint8, device=device)
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
 def swa_attn_fwd(q, k, v, window: int, scale: Optional[float] = None, out=None, lse=None,
-                 causal: bool = True):
-    """Forward: returns (o [B,Hq,Lq,D] in q's dtype (bf16 or fp16), lse [B,Hq,Lq] fp32).
+                 causal: bool = True, workspace=None):
+    """Forward: returns (o [B,Hq,Lq,D] in q's dtype (bf16, fp16 or fp32), lse [B,Hq,Lq] fp32).
 
     q [B,Hq,Lq,D], k and v [B,Hkv,Lk,D] with Lq <= Lk: the queries are the last Lq positions of the
-    keys.  causal=False selects the two-sided window |pos - j| < window.
+    keys.  causal=False selects the two-sided window |pos - j| < window.  fp32 calls use a device
+    workspace of swa_attn_f32_workspace_bytes (allocated here unless given).
     """
     import torch
 
@@ -176,7 +196,12 @@ def swa_attn_fwd(q, k, v, window: int, scale: Optional[float] = None, out=None, 
     ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr())
     f16 = dt == torch.float16
     st = _stream_handle(q.device)
-    if Lq == Lk and causal:
+    if dt == torch.float32:
+        name = "swa_attn_fwd_f32"
+        ws = _f32_workspace(workspace, B, Hq, Hkv, Lq, Lk, D, q.device)
+        rc = lib.swa_attn_fwd_f32(*ptrs, B, Hq, Hkv, Lq, Lk, D, int(window), int(bool(causal)),
+                                  _scale(scale, D), *ws, st)
+    elif Lq == Lk and causal:
         name = "swa_attn_fwd_f16" if f16 else "swa_attn_fwd"
         rc = getattr(lib, name)(*ptrs, B, Hq, Hkv, Lq, D, int(window), _scale(scale, D), st)
     else:
@@ -194,8 +219,9 @@ def swa_attn_bwd_workspace_bytes(B: int, Hq: int, N: int, D: int) -> int:
 
 def swa_attn_bwd(q, k, v, o, do, lse, window: int, scale: Optional[float] = None,
                  dq=None, dk=None, dv=None, workspace=None, causal: bool = True) -> Tuple:
-    """Backward of sum(do * o): returns (dq, dk, dv) in q's dtype (bf16 or fp16), dk/dv summed
-    over each kv group.  Shapes and window as in swa_attn_fwd."""
+    """Backward of sum(do * o): returns (dq, dk, dv) in q's dtype (bf16, fp16 or fp32), dk/dv
+    summed over each kv group.  Shapes, window and workspace as in swa_attn_fwd (bf16 and fp16
+    calls take a Delta workspace of swa_attn_bwd_workspace_bytes)."""
     import torch
 
     lib = load()
@@ -210,14 +236,22 @@ def swa_attn_bwd(q, k, v, o, do, lse, window: int, scale: Optional[float] = None
     dv = torch.empty_like(v) if dv is None else dv
     for t, name, hs, L in ((dq, "dq", Hq, Lq), (dk, "dk", Hkv, Lk), (dv, "dv", Hkv, Lk)):
         _check_tensor(t, name, (B, hs, L, D), dt)
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
+    f16 = dt == torch.float16
+    st = _stream_handle(q.device)
+    if dt == torch.float32:
+        name = "swa_attn_bwd_f32"
+        ws = _f32_workspace(workspace, B, Hq, Hkv, Lq, Lk, D, q.device)
+        rc = lib.swa_attn_bwd_f32(*ptrs, B, Hq, Hkv, Lq, Lk, D, int(window), int(bool(causal)),
+                                  _scale(scale, D), *ws, st)
+        if rc != 0:
+            raise SwaError(rc, name)
+        return dq, dk, dv
     ws_bytes = int(lib.swa_attn_bwd_workspace_bytes(B, Hq, Lq, D))
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-            dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
     ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size())
-    f16 = dt == torch.float16
-    st = _stream_handle(q.device)
     if Lq == Lk and causal:
         name = "swa_attn_bwd_f16" if f16 else "swa_attn_bwd"
         rc = getattr(lib, name)(*ptrs, B, Hq, Hkv, Lq, D, int(window), _scale(scale, D), *ws, st)

@@ -2,6 +2,7 @@
 // per-device error word, and the launch sequence of the forward and the backward.
 #include <cmath>
 #include <cstdint>
+#include <initializer_list>
 #include <mutex>
 
 #include "swa_attn.h"
@@ -272,6 +273,134 @@ swa_status swa_check_device(cudaStream_t stream) {
 }
 
 int swa_version(void) { return 100; }
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// fp32 tensors: rounded to bf16 copies in the caller's workspace, bf16 kernels, widened results.
+// ------------------------------------------------------------------------------------------------
+namespace {
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Byte offsets of the workspace regions: bf16 copies of q, k, v, a query-shaped slot (o in the
+// forward, dO in the backward), bf16 dq, dk, dv, then Delta (fp32).
+struct F32Layout {
+  size_t q16, k16, v16, a16, dq16, dk16, dv16, delta, total;
+  long long q_units, k_units;  // 8-element units of a query / key tensor
+};
+
+F32Layout f32_layout(int B, int Hq, int Hkv, int Lq, int Lk, int D) {
+  F32Layout L;
+  const size_t qe = static_cast<size_t>(B) * Hq * Lq * D;
+  const size_t ke = static_cast<size_t>(B) * Hkv * Lk * D;
+  const size_t qb = round256(qe * 2), kb = round256(ke * 2);
+  size_t off = 0;
+  L.q16 = off; off += qb;
+  L.k16 = off; off += kb;
+  L.v16 = off; off += kb;
+  L.a16 = off; off += qb;
+  L.dq16 = off; off += qb;
+  L.dk16 = off; off += kb;
+  L.dv16 = off; off += kb;
+  L.delta = off; off += round256(static_cast<size_t>(B) * Hq * Lq * sizeof(float));
+  L.total = off;
+  L.q_units = static_cast<long long>(qe / 8);
+  L.k_units = static_cast<long long>(ke / 8);
+  return L;
+}
+
+swa_status f32_prologue(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal,
+                        float scale, const void* workspace, size_t workspace_bytes,
+                        std::initializer_list<const void*> ptrs, swa::Problem* pb) {
+  for (const void* p : ptrs)
+    if (!p) return SWA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_shape(B, Hq, Hkv, Lq, Lk, D, window, scale);
+  if (st != SWA_OK) return st;
+  if (!workspace || workspace_bytes < f32_layout(B, Hq, Hkv, Lq, Lk, D).total)
+    return SWA_ERR_WORKSPACE;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return SWA_ERR_MISALIGNED;
+  if (!aligned16(workspace)) return SWA_ERR_MISALIGNED;
+  unsigned* err = nullptr;
+  if ((st = current_device(&err)) != SWA_OK) return st;
+  *pb = make_problem_ex(B, Hq, Hkv, Lq, Lk, D, window, causal, scale, err, 0);
+  return SWA_OK;
+}
+
+swa::RoundJob round_qkv(const float* q, const float* k, const float* v, uint8_t* ws,
+                        const F32Layout& L) {
+  swa::RoundJob j{};
+  j.src[0] = q; j.dst[0] = reinterpret_cast<uint16_t*>(ws + L.q16);
+  j.src[1] = k; j.dst[1] = reinterpret_cast<uint16_t*>(ws + L.k16);
+  j.src[2] = v; j.dst[2] = reinterpret_cast<uint16_t*>(ws + L.v16);
+  j.end[0] = L.q_units;
+  j.end[1] = L.q_units + L.k_units;
+  j.end[2] = j.end[3] = L.q_units + 2 * L.k_units;
+  return j;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t swa_attn_f32_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq || (D != 64 && D != 128)) return 0;
+  return f32_layout(B, Hq, Hkv, Lq, Lk, D).total;
+}
+
+swa_status swa_attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                            int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal,
+                            float scale, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  swa::Problem pb;
+  swa_status st = f32_prologue(B, Hq, Hkv, Lq, Lk, D, window, causal, scale, workspace,
+                               workspace_bytes, {q, k, v, o, lse}, &pb);
+  if (st != SWA_OK) return st;
+  const F32Layout L = f32_layout(B, Hq, Hkv, Lq, Lk, D);
+  auto* ws = static_cast<uint8_t*>(workspace);
+  if (swa::launch_round_bf16(round_qkv(q, k, v, ws, L), stream) != cudaSuccess) return SWA_ERR_CUDA;
+  if (swa::launch_fwd(pb, ws + L.q16, ws + L.k16, ws + L.v16, ws + L.a16, lse, stream) !=
+      cudaSuccess)
+    return SWA_ERR_CUDA;
+  swa::WidenJob w{};
+  w.src[0] = reinterpret_cast<const uint16_t*>(ws + L.a16);
+  w.dst[0] = o;
+  w.end[0] = w.end[1] = w.end[2] = w.end[3] = L.q_units;
+  return swa::launch_widen_bf16(w, stream) == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+swa_status swa_attn_bwd_f32(const float* q, const float* k, const float* v, const float* o,
+                            const float* dO, const float* lse, float* dq, float* dk, float* dv,
+                            int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal,
+                            float scale, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  swa::Problem pb;
+  swa_status st = f32_prologue(B, Hq, Hkv, Lq, Lk, D, window, causal, scale, workspace,
+                               workspace_bytes, {q, k, v, o, dO, lse, dq, dk, dv}, &pb);
+  if (st != SWA_OK) return st;
+  const F32Layout L = f32_layout(B, Hq, Hkv, Lq, Lk, D);
+  auto* ws = static_cast<uint8_t*>(workspace);
+  float* delta = reinterpret_cast<float*>(ws + L.delta);
+  if (swa::launch_round_bf16(round_qkv(q, k, v, ws, L), stream) != cudaSuccess) return SWA_ERR_CUDA;
+  if (swa::launch_delta_f32(pb, o, dO, delta, ws + L.a16, stream) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (swa::launch_bwd_dkdv(pb, ws + L.q16, ws + L.k16, ws + L.v16, ws + L.a16, lse, delta,
+                           ws + L.dk16, ws + L.dv16, stream) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (swa::launch_bwd_dq(pb, ws + L.q16, ws + L.k16, ws + L.v16, ws + L.a16, lse, delta,
+                         ws + L.dq16, stream) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  swa::WidenJob w{};
+  w.src[0] = reinterpret_cast<const uint16_t*>(ws + L.dq16); w.dst[0] = dq;
+  w.src[1] = reinterpret_cast<const uint16_t*>(ws + L.dk16); w.dst[1] = dk;
+  w.src[2] = reinterpret_cast<const uint16_t*>(ws + L.dv16); w.dst[2] = dv;
+  w.end[0] = L.q_units;
+  w.end[1] = L.q_units + L.k_units;
+  w.end[2] = w.end[3] = L.q_units + 2 * L.k_units;
+  return swa::launch_widen_bf16(w, stream) == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
 
 }  // extern "C"
 

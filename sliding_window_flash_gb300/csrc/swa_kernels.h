@@ -90,4 +90,23 @@ cudaError_t launch_bwd_dq(const Problem& pb, const void* q, const void* k, const
                           const void* dO, const float* lse, const float* delta, void* dq,
                           cudaStream_t stream);
 
+// fp32 tensors around the bf16 kernels: up to four tensors per launch, each a whole number of
+// 8-element units (end[t] = units of tensors 0..t, cumulative; unused entries repeat the total).
+constexpr int kMaxJobTensors = 4;
+struct RoundJob {  // fp32 -> bf16, round to nearest even
+  const float* src[kMaxJobTensors];
+  uint16_t* dst[kMaxJobTensors];
+  long long end[kMaxJobTensors];
+};
+struct WidenJob {  // bf16 -> fp32, exact
+  const uint16_t* src[kMaxJobTensors];
+  float* dst[kMaxJobTensors];
+  long long end[kMaxJobTensors];
+};
+cudaError_t launch_round_bf16(const RoundJob& job, cudaStream_t stream);
+cudaError_t launch_widen_bf16(const WidenJob& job, cudaStream_t stream);
+// Delta from fp32 O and dO, also writing dO rounded to bf16 (Delta uses the rounded dO).
+cudaError_t launch_delta_f32(const Problem& pb, const float* o, const float* dO, float* delta,
+                             void* do16, cudaStream_t stream);
+
 }  // namespace swa

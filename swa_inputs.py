@@ -63,7 +63,8 @@ def _gaussian(shape, seed: int, std: float, device: str,
 def make_inputs(case: Case, device: str = "cpu", with_do: bool = True,
                 dtype: torch.dtype = torch.bfloat16) -> Dict[str, torch.Tensor]:
     """Return {'q','k','v'[, 'do']} as contiguous tensors in [B, H, N, D] layout, bf16 unless
-    `dtype` says fp16 (the same fp32 draws, rounded to the element type).
+    `dtype` says otherwise (the same fp32 draws, rounded to fp16 or bf16, or kept as drawn for
+    fp32).
 
     The same (case, device) always gives the same values.  CPU and CUDA generators give
     different streams, so the tests draw on the CPU and copy to the GPU when the oracle is

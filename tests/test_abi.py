@@ -122,6 +122,72 @@ def test_ex_workspace_follows_the_query_length(lib):
     assert _bwd_ex(lib, ws_bytes=need - 1) == 6
 
 
+def _f32_need(lib, B=1, Hq=2, Hkv=1, Lq=16, Lk=40, D=64):
+    return lib.swa_attn_f32_workspace_bytes(B, Hq, Hkv, Lq, Lk, D)
+
+
+def _fwd_f32(lib, B=1, Hq=2, Hkv=1, Lq=16, Lk=40, D=64, W=4, causal=1, scale=0.125, ws=FAKE,
+             ws_bytes=None, ptrs=None):
+    ws_bytes = _f32_need(lib) if ws_bytes is None else ws_bytes
+    ptrs = [FAKE] * 5 if ptrs is None else ptrs
+    return lib.swa_attn_fwd_f32(*ptrs, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, ws, ws_bytes, None)
+
+
+def _bwd_f32(lib, B=1, Hq=2, Hkv=1, Lq=16, Lk=40, D=64, W=4, causal=1, scale=0.125, ws=FAKE,
+             ws_bytes=None, ptrs=None):
+    ws_bytes = _f32_need(lib) if ws_bytes is None else ws_bytes
+    ptrs = [FAKE] * 9 if ptrs is None else ptrs
+    return lib.swa_attn_bwd_f32(*ptrs, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, ws, ws_bytes, None)
+
+
+def test_f32_workspace_size():
+    """Bytes: bf16 copies of q, k, v, a query-shaped slot, dq, dk, dv, then fp32 Delta, each
+    region rounded up to 256 bytes."""
+    import sliding_window_flash_gb300 as swa
+
+    lib = swa.load()
+
+    def r(x):
+        return (x + 255) // 256 * 256
+
+    B, Hq, Hkv, Lq, Lk, D = 2, 4, 2, 100, 300, 128
+    qb, kb = r(B * Hq * Lq * D * 2), r(B * Hkv * Lk * D * 2)
+    assert _f32_need(lib, B, Hq, Hkv, Lq, Lk, D) == 3 * qb + 4 * kb + r(B * Hq * Lq * 4)
+    assert swa.swa_attn_f32_workspace_bytes(B, Hq, Hkv, Lq, Lk, D) == 3 * qb + 4 * kb + r(
+        B * Hq * Lq * 4)
+    assert _f32_need(lib, Lq=41) == 0 and _f32_need(lib, D=96) == 0 and _f32_need(lib, B=0) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Lq=41), 1), (dict(Lq=0), 1), (dict(causal=2), 1), (dict(W=0), 1),
+    (dict(Hq=3, Hkv=2), 1), (dict(scale=0.0), 1), (dict(D=256), 2),
+    (dict(ws=0), 6), (dict(ws_bytes=0), 6), (dict(ws=FAKE + 8), 3),
+])
+def test_f32_entry_points_reject_bad_arguments(lib, kw, code):
+    assert _fwd_f32(lib, **kw) == code
+    assert _bwd_f32(lib, **kw) == code
+
+
+def test_f32_workspace_too_small_by_one_byte(lib):
+    assert _fwd_f32(lib, ws_bytes=_f32_need(lib) - 1) == 6
+    assert _bwd_f32(lib, ws_bytes=_f32_need(lib) - 1) == 6
+
+
+def test_f32_null_and_misaligned_pointers(lib):
+    for i in range(5):
+        ptrs = [FAKE] * 5
+        ptrs[i] = 0
+        assert _fwd_f32(lib, ptrs=ptrs) == 1
+        ptrs[i] = FAKE + 4
+        assert _fwd_f32(lib, ptrs=ptrs) == 3
+    for i in range(9):
+        ptrs = [FAKE] * 9
+        ptrs[i] = 0
+        assert _bwd_f32(lib, ptrs=ptrs) == 1
+        ptrs[i] = FAKE + 8
+        assert _bwd_f32(lib, ptrs=ptrs) == 3
+
+
 def test_workspace_checks(lib):
     need = lib.swa_attn_bwd_workspace_bytes(2, 4, 100, 128)
     assert need == ((2 * 4 * 100 * 4 + 255) // 256) * 256
@@ -148,5 +214,7 @@ def test_python_binding_refuses_cpu_tensors():
         swa.swa_attn_fwd(q, k, k, 4)
     with pytest.raises(ValueError):
         swa.swa_attn_fwd(q.half(), k.half(), k.half(), 4)
-    with pytest.raises(TypeError):
+    with pytest.raises(ValueError):
         swa.swa_attn_fwd(q.float(), k.float(), k.float(), 4)
+    with pytest.raises(TypeError):
+        swa.swa_attn_fwd(q.double(), k.double(), k.double(), 4)
