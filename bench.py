@@ -17,6 +17,7 @@ scaling, no data-path collective); the barrier and max-over-ranks timing use tor
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -367,6 +368,8 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.no_memory:
         result["memory"] = measure_memory(swa, device)
         result["peak_gb"] = result["memory"]["peak_gb_total"][-1]
+        # the same layer with 256-wide heads, the shape of the pages' backward-memory figure
+        result["memory_d256"] = measure_memory(swa, device, D=256)
     if not args.no_e2e:
         result["e2e"] = measure_e2e(swa, case, device, dist, args, world)
     if rank == 0 and not args.no_extra:
@@ -410,11 +413,12 @@ def _profiled_traffic(kernel: str):
         return None
 
 
-def measure_memory(swa, device) -> dict:
-    """Peak device memory of one layer's fwd + bwd versus N (inputs Q, K, V, dO excluded)."""
-    out = {"N": [], "peak_gb_total": [], "peak_gb_above_inputs": []}
+def measure_memory(swa, device, D: int = 128) -> dict:
+    """Peak device memory of one layer's fwd + bwd versus N (inputs Q, K, V, dO excluded), for the
+    long sliding-window layer with head dim D."""
+    out = {"D": D, "N": [], "peak_gb_total": [], "peak_gb_above_inputs": []}
     for N in (8192, 16384, 32768):
-        case = si.long_swa_case(N)
+        case = dataclasses.replace(si.long_swa_case(N), D=D)
         torch.cuda.synchronize(device)
         torch.cuda.empty_cache()
         inp = si.make_inputs(case, device=str(device))
@@ -527,6 +531,25 @@ def measure_other_workloads(swa, device) -> dict:
                                           case.softmax_scale))
     res["long_swa_fp16"] = {
         "workload": "B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, fp16 tensors",
+        "fwd_ms": f_ms, "bwd_ms": b_ms,
+        "fwd_tflops": fl["fwd"] / (f_ms * 1e-3) / 1e12,
+        "bwd_tflops": fl["bwd"] / (b_ms * 1e-3) / 1e12,
+        "fwd_bwd_tflops": (fl["fwd"] + fl["bwd"]) / ((f_ms + b_ms) * 1e-3) / 1e12,
+    }
+    del inp, o, lse
+    torch.cuda.empty_cache()
+
+    # The headline layer with 256-wide heads (Gemma 4's sliding layers): half-tile kernels.
+    case = dataclasses.replace(si.long_swa_case(32768), D=256)
+    inp = si.make_inputs(case, device=str(device))
+    fl = step_flops(case)
+    o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale)
+    f_ms = timed(lambda: swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
+                                          out=o, lse=lse))
+    b_ms = timed(lambda: swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
+                                          case.softmax_scale))
+    res["long_swa_d256"] = {
+        "workload": "B=1 Hq=32 Hkv=16 N=32768 D=256 W=1024",
         "fwd_ms": f_ms, "bwd_ms": b_ms,
         "fwd_tflops": fl["fwd"] / (f_ms * 1e-3) / 1e12,
         "bwd_tflops": fl["bwd"] / (b_ms * 1e-3) / 1e12,

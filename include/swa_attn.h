@@ -19,7 +19,10 @@
  *     q, o, dO, dq     bf16  [B, Hq,  N, D]
  *     k, v, dk, dv     bf16  [B, Hkv, N, D]
  *     lse              fp32  [B, Hq,  N]      natural log, over the scaled scores
- * Supported: D in {64, 128}; Hq % Hkv == 0; N >= 1; B >= 1; window >= 1; scale finite and > 0.
+ * Supported: D in {64, 128, 256}; Hq % Hkv == 0; N >= 1; B >= 1; window >= 1; scale finite and
+ * > 0.  D = 256 (the head width of Gemma 4's sliding layers, Lab 28 record, numbers entry
+ * "Attention backward memory") runs on kernels that stream half-tiles and compute dK and dV in
+ * two passes; results and arguments are the same.
  * All device pointers must be 16-byte aligned.
  *
  * Ownership: the caller allocates every buffer (device memory), including the backward workspace.
@@ -44,7 +47,7 @@ extern "C" {
 typedef enum {
     SWA_OK = 0,
     SWA_ERR_INVALID_ARG = 1,    /* a size, window or scale outside its domain, or a null pointer  */
-    SWA_ERR_UNSUPPORTED = 2,    /* D not in {64, 128}, or no sm_100-family device current         */
+    SWA_ERR_UNSUPPORTED = 2,    /* D not in {64, 128, 256}, or no sm_103 device current           */
     SWA_ERR_MISALIGNED = 3,     /* a tensor pointer not 16-byte aligned                          */
     SWA_ERR_CUDA = 4,           /* a CUDA runtime / driver call or a launch failed               */
     SWA_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait ran out (reported by swa_check_device) */

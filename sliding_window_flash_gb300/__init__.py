@@ -11,8 +11,8 @@ There is no fallback: if libswa.so is missing or the device is not sm_103, the c
     out = SlidingWindowAttention.apply(q, k, v, window, scale)   # autograd wrapper
 
 Layout: q, o, do, dq [B, Hq, Lq, D]; k, v, dk, dv [B, Hkv, Lk, D], all contiguous and of one
-dtype (bf16, fp16, or fp32 with bf16 tensor-core operands); lse [B, Hq, Lq] fp32.  D in {64, 128};
-Hq % Hkv == 0; Lq <= Lk (the queries are the last Lq key positions).
+dtype (bf16, fp16, or fp32 with bf16 tensor-core operands); lse [B, Hq, Lq] fp32.
+D in {64, 128, 256}; Hq % Hkv == 0; Lq <= Lk (the queries are the last Lq key positions).
 """
 from __future__ import annotations
 

@@ -56,7 +56,7 @@ swa_status check_shape(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window
   if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq || window < 1) return SWA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return SWA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return SWA_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return SWA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return SWA_ERR_UNSUPPORTED;
   // Index arithmetic: row indices bh*L + i in 32 bits, grids in 31 bits.
   const long long q_rows = static_cast<long long>(B) * Hq * Lq;
   const long long k_rows = static_cast<long long>(B) * Hkv * Lk;
@@ -164,7 +164,7 @@ swa_status swa_attn_fwd_ex(const void* q, const void* k, const void* v, void* o,
 }
 
 size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int N, int D) {
-  if (B < 1 || Hq < 1 || N < 1 || (D != 64 && D != 128)) return 0;
+  if (B < 1 || Hq < 1 || N < 1 || (D != 64 && D != 128 && D != 256)) return 0;
   const size_t bytes = static_cast<size_t>(B) * Hq * N * sizeof(float);
   return (bytes + 255) & ~static_cast<size_t>(255);
 }
@@ -244,7 +244,7 @@ const char* swa_strerror(swa_status status) {
   switch (status) {
     case SWA_OK: return "SWA_OK";
     case SWA_ERR_INVALID_ARG: return "SWA_ERR_INVALID_ARG: size, window, scale or pointer invalid";
-    case SWA_ERR_UNSUPPORTED: return "SWA_ERR_UNSUPPORTED: head dim not in {64,128} or device not sm_103";
+    case SWA_ERR_UNSUPPORTED: return "SWA_ERR_UNSUPPORTED: head dim not in {64,128,256} or device not sm_103";
     case SWA_ERR_MISALIGNED: return "SWA_ERR_MISALIGNED: pointer not 16-byte aligned";
     case SWA_ERR_CUDA: return "SWA_ERR_CUDA: CUDA call or kernel launch failed";
     case SWA_ERR_DEVICE_TIMEOUT: return "SWA_ERR_DEVICE_TIMEOUT: a kernel's bounded wait ran out";
@@ -346,7 +346,8 @@ swa::RoundJob round_qkv(const float* q, const float* k, const float* v, uint8_t*
 extern "C" {
 
 size_t swa_attn_f32_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq || (D != 64 && D != 128)) return 0;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq || (D != 64 && D != 128 && D != 256))
+    return 0;
   return f32_layout(B, Hq, Hkv, Lq, Lk, D).total;
 }
 

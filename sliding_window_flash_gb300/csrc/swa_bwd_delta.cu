@@ -54,7 +54,7 @@ cudaError_t launch_bwd_delta(const Problem& pb, const void* o, const void* dO, f
                              cudaStream_t stream) {
   const long long rows = static_cast<long long>(pb.B) * pb.Hq * pb.span.Lq;
   constexpr int kThreads = 256;
-  const long long rows_per_block = (kThreads / 32) * (pb.D == 64 ? 4 : 2);
+  const long long rows_per_block = (kThreads / 32) * (32 / (pb.D / 8));
   long long blocks = (rows + rows_per_block - 1) / rows_per_block;
   const long long cap = 152ll * 8 * 4;  // 4 waves of 8 resident 256-thread blocks per SM
   if (blocks > cap) blocks = cap;
@@ -69,6 +69,10 @@ cudaError_t launch_bwd_delta(const Problem& pb, const void* o, const void* dO, f
     swa_delta_kernel<128, false><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
   else if (pb.D == 128)
     swa_delta_kernel<128, true><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
+  else if (pb.D == 256 && !pb.f16)
+    swa_delta_kernel<256, false><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
+  else if (pb.D == 256)
+    swa_delta_kernel<256, true><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

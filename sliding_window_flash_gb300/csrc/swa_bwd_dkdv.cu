@@ -475,6 +475,7 @@ cudaError_t launch_dkdv_d(const Problem& pb, const void* q, const void* k, const
 cudaError_t launch_bwd_dkdv(const Problem& pb, const void* q, const void* k, const void* v,
                             const void* dO, const float* lse, const float* delta, void* dk,
                             void* dv, cudaStream_t stream) {
+  if (pb.D == 256) return launch_dkdv_d256(pb, q, k, v, dO, lse, delta, dk, dv, stream);
   if (pb.D == 64)
     return pb.f16 ? launch_dkdv_d<64, true>(pb, q, k, v, dO, lse, delta, dk, dv, stream)
                   : launch_dkdv_d<64, false>(pb, q, k, v, dO, lse, delta, dk, dv, stream);

@@ -1,0 +1,1469 @@
+// swa_d256.cu — sliding-window attention with head dimension 256 on sm_103a: forward, dQ, dV and
+// dK kernels ("Off NVIDIA, you fix the platform yourself", Lab 28 record, numbers entry "Attention
+// backward memory": Gemma 4's sliding layers use 256-wide heads).
+//
+// The D <= 128 kernels keep whole 128-row operand tiles in shared memory and both dK and dV in
+// TMEM.  At D = 256 a 128-row tile is 64 KB and dK + dV alone would fill the 512 TMEM columns, so
+// these kernels are built differently:
+//   * operands move as half-tiles (128 rows x 128 columns, two 64-column 128B-swizzled chunks,
+//     32 KB) through a ring of slots, numbered in the order the MMA warp consumes them; two TMA
+//     warps fill alternate items (one warp's copies complete at only ~40 B/clk);
+//   * a product over D is two 8-step MMA groups (one per half-tile); a product with N = D is two
+//     N = 128 MMAs into the two halves of a 256-column accumulator;
+//   * the backward's dK and dV come from separate kernels, each with its 256-column accumulator in
+//     TMEM (dV: S^T double-buffered next to it; dK: S^T and dP^T next to it).
+// Probabilities and dS go back to TMEM as packed 16-bit pairs over the score columns they came
+// from (each half-row thread over the first 32 of its 64 columns); an MMA reading them as the A
+// operand is always issued before the MMA that overwrites those columns, and one thread's
+// tcgen05.mma operations run in issue order.
+//
+// Windows, query offsets (Lq <= Lk), masking and the block walks are the D <= 128 kernels' (Span).
+#include "swa_kernels.h"
+#include "swa_ptx.cuh"
+#include "swa_tmap.h"
+
+namespace swa {
+namespace {
+
+constexpr int kD = 256;
+constexpr int kHalfBytes = kBlockM * 128 * 2;  // one half-tile: 128 rows x 128 columns, 16-bit
+constexpr int kChunk = kBlockM * 128;          // one 64-column chunk: 128 rows x 128 bytes
+constexpr int kFullBytes = 2 * kHalfBytes;     // a whole 128 x 256 tile
+
+// ------------------------------------------------------------------------------------------------
+// Half-tile ring.  Item i sits in slot i % kSlots; its producer is warp (i & 1) of the two TMA
+// warps.  full[s] completes when an item has landed, empty[s] when the MMA reading it has.
+// ------------------------------------------------------------------------------------------------
+struct Item {
+  const CUtensorMap* map;
+  int half;  // column half 0 / 1 (columns 128 half .. +127)
+  int row;   // first row (query or key position)
+  int bh;    // (batch, head) plane
+};
+
+template <int kSlots>
+struct Ring {
+  uint32_t base;       // shared address of slot 0
+  uint32_t full0;      // barrier of slot 0 (full); slot s at +8 s
+  uint32_t empty0;     // barrier of slot 0 (empty)
+  __device__ uint32_t slot(int i) const { return base + (i % kSlots) * kHalfBytes; }
+  __device__ uint32_t full(int i) const { return full0 + 8u * (i % kSlots); }
+  __device__ uint32_t empty(int i) const { return empty0 + 8u * (i % kSlots); }
+  __device__ uint32_t parity(int i) const { return (i / kSlots) & 1; }
+};
+
+// Loads item i (called by its producer lane): waits for the slot's previous item to be consumed.
+template <int kSlots>
+__device__ __forceinline__ bool ring_load(const Ring<kSlots>& rg, int i, const Item& it,
+                                          volatile int* abort_flag, unsigned* err) {
+  if (i >= kSlots && !mbar_wait(rg.empty(i), ((i / kSlots) - 1) & 1, abort_flag, err)) return false;
+  const uint32_t dst = rg.slot(i);
+  mbar_arrive_expect_tx(rg.full(i), kHalfBytes);
+  tma_load_3d(dst, it.map, rg.full(i), 128 * it.half, it.row, it.bh);
+  tma_load_3d(dst + kChunk, it.map, rg.full(i), 128 * it.half + 64, it.row, it.bh);
+  return true;
+}
+
+// Before the CTA exits, no copy may be in flight.  Called by all 32 lanes of both producer
+// warps, `last` being lane 0's last item per slot: the two warps publish their `last` in
+// `s_last` ([2][kSlots] ints) and meet at named barrier 1, then one lane waits (bounded) for the
+// final fill of every slot.  Only the final fill's phase parity is unambiguous: with an odd slot
+// count the producers alternate within a slot, so a producer's own last fill may be followed by
+// the other's, after which the barrier has moved two phases on.
+template <int kSlots>
+__device__ __forceinline__ void ring_drain(const Ring<kSlots>& rg, const int (&last)[kSlots],
+                                           int* s_last, int p, uint32_t lane, unsigned* err) {
+  if (lane == 0)
+    for (int s = 0; s < kSlots; ++s) s_last[p * kSlots + s] = last[s];
+  __syncwarp();
+  named_barrier_sync(1, 64);
+  if (p == 0 && lane == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      const int f = max(s_last[s], s_last[kSlots + s]);
+      if (f >= 0) drain_wait(rg.full(f), rg.parity(f), err);
+    }
+  }
+}
+
+// Column mask of one half-row of scores: keeps columns [lo, hi] of 64, sets the rest to `fill`.
+__device__ __forceinline__ void mask64(float (&x)[64], int lo, int hi, float fill) {
+#pragma unroll
+  for (int c = 0; c < 64; ++c) x[c] = (c >= lo && c <= hi) ? x[c] : fill;
+}
+
+struct Args256 {
+  const float* lse;      // backward input
+  float* lse_out;        // forward output
+  const float* delta;
+  uint16_t* dq;          // dQ kernel output (bf16 or fp16 elements)
+  int BH, Hq, Hkv, G;    // B * Hq, heads, G = Hq / Hkv
+  int nqb, ntiles;       // query-tile kernels: query blocks per head, B * Hq * nqb
+  int BHK;               // key-block kernels: B * Hkv
+  Span span;
+  float scale, scale_log2;  // softmax scale, scale * log2(e)
+  unsigned* err;
+};
+
+struct QTile {
+  int bh, bhk, q0, kb_lo, nkv;
+};
+
+// Query tile t: heaviest query blocks first (a causal window gives later blocks more key blocks).
+__device__ __forceinline__ QTile qtile(int t, const Args256& a, const Span& sp) {
+  QTile f;
+  const int qb = a.nqb - 1 - t / a.BH;
+  f.bh = t % a.BH;
+  f.bhk = (f.bh / a.Hq) * a.Hkv + (f.bh % a.Hq) / a.G;
+  f.q0 = qb * kBlockM;
+  f.kb_lo = sp.first_kblock(f.q0);
+  f.nkv = sp.last_kblock(f.q0) - f.kb_lo + 1;
+  return f;
+}
+
+// ================================================================================================
+// Forward: O = softmax(scale Q K^T, window) V and LSE for one 128-row query tile per iteration.
+// Persistent (one CTA per SM).  Warps (384 threads): 0-7 softmax, two threads per row as in the
+// D <= 128 forward (warp w: TMEM lanes 32 (w % 4).., score columns [64 h, 64 h + 64), h = w / 4);
+// 8 and 11 TMA producers of the K / V ring; 9 MMA issuer and TMEM owner; 10 loads each tile's Q
+// and stores its O (staged in the Q buffer once every S of the tile has completed).
+// Ring order per tile of n key blocks: K_0, then per block j: K_{j+1} (if any), V_j (two halves
+// each) — the order in which S_{j+1} is issued ahead of O += P_j V_j.
+// TMEM: [0,128) S / P buffer 0, [128,256) S / P buffer 1, [256,512) O.
+// ================================================================================================
+constexpr float kRescaleThreshold256 = 8.0f;  // exact path: move the max only past 2^8
+constexpr float kFastSumLimit256 = 4096.0f;   // one-pass block stands if its row sum <= 2^12
+
+struct F256 {
+  static constexpr int kSlots = 5;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffRing = kOffQ + kFullBytes;
+  static constexpr int kOffRed = kOffRing + kSlots * kHalfBytes;  // [2 slots][2 halves][128] fp32
+  static constexpr int kOffBar = kOffRed + 2 * 2 * kBlockM * 4;
+  static constexpr int kQFull = 0;
+  static constexpr int kFull = 1;
+  static constexpr int kEmpty = kFull + kSlots;
+  static constexpr int kSFull = kEmpty + kSlots;  // 2
+  static constexpr int kPFull = kSFull + 2;       // 2
+  static constexpr int kPVDone = kPFull + 2;      // 2
+  static constexpr int kXch = kPVDone + 2;        // [4 lane quarters][2 slots]
+  static constexpr int kOEmpty = kXch + 8;        // the O accumulator has been read
+  static constexpr int kOutFull = kOEmpty + 1;    // staged O tile complete
+  static constexpr int kDrain = kOutFull + 1;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 48;  // + TMEM address,
+  // abort flag, producers' last fills
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static constexpr uint32_t kColS = 0, kColO = 256;
+  static constexpr int kThreads = 384;
+};
+
+template <bool F16>
+__global__ void __launch_bounds__(384, 1)
+    swa_fwd256_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_o, const Args256 a) {
+  using C = F256;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (!smem_base_ok(smem, a.err)) return;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  int& abort_flag = *reinterpret_cast<int*>(tmem_slot + 1);  // raised by a failed wait
+  int* s_last = reinterpret_cast<int*>(tmem_slot + 4);        // producers' last fills
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t sQ = smem_u32(smem + C::kOffQ);
+  float* s_red = reinterpret_cast<float*>(smem + C::kOffRed);
+  const Ring<C::kSlots> rg{smem_u32(smem + C::kOffRing), bar(C::kFull), bar(C::kEmpty)};
+  const int tile_step = static_cast<int>(gridDim.x);
+  const Span sp = a.span;
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(bar(C::kQFull), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bar(C::kFull + s), 1);
+      mbar_init(bar(C::kEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::kSFull + b), 1);
+      mbar_init(bar(C::kPFull + b), 8);
+      mbar_init(bar(C::kPVDone + b), 1);
+    }
+    for (int x = 0; x < 8; ++x) mbar_init(bar(C::kXch + x), 2);  // the two warps of a quarter
+    mbar_init(bar(C::kOEmpty), 8);
+    mbar_init(bar(C::kOutFull), 8);
+    mbar_init(bar(C::kDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8 || warp == 11) {
+    // ------------------------------------------------------------ K / V ring (even / odd items)
+    const int p = warp == 8 ? 0 : 1;
+    int last[C::kSlots];  // lane 0: last item loaded per slot
+    for (int s = 0; s < C::kSlots; ++s) last[s] = -1;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int i = 0;
+      bool ok = true;
+      auto put_block = [&](const CUtensorMap* m, int k0, int bhk) {
+        for (int hf = 0; hf < 2; ++hf, ++i) {
+          if (!ok || (i & 1) != p) continue;
+          ok = ring_load(rg, i, Item{m, hf, k0, bhk}, &abort_flag, a.err);
+          if (ok) last[i % C::kSlots] = i;
+        }
+      };
+      for (int t = blockIdx.x; ok && t < a.ntiles; t += tile_step) {
+        const QTile f = qtile(t, a, sp);
+        put_block(&tm_k, f.kb_lo * kBlockN, f.bhk);
+        for (int j = 0; j < f.nkv; ++j) {
+          if (j + 1 < f.nkv) put_block(&tm_k, (f.kb_lo + j + 1) * kBlockN, f.bhk);
+          put_block(&tm_v, (f.kb_lo + j) * kBlockN, f.bhk);
+        }
+      }
+    }
+    ring_drain(rg, last, s_last, p, lane, a.err);
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ Q loads, O stores
+    auto load_q = [&](int t) {
+      const QTile f = qtile(t, a, sp);
+      mbar_arrive_expect_tx(bar(C::kQFull), kFullBytes);
+      for (int c = 0; c < 4; ++c)
+        tma_load_3d(sQ + c * kChunk, &tm_q, bar(C::kQFull), 64 * c, f.q0, f.bh);
+    };
+    int last_q = -1;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_o);
+      if (static_cast<int>(blockIdx.x) < a.ntiles) {
+        load_q(blockIdx.x);
+        last_q = 0;
+      }
+    }
+    for (int t = blockIdx.x, it = 0; t < a.ntiles; t += tile_step, ++it) {
+      if (!warp_wait(bar(C::kOutFull), it & 1, &abort_flag, a.err)) break;
+      if (lane == 0) {
+        const QTile f = qtile(t, a, sp);
+        for (int c = 0; c < 4; ++c) tma_store_3d(&tm_o, sQ + c * kChunk, 64 * c, f.q0, f.bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the Q buffer may be refilled once the store has read it
+        if (t + tile_step < a.ntiles) {
+          load_q(t + tile_step);
+          last_q = it + 1;
+        }
+      }
+      __syncwarp();
+    }
+    if (lane == 0 && last_q >= 0) drain_wait(bar(C::kQFull), last_q & 1, a.err);
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockM, kBlockN, false, false);
+    constexpr uint32_t kIdO = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockM, 128, false, true);
+    int i = 0;  // ring items consumed
+    // S_gg = Q_lo K_lo^T + Q_hi K_hi^T into S buffer gg & 1.  That buffer last held P_{gg-2},
+    // whose P V was issued before this.
+    auto issue_s = [&](int gg) -> bool {
+      const uint32_t d = tmem + C::kColS + 128u * (gg & 1);
+      for (int hf = 0; hf < 2; ++hf, ++i) {
+        if (!warp_wait(rg.full(i), rg.parity(i), &abort_flag, a.err)) return false;
+        tc_fence_after();
+        umma_ss_kmajor_x8(d, smem_desc_sw128(sQ + hf * kHalfBytes, 16, 1024),
+                          smem_desc_sw128(rg.slot(i), 16, 1024), kIdS, hf);
+        umma_commit_w(rg.empty(i));
+      }
+      umma_commit_w(bar(C::kSFull + (gg & 1)));
+      return true;
+    };
+    // O[:, 128 hf ..] (+)= P_gg V_hf, P_gg packed over S buffer gg & 1 (two 32-column halves).
+    auto issue_pv = [&](int gg, bool first) -> bool {
+      const int pb = gg & 1;
+      if (!warp_wait(bar(C::kPFull + pb), (gg >> 1) & 1, &abort_flag, a.err)) return false;
+      for (int hf = 0; hf < 2; ++hf, ++i) {
+        if (!warp_wait(rg.full(i), rg.parity(i), &abort_flag, a.err)) return false;
+        tc_fence_after();
+        umma_ts_mnmajor_x8_split(tmem + C::kColO + 128u * hf, tmem + C::kColS + 128u * pb,
+                                 smem_desc_sw128(rg.slot(i), kChunk, 1024), kIdO,
+                                 first ? 0u : 1u);
+        umma_commit_w(rg.empty(i));
+      }
+      umma_commit_w(bar(C::kPVDone + pb));
+      return true;
+    };
+    int g = 0;  // key blocks issued so far by this CTA
+    bool ok = true;
+    for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
+      const QTile f = qtile(t, a, sp);
+      ok = warp_wait(bar(C::kQFull), it & 1, &abort_flag, a.err);
+      if (ok) ok = issue_s(g);
+      for (int j = 0; ok && j < f.nkv; ++j) {
+        if (j + 1 < f.nkv) ok = issue_s(g + j + 1);
+        // The first P V of a tile overwrites O: the previous tile's epilogue must have read it.
+        if (ok && j == 0 && it > 0)
+          ok = warp_wait(bar(C::kOEmpty), (it - 1) & 1, &abort_flag, a.err);
+        if (ok) ok = issue_pv(g + j, j == 0);
+      }
+      g += f.nkv;
+    }
+    umma_commit_w(bar(C::kDrain));  // every issued MMA completes before TMEM is released
+    warp_drain_wait(bar(C::kDrain), 0, a.err);
+  } else {
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const int r = static_cast<int>(threadIdx.x & 127);  // row within the tile == TMEM lane
+    const uint32_t h = warp >> 2;                          // column half of every score tile
+    const uint32_t quarter = warp & 3u;
+    const uint32_t lane_base = (quarter * 32u) << 16;
+    const float sl2 = a.scale_log2;
+    int xn = 0;  // exchanges done so far
+    // Swap a per-row value with the thread that owns the other half of the row (slot xn & 1 was
+    // last used two exchanges ago, and the partner passed the exchange in between only after
+    // reading it).
+    auto exchange = [&](float v, float* other) -> bool {
+      float* red = s_red + (xn & 1) * 2 * kBlockM;
+      red[h * kBlockM + r] = v;
+      __syncwarp();
+      const uint32_t xb = bar(C::kXch + quarter * 2 + (xn & 1));
+      if (lane == 0) mbar_arrive(xb);
+      if (!warp_wait(xb, (xn >> 1) & 1, &abort_flag, a.err)) return false;
+      *other = red[(h ^ 1u) * kBlockM + r];
+      ++xn;
+      return true;
+    };
+    int g = 0;  // key blocks consumed so far by this CTA
+    bool ok = true;
+    for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
+      const QTile f = qtile(t, a, sp);
+      const int q0 = f.q0;
+      const int row = q0 + r;
+      float m_ref = SWA_NEG_INF;  // reference max (log2 domain) that P and l are taken against
+      float l = 0.f;              // partial row sum over this thread's half of the columns
+      for (int j = 0; j < f.nkv; ++j) {
+        const int gg = g + j;
+        const int k0 = (f.kb_lo + j) * kBlockN;
+        const int sb = gg & 1;
+        if (!(ok = warp_wait(bar(C::kSFull + sb), (gg >> 1) & 1, &abort_flag, a.err))) break;
+        tc_fence_after();
+        const uint32_t s_col = tmem + lane_base + C::kColS + 128u * sb + 64u * h;
+        float x[64];  // raw scores S (the scale is applied inside the exponent)
+        {
+          uint32_t rr[2][32];
+          tmem_ld32(s_col, rr[0]);
+          tmem_ld32(s_col + 32u, rr[1]);
+          tmem_wait_ld_all();
+          reg_fence(rr[0]);
+          reg_fence(rr[1]);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(rr[c >> 5][c & 31]);
+        }
+        if (!sp.interior(q0, k0)) {
+          // Columns c (keys k0 + 64h + c) visible to row `row`, and inside the key sequence.
+          const int rel = row + sp.off - k0 - 64 * static_cast<int>(h);
+          mask64(x, rel - sp.dmax, min(rel - sp.dmin, sp.Lk - 1 - k0 - 64 * static_cast<int>(h)),
+                 SWA_NEG_INF);
+        }
+        uint32_t pk[32];
+        auto exponentiate = [&](float m) -> float {
+          const float2 scale2 = make_float2(sl2, sl2), neg_m2 = make_float2(-m, -m);
+          float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 tt = __ffma2_rn(make_float2(x[2 * c], x[2 * c + 1]), scale2, neg_m2);
+            const float2 e = make_float2(ex2(tt.x), ex2(tt.y));
+            rs2[c & 3] = __fadd2_rn(rs2[c & 3], e);
+            pk[c] = Elem<F16>::pack(e.x, e.y);
+          }
+          return ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) +
+                 ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
+        };
+        // One pass against the running reference max; redone exactly on a tile's first block or
+        // when a row's block sum exceeds 2^12 (both halves of a row decide alike).
+        bool redo = true;
+        float bsum = 0.f;
+        if (__all_sync(0xffffffffu, m_ref != SWA_NEG_INF)) {
+          bsum = exponentiate(m_ref);
+          float other;
+          if (!(ok = exchange(bsum, &other))) break;
+          redo = __any_sync(0xffffffffu, !(bsum + other <= kFastSumLimit256));
+        }
+        bool resc = false;
+        float factor = 1.f;
+        if (redo) {
+          float m8[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) m8[c] = x[c];
+#pragma unroll
+          for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+          float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
+          float mx_other;
+          if (!(ok = exchange(mx, &mx_other))) break;
+          mx = fmaxf(mx, mx_other);
+          const float m_new = fmaxf(m_ref, mx);
+          resc = m_new > m_ref + kRescaleThreshold256;
+          if (resc) {
+            factor = ex2(m_ref - m_new);  // 0 when m_ref is -inf
+            l *= factor;
+            m_ref = m_new;
+          }
+          bsum = exponentiate((m_ref == SWA_NEG_INF) ? 0.f : m_ref);
+        }
+        l += bsum;
+        // Rescaling O needs this tile's P V of block gg - 1 (and so every earlier one) to have
+        // landed; a tile's first block needs none (its P V overwrites O).
+        if (j >= 1 && __any_sync(0xffffffffu, resc)) {
+          if (!(ok = warp_wait(bar(C::kPVDone + (sb ^ 1)), ((gg - 1) >> 1) & 1, &abort_flag,
+                               a.err)))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            const uint32_t oc = tmem + lane_base + C::kColO + 128u * h + c0;
+            uint32_t rr[32];
+            tmem_ld32(oc, rr);
+            tmem_wait_ld(rr);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * factor);
+            tmem_st32(oc, rr);
+          }
+        } else {
+          tc_fence_after();
+        }
+        // keys [64h, 64h + 64) -> packed P over the first 32 of this thread's S columns (the
+        // landing of S_gg implies P V_{gg-2}, which read the previous P here, has completed).
+        tmem_st32(s_col, pk);
+        tmem_wait_st();
+        warp_arrive(bar(C::kPFull + sb));
+      }
+      if (!ok) break;
+      g += f.nkv;
+
+      // ---------------------------------------------------------- tile epilogue
+      float l_other = 0.f;
+      if (!(ok = exchange(l, &l_other))) break;
+      const int last = g - 1;
+      if (!(ok = warp_wait(bar(C::kPVDone + (last & 1)), (last >> 1) & 1, &abort_flag, a.err)))
+        break;
+      tc_fence_after();
+      const float l_row = l + l_other;
+      const float inv_l = 1.f / l_row;
+      const float m_use = (m_ref == SWA_NEG_INF) ? 0.f : m_ref;
+      if (row < sp.Lq && h == 0)
+        a.lse_out[static_cast<size_t>(f.bh) * sp.Lq + row] = (m_use + log2f(l_row)) * kLn2;
+      // O / l -> 16-bit, staged in the Q buffer (every S of the tile has completed) in the
+      // swizzled layout of the TMA map; warp 10 stores it.
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + C::kColO + 128u * h + 32u * c4, rr);
+        tmem_wait_ld(rr);
+        uint32_t o16[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          o16[c] = Elem<F16>::pack(__uint_as_float(rr[2 * c]) * inv_l,
+                                   __uint_as_float(rr[2 * c + 1]) * inv_l);
+        stage_row32_sw128(sQ, r, 128u * h + 32u * c4, o16);
+      }
+      warp_arrive(bar(C::kOEmpty));  // the next tile's first P V may overwrite O now
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kOutFull));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================================================
+// dQ: per 128-row query tile, walking the window's key blocks (the forward's walk),
+//   S = Q K_j^T,  P = exp(scale S - LSE) (masked),  dP = dO V_j^T,  dS = P (dP - Delta),
+//   dQ += dS K_j,  dQ *= scale at the end.
+// Persistent.  Warps (384 threads): 0-7 compute (two threads per row), 8 and 11 TMA producers of
+// the K / V ring, 9 MMA issuer and TMEM owner, 10 loads each tile's Q and dO (64 KB each, held for
+// the whole tile).  dS goes over the dP columns it came from and is the A operand of dQ += dS K_j;
+// dP_{j+1} is issued after that MMA, S_{j+1} as soon as the compute warps have read S_j.  K_j is
+// streamed twice (for S_j, then again for dQ += dS_j K_j) because the ring holds only three
+// half-tiles next to Q and dO.
+// Ring order per tile of n key blocks: K_0, V_0, then per block j: K_{j+1} (if any), K_j,
+// V_{j+1} (if any).
+// TMEM: [0,128) S, [128,256) dP / dS, [256,512) dQ.
+// ================================================================================================
+struct Q256 {
+  static constexpr int kSlots = 3;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kOffQ + kFullBytes;
+  static constexpr int kOffRing = kOffDO + kFullBytes;
+  static constexpr int kOffBar = kOffRing + kSlots * kHalfBytes;
+  static constexpr int kQDFull = 0;
+  static constexpr int kQDEmpty = 1;
+  static constexpr int kFull = 2;
+  static constexpr int kEmpty = kFull + kSlots;
+  static constexpr int kSFull = kEmpty + kSlots;
+  static constexpr int kSEmpty = kSFull + 1;
+  static constexpr int kDPFull = kSEmpty + 1;
+  static constexpr int kDSFull = kDPFull + 1;
+  static constexpr int kDQDone = kDSFull + 1;   // a tile's last dQ MMA has completed
+  static constexpr int kDQEmpty = kDQDone + 1;  // the epilogue has read the dQ accumulator
+  static constexpr int kDrain = kDQEmpty + 1;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 48;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  static constexpr int kThreads = 384;
+};
+
+template <bool F16>
+__global__ void __launch_bounds__(384, 1)
+    swa_dq256_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const Args256 a) {
+  using C = Q256;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (!smem_base_ok(smem, a.err)) return;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  int& abort_flag = *reinterpret_cast<int*>(tmem_slot + 1);
+  int* s_last = reinterpret_cast<int*>(tmem_slot + 4);  // producers' last fills
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t sQ = smem_u32(smem + C::kOffQ);
+  const uint32_t sDO = smem_u32(smem + C::kOffDO);
+  const Ring<C::kSlots> rg{smem_u32(smem + C::kOffRing), bar(C::kFull), bar(C::kEmpty)};
+  const int tile_step = static_cast<int>(gridDim.x);
+  const Span sp = a.span;
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(bar(C::kQDFull), 1);
+    mbar_init(bar(C::kQDEmpty), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bar(C::kFull + s), 1);
+      mbar_init(bar(C::kEmpty + s), 1);
+    }
+    mbar_init(bar(C::kSFull), 1);
+    mbar_init(bar(C::kSEmpty), 8);
+    mbar_init(bar(C::kDPFull), 1);
+    mbar_init(bar(C::kDSFull), 8);
+    mbar_init(bar(C::kDQDone), 1);
+    mbar_init(bar(C::kDQEmpty), 8);
+    mbar_init(bar(C::kDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8 || warp == 11) {
+    // ------------------------------------------------------------ K / V ring (even / odd items)
+    const int p = warp == 8 ? 0 : 1;
+    int last[C::kSlots];  // lane 0: last item loaded per slot
+    for (int s = 0; s < C::kSlots; ++s) last[s] = -1;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int i = 0;
+      bool ok = true;
+      auto put_block = [&](const CUtensorMap* m, int k0, int bhk) {
+        for (int hf = 0; hf < 2; ++hf, ++i) {
+          if (!ok || (i & 1) != p) continue;
+          ok = ring_load(rg, i, Item{m, hf, k0, bhk}, &abort_flag, a.err);
+          if (ok) last[i % C::kSlots] = i;
+        }
+      };
+      for (int t = blockIdx.x; ok && t < a.ntiles; t += tile_step) {
+        const QTile f = qtile(t, a, sp);
+        put_block(&tm_k, f.kb_lo * kBlockN, f.bhk);
+        put_block(&tm_v, f.kb_lo * kBlockN, f.bhk);
+        for (int j = 0; j < f.nkv; ++j) {
+          if (j + 1 < f.nkv) put_block(&tm_k, (f.kb_lo + j + 1) * kBlockN, f.bhk);
+          put_block(&tm_k, (f.kb_lo + j) * kBlockN, f.bhk);
+          if (j + 1 < f.nkv) put_block(&tm_v, (f.kb_lo + j + 1) * kBlockN, f.bhk);
+        }
+      }
+    }
+    ring_drain(rg, last, s_last, p, lane, a.err);
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ Q and dO of each tile
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      int last = -1;
+      for (int t = blockIdx.x, it = 0; t < a.ntiles; t += tile_step, ++it) {
+        const QTile f = qtile(t, a, sp);
+        // Q / dO of the previous tile are free once its last S and dP have completed.
+        if (it >= 1 && !mbar_wait(bar(C::kQDEmpty), (it - 1) & 1, &abort_flag, a.err)) break;
+        mbar_arrive_expect_tx(bar(C::kQDFull), 2 * kFullBytes);
+        for (int c = 0; c < 4; ++c) {
+          tma_load_3d(sQ + c * kChunk, &tm_q, bar(C::kQDFull), 64 * c, f.q0, f.bh);
+          tma_load_3d(sDO + c * kChunk, &tm_do, bar(C::kQDFull), 64 * c, f.q0, f.bh);
+        }
+        last = it;
+      }
+      if (last >= 0) drain_wait(bar(C::kQDFull), last & 1, a.err);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdSq = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockM, kBlockN, false, false);
+    constexpr uint32_t kIdDq = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockM, 128, false, true);
+    int i = 0;  // ring items consumed
+    // X (+)= A_lo B_lo^T + A_hi B_hi^T over D, B from the next two ring items.
+    auto product_d = [&](uint32_t d, uint32_t a_tile) -> bool {
+      for (int hf = 0; hf < 2; ++hf, ++i) {
+        if (!warp_wait(rg.full(i), rg.parity(i), &abort_flag, a.err)) return false;
+        tc_fence_after();
+        umma_ss_kmajor_x8(d, smem_desc_sw128(a_tile + hf * kHalfBytes, 16, 1024),
+                          smem_desc_sw128(rg.slot(i), 16, 1024), kIdSq, hf);
+        umma_commit_w(rg.empty(i));
+      }
+      return true;
+    };
+    auto issue_s = [&](int gg) -> bool {  // S = Q K_gg^T once S_{gg-1} has been read
+      if (gg >= 1 && !warp_wait(bar(C::kSEmpty), (gg - 1) & 1, &abort_flag, a.err)) return false;
+      if (!product_d(tmem + C::kColS, sQ)) return false;
+      umma_commit_w(bar(C::kSFull));
+      return true;
+    };
+    auto issue_dp = [&](bool tile_last) -> bool {  // dP = dO V^T (after dQ of the previous block)
+      if (!product_d(tmem + C::kColDP, sDO)) return false;
+      umma_commit_w(bar(C::kDPFull));
+      if (tile_last) umma_commit_w(bar(C::kQDEmpty));  // every S and dP of the tile is issued
+      return true;
+    };
+    auto issue_dq = [&](int gg, bool first, bool tile_last) -> bool {  // dQ += dS K_gg
+      if (!warp_wait(bar(C::kDSFull), gg & 1, &abort_flag, a.err)) return false;
+      for (int hf = 0; hf < 2; ++hf, ++i) {
+        if (!warp_wait(rg.full(i), rg.parity(i), &abort_flag, a.err)) return false;
+        tc_fence_after();
+        umma_ts_mnmajor_x8_split(tmem + C::kColDQ + 128u * hf, tmem + C::kColDP,
+                                 smem_desc_sw128(rg.slot(i), kChunk, 1024), kIdDq,
+                                 first ? 0u : 1u);
+        umma_commit_w(rg.empty(i));
+      }
+      if (tile_last) umma_commit_w(bar(C::kDQDone));
+      return true;
+    };
+    int g = 0;  // key blocks issued so far by this CTA
+    bool ok = true;
+    for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
+      const QTile f = qtile(t, a, sp);
+      const int n = f.nkv;
+      ok = warp_wait(bar(C::kQDFull), it & 1, &abort_flag, a.err);
+      if (ok) ok = issue_s(g);
+      if (ok) ok = issue_dp(n == 1);
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n) ok = issue_s(g + j + 1);
+        // The first dQ of a tile overwrites the accumulator: the previous tile's epilogue must
+        // have read it.
+        if (ok && j == 0 && it > 0)
+          ok = warp_wait(bar(C::kDQEmpty), (it - 1) & 1, &abort_flag, a.err);
+        if (ok) ok = issue_dq(g + j, j == 0, j + 1 == n);
+        if (ok && j + 1 < n) ok = issue_dp(j + 2 == n);
+      }
+      g += n;
+    }
+    umma_commit_w(bar(C::kDrain));
+    warp_drain_wait(bar(C::kDrain), 0, a.err);
+  } else {
+    // ------------------------------------------------------------ compute (warps 0-7)
+    const int r = static_cast<int>(threadIdx.x & 127);  // query row within the tile = TMEM lane
+    const uint32_t h = warp >> 2;                          // column half of every score tile
+    const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
+    const float sl2 = a.scale_log2;
+    int g = 0;
+    bool ok = true;
+    for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
+      const QTile f = qtile(t, a, sp);
+      const int q0 = f.q0;
+      const int row = q0 + r;
+      const bool in_range = row < sp.Lq;
+      const size_t grow = static_cast<size_t>(f.bh) * sp.Lq + row;
+      // Rows past the end see P = 0 (their LSE is taken as +inf), so they add nothing.
+      const float lse2 = in_range ? a.lse[grow] * kLog2e : SWA_POS_INF;
+      const float dlt = in_range ? a.delta[grow] : 0.f;
+      for (int j = 0; j < f.nkv; ++j) {
+        const int gg = g + j;
+        const int k0 = (f.kb_lo + j) * kBlockN;
+        if (!(ok = warp_wait(bar(C::kSFull), gg & 1, &abort_flag, a.err))) break;
+        tc_fence_after();
+        float p[64];
+        {
+          uint32_t rr[2][32];
+          tmem_ld32(tmem + lane_base + C::kColS + 64u * h, rr[0]);
+          tmem_ld32(tmem + lane_base + C::kColS + 64u * h + 32u, rr[1]);
+          tmem_wait_ld_all();
+          reg_fence(rr[0]);
+          reg_fence(rr[1]);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) p[c] = __uint_as_float(rr[c >> 5][c & 31]);
+        }
+        warp_arrive(bar(C::kSEmpty));
+        if (!sp.interior(q0, k0)) {
+          const int rel = row + sp.off - k0 - 64 * static_cast<int>(h);
+          mask64(p, rel - sp.dmax, min(rel - sp.dmin, sp.Lk - 1 - k0 - 64 * static_cast<int>(h)),
+                 SWA_NEG_INF);
+        }
+        {
+          const float2 scale2 = make_float2(sl2, sl2), neg_l2 = make_float2(-lse2, -lse2);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 tt = __ffma2_rn(make_float2(p[2 * c], p[2 * c + 1]), scale2, neg_l2);
+            p[2 * c] = ex2(tt.x);
+            p[2 * c + 1] = ex2(tt.y);
+          }
+        }
+        // dP_gg landing also means dQ_{gg-1} has finished reading the previous dS here.
+        if (!(ok = warp_wait(bar(C::kDPFull), gg & 1, &abort_flag, a.err))) break;
+        tc_fence_after();
+        {
+          const uint32_t dcol = tmem + lane_base + C::kColDP + 64u * h;
+          uint32_t rr[2][32];
+          tmem_ld32(dcol, rr[0]);
+          tmem_ld32(dcol + 32u, rr[1]);
+          tmem_wait_ld_all();
+          reg_fence(rr[0]);
+          reg_fence(rr[1]);
+          uint32_t pk[32];
+          const float2 neg_d2 = make_float2(-dlt, -dlt);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t d0 = rr[c >> 4][(2 * c) & 31], d1 = rr[c >> 4][(2 * c + 1) & 31];
+            const float2 ds = __fmul2_rn(
+                make_float2(p[2 * c], p[2 * c + 1]),
+                __fadd2_rn(make_float2(__uint_as_float(d0), __uint_as_float(d1)), neg_d2));
+            pk[c] = Elem<F16>::pack(ds.x, ds.y);
+          }
+          tmem_st32(dcol, pk);  // over the first 32 of this thread's dP columns
+        }
+        tmem_wait_st();
+        warp_arrive(bar(C::kDSFull));
+      }
+      if (!ok) break;
+      g += f.nkv;
+
+      // ---------------------------------------------------------- tile epilogue
+      if (!(ok = warp_wait(bar(C::kDQDone), it & 1, &abort_flag, a.err))) break;
+      tc_fence_after();
+      uint16_t* dst_row = a.dq + grow * kD + 128 * h;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + C::kColDQ + 128u * h + 32u * c4, rr);
+        tmem_wait_ld(rr);
+        if (in_range) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = Elem<F16>::pack(__uint_as_float(rr[2 * c]) * a.scale,
+                                    __uint_as_float(rr[2 * c + 1]) * a.scale);
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c4);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      warp_arrive(bar(C::kDQEmpty));  // the next tile's first dQ may overwrite the accumulator
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================================================
+// Key-block kernels (dV, dK): one CTA per 128-row key block of one (batch, kv head), walking for
+// each of the G query heads of the group the query blocks that can see the block (as the D <= 128
+// dK / dV kernel does), transposed so the key rows sit on TMEM lanes; the accumulator sums over
+// the whole group (the grouped-query reduction, no atomics).  A key block no query sees stores
+// zeros.
+// ================================================================================================
+struct KWalk {
+  int bhk, k0, qb_lo, nq, T;   // T = G * nq (query head, query block) tiles
+  int q_int_lo, q_int_hi;      // query tiles q0 in [q_int_lo, q_int_hi] need no mask
+  int b, hk;
+  __device__ int q0(int t) const { return (qb_lo + t % nq) * kBlockM; }
+};
+
+__device__ __forceinline__ KWalk kwalk(const Args256& a, const Span& sp) {
+  KWalk w;
+  const int kb = static_cast<int>(blockIdx.x) / a.BHK;
+  w.bhk = static_cast<int>(blockIdx.x) % a.BHK;
+  w.b = w.bhk / a.Hkv;
+  w.hk = w.bhk % a.Hkv;
+  w.k0 = kb * kBlockN;
+  w.qb_lo = sp.first_qblock(w.k0);
+  const int qb_hi = sp.last_qblock(w.k0);
+  w.nq = qb_hi >= w.qb_lo ? qb_hi - w.qb_lo + 1 : 0;
+  w.T = a.G * w.nq;
+  w.q_int_lo = w.k0 + kBlockN - 1 + sp.dmin - sp.off;
+  w.q_int_hi = (w.k0 + kBlockN <= sp.Lk)
+                   ? min(w.k0 + sp.dmax - sp.off - (kBlockM - 1), sp.Lq - kBlockM)
+                   : -1;
+  return w;
+}
+
+__device__ __forceinline__ int walk_bhq(const KWalk& w, const Args256& a, int t) {
+  return w.b * a.Hq + w.hk * a.G + t / w.nq;
+}
+
+// P^T = 2^(scale log2(e) S^T - LSE log2(e)) for this thread's 64 query columns, from the S^T
+// columns at `s_col` and the negated LSE log2(e) of those queries in shared memory; queries the key
+// row does not see get 0 (queries past the end have -LSE = -inf, so P = 0 there already).
+__device__ __forceinline__ void p_transposed(float (&p)[64], uint32_t s_col, const float* nl2,
+                                             float sl2, bool masked, int lo, int hi) {
+  const float4* l4 = reinterpret_cast<const float4*>(nl2);
+  float4 lv[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) lv[c] = l4[c];
+  uint32_t rr[2][32];
+  tmem_ld32(s_col, rr[0]);
+  tmem_ld32(s_col + 32u, rr[1]);
+  tmem_wait_ld_all();
+  reg_fence(rr[0]);
+  reg_fence(rr[1]);
+  const float2 scale2 = make_float2(sl2, sl2);
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const uint32_t* src = &rr[c >> 3][(4 * c) & 31];
+    const float2 t0 = __ffma2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                 scale2, make_float2(lv[c].x, lv[c].y));
+    const float2 t1 = __ffma2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                 scale2, make_float2(lv[c].z, lv[c].w));
+    p[4 * c + 0] = ex2(t0.x);
+    p[4 * c + 1] = ex2(t0.y);
+    p[4 * c + 2] = ex2(t1.x);
+    p[4 * c + 3] = ex2(t1.y);
+  }
+  if (masked) mask64(p, lo, hi, 0.f);
+}
+
+// Epilogue of the key-block kernels: acc (TMEM columns [256, 512), this thread's 128-column half)
+// times `mul` -> 16-bit, staged into the 64 KB tile at `stage`, then one warp stores it with four
+// tensor stores (rows past Lk are not written).  With no visiting query the tile is zeros.
+template <bool F16>
+__device__ __forceinline__ void key_epilogue(uint32_t tmem_row, uint32_t stage, int r, uint32_t h,
+                                             float mul, bool zero, uint32_t out_full_bar,
+                                             const CUtensorMap* map, int k0, int bhk,
+                                             volatile int* abort_flag, unsigned* err) {
+#pragma unroll
+  for (int c4 = 0; c4 < 4; ++c4) {
+    uint32_t rr[32];
+    if (!zero) {
+      tmem_ld32(tmem_row + 128u * h + 32u * c4, rr);
+      tmem_wait_ld(rr);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) rr[c] = 0u;
+    }
+    uint32_t o16[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      o16[c] = Elem<F16>::pack(__uint_as_float(rr[2 * c]) * mul,
+                               __uint_as_float(rr[2 * c + 1]) * mul);
+    stage_row32_sw128(stage, static_cast<uint32_t>(r), 128u * h + 32u * c4, o16);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if ((threadIdx.x & 31u) == 0) mbar_arrive(out_full_bar);
+  if (threadIdx.x < 32 && warp_wait(out_full_bar, 0, abort_flag, err) && threadIdx.x == 0) {
+    for (int c = 0; c < 4; ++c) tma_store_3d(map, stage + c * kChunk, 64 * c, k0, bhk);
+    bulk_commit_group();
+    bulk_wait_group_read0();
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// dV = sum over the walk of P_t^T dO_t.  Warps (352 threads): 0-7 compute (warp w: key rows
+// 32 (w % 4).., query columns [64 h, 64 h + 64), h = w / 4), 8 and 10 TMA producers (warp 8 also
+// loads K once), 9 MMA issuer and TMEM owner.  S^T is double-buffered: S^T_{t+1} is computed while
+// the compute warps turn S^T_t into P^T_t, which is written over S^T_t and read by dV += P^T dO.
+// Ring order: Q_0, then per tile t: Q_{t+1} (if any), dO_t (two halves each).
+// TMEM: [0,128) S^T / P^T buffer 0, [128,256) buffer 1, [256,512) dV.
+// ------------------------------------------------------------------------------------------------
+struct V256 {
+  static constexpr int kSlots = 5;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffRing = kOffK + kFullBytes;
+  static constexpr int kOffRow = kOffRing + kSlots * kHalfBytes;  // [2 slots][128] -LSE log2(e)
+  static constexpr int kOffBar = kOffRow + 2 * kBlockM * 4;
+  static constexpr int kKFull = 0;
+  static constexpr int kFull = 1;
+  static constexpr int kEmpty = kFull + kSlots;
+  static constexpr int kSFull = kEmpty + kSlots;  // 2
+  static constexpr int kPFull = kSFull + 2;       // 2
+  static constexpr int kVecFull = kPFull + 2;     // 2
+  static constexpr int kDone = kVecFull + 2;
+  static constexpr int kOutFull = kDone + 1;
+  static constexpr int kDrain = kOutFull + 1;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 48;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static constexpr uint32_t kColS = 0, kColAcc = 256;
+  static constexpr int kThreads = 352;
+};
+
+template <bool F16>
+__global__ void __launch_bounds__(352, 1)
+    swa_dv256_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_dv, const Args256 a) {
+  using C = V256;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (!smem_base_ok(smem, a.err)) return;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  int& abort_flag = *reinterpret_cast<int*>(tmem_slot + 1);
+  int* s_last = reinterpret_cast<int*>(tmem_slot + 4);  // producers' last fills
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t sK = smem_u32(smem + C::kOffK);
+  float* s_rows = reinterpret_cast<float*>(smem + C::kOffRow);
+  const Ring<C::kSlots> rg{smem_u32(smem + C::kOffRing), bar(C::kFull), bar(C::kEmpty)};
+  const Span sp = a.span;
+  const KWalk w = kwalk(a, sp);
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(bar(C::kKFull), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bar(C::kFull + s), 1);
+      mbar_init(bar(C::kEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::kSFull + b), 1);
+      mbar_init(bar(C::kPFull + b), 8);
+      mbar_init(bar(C::kVecFull + b), 8);
+    }
+    mbar_init(bar(C::kDone), 1);
+    mbar_init(bar(C::kOutFull), 8);
+    mbar_init(bar(C::kDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ K once; Q / dO ring
+    const int p = warp == 8 ? 0 : 1;
+    int last[C::kSlots];  // lane 0: last item loaded per slot
+    for (int s = 0; s < C::kSlots; ++s) last[s] = -1;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      if (p == 0) {
+        tma_prefetch_desc(&tm_k);
+        mbar_arrive_expect_tx(bar(C::kKFull), kFullBytes);
+        for (int c = 0; c < 4; ++c)
+          tma_load_3d(sK + c * kChunk, &tm_k, bar(C::kKFull), 64 * c, w.k0, w.bhk);
+      }
+      int i = 0;
+      bool ok = true;
+      auto put_tile = [&](const CUtensorMap* m, int t) {
+        for (int hf = 0; hf < 2; ++hf, ++i) {
+          if (!ok || (i & 1) != p) continue;
+          ok = ring_load(rg, i, Item{m, hf, w.q0(t), walk_bhq(w, a, t)}, &abort_flag, a.err);
+          if (ok) last[i % C::kSlots] = i;
+        }
+      };
+      if (w.T > 0) put_tile(&tm_q, 0);
+      for (int t = 0; ok && t < w.T; ++t) {
+        if (t + 1 < w.T) put_tile(&tm_q, t + 1);
+        put_tile(&tm_do, t);
+      }
+      if (p == 0) drain_wait(bar(C::kKFull), 0, a.err);
+    }
+    ring_drain(rg, last, s_last, p, lane, a.err);
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockN, kBlockM, false, false);
+    constexpr uint32_t kIdAcc = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockN, 128, false, true);
+    int i = 0;
+    auto issue_s = [&](int t) -> bool {  // S^T_t = K_lo Q_lo^T + K_hi Q_hi^T into buffer t & 1
+      const uint32_t d = tmem + C::kColS + 128u * (t & 1);
+      for (int hf = 0; hf < 2; ++hf, ++i) {
+        if (!warp_wait(rg.full(i), rg.parity(i), &abort_flag, a.err)) return false;
+        tc_fence_after();
+        umma_ss_kmajor_x8(d, smem_desc_sw128(sK + hf * kHalfBytes, 16, 1024),
+                          smem_desc_sw128(rg.slot(i), 16, 1024), kIdS, hf);
+        umma_commit_w(rg.empty(i));
+      }
+      umma_commit_w(bar(C::kSFull + (t & 1)));
+      return true;
+    };
+    auto issue_dv = [&](int t) -> bool {  // dV[:, 128 hf ..] (+)= P_t^T dO_t[:, 128 hf ..]
+      const int pb = t & 1;
+      if (!warp_wait(bar(C::kPFull + pb), (t >> 1) & 1, &abort_flag, a.err)) return false;
+      for (int hf = 0; hf < 2; ++hf, ++i) {
+        if (!warp_wait(rg.full(i), rg.parity(i), &abort_flag, a.err)) return false;
+        tc_fence_after();
+        umma_ts_mnmajor_x8_split(tmem + C::kColAcc + 128u * hf, tmem + C::kColS + 128u * pb,
+                                 smem_desc_sw128(rg.slot(i), kChunk, 1024), kIdAcc,
+                                 t > 0 ? 1u : 0u);
+        umma_commit_w(rg.empty(i));
+      }
+      return true;
+    };
+    bool ok = warp_wait(bar(C::kKFull), 0, &abort_flag, a.err);
+    if (ok && w.T > 0) ok = issue_s(0);
+    for (int t = 0; ok && t < w.T; ++t) {
+      if (t + 1 < w.T) ok = issue_s(t + 1);  // buffer (t+1)&1 last held P^T_{t-1}, read by dV_{t-1}
+      if (ok) ok = issue_dv(t);
+    }
+    if (ok) umma_commit_w(bar(C::kDone));
+    umma_commit_w(bar(C::kDrain));
+    warp_drain_wait(bar(C::kDrain), 0, a.err);
+  } else {
+    // ------------------------------------------------------------ compute (warps 0-7)
+    const int r = static_cast<int>(threadIdx.x & 127);  // key row within the block = TMEM lane
+    const uint32_t h = warp >> 2;
+    const int key = w.k0 + r;
+    const int vis_lo = key + sp.dmin - sp.off, vis_hi = key + sp.dmax - sp.off;
+    const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
+    float nxt = 0.f;  // LSE of query q0(t) + r, fetched a tile ahead (h = 0 threads)
+    auto fetch_row = [&](int t) {
+      const int q = w.q0(t) + r;
+      nxt = q < sp.Lq ? a.lse[static_cast<size_t>(walk_bhq(w, a, t)) * sp.Lq + q] : SWA_POS_INF;
+    };
+    if (w.T > 0 && h == 0) fetch_row(0);
+    bool ok = true;
+    for (int t = 0; t < w.T; ++t) {
+      const int q0 = w.q0(t);
+      // Slot t & 1 was last read in tile t - 2; every warp has since arrived for tile t - 1.
+      float* nl2 = s_rows + (t & 1) * kBlockM;
+      if (h == 0) nl2[r] = -nxt * kLog2e;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kVecFull + (t & 1)));
+      if (!(ok = warp_wait(bar(C::kVecFull + (t & 1)), (t >> 1) & 1, &abort_flag, a.err))) break;
+      if (t + 1 < w.T && h == 0) fetch_row(t + 1);
+      if (!(ok = warp_wait(bar(C::kSFull + (t & 1)), (t >> 1) & 1, &abort_flag, a.err))) break;
+      tc_fence_after();
+      const uint32_t s_col = tmem + lane_base + C::kColS + 128u * (t & 1) + 64u * h;
+      float p[64];
+      const int base = q0 + 64 * static_cast<int>(h);
+      p_transposed(p, s_col, nl2 + 64 * h, a.scale_log2, !(q0 >= w.q_int_lo && q0 <= w.q_int_hi),
+                   vis_lo - base, vis_hi - base);
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pk[c] = Elem<F16>::pack(p[2 * c], p[2 * c + 1]);
+      tmem_st32(s_col, pk);
+      tmem_wait_st();
+      warp_arrive(bar(C::kPFull + (t & 1)));
+    }
+    if (ok && warp_wait(bar(C::kDone), 0, &abort_flag, a.err)) {
+      tc_fence_after();
+      // dV -> 16-bit, staged in the K buffer (every MMA has completed).
+      key_epilogue<F16>(tmem + lane_base + C::kColAcc, sK, r, h, 1.f, w.T == 0, bar(C::kOutFull),
+                        &tm_dv, w.k0, w.bhk, &abort_flag, a.err);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// dK = scale * sum over the walk of dS_t^T Q_t, dS^T = P^T (dP^T - Delta), dP^T = V dO^T.
+// Warps (352 threads): 0-7 compute, 8 and 10 TMA producers (warp 8 also loads K, warp 10 V, once
+// each), 9 MMA issuer and TMEM owner.  S^T_{t+1} is issued as soon as the compute warps have read
+// S^T_t; dS^T goes over the dP^T columns it came from and is the A operand of dK += dS^T Q_t,
+// after which dP^T_{t+1} is issued.  Q_t is streamed twice (for S^T, then for dK) because the
+// ring holds only three half-tiles next to K and V.
+// Ring order: Q_0, dO_0, then per tile t: Q_{t+1} (if any), Q_t, dO_{t+1} (if any).
+// TMEM: [0,128) S^T, [128,256) dP^T / dS^T, [256,512) dK.
+// ------------------------------------------------------------------------------------------------
+struct K256 {
+  static constexpr int kSlots = 3;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kFullBytes;
+  static constexpr int kOffRing = kOffV + kFullBytes;
+  static constexpr int kOffRow = kOffRing + kSlots * kHalfBytes;  // [2 slots][-LSE log2e | -Delta]
+  static constexpr int kOffBar = kOffRow + 2 * 2 * kBlockM * 4;
+  static constexpr int kKVFull = 0;
+  static constexpr int kFull = 1;
+  static constexpr int kEmpty = kFull + kSlots;
+  static constexpr int kSFull = kEmpty + kSlots;
+  static constexpr int kSEmpty = kSFull + 1;
+  static constexpr int kDPFull = kSEmpty + 1;
+  static constexpr int kDSFull = kDPFull + 1;
+  static constexpr int kVecFull = kDSFull + 1;  // 2
+  static constexpr int kDone = kVecFull + 2;
+  static constexpr int kOutFull = kDone + 1;
+  static constexpr int kDrain = kOutFull + 1;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 48;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
+  static constexpr int kThreads = 352;
+};
+
+template <bool F16>
+__global__ void __launch_bounds__(352, 1)
+    swa_dk256_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_dk, const Args256 a) {
+  using C = K256;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (!smem_base_ok(smem, a.err)) return;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  int& abort_flag = *reinterpret_cast<int*>(tmem_slot + 1);
+  int* s_last = reinterpret_cast<int*>(tmem_slot + 4);  // producers' last fills
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t sK = smem_u32(smem + C::kOffK);
+  const uint32_t sV = smem_u32(smem + C::kOffV);
+  float* s_rows = reinterpret_cast<float*>(smem + C::kOffRow);
+  const Ring<C::kSlots> rg{smem_u32(smem + C::kOffRing), bar(C::kFull), bar(C::kEmpty)};
+  const Span sp = a.span;
+  const KWalk w = kwalk(a, sp);
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(bar(C::kKVFull), 2);  // one arrival per producer warp
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bar(C::kFull + s), 1);
+      mbar_init(bar(C::kEmpty + s), 1);
+    }
+    mbar_init(bar(C::kSFull), 1);
+    mbar_init(bar(C::kSEmpty), 8);
+    mbar_init(bar(C::kDPFull), 1);
+    mbar_init(bar(C::kDSFull), 8);
+    mbar_init(bar(C::kVecFull + 0), 8);
+    mbar_init(bar(C::kVecFull + 1), 8);
+    mbar_init(bar(C::kDone), 1);
+    mbar_init(bar(C::kOutFull), 8);
+    mbar_init(bar(C::kDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ K / V once; Q / dO ring
+    const int p = warp == 8 ? 0 : 1;
+    int last[C::kSlots];  // lane 0: last item loaded per slot
+    for (int s = 0; s < C::kSlots; ++s) last[s] = -1;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      {
+        const CUtensorMap* m = p == 0 ? &tm_k : &tm_v;
+        const uint32_t dst = p == 0 ? sK : sV;
+        mbar_arrive_expect_tx(bar(C::kKVFull), kFullBytes);
+        for (int c = 0; c < 4; ++c)
+          tma_load_3d(dst + c * kChunk, m, bar(C::kKVFull), 64 * c, w.k0, w.bhk);
+      }
+      int i = 0;
+      bool ok = true;
+      auto put_tile = [&](const CUtensorMap* m, int t) {
+        for (int hf = 0; hf < 2; ++hf, ++i) {
+          if (!ok || (i & 1) != p) continue;
+          ok = ring_load(rg, i, Item{m, hf, w.q0(t), walk_bhq(w, a, t)}, &abort_flag, a.err);
+          if (ok) last[i % C::kSlots] = i;
+        }
+      };
+      if (w.T > 0) {
+        put_tile(&tm_q, 0);
+        put_tile(&tm_do, 0);
+      }
+      for (int t = 0; ok && t < w.T; ++t) {
+        if (t + 1 < w.T) put_tile(&tm_q, t + 1);
+        put_tile(&tm_q, t);
+        if (t + 1 < w.T) put_tile(&tm_do, t + 1);
+      }
+      drain_wait(bar(C::kKVFull), 0, a.err);
+    }
+    ring_drain(rg, last, s_last, p, lane, a.err);
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockN, kBlockM, false, false);
+    constexpr uint32_t kIdAcc = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockN, 128, false, true);
+    int i = 0;
+    auto product_d = [&](uint32_t d, uint32_t a_tile) -> bool {  // (+)= A_hf B_hf^T over D
+      for (int hf = 0; hf < 2; ++hf, ++i) {
+        if (!warp_wait(rg.full(i), rg.parity(i), &abort_flag, a.err)) return false;
+        tc_fence_after();
+        umma_ss_kmajor_x8(d, smem_desc_sw128(a_tile + hf * kHalfBytes, 16, 1024),
+                          smem_desc_sw128(rg.slot(i), 16, 1024), kIdS, hf);
+        umma_commit_w(rg.empty(i));
+      }
+      return true;
+    };
+    auto issue_s = [&](int t) -> bool {  // S^T = K Q_t^T once S^T_{t-1} has been read
+      if (t >= 1 && !warp_wait(bar(C::kSEmpty), (t - 1) & 1, &abort_flag, a.err)) return false;
+      if (!product_d(tmem + C::kColS, sK)) return false;
+      umma_commit_w(bar(C::kSFull));
+      return true;
+    };
+    auto issue_dp = [&]() -> bool {  // dP^T = V dO_t^T, after dK of the previous tile
+      if (!product_d(tmem + C::kColDP, sV)) return false;
+      umma_commit_w(bar(C::kDPFull));
+      return true;
+    };
+    auto issue_dk = [&](int t) -> bool {  // dK[:, 128 hf ..] (+)= dS_t^T Q_t[:, 128 hf ..]
+      if (!warp_wait(bar(C::kDSFull), t & 1, &abort_flag, a.err)) return false;
+      for (int hf = 0; hf < 2; ++hf, ++i) {
+        if (!warp_wait(rg.full(i), rg.parity(i), &abort_flag, a.err)) return false;
+        tc_fence_after();
+        umma_ts_mnmajor_x8_split(tmem + C::kColAcc + 128u * hf, tmem + C::kColDP,
+                                 smem_desc_sw128(rg.slot(i), kChunk, 1024), kIdAcc,
+                                 t > 0 ? 1u : 0u);
+        umma_commit_w(rg.empty(i));
+      }
+      return true;
+    };
+    bool ok = warp_wait(bar(C::kKVFull), 0, &abort_flag, a.err);
+    if (ok && w.T > 0) ok = issue_s(0);
+    if (ok && w.T > 0) ok = issue_dp();
+    for (int t = 0; ok && t < w.T; ++t) {
+      if (t + 1 < w.T) ok = issue_s(t + 1);
+      if (ok) ok = issue_dk(t);
+      if (ok && t + 1 < w.T) ok = issue_dp();
+    }
+    if (ok) umma_commit_w(bar(C::kDone));
+    umma_commit_w(bar(C::kDrain));
+    warp_drain_wait(bar(C::kDrain), 0, a.err);
+  } else {
+    // ------------------------------------------------------------ compute (warps 0-7)
+    const int r = static_cast<int>(threadIdx.x & 127);
+    const uint32_t h = warp >> 2;
+    const int key = w.k0 + r;
+    const int vis_lo = key + sp.dmin - sp.off, vis_hi = key + sp.dmax - sp.off;
+    const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
+    // h = 0 threads fetch LSE, h = 1 threads Delta, of query q0(t) + r, a tile ahead.
+    float nxt = 0.f;
+    auto fetch_row = [&](int t) {
+      const int q = w.q0(t) + r;
+      if (q < sp.Lq) {
+        const size_t gi = static_cast<size_t>(walk_bhq(w, a, t)) * sp.Lq + q;
+        nxt = h == 0 ? a.lse[gi] : a.delta[gi];
+      } else {
+        nxt = h == 0 ? SWA_POS_INF : 0.f;
+      }
+    };
+    if (w.T > 0) fetch_row(0);
+    bool ok = true;
+    for (int t = 0; t < w.T; ++t) {
+      const int q0 = w.q0(t);
+      float* nl2 = s_rows + (t & 1) * 2 * kBlockM;  // -LSE log2(e)
+      float* nd = nl2 + kBlockM;                     // -Delta
+      if (h == 0)
+        nl2[r] = -nxt * kLog2e;
+      else
+        nd[r] = -nxt;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kVecFull + (t & 1)));
+      if (!(ok = warp_wait(bar(C::kVecFull + (t & 1)), (t >> 1) & 1, &abort_flag, a.err))) break;
+      if (t + 1 < w.T) fetch_row(t + 1);
+      if (!(ok = warp_wait(bar(C::kSFull), t & 1, &abort_flag, a.err))) break;
+      tc_fence_after();
+      float p[64];
+      const int base = q0 + 64 * static_cast<int>(h);
+      p_transposed(p, tmem + lane_base + C::kColS + 64u * h, nl2 + 64 * h, a.scale_log2,
+                   !(q0 >= w.q_int_lo && q0 <= w.q_int_hi), vis_lo - base, vis_hi - base);
+      warp_arrive(bar(C::kSEmpty));  // S^T_{t+1} may overwrite S^T_t now
+      if (!(ok = warp_wait(bar(C::kDPFull), t & 1, &abort_flag, a.err))) break;
+      tc_fence_after();
+      {
+        const uint32_t dcol = tmem + lane_base + C::kColDP + 64u * h;
+        const float4* d4 = reinterpret_cast<const float4*>(nd + 64 * h);
+        float4 dv4[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) dv4[c] = d4[c];
+        uint32_t rr[2][32];
+        tmem_ld32(dcol, rr[0]);
+        tmem_ld32(dcol + 32u, rr[1]);
+        tmem_wait_ld_all();
+        reg_fence(rr[0]);
+        reg_fence(rr[1]);
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t* src = &rr[c >> 3][(4 * c) & 31];
+          const float2 d0 = __fadd2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                       make_float2(dv4[c].x, dv4[c].y));
+          const float2 d1 = __fadd2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                       make_float2(dv4[c].z, dv4[c].w));
+          const float2 s0 = __fmul2_rn(make_float2(p[4 * c], p[4 * c + 1]), d0);
+          const float2 s1 = __fmul2_rn(make_float2(p[4 * c + 2], p[4 * c + 3]), d1);
+          pk[2 * c] = Elem<F16>::pack(s0.x, s0.y);
+          pk[2 * c + 1] = Elem<F16>::pack(s1.x, s1.y);
+        }
+        tmem_st32(dcol, pk);  // over the first 32 of this thread's dP^T columns
+      }
+      tmem_wait_st();
+      warp_arrive(bar(C::kDSFull));
+    }
+    if (ok && warp_wait(bar(C::kDone), 0, &abort_flag, a.err)) {
+      tc_fence_after();
+      // dK * scale -> 16-bit, staged in the K buffer (every MMA has completed).
+      key_epilogue<F16>(tmem + lane_base + C::kColAcc, sK, r, h, a.scale, w.T == 0,
+                        bar(C::kOutFull), &tm_dk, w.k0, w.bhk, &abort_flag, a.err);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================================================
+// Host launchers
+// ================================================================================================
+Args256 make_args(const Problem& pb, const float* lse, const float* delta, void* dq,
+                  float* lse_out = nullptr) {
+  Args256 a;
+  a.lse = lse;
+  a.lse_out = lse_out;
+  a.delta = delta;
+  a.dq = static_cast<uint16_t*>(dq);
+  a.BH = pb.B * pb.Hq;
+  a.Hq = pb.Hq;
+  a.Hkv = pb.Hkv;
+  a.G = pb.Hq / pb.Hkv;
+  a.nqb = (pb.span.Lq + kBlockM - 1) / kBlockM;
+  a.ntiles = a.nqb * a.BH;
+  a.BHK = pb.B * pb.Hkv;
+  a.span = pb.span;
+  a.scale = pb.scale;
+  a.scale_log2 = pb.scale * kLog2e;
+  a.err = pb.err;
+  return a;
+}
+
+// Maps of the query-shaped (Lq rows) and key-shaped (Lk rows) tensors of one call.
+bool qmap(CUtensorMap* m, const void* p, const Problem& pb) {
+  return make_tmap_3d(m, p, static_cast<uint64_t>(pb.B) * pb.Hq, pb.span.Lq, kD, kBlockM, pb.f16);
+}
+bool kmap(CUtensorMap* m, const void* p, const Problem& pb) {
+  return make_tmap_3d(m, p, static_cast<uint64_t>(pb.B) * pb.Hkv, pb.span.Lk, kD, kBlockN, pb.f16);
+}
+
+template <typename Kern>
+cudaError_t set_smem(Kern kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <bool F16>
+cudaError_t fwd256(const Problem& pb, const void* q, const void* k, const void* v, void* o,
+                   float* lse, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, to;
+  if (!qmap(&tq, q, pb) || !qmap(&to, o, pb) || !kmap(&tk, k, pb) || !kmap(&tv, v, pb))
+    return cudaErrorInvalidValue;
+  auto kern = swa_fwd256_kernel<F16>;
+  cudaError_t e = set_smem(kern, F256::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const Args256 a = make_args(pb, nullptr, nullptr, nullptr, lse);
+  const int grid = a.ntiles < sm_count() ? a.ntiles : sm_count();
+  kern<<<grid, F256::kThreads, F256::kSmemBytes, stream>>>(tq, tk, tv, to, a);
+  return cudaGetLastError();
+}
+
+template <bool F16>
+cudaError_t dq256(const Problem& pb, const void* q, const void* k, const void* v, const void* dO,
+                  const float* lse, const float* delta, void* dq, cudaStream_t stream) {
+  CUtensorMap tq, tdo, tk, tv;
+  if (!qmap(&tq, q, pb) || !qmap(&tdo, dO, pb) || !kmap(&tk, k, pb) || !kmap(&tv, v, pb))
+    return cudaErrorInvalidValue;
+  auto kern = swa_dq256_kernel<F16>;
+  cudaError_t e = set_smem(kern, Q256::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const Args256 a = make_args(pb, lse, delta, dq);
+  const int grid = a.ntiles < sm_count() ? a.ntiles : sm_count();
+  kern<<<grid, Q256::kThreads, Q256::kSmemBytes, stream>>>(tq, tdo, tk, tv, a);
+  return cudaGetLastError();
+}
+
+template <bool F16>
+cudaError_t dkdv256(const Problem& pb, const void* q, const void* k, const void* v,
+                    const void* dO, const float* lse, const float* delta, void* dk, void* dv,
+                    cudaStream_t stream) {
+  CUtensorMap tq, tdo, tk, tv, tdk, tdv;
+  if (!qmap(&tq, q, pb) || !qmap(&tdo, dO, pb) || !kmap(&tk, k, pb) || !kmap(&tv, v, pb) ||
+      !kmap(&tdk, dk, pb) || !kmap(&tdv, dv, pb))
+    return cudaErrorInvalidValue;
+  const Args256 a = make_args(pb, lse, delta, nullptr);
+  const unsigned grid = static_cast<unsigned>((pb.span.Lk + kBlockN - 1) / kBlockN) *
+                        static_cast<unsigned>(a.BHK);
+  auto kk = swa_dk256_kernel<F16>;
+  cudaError_t e = set_smem(kk, K256::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kk<<<grid, K256::kThreads, K256::kSmemBytes, stream>>>(tq, tdo, tk, tv, tdk, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  auto kv = swa_dv256_kernel<F16>;
+  if ((e = set_smem(kv, V256::kSmemBytes)) != cudaSuccess) return e;
+  kv<<<grid, V256::kThreads, V256::kSmemBytes, stream>>>(tq, tdo, tk, tdv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_d256(const Problem& pb, const void* q, const void* k, const void* v,
+                            void* o, float* lse, cudaStream_t stream) {
+  return pb.f16 ? fwd256<true>(pb, q, k, v, o, lse, stream)
+                : fwd256<false>(pb, q, k, v, o, lse, stream);
+}
+
+cudaError_t launch_dq_d256(const Problem& pb, const void* q, const void* k, const void* v,
+                           const void* dO, const float* lse, const float* delta, void* dq,
+                           cudaStream_t stream) {
+  return pb.f16 ? dq256<true>(pb, q, k, v, dO, lse, delta, dq, stream)
+                : dq256<false>(pb, q, k, v, dO, lse, delta, dq, stream);
+}
+
+cudaError_t launch_dkdv_d256(const Problem& pb, const void* q, const void* k, const void* v,
+                             const void* dO, const float* lse, const float* delta, void* dk,
+                             void* dv, cudaStream_t stream) {
+  return pb.f16 ? dkdv256<true>(pb, q, k, v, dO, lse, delta, dk, dv, stream)
+                : dkdv256<false>(pb, q, k, v, dO, lse, delta, dk, dv, stream);
+}
+
+}  // namespace swa

@@ -136,6 +136,8 @@ cudaError_t launch_delta_f32(const Problem& pb, const float* o, const float* dO,
     swa_delta_f32_kernel<64><<<grid_for(lanes), kThreads, 0, stream>>>(o, dO, delta, pd, rows);
   else if (pb.D == 128)
     swa_delta_f32_kernel<128><<<grid_for(lanes), kThreads, 0, stream>>>(o, dO, delta, pd, rows);
+  else if (pb.D == 256)
+    swa_delta_f32_kernel<256><<<grid_for(lanes), kThreads, 0, stream>>>(o, dO, delta, pd, rows);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

@@ -522,6 +522,7 @@ cudaError_t launch_fwd_d(const Problem& pb, const void* q, const void* k, const 
 
 cudaError_t launch_fwd(const Problem& pb, const void* q, const void* k, const void* v, void* o,
                        float* lse, cudaStream_t stream) {
+  if (pb.D == 256) return launch_fwd_d256(pb, q, k, v, o, lse, stream);
   if (pb.D == 64)
     return pb.f16 ? launch_fwd_d<64, true>(pb, q, k, v, o, lse, stream)
                   : launch_fwd_d<64, false>(pb, q, k, v, o, lse, stream);

@@ -90,6 +90,17 @@ cudaError_t launch_bwd_dq(const Problem& pb, const void* q, const void* k, const
                           const void* dO, const float* lse, const float* delta, void* dq,
                           cudaStream_t stream);
 
+// Head dimension 256 (swa_d256.cu): the same operations with half-tile streaming; dK and dV come
+// from two kernels.  launch_fwd / launch_bwd_dq / launch_bwd_dkdv dispatch here for D = 256.
+cudaError_t launch_fwd_d256(const Problem& pb, const void* q, const void* k, const void* v,
+                            void* o, float* lse, cudaStream_t stream);
+cudaError_t launch_dq_d256(const Problem& pb, const void* q, const void* k, const void* v,
+                           const void* dO, const float* lse, const float* delta, void* dq,
+                           cudaStream_t stream);
+cudaError_t launch_dkdv_d256(const Problem& pb, const void* q, const void* k, const void* v,
+                             const void* dO, const float* lse, const float* delta, void* dk,
+                             void* dv, cudaStream_t stream);
+
 // fp32 tensors around the bf16 kernels: up to four tensors per launch, each a whole number of
 // 8-element units (end[t] = units of tensors 0..t, cumulative; unused entries repeat the total).
 constexpr int kMaxJobTensors = 4;

@@ -331,7 +331,8 @@ __device__ __forceinline__ void umma_ss_kmajor_x4(uint32_t d_tmem, uint64_t a_de
       : "memory");
 }
 
-// S-type product over the head dimension D (64 or 128): D / 16 MMAs.
+// S-type product over the head dimension D (64 or 128; D = 256 runs as two 128 halves): D / 16
+// MMAs.
 template <int D>
 __device__ __forceinline__ void umma_ss_kmajor_d(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                  uint32_t idesc, uint32_t accumulate) {

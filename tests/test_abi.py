@@ -80,7 +80,7 @@ def _bwd(lib, B=1, Hq=2, Hkv=1, N=16, D=64, W=4, scale=0.125, ptrs=None, ws=FAKE
     (dict(N=0), 1), (dict(B=0), 1), (dict(Hq=0), 1), (dict(Hkv=0), 1), (dict(W=0), 1),
     (dict(W=-3), 1), (dict(Hq=3, Hkv=2), 1), (dict(scale=0.0), 1), (dict(scale=-1.0), 1),
     (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
-    (dict(D=96), 2), (dict(D=256), 2), (dict(D=32), 2),
+    (dict(D=96), 2), (dict(D=512), 2), (dict(D=32), 2),
 ])
 @pytest.mark.parametrize("f16", [False, True], ids=["bf16", "fp16"])
 def test_fwd_rejects_bad_sizes(lib, kw, code, f16):
@@ -110,7 +110,7 @@ def _bwd_ex(lib, B=1, Hq=2, Hkv=1, Lq=16, Lk=40, D=64, W=4, causal=1, scale=0.12
 
 @pytest.mark.parametrize("kw,code", [
     (dict(Lq=41), 1), (dict(Lq=0), 1), (dict(Lk=0), 1), (dict(causal=2), 1), (dict(causal=-1), 1),
-    (dict(f16=2), 1), (dict(W=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(D=256), 2),
+    (dict(f16=2), 1), (dict(W=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(D=512), 2),
 ])
 def test_ex_entry_points_reject_bad_arguments(lib, kw, code):
     assert _fwd_ex(lib, **kw) == code
@@ -160,7 +160,7 @@ def test_f32_workspace_size():
 
 @pytest.mark.parametrize("kw,code", [
     (dict(Lq=41), 1), (dict(Lq=0), 1), (dict(causal=2), 1), (dict(W=0), 1),
-    (dict(Hq=3, Hkv=2), 1), (dict(scale=0.0), 1), (dict(D=256), 2),
+    (dict(Hq=3, Hkv=2), 1), (dict(scale=0.0), 1), (dict(D=512), 2),
     (dict(ws=0), 6), (dict(ws_bytes=0), 6), (dict(ws=FAKE + 8), 3),
 ])
 def test_f32_entry_points_reject_bad_arguments(lib, kw, code):
@@ -186,6 +186,16 @@ def test_f32_null_and_misaligned_pointers(lib):
         assert _bwd_f32(lib, ptrs=ptrs) == 1
         ptrs[i] = FAKE + 8
         assert _bwd_f32(lib, ptrs=ptrs) == 3
+
+
+def test_head_dims(lib):
+    """D in {64, 128, 256} passes the checks (workspaces are sized), anything else is refused."""
+    for D in (64, 128, 256):
+        assert lib.swa_attn_bwd_workspace_bytes(1, 2, 100, D) > 0
+        assert _f32_need(lib, D=D) > 0
+    for D in (32, 96, 192, 512):
+        assert lib.swa_attn_bwd_workspace_bytes(1, 2, 100, D) == 0
+        assert _fwd_ex(lib, D=D) == 2 and _bwd_ex(lib, D=D) == 2
 
 
 def test_workspace_checks(lib):
