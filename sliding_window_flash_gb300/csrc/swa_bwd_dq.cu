@@ -277,6 +277,40 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t h = warp >> 2;                          // column half of every tile
     const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
     const float sl2 = a.scale_log2;
+    // dQ * scale of tile `pit` -> 16-bit, written straight from registers: each thread owns 64
+    // or 128 contiguous bytes of its row.
+    auto epilogue = [&](int pit, size_t pgrow, bool pin) -> bool {
+      if (!warp_wait(bar(C::kDQDone), pit & 1, &abort_flag, a.err)) return false;
+      tc_fence_after();
+      constexpr int kHalf = D / 2;
+      uint32_t rr[kHalf / 32][32];
+#pragma unroll
+      for (int c4 = 0; c4 < kHalf / 32; ++c4)
+        tmem_ld32(tmem + lane_base + C::kColDQ + kHalf * h + 32u * c4, rr[c4]);
+      tmem_wait_ld_all();
+#pragma unroll
+      for (int c4 = 0; c4 < kHalf / 32; ++c4) reg_fence(rr[c4]);
+      warp_arrive(bar(C::kDQEmpty));  // the next tile's first dQ may overwrite the accumulator
+      if (pin) {
+        uint16_t* dst_row = a.dq + pgrow * D + kHalf * h;
+#pragma unroll
+        for (int c4 = 0; c4 < kHalf / 32; ++c4) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = Elem<F16>::pack(__uint_as_float(rr[c4][2 * i]) * a.scale,
+                                    __uint_as_float(rr[c4][2 * i + 1]) * a.scale);
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c4);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      return true;
+    };
+    int prev_it = -1;  // tile whose epilogue is still to run
+    size_t prev_grow = 0;
+    bool prev_in = false;
     int g = 0;  // key blocks consumed so far by this CTA
     bool ok = true;
     for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
@@ -305,6 +339,10 @@ __global__ void __launch_bounds__(352, 1)
           for (int i = 0; i < 64; ++i) p[i] = __uint_as_float(rr[i >> 5][i & 31]);
         }
         warp_arrive(bar(C::kSEmpty));
+        if (j == 0 && prev_it >= 0) {  // the previous tile's epilogue (see below)
+          if (!(ok = epilogue(prev_it, prev_grow, prev_in))) break;
+          prev_it = -1;
+        }
         // Masked cells get S = -inf, so P = 0 there.
         if (!sp.interior(q0, k0)) {
           // Columns c (keys k0 + 64h + c) visible to row `row`, and inside the key sequence.
@@ -357,36 +395,13 @@ __global__ void __launch_bounds__(352, 1)
       if (!ok) break;
       g += f.nkv;
 
-      // ---------------------------------------------------------------- tile epilogue
-      if (!(ok = warp_wait(bar(C::kDQDone), it & 1, &abort_flag, a.err))) break;
-      tc_fence_after();
-      constexpr int kHalf = D / 2;
-      uint32_t rr[kHalf / 32][32];
-#pragma unroll
-      for (int c4 = 0; c4 < kHalf / 32; ++c4)
-        tmem_ld32(tmem + lane_base + C::kColDQ + kHalf * h + 32u * c4, rr[c4]);
-      tmem_wait_ld_all();
-#pragma unroll
-      for (int c4 = 0; c4 < kHalf / 32; ++c4) reg_fence(rr[c4]);
-      warp_arrive(bar(C::kDQEmpty));  // the next tile's first dQ may overwrite the accumulator
-      // dQ * scale -> bf16, written straight from registers: each thread owns 64 or 128
-      // contiguous bytes of its row; the stores drain while the next tile runs.
-      if (in_range) {
-        uint16_t* dst_row = a.dq + grow * D + kHalf * h;
-#pragma unroll
-        for (int c4 = 0; c4 < kHalf / 32; ++c4) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = Elem<F16>::pack(__uint_as_float(rr[c4][2 * i]) * a.scale,
-                                __uint_as_float(rr[c4][2 * i + 1]) * a.scale);
-          uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c4);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-        }
-      }
+      // The epilogue of this tile runs once the next tile's first S has been read (or after the
+      // last tile): the MMA computes that tile's next scores while these stores drain.
+      prev_it = it;
+      prev_grow = grow;
+      prev_in = in_range;
     }
+    if (ok && prev_it >= 0) epilogue(prev_it, prev_grow, prev_in);
   }
 
   tc_fence_before();
