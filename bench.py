@@ -441,28 +441,24 @@ def measure_memory(swa, device, D: int = 128) -> dict:
 
 
 def measure_e2e(swa, case, device, dist, args, world) -> dict:
-    """Same metric through the public API with host buffers: each step copies Q, K, V, dO from pinned
-    host memory, runs fwd + bwd, and copies O, LSE, dQ, dK, dV back to pinned host memory."""
+    """Same metric through the public host-buffer call (swa_attn_fwd_bwd_host): each step copies
+    Q, K, V, dO from pinned host memory and O, LSE, dQ, dK, dV back to pinned host memory, the
+    library pipelining those copies with the kernels over chunks of (batch, kv head) groups."""
     host = {k_: v_.cpu().pin_memory() for k_, v_ in si.make_inputs(case, device=str(device)).items()}
-    dev = {k_: torch.empty(v_.shape, dtype=v_.dtype, device=device) for k_, v_ in host.items()}
-    o = torch.empty_like(dev["q"])
-    lse = torch.empty(case.B, case.Hq, case.N, dtype=torch.float32, device=device)
-    dq, dk, dv = torch.empty_like(dev["q"]), torch.empty_like(dev["k"]), torch.empty_like(dev["v"])
-    ws = torch.empty(swa.swa_attn_bwd_workspace_bytes(case.B, case.Hq, case.N, case.D),
+    outs = (torch.empty_like(host["q"]).pin_memory(),
+            torch.empty((case.B, case.Hq, case.N), dtype=torch.float32).pin_memory(),
+            torch.empty_like(host["q"]).pin_memory(), torch.empty_like(host["k"]).pin_memory(),
+            torch.empty_like(host["v"]).pin_memory())
+    U = swa.default_units_per_chunk(case.B, case.Hkv)
+    ws = torch.empty(swa.swa_attn_host_workspace_bytes(case.B, case.Hq, case.Hkv, case.N, case.D, U),
                      dtype=torch.uint8, device=device)
-    outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
-    host_out = {k_: torch.empty(v_.shape, dtype=v_.dtype).pin_memory() for k_, v_ in outs.items()}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs)
 
     def step():
-        for k_ in host:
-            dev[k_].copy_(host[k_], non_blocking=True)
-        swa.swa_attn_fwd(dev["q"], dev["k"], dev["v"], case.W, case.softmax_scale, out=o, lse=lse)
-        swa.swa_attn_bwd(dev["q"], dev["k"], dev["v"], o, dev["do"], lse, case.W, case.softmax_scale,
-                         dq=dq, dk=dk, dv=dv, workspace=ws)
-        for k_ in outs:
-            host_out[k_].copy_(outs[k_], non_blocking=True)
+        swa.swa_attn_fwd_bwd_host(host["q"], host["k"], host["v"], host["do"], case.W,
+                                  case.softmax_scale, outs=outs, units_per_chunk=U, workspace=ws,
+                                  device=device)
 
     for _ in range(max(1, args.warmup)):
         step()
@@ -482,7 +478,8 @@ def measure_e2e(swa, case, device, dist, args, world) -> dict:
     val = aggregate_tflops(world, fl["fwd"] + fl["bwd"], steps, ms)
     swa.swa_check_device(device)
     return {"value": val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms / steps, "steps": steps}
+            "ms_per_step": ms / steps, "steps": steps, "units_per_chunk": U,
+            "api": "swa_attn_fwd_bwd_host"}
 
 
 def measure_other_workloads(swa, device) -> dict:

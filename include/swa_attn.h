@@ -160,6 +160,26 @@ swa_status swa_attn_bwd_f32(const float* q, const float* k, const float* v, cons
                             cudaStream_t stream);
 
 /*
+ * Forward and backward of one layer whose tensors live in host memory: q, k, v, dO in and
+ * o, lse, dq, dk, dv out (host pointers, equal lengths, causal window; layouts as above, bf16).
+ * The (batch, kv head) groups are processed in chunks of `units_per_chunk`: chunk c + 1 is copied
+ * in while chunk c runs the same kernels as swa_attn_fwd / swa_attn_bwd and chunk c - 1 is copied
+ * out, on three library streams forked from `stream` and joined back into it, so the call is
+ * asynchronous on `stream` like the others and its results equal theirs bit for bit.  Host
+ * buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to overlap.
+ *   workspace : device scratch of at least swa_attn_host_workspace_bytes(...) bytes (two chunks'
+ *               tensors), 16-byte aligned, caller-owned.
+ * The library creates its three streams and their events once per device and keeps them.
+ * Errors as for swa_attn_bwd; units_per_chunk < 1 is SWA_ERR_INVALID_ARG.
+ */
+size_t swa_attn_host_workspace_bytes(int B, int Hq, int Hkv, int N, int D, int units_per_chunk);
+swa_status swa_attn_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO,
+                                 void* o, float* lse, void* dq, void* dk, void* dv, int B, int Hq,
+                                 int Hkv, int N, int D, int window, float scale,
+                                 int units_per_chunk, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/*
  * The three phases swa_attn_bwd runs, callable one by one (same arguments, same checks, same
  * kernels), e.g. to time each kernel or to run the dK/dV and dQ phases on two streams once the
  * preprocess has finished.  `delta` is the workspace of swa_attn_bwd (fp32 [B,Hq,N]).

@@ -29,6 +29,8 @@ __all__ = [
     "swa_attn_bwd",
     "swa_attn_bwd_workspace_bytes",
     "swa_attn_f32_workspace_bytes",
+    "swa_attn_fwd_bwd_host",
+    "swa_attn_host_workspace_bytes",
     "swa_attn_bwd_phases",
     "swa_check_device",
     "SlidingWindowAttention",
@@ -72,6 +74,11 @@ SIGNATURES = {
     "swa_attn_f32_workspace_bytes": (ctypes.c_size_t, [_c_int] * 6),
     "swa_attn_fwd_f32": (_c_int, [_vp] * 5 + [_c_int] * 8 + [_c_float, _vp, ctypes.c_size_t, _vp]),
     "swa_attn_bwd_f32": (_c_int, [_vp] * 9 + [_c_int] * 8 + [_c_float, _vp, ctypes.c_size_t, _vp]),
+    "swa_attn_host_workspace_bytes": (ctypes.c_size_t, [_c_int] * 6),
+    "swa_attn_fwd_bwd_host": (
+        _c_int,
+        [_vp] * 9 + [_c_int] * 6 + [_c_float, _c_int, _vp, ctypes.c_size_t, _vp],
+    ),
     "swa_attn_bwd_preprocess": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_vp]),
     "swa_attn_bwd_dkdv": (_c_int, [_vp] * 8 + [_c_int] * 6 + [_c_float, _vp]),
     "swa_attn_bwd_dq": (_c_int, [_vp] * 7 + [_c_int] * 6 + [_c_float, _vp]),
@@ -307,6 +314,59 @@ def swa_attn_bwd_phases(q, k, v, o, do, lse, window: int, scale: Optional[float]
         raise SwaError(rc, "swa_attn_bwd_dq")
     mark(3)
     return dq, dk, dv
+
+
+def swa_attn_host_workspace_bytes(B: int, Hq: int, Hkv: int, N: int, D: int,
+                                  units_per_chunk: int) -> int:
+    return int(load().swa_attn_host_workspace_bytes(B, Hq, Hkv, N, D, units_per_chunk))
+
+
+def default_units_per_chunk(B: int, Hkv: int) -> int:
+    """About eight chunks of (batch, kv head) groups per call."""
+    return max(1, -(-(B * Hkv) // 8))
+
+
+def swa_attn_fwd_bwd_host(q, k, v, do, window: int, scale: Optional[float] = None,
+                          outs=None, units_per_chunk: Optional[int] = None, workspace=None,
+                          device=None) -> Tuple:
+    """Forward and backward of one layer whose tensors live in host memory (equal lengths, causal
+    window): returns (o, lse, dq, dk, dv) as host tensors, filled asynchronously on the current
+    stream of `device` (synchronize before reading them).
+
+    q, do [B,Hq,N,D] and k, v [B,Hkv,N,D] are CPU tensors, pinned for the copies to overlap the
+    kernels; `outs` (o, lse, dq, dk, dv) are pinned CPU tensors allocated here unless given.  The
+    library copies (batch, kv head) groups in chunks and runs the same kernels on each chunk while
+    the next one is copied in and the previous one out.
+    """
+    import torch
+
+    lib = load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    B, Hq, Hkv, N, Lk, D = _dims(q, k)
+    dt = q.dtype
+    if dt != torch.bfloat16:
+        raise TypeError("the host pipeline takes bf16 tensors")
+    for t, name, hs in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (do, "do", Hq)):
+        if t.device.type != "cpu" or t.dtype != dt or tuple(t.shape) != (B, hs, N, D) or \
+                not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU {dt} tensor [B, {hs}, N, D]")
+    if outs is None:
+        outs = (torch.empty_like(q).pin_memory(),
+                torch.empty((B, Hq, N), dtype=torch.float32).pin_memory(),
+                torch.empty_like(q).pin_memory(), torch.empty_like(k).pin_memory(),
+                torch.empty_like(v).pin_memory())
+    U = default_units_per_chunk(B, Hkv) if units_per_chunk is None else int(units_per_chunk)
+    n = swa_attn_host_workspace_bytes(B, Hq, Hkv, N, D, U)
+    if workspace is None:
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+    ptrs = [t.data_ptr() for t in (q, k, v, do)] + [t.data_ptr() for t in outs]
+    rc = lib.swa_attn_fwd_bwd_host(*ptrs, B, Hq, Hkv, N, D, int(window), _scale(scale, D), U,
+                                   workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(),
+                                   _stream_handle(dev))
+    if rc != 0:
+        raise SwaError(rc, "swa_attn_fwd_bwd_host")
+    return tuple(outs)
 
 
 def swa_check_device(device=None) -> None:

@@ -406,6 +406,164 @@ swa_status swa_attn_bwd_f32(const float* q, const float* k, const float* v, cons
 }  // extern "C"
 
 // ------------------------------------------------------------------------------------------------
+// Host-resident tensors: forward + backward of one layer, pipelined over (batch, kv head) groups.
+// ------------------------------------------------------------------------------------------------
+namespace {
+
+constexpr int kHostSlots = 2;  // device buffer sets in flight
+
+// Streams and events of the host pipeline, created once per device.
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
+  cudaEvent_t fork = nullptr, join_comp = nullptr, join_out = nullptr;
+  cudaEvent_t in_done[kHostSlots] = {}, comp_done[kHostSlots] = {}, out_done[kHostSlots] = {};
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[kMaxDevices];
+
+swa_status host_pipe(HostPipe** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SWA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SWA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ready) {
+    const unsigned sf = cudaStreamNonBlocking;
+    const unsigned ef = cudaEventDisableTiming;
+    bool ok = cudaStreamCreateWithFlags(&hp.in, sf) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.comp, sf) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.out, sf) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.fork, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.join_comp, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.join_out, ef) == cudaSuccess;
+    for (int i = 0; ok && i < kHostSlots; ++i)
+      ok = cudaEventCreateWithFlags(&hp.in_done[i], ef) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.comp_done[i], ef) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.out_done[i], ef) == cudaSuccess;
+    if (!ok) return SWA_ERR_CUDA;
+    hp.ready = true;
+  }
+  *out = &hp;
+  return SWA_OK;
+}
+
+// Byte sizes of one slot's buffers for `units` (batch, kv head) groups of G query heads.
+struct HostSlot {
+  size_t q, k, lse, total;  // q-shaped, k-shaped, lse-shaped sizes (each rounded to 256 bytes)
+};
+
+HostSlot host_slot(int units, int G, int N, int D) {
+  HostSlot h;
+  h.q = round256(static_cast<size_t>(units) * G * N * D * 2);
+  h.k = round256(static_cast<size_t>(units) * N * D * 2);
+  h.lse = round256(static_cast<size_t>(units) * G * N * sizeof(float));
+  h.total = 4 * h.q + 4 * h.k + 2 * h.lse;  // q, dO, o, dq | k, v, dk, dv | lse, delta
+  return h;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t swa_attn_host_workspace_bytes(int B, int Hq, int Hkv, int N, int D, int units_per_chunk) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || Hq % Hkv != 0 || units_per_chunk < 1 ||
+      (D != 64 && D != 128 && D != 256))
+    return 0;
+  const int units = units_per_chunk < B * Hkv ? units_per_chunk : B * Hkv;
+  return kHostSlots * host_slot(units, Hq / Hkv, N, D).total;
+}
+
+swa_status swa_attn_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO,
+                                 void* o, float* lse, void* dq, void* dk, void* dv, int B, int Hq,
+                                 int Hkv, int N, int D, int window, float scale,
+                                 int units_per_chunk, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+  const void* ptrs[] = {q, k, v, dO, o, lse, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!p) return SWA_ERR_INVALID_ARG;
+  if (units_per_chunk < 1) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
+  if (st != SWA_OK) return st;
+  if (!workspace ||
+      workspace_bytes < swa_attn_host_workspace_bytes(B, Hq, Hkv, N, D, units_per_chunk))
+    return SWA_ERR_WORKSPACE;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return SWA_ERR_MISALIGNED;
+  if (!aligned16(workspace)) return SWA_ERR_MISALIGNED;
+  unsigned* err = nullptr;
+  if ((st = current_device(&err)) != SWA_OK) return st;
+  HostPipe* hp = nullptr;
+  if ((st = host_pipe(&hp)) != SWA_OK) return st;
+
+  const int G = Hq / Hkv, total = B * Hkv;
+  const int U = units_per_chunk < total ? units_per_chunk : total;
+  const HostSlot hs = host_slot(U, G, N, D);
+  const size_t q_unit = static_cast<size_t>(G) * N * D * 2, k_unit = static_cast<size_t>(N) * D * 2;
+  const size_t l_unit = static_cast<size_t>(G) * N * sizeof(float);
+  auto* ws = static_cast<uint8_t*>(workspace);
+  auto h2d = [&](void* dst, const void* src, size_t bytes) {
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, hp->in) == cudaSuccess;
+  };
+  auto d2h = [&](void* dst, const void* src, size_t bytes) {
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, hp->out) == cudaSuccess;
+  };
+  auto at = [](const void* base, size_t off) {
+    return static_cast<uint8_t*>(const_cast<void*>(base)) + off;
+  };
+
+  // Fork: the three streams start after the work already queued on `stream`.
+  if (cudaEventRecord(hp->fork, stream) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->in, hp->fork, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->comp, hp->fork, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->out, hp->fork, 0) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  const int chunks = (total + U - 1) / U;
+  for (int c = 0; c < chunks; ++c) {
+    const int u0 = c * U, n = (total - u0) < U ? (total - u0) : U;
+    const int slot = c % kHostSlots;
+    uint8_t* b = ws + slot * hs.total;
+    uint8_t *sq = b, *sdo = b + hs.q, *so = b + 2 * hs.q, *sdq = b + 3 * hs.q;
+    uint8_t *sk = b + 4 * hs.q, *sv = sk + hs.k, *sdk = sk + 2 * hs.k, *sdv = sk + 3 * hs.k;
+    float* slse = reinterpret_cast<float*>(sk + 4 * hs.k);
+    float* sdelta = reinterpret_cast<float*>(sk + 4 * hs.k + hs.lse);
+    // inputs of chunk c, once the slot's previous outputs have left
+    if (c >= kHostSlots && cudaStreamWaitEvent(hp->in, hp->out_done[slot], 0) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    if (!h2d(sq, at(q, u0 * q_unit), n * q_unit) || !h2d(sk, at(k, u0 * k_unit), n * k_unit) ||
+        !h2d(sv, at(v, u0 * k_unit), n * k_unit) || !h2d(sdo, at(dO, u0 * q_unit), n * q_unit) ||
+        cudaEventRecord(hp->in_done[slot], hp->in) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    // forward and backward of the chunk's n groups: one problem with B = 1, Hq = n G, Hkv = n
+    if (cudaStreamWaitEvent(hp->comp, hp->in_done[slot], 0) != cudaSuccess) return SWA_ERR_CUDA;
+    const swa::Problem pb = make_problem(1, n * G, n, N, D, window, scale, err);
+    if (swa::launch_fwd(pb, sq, sk, sv, so, slse, hp->comp) != cudaSuccess ||
+        swa::launch_bwd_delta(pb, so, sdo, sdelta, hp->comp) != cudaSuccess ||
+        swa::launch_bwd_dkdv(pb, sq, sk, sv, sdo, slse, sdelta, sdk, sdv, hp->comp) !=
+            cudaSuccess ||
+        swa::launch_bwd_dq(pb, sq, sk, sv, sdo, slse, sdelta, sdq, hp->comp) != cudaSuccess ||
+        cudaEventRecord(hp->comp_done[slot], hp->comp) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    // outputs of chunk c
+    if (cudaStreamWaitEvent(hp->out, hp->comp_done[slot], 0) != cudaSuccess) return SWA_ERR_CUDA;
+    if (!d2h(at(o, u0 * q_unit), so, n * q_unit) || !d2h(at(lse, u0 * l_unit), slse, n * l_unit) ||
+        !d2h(at(dq, u0 * q_unit), sdq, n * q_unit) || !d2h(at(dk, u0 * k_unit), sdk, n * k_unit) ||
+        !d2h(at(dv, u0 * k_unit), sdv, n * k_unit) ||
+        cudaEventRecord(hp->out_done[slot], hp->out) != cudaSuccess)
+      return SWA_ERR_CUDA;
+  }
+  // Join: `stream` continues once every copy and kernel above has finished.
+  if (cudaEventRecord(hp->join_comp, hp->comp) != cudaSuccess ||
+      cudaEventRecord(hp->join_out, hp->out) != cudaSuccess ||
+      cudaStreamWaitEvent(stream, hp->join_comp, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(stream, hp->join_out, 0) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  return SWA_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
 // Backward without caller workspace: the Delta scratch is a fixed device array of this file.
 // ------------------------------------------------------------------------------------------------
 namespace {

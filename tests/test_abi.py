@@ -198,6 +198,50 @@ def test_head_dims(lib):
         assert _fwd_ex(lib, D=D) == 2 and _bwd_ex(lib, D=D) == 2
 
 
+def _host(lib, B=1, Hq=2, Hkv=1, N=16, D=64, W=4, scale=0.125, U=1, ws=FAKE, ws_bytes=None,
+          ptrs=None):
+    ws_bytes = lib.swa_attn_host_workspace_bytes(B, Hq, Hkv, N, D, U) if ws_bytes is None \
+        else ws_bytes
+    ptrs = [FAKE] * 9 if ptrs is None else ptrs
+    return lib.swa_attn_fwd_bwd_host(*ptrs, B, Hq, Hkv, N, D, W, scale, U, ws, ws_bytes, None)
+
+
+def test_host_pipeline_workspace_size(lib):
+    """Two slots, each q, dO, o, dq (q-shaped), k, v, dk, dv (k-shaped), lse and Delta for
+    min(U, B Hkv) groups, every buffer rounded up to 256 bytes."""
+    def r(x):
+        return (x + 255) // 256 * 256
+
+    B, Hq, Hkv, N, D = 2, 8, 2, 300, 128
+    for U in (1, 3, 4, 9):
+        u = min(U, B * Hkv)
+        G = Hq // Hkv
+        slot = 4 * r(u * G * N * D * 2) + 4 * r(u * N * D * 2) + 2 * r(u * G * N * 4)
+        assert lib.swa_attn_host_workspace_bytes(B, Hq, Hkv, N, D, U) == 2 * slot
+    assert lib.swa_attn_host_workspace_bytes(B, Hq, Hkv, N, D, 0) == 0
+    assert lib.swa_attn_host_workspace_bytes(B, Hq, 3, N, D, 1) == 0
+    assert lib.swa_attn_host_workspace_bytes(B, Hq, Hkv, N, 96, 1) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(U=0, ws_bytes=1 << 20), 1), (dict(W=0), 1), (dict(N=0, ws_bytes=1 << 20), 1),
+    (dict(Hq=3, Hkv=2, ws_bytes=1 << 20), 1), (dict(D=512, ws_bytes=1 << 20), 2),
+    (dict(ws=0), 6), (dict(ws_bytes=0), 6), (dict(ws=FAKE + 8), 3),
+])
+def test_host_pipeline_rejects_bad_arguments(lib, kw, code):
+    assert _host(lib, **kw) == code
+
+
+def test_host_pipeline_null_and_misaligned(lib):
+    for i in range(9):
+        ptrs = [FAKE] * 9
+        ptrs[i] = 0
+        assert _host(lib, ptrs=ptrs) == 1
+        ptrs[i] = FAKE + 4
+        assert _host(lib, ptrs=ptrs) == 3
+    assert _host(lib, ws_bytes=lib.swa_attn_host_workspace_bytes(1, 2, 1, 16, 64, 1) - 1) == 6
+
+
 def test_workspace_checks(lib):
     need = lib.swa_attn_bwd_workspace_bytes(2, 4, 100, 128)
     assert need == ((2 * 4 * 100 * 4 + 255) // 256) * 256

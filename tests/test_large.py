@@ -152,3 +152,19 @@ def test_query_suffix_8192_of_32768(swa):
     keys = _sample(rng, case.N - first_seen, 16, must=(0, 1023, 1024, case.N - first_seen - 1))
     keys = keys + first_seen
     _check_sampled(case, inp, gpu, heads=[3, 30], rows=rows, kv_heads=[1], keys=keys)
+
+
+def test_d256_layer_n32768(swa):
+    """The long sliding-window layer with 256-wide heads, as bench.py times it."""
+    import dataclasses
+
+    case = dataclasses.replace(si.long_swa_case(32768), D=256)
+    inp = si.make_inputs(case)
+    gpu = _run(swa, case, inp)
+    for key, t in gpu.items():
+        assert torch.isfinite(t.float()).all(), key
+    rng = np.random.default_rng(6)
+    N = case.N
+    rows = _sample(rng, N, 16, must=(0, 127, 128, 1023, 1024, N - 1))
+    keys = _sample(rng, N, 16, must=(0, 128, N - 129, N - 1))
+    _check_sampled(case, inp, gpu, heads=[0, 31], rows=rows, kv_heads=[9], keys=keys)
