@@ -167,8 +167,10 @@ swa_status swa_attn_bwd_f32(const float* q, const float* k, const float* v, cons
  * out, on three library streams forked from `stream` and joined back into it, so the call is
  * asynchronous on `stream` like the others and its results equal theirs bit for bit.  Host
  * buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to overlap.
- *   workspace : device scratch of at least swa_attn_host_workspace_bytes(...) bytes (two chunks'
- *               tensors), 16-byte aligned, caller-owned.
+ *   workspace : device scratch, 16-byte aligned, caller-owned.  swa_attn_host_workspace_bytes
+ *               gives three chunks' tensors (copy-in, kernels and copy-out each on their own
+ *               chunk); two thirds of it is the minimum (the copy-in of a chunk then also waits
+ *               for the copy-out of the chunk two before it).
  * The library creates its three streams and their events once per device and keeps them.
  * Errors as for swa_attn_bwd; units_per_chunk < 1 is SWA_ERR_INVALID_ARG.
  */

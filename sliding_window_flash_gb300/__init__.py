@@ -322,8 +322,9 @@ def swa_attn_host_workspace_bytes(B: int, Hq: int, Hkv: int, N: int, D: int,
 
 
 def default_units_per_chunk(B: int, Hkv: int) -> int:
-    """About eight chunks of (batch, kv head) groups per call."""
-    return max(1, -(-(B * Hkv) // 8))
+    """About sixteen chunks of (batch, kv head) groups per call (on the N=32768 layer, one group
+    per chunk with three buffer sets measured fastest: 5.56 ms against 6.2-6.7 ms for 2-4)."""
+    return max(1, -(-(B * Hkv) // 16))
 
 
 def swa_attn_fwd_bwd_host(q, k, v, do, window: int, scale: Optional[float] = None,

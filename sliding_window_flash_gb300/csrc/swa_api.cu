@@ -410,14 +410,15 @@ swa_status swa_attn_bwd_f32(const float* q, const float* k, const float* v, cons
 // ------------------------------------------------------------------------------------------------
 namespace {
 
-constexpr int kHostSlots = 2;  // device buffer sets in flight
+constexpr int kMaxHostSlots = 3;  // device buffer sets in flight (one per pipeline stage)
 
 // Streams and events of the host pipeline, created once per device.
 struct HostPipe {
   bool ready = false;
   cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
   cudaEvent_t fork = nullptr, join_comp = nullptr, join_out = nullptr;
-  cudaEvent_t in_done[kHostSlots] = {}, comp_done[kHostSlots] = {}, out_done[kHostSlots] = {};
+  cudaEvent_t in_done[kMaxHostSlots] = {}, comp_done[kMaxHostSlots] = {},
+              out_done[kMaxHostSlots] = {};
 };
 std::mutex g_pipe_mu;
 HostPipe g_pipe[kMaxDevices];
@@ -437,7 +438,7 @@ swa_status host_pipe(HostPipe** out) {
               cudaEventCreateWithFlags(&hp.fork, ef) == cudaSuccess &&
               cudaEventCreateWithFlags(&hp.join_comp, ef) == cudaSuccess &&
               cudaEventCreateWithFlags(&hp.join_out, ef) == cudaSuccess;
-    for (int i = 0; ok && i < kHostSlots; ++i)
+    for (int i = 0; ok && i < kMaxHostSlots; ++i)
       ok = cudaEventCreateWithFlags(&hp.in_done[i], ef) == cudaSuccess &&
            cudaEventCreateWithFlags(&hp.comp_done[i], ef) == cudaSuccess &&
            cudaEventCreateWithFlags(&hp.out_done[i], ef) == cudaSuccess;
@@ -471,7 +472,7 @@ size_t swa_attn_host_workspace_bytes(int B, int Hq, int Hkv, int N, int D, int u
       (D != 64 && D != 128 && D != 256))
     return 0;
   const int units = units_per_chunk < B * Hkv ? units_per_chunk : B * Hkv;
-  return kHostSlots * host_slot(units, Hq / Hkv, N, D).total;
+  return kMaxHostSlots * host_slot(units, Hq / Hkv, N, D).total;
 }
 
 swa_status swa_attn_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO,
@@ -485,9 +486,13 @@ swa_status swa_attn_fwd_bwd_host(const void* q, const void* k, const void* v, co
   if (units_per_chunk < 1) return SWA_ERR_INVALID_ARG;
   swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
   if (st != SWA_OK) return st;
-  if (!workspace ||
-      workspace_bytes < swa_attn_host_workspace_bytes(B, Hq, Hkv, N, D, units_per_chunk))
-    return SWA_ERR_WORKSPACE;
+  // Three buffer sets let H2D, kernels and D2H each work on its own chunk; two also work (the
+  // next chunk's copy-in then waits for an older chunk's copy-out).
+  const int G0 = Hq / Hkv, total0 = B * Hkv;
+  const size_t slot_bytes =
+      host_slot(units_per_chunk < total0 ? units_per_chunk : total0, G0, N, D).total;
+  if (!workspace || workspace_bytes < 2 * slot_bytes) return SWA_ERR_WORKSPACE;
+  const int nslots = workspace_bytes >= 3 * slot_bytes ? 3 : 2;
   for (const void* p : ptrs)
     if (!aligned16(p)) return SWA_ERR_MISALIGNED;
   if (!aligned16(workspace)) return SWA_ERR_MISALIGNED;
@@ -521,14 +526,14 @@ swa_status swa_attn_fwd_bwd_host(const void* q, const void* k, const void* v, co
   const int chunks = (total + U - 1) / U;
   for (int c = 0; c < chunks; ++c) {
     const int u0 = c * U, n = (total - u0) < U ? (total - u0) : U;
-    const int slot = c % kHostSlots;
+    const int slot = c % nslots;
     uint8_t* b = ws + slot * hs.total;
     uint8_t *sq = b, *sdo = b + hs.q, *so = b + 2 * hs.q, *sdq = b + 3 * hs.q;
     uint8_t *sk = b + 4 * hs.q, *sv = sk + hs.k, *sdk = sk + 2 * hs.k, *sdv = sk + 3 * hs.k;
     float* slse = reinterpret_cast<float*>(sk + 4 * hs.k);
     float* sdelta = reinterpret_cast<float*>(sk + 4 * hs.k + hs.lse);
     // inputs of chunk c, once the slot's previous outputs have left
-    if (c >= kHostSlots && cudaStreamWaitEvent(hp->in, hp->out_done[slot], 0) != cudaSuccess)
+    if (c >= nslots && cudaStreamWaitEvent(hp->in, hp->out_done[slot], 0) != cudaSuccess)
       return SWA_ERR_CUDA;
     if (!h2d(sq, at(q, u0 * q_unit), n * q_unit) || !h2d(sk, at(k, u0 * k_unit), n * k_unit) ||
         !h2d(sv, at(v, u0 * k_unit), n * k_unit) || !h2d(sdo, at(dO, u0 * q_unit), n * q_unit) ||
