@@ -242,6 +242,14 @@ const char* swa_strerror(swa_status status);
  */
 swa_status swa_check_device(cudaStream_t stream);
 
+/*
+ * Self-test of the failure path: launches on `stream` one block that waits, with the kernels'
+ * own bounded wait, on a barrier nothing arrives on.  After about a second the wait runs out,
+ * sets the error word and the block exits, so a following swa_check_device returns
+ * SWA_ERR_DEVICE_TIMEOUT and the context stays usable.  Returns SWA_OK once launched.
+ */
+swa_status swa_selftest_wait_timeout(cudaStream_t stream);
+
 /* Library ABI version (major*100 + minor). */
 int swa_version(void);
 

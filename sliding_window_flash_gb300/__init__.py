@@ -85,6 +85,7 @@ SIGNATURES = {
     "swa_attn_bwd_noalloc": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_c_float, _vp]),
     "swa_strerror": (ctypes.c_char_p, [_c_int]),
     "swa_check_device": (_c_int, [_vp]),
+    "swa_selftest_wait_timeout": (_c_int, [_vp]),
     "swa_version": (_c_int, []),
 }
 

@@ -272,6 +272,13 @@ swa_status swa_check_device(cudaStream_t stream) {
   return SWA_OK;
 }
 
+swa_status swa_selftest_wait_timeout(cudaStream_t stream) {
+  unsigned* err = nullptr;
+  swa_status st = current_device(&err);
+  if (st != SWA_OK) return st;
+  return swa::launch_wait_timeout_selftest(err, stream) == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
 int swa_version(void) { return 100; }
 
 }  // extern "C"

@@ -101,6 +101,9 @@ cudaError_t launch_dkdv_d256(const Problem& pb, const void* q, const void* k, co
                              const void* dO, const float* lse, const float* delta, void* dk,
                              void* dv, cudaStream_t stream);
 
+// One block whose single bounded wait runs out (the failure path of every kernel's waits).
+cudaError_t launch_wait_timeout_selftest(unsigned* err, cudaStream_t stream);
+
 // fp32 tensors around the bf16 kernels: up to four tensors per launch, each a whole number of
 // 8-element units (end[t] = units of tensors 0..t, cumulative; unused entries repeat the total).
 constexpr int kMaxJobTensors = 4;
