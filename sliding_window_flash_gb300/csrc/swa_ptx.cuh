@@ -208,68 +208,17 @@ __host__ __device__ constexpr uint32_t idesc_f16kind(uint32_t fmt, int M, int N,
          ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
-  return idesc_f16kind(1u, M, N, a_mn_major, b_mn_major);
-}
 
 // ------------------------------------------------------------------------------------------------
-// tcgen05: MMA and commit (issued by one thread)
+// tcgen05: MMA and commit
 // ------------------------------------------------------------------------------------------------
-
-// D[tmem] (=|+=) A[smem] * B[smem]
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (=|+=) A[tmem] * B[smem]
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrives once on `bar` when every tcgen05 operation issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
 
 // Warp-converged forms: every lane of the issuing warp executes these, one elected lane issues.
 // Keeping the MMA warp converged (rather than running its loop on one lane) keeps the tensor pipe
 // fed: branches inside a single-lane region stall the issue of the next MMA.
-__device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e, p;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
-__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e, p;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
+// Arrives once on `bar` when every tcgen05 operation issued so far by the issuing thread has
+// completed.
 __device__ __forceinline__ void umma_commit_w(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -557,16 +506,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
-// Stores 32 packed bf16 pairs (64 columns, one 128-byte row of a 64-column chunk) of row `row`
-// into a 128B-swizzled chunk at `chunk`, the layout a 3-D TMA store with 64 x 128 boxes reads.
-__device__ __forceinline__ void store_half_row_sw128(uint32_t chunk, uint32_t row,
-                                                     const uint32_t (&pk)[32]) {
-#pragma unroll
-  for (int u = 0; u < 8; ++u)
-    st_shared_v4(chunk + sw128_offset(row, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
-                 pk[4 * u + 3]);
-}
-
 // Stages 16 packed bf16 pairs = columns [c0, c0 + 32) of row `row` of a 128-row tile whose
 // 64-column chunks (128 rows x 128 bytes, 128B-swizzled) start at `tile` + chunk * 16 KB.
 __device__ __forceinline__ void stage_row32_sw128(uint32_t tile, uint32_t row, uint32_t c0,
@@ -577,21 +516,6 @@ __device__ __forceinline__ void stage_row32_sw128(uint32_t tile, uint32_t row, u
   for (int u = 0; u < 4; ++u)
     st_shared_v4(chunk + sw128_offset(row, unit0 + u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
                  pk[4 * u + 3]);
-}
-
-// Stores one thread's row of 128 bf16 values (64 packed pairs) into a 128 x 128 K-major operand
-// tile with 128-byte swizzle: two 64-column chunks of 128 rows x 128 bytes.
-__device__ __forceinline__ void store_row_sw128_128(uint32_t tile, uint32_t row,
-                                                    const uint32_t (&pk)[64]) {
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int b0 = h * 32 + u * 4;
-      st_shared_v4(tile + h * (128 * 128) + sw128_offset(row, u), pk[b0], pk[b0 + 1], pk[b0 + 2],
-                   pk[b0 + 3]);
-    }
-  }
 }
 
 }  // namespace swa
