@@ -85,3 +85,48 @@ def test_last_key_block_gradients(swa):
     dv = out["dv"][0, 0, keys].cpu().double().numpy()
     assert np.linalg.norm(dk - dk_r) / np.linalg.norm(dk_r) <= 1e-2
     assert np.linalg.norm(dv - dv_r) / np.linalg.norm(dv_r) <= 1e-2
+
+
+@pytest.mark.parametrize("D,dtype,Lq,Lk,W,causal", [
+    (256, torch.bfloat16, 300, 300, 64, True),
+    (256, torch.float16, 100, 700, 30, True),    # early key blocks seen by no query
+    (128, torch.float32, 200, 650, 40, False),
+    (64, torch.bfloat16, 1, 500, 3, True),
+    (128, torch.float16, 129, 129, 1, False),
+    (256, torch.float32, 257, 257, 300, False),
+])
+def test_every_output_written_on_every_path(swa, D, dtype, Lq, Lk, W, causal):
+    """Outputs pre-filled with NaN come back finite for every head dim, element type, query
+    offset and window kind (key blocks that no query sees must be written as zeros)."""
+    dev = torch.device("cuda:0")
+    case = si.Case(B=1, Hq=4, Hkv=2, N=Lk, D=D, W=W, seed=15)
+    inp = si.make_inputs(case, dtype=dtype)
+    for key in ("q", "do"):
+        inp[key] = inp[key][:, :, Lk - Lq:].contiguous()
+    g = {k: v.to(dev) for k, v in inp.items()}
+    o, dq = torch.full_like(g["q"], float("nan")), torch.full_like(g["q"], float("nan"))
+    dk, dv = torch.full_like(g["k"], float("nan")), torch.full_like(g["v"], float("nan"))
+    lse = torch.full((1, 4, Lq), float("nan"), dtype=torch.float32, device=dev)
+    swa.swa_attn_fwd(g["q"], g["k"], g["v"], W, case.softmax_scale, out=o, lse=lse,
+                     causal=causal)
+    swa.swa_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, W, case.softmax_scale, dq=dq,
+                     dk=dk, dv=dv, causal=causal)
+    swa.swa_check_device()
+    for name, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert torch.isfinite(t.float()).all(), name
+
+
+def test_host_pipeline_writes_every_output(swa):
+    case = si.Case(B=2, Hq=4, Hkv=2, N=333, D=128, W=50, seed=16)
+    inp = {k: v.pin_memory() for k, v in si.make_inputs(case).items()}
+    outs = (torch.full_like(inp["q"], float("nan")).pin_memory(),
+            torch.full((2, 4, 333), float("nan"), dtype=torch.float32).pin_memory(),
+            torch.full_like(inp["q"], float("nan")).pin_memory(),
+            torch.full_like(inp["k"], float("nan")).pin_memory(),
+            torch.full_like(inp["v"], float("nan")).pin_memory())
+    swa.swa_attn_fwd_bwd_host(inp["q"], inp["k"], inp["v"], inp["do"], case.W, case.softmax_scale,
+                              outs=outs, units_per_chunk=3)
+    torch.cuda.synchronize()
+    swa.swa_check_device()
+    for t in outs:
+        assert torch.isfinite(t.float()).all()
