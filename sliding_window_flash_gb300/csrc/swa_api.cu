@@ -421,9 +421,10 @@ constexpr int kMaxHostSlots = 3;  // device buffer sets in flight (one per pipel
 
 // Streams and events of the host pipeline, created once per device.
 struct HostPipe {
+  std::mutex enqueue;  // one call at a time enqueues on the shared streams and events
   bool ready = false;
   cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
-  cudaEvent_t fork = nullptr, join_comp = nullptr, join_out = nullptr;
+  cudaEvent_t fork = nullptr, join_in = nullptr, join_comp = nullptr, join_out = nullptr;
   cudaEvent_t in_done[kMaxHostSlots] = {}, comp_done[kMaxHostSlots] = {},
               out_done[kMaxHostSlots] = {};
 };
@@ -443,6 +444,7 @@ swa_status host_pipe(HostPipe** out) {
               cudaStreamCreateWithFlags(&hp.comp, sf) == cudaSuccess &&
               cudaStreamCreateWithFlags(&hp.out, sf) == cudaSuccess &&
               cudaEventCreateWithFlags(&hp.fork, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.join_in, ef) == cudaSuccess &&
               cudaEventCreateWithFlags(&hp.join_comp, ef) == cudaSuccess &&
               cudaEventCreateWithFlags(&hp.join_out, ef) == cudaSuccess;
     for (int i = 0; ok && i < kMaxHostSlots; ++i)
@@ -524,14 +526,17 @@ swa_status swa_attn_fwd_bwd_host(const void* q, const void* k, const void* v, co
     return static_cast<uint8_t*>(const_cast<void*>(base)) + off;
   };
 
+  std::lock_guard<std::mutex> lk(hp->enqueue);
   // Fork: the three streams start after the work already queued on `stream`.
   if (cudaEventRecord(hp->fork, stream) != cudaSuccess ||
       cudaStreamWaitEvent(hp->in, hp->fork, 0) != cudaSuccess ||
       cudaStreamWaitEvent(hp->comp, hp->fork, 0) != cudaSuccess ||
       cudaStreamWaitEvent(hp->out, hp->fork, 0) != cudaSuccess)
     return SWA_ERR_CUDA;
+  // From here on a failure stops enqueueing but still joins the streams back into `stream`.
+  swa_status result = SWA_OK;
   const int chunks = (total + U - 1) / U;
-  for (int c = 0; c < chunks; ++c) {
+  for (int c = 0; c < chunks && result == SWA_OK; ++c) {
     const int u0 = c * U, n = (total - u0) < U ? (total - u0) : U;
     const int slot = c % nslots;
     uint8_t* b = ws + slot * hs.total;
@@ -540,37 +545,54 @@ swa_status swa_attn_fwd_bwd_host(const void* q, const void* k, const void* v, co
     float* slse = reinterpret_cast<float*>(sk + 4 * hs.k);
     float* sdelta = reinterpret_cast<float*>(sk + 4 * hs.k + hs.lse);
     // inputs of chunk c, once the slot's previous outputs have left
-    if (c >= nslots && cudaStreamWaitEvent(hp->in, hp->out_done[slot], 0) != cudaSuccess)
-      return SWA_ERR_CUDA;
+    if (c >= nslots && cudaStreamWaitEvent(hp->in, hp->out_done[slot], 0) != cudaSuccess) {
+      result = SWA_ERR_CUDA;
+      break;
+    }
     if (!h2d(sq, at(q, u0 * q_unit), n * q_unit) || !h2d(sk, at(k, u0 * k_unit), n * k_unit) ||
         !h2d(sv, at(v, u0 * k_unit), n * k_unit) || !h2d(sdo, at(dO, u0 * q_unit), n * q_unit) ||
-        cudaEventRecord(hp->in_done[slot], hp->in) != cudaSuccess)
-      return SWA_ERR_CUDA;
+        cudaEventRecord(hp->in_done[slot], hp->in) != cudaSuccess) {
+      result = SWA_ERR_CUDA;
+      break;
+    }
     // forward and backward of the chunk's n groups: one problem with B = 1, Hq = n G, Hkv = n
-    if (cudaStreamWaitEvent(hp->comp, hp->in_done[slot], 0) != cudaSuccess) return SWA_ERR_CUDA;
+    if (cudaStreamWaitEvent(hp->comp, hp->in_done[slot], 0) != cudaSuccess) {
+      result = SWA_ERR_CUDA;
+      break;
+    }
     const swa::Problem pb = make_problem(1, n * G, n, N, D, window, scale, err);
     if (swa::launch_fwd(pb, sq, sk, sv, so, slse, hp->comp) != cudaSuccess ||
         swa::launch_bwd_delta(pb, so, sdo, sdelta, hp->comp) != cudaSuccess ||
         swa::launch_bwd_dkdv(pb, sq, sk, sv, sdo, slse, sdelta, sdk, sdv, hp->comp) !=
             cudaSuccess ||
         swa::launch_bwd_dq(pb, sq, sk, sv, sdo, slse, sdelta, sdq, hp->comp) != cudaSuccess ||
-        cudaEventRecord(hp->comp_done[slot], hp->comp) != cudaSuccess)
-      return SWA_ERR_CUDA;
+        cudaEventRecord(hp->comp_done[slot], hp->comp) != cudaSuccess) {
+      result = SWA_ERR_CUDA;
+      break;
+    }
     // outputs of chunk c
-    if (cudaStreamWaitEvent(hp->out, hp->comp_done[slot], 0) != cudaSuccess) return SWA_ERR_CUDA;
+    if (cudaStreamWaitEvent(hp->out, hp->comp_done[slot], 0) != cudaSuccess) {
+      result = SWA_ERR_CUDA;
+      break;
+    }
     if (!d2h(at(o, u0 * q_unit), so, n * q_unit) || !d2h(at(lse, u0 * l_unit), slse, n * l_unit) ||
         !d2h(at(dq, u0 * q_unit), sdq, n * q_unit) || !d2h(at(dk, u0 * k_unit), sdk, n * k_unit) ||
         !d2h(at(dv, u0 * k_unit), sdv, n * k_unit) ||
-        cudaEventRecord(hp->out_done[slot], hp->out) != cudaSuccess)
-      return SWA_ERR_CUDA;
+        cudaEventRecord(hp->out_done[slot], hp->out) != cudaSuccess) {
+      result = SWA_ERR_CUDA;
+      break;
+    }
   }
-  // Join: `stream` continues once every copy and kernel above has finished.
+  // Join: `stream` continues once every copy and kernel above has finished (also after a
+  // failure part-way, so no enqueued work outlives the call's ordering on `stream`).
   if (cudaEventRecord(hp->join_comp, hp->comp) != cudaSuccess ||
       cudaEventRecord(hp->join_out, hp->out) != cudaSuccess ||
+      cudaEventRecord(hp->join_in, hp->in) != cudaSuccess ||
+      cudaStreamWaitEvent(stream, hp->join_in, 0) != cudaSuccess ||
       cudaStreamWaitEvent(stream, hp->join_comp, 0) != cudaSuccess ||
       cudaStreamWaitEvent(stream, hp->join_out, 0) != cudaSuccess)
     return SWA_ERR_CUDA;
-  return SWA_OK;
+  return result;
 }
 
 }  // extern "C"

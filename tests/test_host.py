@@ -71,3 +71,41 @@ def test_host_pipeline_back_to_back_calls(swa):
         torch.cuda.synchronize()
         for a, b in zip(r, s1):
             assert torch.equal(a, b)
+
+
+def test_host_pipeline_from_two_host_threads(swa):
+    """Calls from two host threads on one device (each on its own torch stream) are serialised
+    while they enqueue on the library's shared streams: both results stay exact."""
+    import threading
+
+    cases = [si.Case(B=1, Hq=4, Hkv=2, N=300, D=128, W=80, seed=20 + i) for i in range(2)]
+    inps = [_pinned(si.make_inputs(c)) for c in cases]
+    dev = torch.device("cuda:0")
+    expected = []
+    for c, inp in zip(cases, inps):
+        r = swa.swa_attn_fwd_bwd_host(inp["q"], inp["k"], inp["v"], inp["do"], c.W,
+                                      c.softmax_scale, units_per_chunk=1)
+        torch.cuda.synchronize(dev)
+        expected.append([t.clone() for t in r])
+    results = [None, None]
+
+    def run(i):
+        torch.cuda.set_device(dev)
+        s = torch.cuda.Stream(dev)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                r = swa.swa_attn_fwd_bwd_host(inps[i]["q"], inps[i]["k"], inps[i]["v"],
+                                              inps[i]["do"], cases[i].W, cases[i].softmax_scale,
+                                              units_per_chunk=1)
+            s.synchronize()
+        results[i] = r
+
+    th = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    swa.swa_check_device()
+    for i in range(2):
+        for a, b in zip(results[i], expected[i]):
+            assert torch.equal(a, b)
