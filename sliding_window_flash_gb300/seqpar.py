@@ -145,3 +145,40 @@ def seq_bwd(q, k_ext, v_ext, o, do, lse, window: int, scale: Optional[float] = N
         acc[:, :, :, a - base:b - base] += buf.view(dk_ext.dtype).to(acc.dtype)
     out = acc.to(dk_ext.dtype)
     return dq, out[0], out[1]
+
+
+def _make_autograd():
+    import torch
+
+    class SequenceShardedAttention(torch.autograd.Function):
+        """o = attention over this rank's chunk of a sequence sharded across `group` (causal
+        window); the backward returns this rank's dq and its owned rows of dk, dv."""
+
+        @staticmethod
+        def forward(ctx, q, k, v, window: int, scale: Optional[float] = None, group=None,
+                    fwd_fn: Optional[Callable] = None, bwd_fn: Optional[Callable] = None):
+            o, lse, k_ext, v_ext = seq_fwd(q, k, v, window, scale, group, fwd_fn)
+            ctx.save_for_backward(q, k_ext, v_ext, o, lse)
+            ctx.window, ctx.scale, ctx.group, ctx.bwd_fn = window, scale, group, bwd_fn
+            return o
+
+        @staticmethod
+        def backward(ctx, do):
+            q, k_ext, v_ext, o, lse = ctx.saved_tensors
+            dq, dk, dv = seq_bwd(q, k_ext, v_ext, o, do.contiguous(), lse, ctx.window, ctx.scale,
+                                 ctx.group, ctx.bwd_fn)
+            return dq, dk, dv, None, None, None, None, None
+
+    return SequenceShardedAttention
+
+
+class _LazyAutograd:
+    _cls = None
+
+    def __getattr__(self, name):
+        if _LazyAutograd._cls is None:
+            _LazyAutograd._cls = _make_autograd()
+        return getattr(_LazyAutograd._cls, name)
+
+
+SequenceShardedAttention = _LazyAutograd()

@@ -77,6 +77,46 @@ def test_sharded_equals_unsharded(world, W):
         np.testing.assert_allclose(got, ref[name], rtol=1e-10, atol=1e-12, err_msg=name)
 
 
+def _autograd_worker(rank, world, W, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    case = _case(world, W)
+    full = si.make_inputs(case)
+    sl = slice(rank * L, (rank + 1) * L)
+    q, k, v, do = (full[n][:, :, sl].double().contiguous() for n in ("q", "k", "v", "do"))
+    for t in (q, k, v):
+        t.requires_grad_(True)
+    o = seqpar.SequenceShardedAttention.apply(q, k, v, W, case.softmax_scale, None, _oracle_fwd,
+                                              _oracle_bwd)
+    o.backward(do)
+    out[rank] = {"o": o.detach().numpy(), "dq": q.grad.numpy(), "dk": k.grad.numpy(),
+                 "dv": v.grad.numpy()}
+    dist.destroy_process_group()
+
+
+def test_autograd_wrapper_two_ranks():
+    """SequenceShardedAttention through torch autograd reproduces the unsharded gradients."""
+    from oracle import swa_oracle as orc
+
+    world, W = 2, 30
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    procs = [ctx.Process(target=_autograd_worker, args=(r, world, W, port, out))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+        assert p.exitcode == 0
+    case = _case(world, W)
+    full = si.make_inputs(case)
+    ref = orc.oracle_backward(full["q"], full["k"], full["v"], full["do"], W, case.softmax_scale)
+    for name in ("o", "dq", "dk", "dv"):
+        got = np.concatenate([out[r][name] for r in range(world)], axis=2)
+        np.testing.assert_allclose(got, ref[name], rtol=1e-10, atol=1e-12, err_msg=name)
+
+
 @pytest.mark.parametrize("world,W", [(2, 1), (4, 30), (4, 200), (3, 48)])
 def test_plans_match_and_cover(world, W):
     """Every receive has the matching send, and a rank's halo is exactly the min(W - 1, r L)
