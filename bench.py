@@ -460,7 +460,9 @@ def measure_e2e(swa, case, device, dist, args, world) -> dict:
                                   case.softmax_scale, outs=outs, units_per_chunk=U, workspace=ws,
                                   device=device)
 
-    for _ in range(max(1, args.warmup)):
+    # The first calls on freshly pinned host buffers run slow (one-time mapping of the pages for
+    # the copy engines: up to ~4x the steady state), so the warm-up is at least five calls.
+    for _ in range(max(5, args.warmup)):
         step()
     torch.cuda.synchronize(device)
     stream = torch.cuda.current_stream(device)
