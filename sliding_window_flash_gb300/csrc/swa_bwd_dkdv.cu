@@ -116,6 +116,13 @@ __global__ void __launch_bounds__(352, 1)
   auto tile_q0 = [&](int t) { return (qb_lo + t % nq) * kBlockM; };
   auto tile_bhq = [&](int t) { return b * a.Hq + hk * a.G + t / nq; };
 
+  if (T == 0) {
+    // No query sees this key block: its dK and dV rows are zero.  Written straight from the
+    // threads, before any barrier, tensor memory or copy is set up.
+    zero_key_rows(a.dk, a.dv, bhk, k0, sp.Lk, D);
+    return;
+  }
+
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     abort_flag = 0;

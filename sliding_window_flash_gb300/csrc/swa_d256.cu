@@ -96,6 +96,8 @@ struct Args256 {
   float* lse_out;        // forward output
   const float* delta;
   uint16_t* dq;          // dQ kernel output (bf16 or fp16 elements)
+  uint16_t* dk;          // dK / dV kernel outputs, for key blocks no query sees (zeros)
+  uint16_t* dv;
   int BH, Hq, Hkv, G;    // B * Hq, heads, G = Hq / Hkv
   int nqb, ntiles;       // query-tile kernels: query blocks per head, B * Hq * nqb
   int BHK;               // key-block kernels: B * Hkv
@@ -946,6 +948,10 @@ __global__ void __launch_bounds__(352, 1)
   const Ring<C::kSlots> rg{smem_u32(smem + C::kOffRing), bar(C::kFull), bar(C::kEmpty)};
   const Span sp = a.span;
   const KWalk w = kwalk(a, sp);
+  if (w.T == 0) {  // no query sees this key block: its dV rows are zero
+    zero_key_rows(a.dv, nullptr, w.bhk, w.k0, sp.Lk, kD);
+    return;
+  }
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -1154,6 +1160,10 @@ __global__ void __launch_bounds__(352, 1)
   const Ring<C::kSlots> rg{smem_u32(smem + C::kOffRing), bar(C::kFull), bar(C::kEmpty)};
   const Span sp = a.span;
   const KWalk w = kwalk(a, sp);
+  if (w.T == 0) {  // no query sees this key block: its dK rows are zero
+    zero_key_rows(a.dk, nullptr, w.bhk, w.k0, sp.Lk, kD);
+    return;
+  }
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -1363,6 +1373,7 @@ Args256 make_args(const Problem& pb, const float* lse, const float* delta, void*
   Args256 a;
   a.lse = lse;
   a.lse_out = lse_out;
+  a.dk = a.dv = nullptr;
   a.delta = delta;
   a.dq = static_cast<uint16_t*>(dq);
   a.BH = pb.B * pb.Hq;
@@ -1430,7 +1441,9 @@ cudaError_t dkdv256(const Problem& pb, const void* q, const void* k, const void*
   if (!qmap(&tq, q, pb) || !qmap(&tdo, dO, pb) || !kmap(&tk, k, pb) || !kmap(&tv, v, pb) ||
       !kmap(&tdk, dk, pb) || !kmap(&tdv, dv, pb))
     return cudaErrorInvalidValue;
-  const Args256 a = make_args(pb, lse, delta, nullptr);
+  Args256 a = make_args(pb, lse, delta, nullptr);
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
   const unsigned grid = static_cast<unsigned>((pb.span.Lk + kBlockN - 1) / kBlockN) *
                         static_cast<unsigned>(a.BHK);
   auto kk = swa_dk256_kernel<F16>;

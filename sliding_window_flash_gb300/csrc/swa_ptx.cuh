@@ -518,4 +518,20 @@ __device__ __forceinline__ void stage_row32_sw128(uint32_t tile, uint32_t row, u
                  pk[4 * u + 3]);
 }
 
+// Writes zeros to rows [k0, min(k0 + 128, L)) of plane `bh` of one or two (t1 may be null)
+// [BH, L, D] 16-bit tensors, with 16-byte stores spread over the whole block.
+__device__ __forceinline__ void zero_key_rows(uint16_t* t0, uint16_t* t1, int bh, int k0, int L,
+                                              int D) {
+  const int rows = min(128, L - k0);
+  if (rows <= 0) return;
+  const size_t base = (static_cast<size_t>(bh) * L + k0) * D;
+  const int units = rows * D / 8;  // 16-byte units per tensor
+  const int total = t1 ? 2 * units : units;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int u = static_cast<int>(threadIdx.x); u < total; u += static_cast<int>(blockDim.x)) {
+    uint16_t* t = u < units ? t0 : t1;
+    reinterpret_cast<uint4*>(t + base)[u < units ? u : u - units] = z;
+  }
+}
+
 }  // namespace swa
