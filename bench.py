@@ -415,7 +415,7 @@ def _profiled_traffic(kernel: str):
 
 def measure_memory(swa, device, D: int = 128) -> dict:
     """Peak device memory of one layer's fwd + bwd versus N (inputs Q, K, V, dO excluded), for the
-    long sliding-window layer with head dim D."""
+    long sliding-window layer with head dim D, and the fwd + bwd time at each N."""
     out = {"D": D, "N": [], "peak_gb_total": [], "peak_gb_above_inputs": []}
     for N in (8192, 16384, 32768):
         case = dataclasses.replace(si.long_swa_case(N), D=D)
@@ -430,6 +430,20 @@ def measure_memory(swa, device, D: int = 128) -> dict:
                                       case.softmax_scale)
         torch.cuda.synchronize(device)
         peak = torch.cuda.max_memory_allocated(device)
+        # time of one fwd + bwd at this length (after the memory-tracked one; 5 repetitions)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record()
+        for _ in range(5):
+            swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale, out=o,
+                             lse=lse)
+            swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
+                             case.softmax_scale, dq=dq, dk=dk, dv=dv)
+        ev[1].record()
+        torch.cuda.synchronize(device)
+        ms = ev[0].elapsed_time(ev[1]) / 5
+        fl = step_flops(case)
+        out.setdefault("fwd_bwd_ms", []).append(ms)
+        out.setdefault("fwd_bwd_tflops", []).append((fl["fwd"] + fl["bwd"]) / (ms * 1e-3) / 1e12)
         out["N"].append(N)
         out["peak_gb_total"].append(peak / 1e9)
         out["peak_gb_above_inputs"].append((peak - base) / 1e9)

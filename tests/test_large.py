@@ -74,8 +74,9 @@ def _sample(rng, N, n, must=()):
     return np.array(sorted(s))
 
 
-def test_long_swa_layer_n32768(swa):
-    case = si.long_swa_case(32768)
+@pytest.mark.parametrize("N", [8192, 16384, 32768])
+def test_long_swa_layer(swa, N):
+    case = si.long_swa_case(N)
     inp = si.make_inputs(case)
     gpu = _run(swa, case, inp)
     for key, t in gpu.items():
