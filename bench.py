@@ -552,6 +552,25 @@ def measure_other_workloads(swa, device) -> dict:
     del inp, o, lse
     torch.cuda.empty_cache()
 
+    # The headline layer with 64-wide heads.
+    case = dataclasses.replace(si.long_swa_case(32768), D=64)
+    inp = si.make_inputs(case, device=str(device))
+    fl = step_flops(case)
+    o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale)
+    f_ms = timed(lambda: swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
+                                          out=o, lse=lse))
+    b_ms = timed(lambda: swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
+                                          case.softmax_scale))
+    res["long_swa_d64"] = {
+        "workload": "B=1 Hq=32 Hkv=16 N=32768 D=64 W=1024",
+        "fwd_ms": f_ms, "bwd_ms": b_ms,
+        "fwd_tflops": fl["fwd"] / (f_ms * 1e-3) / 1e12,
+        "bwd_tflops": fl["bwd"] / (b_ms * 1e-3) / 1e12,
+        "fwd_bwd_tflops": (fl["fwd"] + fl["bwd"]) / ((f_ms + b_ms) * 1e-3) / 1e12,
+    }
+    del inp, o, lse
+    torch.cuda.empty_cache()
+
     # The headline layer with 256-wide heads (Gemma 4's sliding layers): half-tile kernels.
     case = dataclasses.replace(si.long_swa_case(32768), D=256)
     inp = si.make_inputs(case, device=str(device))

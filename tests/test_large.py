@@ -169,3 +169,19 @@ def test_d256_layer_n32768(swa):
     rows = _sample(rng, N, 16, must=(0, 127, 128, 1023, 1024, N - 1))
     keys = _sample(rng, N, 16, must=(0, 128, N - 129, N - 1))
     _check_sampled(case, inp, gpu, heads=[0, 31], rows=rows, kv_heads=[9], keys=keys)
+
+
+def test_d64_layer_n32768(swa):
+    """The long sliding-window layer with 64-wide heads, as bench.py times it."""
+    import dataclasses
+
+    case = dataclasses.replace(si.long_swa_case(32768), D=64)
+    inp = si.make_inputs(case)
+    gpu = _run(swa, case, inp)
+    for key, t in gpu.items():
+        assert torch.isfinite(t.float()).all(), key
+    rng = np.random.default_rng(7)
+    N = case.N
+    rows = _sample(rng, N, 16, must=(0, 127, 128, 1023, 1024, N - 1))
+    keys = _sample(rng, N, 16, must=(0, 128, N - 129, N - 1))
+    _check_sampled(case, inp, gpu, heads=[1, 30], rows=rows, kv_heads=[4], keys=keys)
