@@ -14,10 +14,12 @@
 // Warp roles (352 threads): warps 0-7 compute — warp w handles TMEM lanes 32(w%4)..+31 (key rows)
 // and query columns [64 h, 64 h + 64) of every tile, h = w / 4; warp 8 TMA producer of K (once)
 // and of the Q_t ring, warp 10 of V (once) and of the dO_t ring — two issuing warps, because one
-// warp's TMA copies complete at only ~40 B/clk on this GPU; warp 9 MMA issuer and TMEM owner.  P^T and dS^T go
-// back to TMEM as bf16 pairs, each half over the first 32 of the 64 S^T / dP^T columns it read, and
-// are the A operands of dV += P^T dO and dK += dS^T Q.  TMEM columns: [0,128) S^T / P^T,
-// [128,256) dP^T / dS^T, [256, 256+D) dK, [256+D, 256+2D) dV.
+// warp's TMA copies complete at only ~40 B/clk on this GPU; warp 9 MMA issuer and TMEM owner.
+// A compute thread reads its S^T values and releases the S^T columns at once, so the next tile's
+// S^T is computed while it exponentiates; once dP^T has landed and been read, P^T and dS^T go
+// back to TMEM as bf16 pairs over the dP^T columns (each half of a row: P^T over the first 32 of
+// its 64 columns, dS^T over the last 32) and are the A operands of dV += P^T dO and dK += dS^T Q.
+// TMEM columns: [0,128) S^T, [128,256) dP^T / P^T + dS^T, [256, 256+D) dK, [256+D, 256+2D) dV.
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 #include "swa_tmap.h"
@@ -45,7 +47,8 @@ struct DkdvCfg {
   static constexpr int kDOFull = kQEmpty + kQStages;
   static constexpr int kDOEmpty = kDOFull + kDOStages;
   static constexpr int kSFull = kDOEmpty + kDOStages;
-  static constexpr int kDPFull = kSFull + 1;
+  static constexpr int kSEmpty = kSFull + 1;  // every compute warp has read S^T
+  static constexpr int kDPFull = kSEmpty + 1;
   static constexpr int kPFull = kDPFull + 1;
   static constexpr int kDSFull = kPFull + 1;
   static constexpr int kVecFull = kDSFull + 1;  // 2 slots
@@ -136,6 +139,7 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(bar(C::kDOEmpty + s), 1);
     }
     mbar_init(bar(C::kSFull), 1);
+    mbar_init(bar(C::kSEmpty), C::kComputeThreads / 32);
     mbar_init(bar(C::kDPFull), 1);
     mbar_init(bar(C::kPFull), C::kComputeThreads / 32);
     mbar_init(bar(C::kDSFull), C::kComputeThreads / 32);
@@ -209,14 +213,16 @@ __global__ void __launch_bounds__(352, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
-    // Issue order: S_0, dP_0, then per tile t: dV += P_t^T dO_t, S_{t+1}, dK += dS_t^T Q_t, dP_{t+1}.
-    // The MMAs run in that order, so S_{t+1} overwrites the S^T / P^T columns only after dV_t has
-    // read P_t^T, and dP_{t+1} overwrites dP^T / dS^T only after dK_t has read dS_t^T.
+    // Issue order: S_0, dP_0, then per tile t: S_{t+1}, dV += P_t^T dO_t, dK += dS_t^T Q_t,
+    // dP_{t+1}.  S_{t+1} overwrites the S^T columns once every compute warp has read S_t^T
+    // (S_EMPTY); the MMAs run in issue order, so dP_{t+1} overwrites P_t^T / dS_t^T only after
+    // dV_t and dK_t have read them.
     {  // the whole warp, converged; one elected lane issues
       constexpr uint32_t kIdS = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockN, kBlockM, false, false);  // S^T, dP^T
       constexpr uint32_t kIdAcc = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockN, D, false, true);       // dV, dK
       auto issue_s = [&](int t) -> bool {  // S^T = K Q_t^T
         const int s = t % C::kQStages;
+        if (t > 0 && !warp_wait(bar(C::kSEmpty), (t - 1) & 1, &abort_flag, a.err)) return false;
         if (!warp_wait(bar(C::kQFull + s), (t / C::kQStages) & 1, &abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t sQ = sQ0 + s * C::kTileBytes;
@@ -252,11 +258,11 @@ __global__ void __launch_bounds__(352, 1)
       if (ok && T > 0) ok = issue_dp(0);
       for (int t = 0; ok && t < T; ++t) {
         const int sq = t % C::kQStages, sd = t % C::kDOStages;
-        ok = issue_acc(t, C::kPFull, C::kColS, sDO0 + sd * C::kTileBytes, C::kColDV);  // dV
+        if (t + 1 < T && !(ok = issue_s(t + 1))) break;
+        ok = issue_acc(t, C::kPFull, C::kColDP, sDO0 + sd * C::kTileBytes, C::kColDV);  // dV
         if (!ok) break;
         umma_commit_w(bar(C::kDOEmpty + sd));
-        if (t + 1 < T && !(ok = issue_s(t + 1))) break;
-        ok = issue_acc(t, C::kDSFull, C::kColDP, sQ0 + sq * C::kTileBytes, C::kColDK);  // dK
+        ok = issue_acc(t, C::kDSFull, C::kColDP + 32u, sQ0 + sq * C::kTileBytes, C::kColDK);  // dK
         if (!ok) break;
         umma_commit_w(bar(C::kQEmpty + sq));
         if (t + 1 < T) ok = issue_dp(t + 1);
@@ -320,6 +326,9 @@ __global__ void __launch_bounds__(352, 1)
         tmem_wait_ld_all();
         reg_fence(rr[0]);
         reg_fence(rr[1]);
+        // S^T is in registers: the next tile's S^T may overwrite its columns.
+        tc_fence_before();
+        warp_arrive(bar(C::kSEmpty));
         // P^T = 2^(scale log2(e) S^T - LSE log2(e)), two queries per packed FFMA.
         const float2 scale2 = make_float2(sl2, sl2);
 #pragma unroll
@@ -343,34 +352,25 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : 0.f;
       }
-      {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = Elem<F16>::pack(p[2 * c], p[2 * c + 1]);
-        tmem_st32(tmem + lane_base + C::kColS + 64u * h, pk);
-      }
-      tmem_wait_st();
-      warp_arrive(bar(C::kPFull));
 
       if (!(ok = warp_wait(bar(C::kDPFull), t & 1, &abort_flag, a.err))) break;
       tc_fence_after();
       {
-        const float4* d4 = reinterpret_cast<const float4*>(s_delta + 64 * h);
-        float4 dv4[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) dv4[i] = d4[i];
+        const uint32_t dp_col = tmem + lane_base + C::kColDP + 64u * h;
         uint32_t rr[2][32];
-        tmem_ld32(tmem + lane_base + C::kColDP + 64u * h, rr[0]);
-        tmem_ld32(tmem + lane_base + C::kColDP + 64u * h + 32u, rr[1]);
+        tmem_ld32(dp_col, rr[0]);
+        tmem_ld32(dp_col + 32u, rr[1]);
         tmem_wait_ld_all();
         reg_fence(rr[0]);
         reg_fence(rr[1]);
-        // dS^T = P^T (dP^T - Delta), two queries per packed FADD / FMUL.
-        uint32_t pk[32];
+        // dS^T = P^T (dP^T - Delta), two queries per packed FADD / FMUL; computing it first frees
+        // the dP^T registers before P^T is packed.
+        const float4* d4 = reinterpret_cast<const float4*>(s_delta + 64 * h);
+        uint32_t pk_ds[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = 4 * i;
-          const float4 nd = dv4[i];  // -Delta of queries c .. c + 3
+          const float4 nd = d4[i];  // -Delta of queries c .. c + 3
           const uint32_t* src = &rr[i >> 3][(4 * i) & 31];
           const float2 d0 = __fadd2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])),
                                        make_float2(nd.x, nd.y));
@@ -378,12 +378,19 @@ __global__ void __launch_bounds__(352, 1)
                                        make_float2(nd.z, nd.w));
           const float2 s0 = __fmul2_rn(make_float2(p[c], p[c + 1]), d0);
           const float2 s1 = __fmul2_rn(make_float2(p[c + 2], p[c + 3]), d1);
-          pk[2 * i] = Elem<F16>::pack(s0.x, s0.y);
-          pk[2 * i + 1] = Elem<F16>::pack(s1.x, s1.y);
+          pk_ds[2 * i] = Elem<F16>::pack(s0.x, s0.y);
+          pk_ds[2 * i + 1] = Elem<F16>::pack(s1.x, s1.y);
         }
-        tmem_st32(tmem + lane_base + C::kColDP + 64u * h, pk);
+        // dP^T has been read: P^T goes over the first 32 of this half's 64 columns, dS^T over the
+        // last 32.
+        uint32_t pk_p[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pk_p[c] = Elem<F16>::pack(p[2 * c], p[2 * c + 1]);
+        tmem_st32(dp_col, pk_p);
+        tmem_st32(dp_col + 32u, pk_ds);
       }
       tmem_wait_st();
+      warp_arrive(bar(C::kPFull));
       warp_arrive(bar(C::kDSFull));
     }
     if (ok && warp_wait(bar(C::kDone), 0, &abort_flag, a.err)) {
