@@ -164,8 +164,10 @@ swa_status swa_attn_bwd_f32(const float* q, const float* k, const float* v, cons
  * o, lse, dq, dk, dv out (host pointers, equal lengths, causal window; layouts as above, bf16).
  * The (batch, kv head) groups are processed in chunks of `units_per_chunk`: chunk c + 1 is copied
  * in while chunk c runs the same kernels as swa_attn_fwd / swa_attn_bwd and chunk c - 1 is copied
- * out, on three library streams forked from `stream` and joined back into it, so the call is
- * asynchronous on `stream` like the others and its results equal theirs bit for bit.  Host
+ * out (a chunk's forward starts once its q, k, v are in, and its o and lse go back as soon as the
+ * forward has written them).  This runs on three library streams forked from `stream` and joined
+ * back into it, so the call is asynchronous on `stream` like the others and its results equal
+ * theirs bit for bit.  Host
  * buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to overlap.
  *   workspace : device scratch, 16-byte aligned, caller-owned.  swa_attn_host_workspace_bytes
  *               gives three chunks' tensors (copy-in, kernels and copy-out each on their own

@@ -425,7 +425,8 @@ struct HostPipe {
   bool ready = false;
   cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
   cudaEvent_t fork = nullptr, join_in = nullptr, join_comp = nullptr, join_out = nullptr;
-  cudaEvent_t in_done[kMaxHostSlots] = {}, comp_done[kMaxHostSlots] = {},
+  cudaEvent_t in_fwd[kMaxHostSlots] = {}, in_done[kMaxHostSlots] = {},
+              fwd_done[kMaxHostSlots] = {}, comp_done[kMaxHostSlots] = {},
               out_done[kMaxHostSlots] = {};
 };
 std::mutex g_pipe_mu;
@@ -448,7 +449,9 @@ swa_status host_pipe(HostPipe** out) {
               cudaEventCreateWithFlags(&hp.join_comp, ef) == cudaSuccess &&
               cudaEventCreateWithFlags(&hp.join_out, ef) == cudaSuccess;
     for (int i = 0; ok && i < kMaxHostSlots; ++i)
-      ok = cudaEventCreateWithFlags(&hp.in_done[i], ef) == cudaSuccess &&
+      ok = cudaEventCreateWithFlags(&hp.in_fwd[i], ef) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.in_done[i], ef) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.fwd_done[i], ef) == cudaSuccess &&
            cudaEventCreateWithFlags(&hp.comp_done[i], ef) == cudaSuccess &&
            cudaEventCreateWithFlags(&hp.out_done[i], ef) == cudaSuccess;
     if (!ok) return SWA_ERR_CUDA;
@@ -549,20 +552,29 @@ swa_status swa_attn_fwd_bwd_host(const void* q, const void* k, const void* v, co
       result = SWA_ERR_CUDA;
       break;
     }
+    // Q, K, V first (the forward needs only those), then dO.
     if (!h2d(sq, at(q, u0 * q_unit), n * q_unit) || !h2d(sk, at(k, u0 * k_unit), n * k_unit) ||
-        !h2d(sv, at(v, u0 * k_unit), n * k_unit) || !h2d(sdo, at(dO, u0 * q_unit), n * q_unit) ||
+        !h2d(sv, at(v, u0 * k_unit), n * k_unit) ||
+        cudaEventRecord(hp->in_fwd[slot], hp->in) != cudaSuccess ||
+        !h2d(sdo, at(dO, u0 * q_unit), n * q_unit) ||
         cudaEventRecord(hp->in_done[slot], hp->in) != cudaSuccess) {
       result = SWA_ERR_CUDA;
       break;
     }
-    // forward and backward of the chunk's n groups: one problem with B = 1, Hq = n G, Hkv = n
-    if (cudaStreamWaitEvent(hp->comp, hp->in_done[slot], 0) != cudaSuccess) {
+    // forward and backward of the chunk's n groups: one problem with B = 1, Hq = n G, Hkv = n.
+    // The forward starts while dO is still being copied.
+    if (cudaStreamWaitEvent(hp->comp, hp->in_fwd[slot], 0) != cudaSuccess) {
       result = SWA_ERR_CUDA;
       break;
     }
     const swa::Problem pb = make_problem(1, n * G, n, N, D, window, scale, err);
     if (swa::launch_fwd(pb, sq, sk, sv, so, slse, hp->comp) != cudaSuccess ||
-        swa::launch_bwd_delta(pb, so, sdo, sdelta, hp->comp) != cudaSuccess ||
+        cudaEventRecord(hp->fwd_done[slot], hp->comp) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->comp, hp->in_done[slot], 0) != cudaSuccess) {
+      result = SWA_ERR_CUDA;
+      break;
+    }
+    if (swa::launch_bwd_delta(pb, so, sdo, sdelta, hp->comp) != cudaSuccess ||
         swa::launch_bwd_dkdv(pb, sq, sk, sv, sdo, slse, sdelta, sdk, sdv, hp->comp) !=
             cudaSuccess ||
         swa::launch_bwd_dq(pb, sq, sk, sv, sdo, slse, sdelta, sdq, hp->comp) != cudaSuccess ||
@@ -570,13 +582,15 @@ swa_status swa_attn_fwd_bwd_host(const void* q, const void* k, const void* v, co
       result = SWA_ERR_CUDA;
       break;
     }
-    // outputs of chunk c
-    if (cudaStreamWaitEvent(hp->out, hp->comp_done[slot], 0) != cudaSuccess) {
+    // outputs of chunk c: O and LSE as soon as the forward has written them (the backward only
+    // reads them), the gradients after the backward
+    if (cudaStreamWaitEvent(hp->out, hp->fwd_done[slot], 0) != cudaSuccess ||
+        !d2h(at(o, u0 * q_unit), so, n * q_unit) || !d2h(at(lse, u0 * l_unit), slse, n * l_unit) ||
+        cudaStreamWaitEvent(hp->out, hp->comp_done[slot], 0) != cudaSuccess) {
       result = SWA_ERR_CUDA;
       break;
     }
-    if (!d2h(at(o, u0 * q_unit), so, n * q_unit) || !d2h(at(lse, u0 * l_unit), slse, n * l_unit) ||
-        !d2h(at(dq, u0 * q_unit), sdq, n * q_unit) || !d2h(at(dk, u0 * k_unit), sdk, n * k_unit) ||
+    if (!d2h(at(dq, u0 * q_unit), sdq, n * q_unit) || !d2h(at(dk, u0 * k_unit), sdk, n * k_unit) ||
         !d2h(at(dv, u0 * k_unit), sdv, n * k_unit) ||
         cudaEventRecord(hp->out_done[slot], hp->out) != cudaSuccess) {
       result = SWA_ERR_CUDA;
