@@ -36,6 +36,20 @@ def walk_length(case: si.Case, key_block: int) -> int:
     return G * (q_hi - q_lo + 1)
 
 
+def test_walk_length_matches_brute_force():
+    """walk_length agrees with counting, over the oracle's own visibility predicate, the query
+    blocks holding at least one query that sees a key of the block."""
+    import numpy as np
+    for case in CASES:
+        i = np.arange(case.N)[:, None]
+        j = np.arange(case.N)[None, :]
+        vis = orc.visible(i, j, case.W)
+        for kb in range((case.N + 127) // 128):
+            seen = vis[:, 128 * kb:128 * (kb + 1)].any(axis=1)
+            qblocks = {q // 128 for q in np.nonzero(seen)[0]}
+            assert walk_length(case, kb) == (case.Hq // case.Hkv) * len(qblocks), (case, kb)
+
+
 def test_walk_lengths_cover_the_edge_cases():
     """The cases above reach walks of 1, 2, 3 and 6 tiles (a host-side check of the case list)."""
     lengths = {walk_length(c, kb) for c in CASES for kb in range((c.N + 127) // 128)}
