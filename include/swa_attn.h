@@ -62,8 +62,8 @@ typedef enum {
  *   o, lse  : outputs (device); fully overwritten for rows 0..N-1.
  *   window  : W >= 1; values >= N mean full causal attention.
  *   scale   : softmax scale applied to <q, k> (typically 1/sqrt(D)).
- * Saved state for the backward is exactly (o, lse) — the lab's windowed forward that "may emit the
- * logsumexp under a window" (Lab 28, "Method and disclosure").
+ * Saved state for the backward is exactly (o, lse): the lab's windowed forward keeps the per-row
+ * log-sum-exp under the window for the backward (Lab 28, "Method and disclosure").
  */
 swa_status swa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                         int B, int Hq, int Hkv, int N, int D, int window, float scale,
@@ -121,8 +121,9 @@ swa_status swa_attn_bwd_f16(const void* q, const void* k, const void* v, const v
  *   f16          : 0 -> bf16 tensors, 1 -> fp16 tensors; other values SWA_ERR_INVALID_ARG.
  *   workspace    : at least swa_attn_bwd_workspace_bytes(B, Hq, Lq, D) bytes.
  * Key blocks that no query sees (a short query suffix under a narrow window) get dk = dv = 0.
- * The pages' gradient sweep covers "queries shorter than keys" and windows "causal and not"
- * (Lab 28, numbers entry "Gradient parity, small shapes"); neither is defined there further, and
+ * The pages' gradient sweep includes query sequences shorter than the key sequence, and both causal
+ * and non-causal windows (Lab 28, numbers entry "Gradient parity, small shapes"); neither is
+ * defined there further, and
  * the alignment and two-sided window above are this library's reading.  With Lq = Lk, causal = 1
  * these are swa_attn_fwd / swa_attn_bwd (f16 = 1: the _f16 forms).
  */

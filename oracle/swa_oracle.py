@@ -36,10 +36,11 @@ Where these come from:
     the log-sum-exp, and the backward recomputes what it needs.  LSE here is that saved quantity.
   * The pages print no formulas; the lines above are the standard scaled-dot-product attention and
     its hand-derived gradient.  Delta is the usual row-sum identity sum_j P[i,j] dP[i,j] = <dO[i], O[i]>.
-  * Grouped-query mapping (pages: "grouped-query ratios" only): consecutive query heads share a kv
-    head, hk = hq // G.
-  * Lab 28's gradient sweep also covers "queries shorter than keys" and windows "causal and not"
-    (record, numbers entry "Gradient parity, small shapes") without defining either.  Readings:
+  * Grouped-query mapping (the pages name grouped-query ratios but not the mapping): consecutive
+    query heads share a kv head, hk = hq // G.
+  * Lab 28's gradient sweep also includes query sequences shorter than the key sequence, and both
+    causal and non-causal windows (record, numbers entry "Gradient parity, small shapes"), without
+    defining either.  Readings:
     shorter queries are the last Lq positions of the key sequence (bottom-right alignment, the
     usual convention for a query suffix attending to a longer context), and a non-causal window of
     size W sees the keys within W - 1 positions on either side, |pos(i) - j| < W, so that W = 1 is
