@@ -24,10 +24,10 @@ What is computed (per batch b and query head hq; kv head hk = hq // (Hq / Hkv));
 
 Where these come from:
   * "Off NVIDIA, you fix the platform yourself" (Layer2C Lab 28), section "What was broken?":
-    attention builds a table of scores, one row per word and one column per earlier word; under a
-    sliding window each word sees only the 1,024 words before it.  The dense path that builds the
-    whole table is the one the lab measured at 198 GB (lab record, numbers entry "Attention
-    backward memory").
+    the attention scores form a matrix with a row per query token and a column per key token, and
+    a 1,024-token sliding window limits each row to the preceding 1,024 tokens.  The dense path
+    that builds the whole matrix is the one the lab measured at 198 GB (lab record, numbers entry
+    "Attention backward memory").
   * Same lab, section "What did fixing it take?" and the record's numbers entry "Gradient parity":
     at a one-token window the true gradient is zero.  That fixes the reading that the window
     includes the query itself (W = 1 leaves exactly one visible key, so the softmax is the constant

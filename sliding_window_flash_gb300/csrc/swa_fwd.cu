@@ -3,8 +3,8 @@
 // A tile is one 128-row query block of one (batch, query head):
 //   O[q0:q0+128] = softmax(scale * Q K^T, window mask) V,  LSE = natural-log row log-sum-exp,
 // walking only the key blocks kb_lo..kb_hi that the window reaches ("Off NVIDIA, you fix the
-// platform yourself", Lab 28, "What did fixing it take?": skip blocks wholly outside the window,
-// mask the cells at its edge; the first block a query tile visits is no longer block zero).
+// platform yourself", Lab 28, "What did fixing it take?": blocks outside the window are not visited,
+// blocks its boundary crosses are masked, and a query tile's walk can start past block 0).
 // Only O and LSE are written (mlx-train-perf README, flash-attention section: the saved state is
 // the output and the log-sum-exp).
 //
