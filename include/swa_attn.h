@@ -10,8 +10,8 @@
  *     LSE[i]  = ln sum_j exp(S[i, j]),  P = exp(S - LSE),  O = P V
  *
  * This is the attention of "Off NVIDIA, you fix the platform yourself" (Layer2C Lab 28), section
- * "What was broken?": a score table with one row per token and one column per earlier token, where
- * under a sliding window each token sees only the W tokens before it.  As in the mlx-train-perf
+ * "What was broken?": attention scores form a matrix with a row per query and a column per key,
+ * and a sliding window of W limits each query to the W most recent positions, itself included.  As in the mlx-train-perf
  * README (flash-attention section) only O and the per-row log-sum-exp are saved by the forward,
  * and the backward recomputes the score tiles it needs; the N x N matrix is never stored.
  *

@@ -29,7 +29,7 @@ Where these come from:
     that builds the whole matrix is the one the lab measured at 198 GB (lab record, numbers entry
     "Attention backward memory").
   * Same lab, section "What did fixing it take?" and the record's numbers entry "Gradient parity":
-    at a one-token window the true gradient is zero.  That fixes the reading that the window
+    the exact gradient vanishes at a one-token window.  That fixes the reading that the window
     includes the query itself (W = 1 leaves exactly one visible key, so the softmax is the constant
     1 and dQ = dK = 0).
   * mlx-train-perf README, flash-attention section: the saved state is the attention output and

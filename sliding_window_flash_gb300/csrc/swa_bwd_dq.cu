@@ -6,7 +6,7 @@
 //   dQ += dS K_j,
 // with a final dQ *= scale.  dQ accumulates in TMEM (fp32) and is initialised by the first visited
 // key block rather than block zero ("Off NVIDIA, you fix the platform yourself", Lab 28, "Method and
-// disclosure": dQ is initialized on each query tile's first visited key tile).  One bf16 rounding
+// disclosure": a query tile's dQ starts at the first key tile it visits).  One bf16 rounding
 // at the store; S and dP stay fp32 in TMEM and only dS is rounded to bf16 as an MMA operand (the
 // lab's fp32-score-tile experiment showed the error of bf16 score scratch).
 //

@@ -12,7 +12,7 @@
 //   widen   up to four bf16 tensors -> fp32 (one 16-byte load, two 16-byte stores per unit);
 //   delta   Delta_i = sum_d bf16(dO_id) * O_id from fp32 O and dO, writing bf16(dO) on the way,
 //           so Delta is formed from the same rounded dO that the dP = dO V^T contraction uses
-//           (with a one-key window dP - Delta then vanishes exactly, as the true gradient does).
+//           (with a one-key window dP - Delta then vanishes exactly, as the exact gradient does).
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 

@@ -2,7 +2,7 @@
 
   * window 1: each query sees only itself, so O is exactly the V row (the softmax over one key is
     1), dV is the group sum of dO up to one bf16 rounding, and dQ = dK = 0 up to rounding
-    (Lab 28 record, numbers entry "Gradient parity": at window 1 the true gradient is zero);
+    (Lab 28 record, numbers entry "Gradient parity": the exact gradient vanishes at window 1);
   * a window at least the sequence length is plain causal attention: W = N and W = 10 N give
     bit-identical results;
   * every output row is written: outputs pre-filled with NaN come back finite (the lab's silent

@@ -5,7 +5,7 @@ Pins (what they fix and why a plausible mistake fails one of them):
   * general W    ->  torch SDPA with a boolean band mask built by a different route (tril minus
                      tril), again with autograd for the gradients.
   * W = 1        ->  closed form: O = V row, LSE = scale <q_i, k_i>, dV = group sum of dO, dQ = dK = 0
-                     (the lab's "at window 1 the true gradient is zero").
+                     (the lab states the exact gradient vanishes at window 1).
   * finite differences of L = sum(dO * O) on tiny shapes.
   * brute force with Python loops on N <= 8.
   * structural invariants: softmax rows sum to 1, sum_j dS[i, j] = 0, dK/dV support in [i-W+1, i].

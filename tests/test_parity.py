@@ -3,7 +3,7 @@ inputs.  Bar: norm-wise relative error <= 1e-2 for O, dQ, dK, dV and max |LSE di
 
 Where the exact gradient is zero (window 1, or N = 1, for dQ and dK) a relative error is undefined;
 there the GPU gradient's norm must be <= 1e-2 of the same gradient's norm at window 2 on the same
-inputs (computed by the oracle), i.e. "only rounding is left" (Lab 28 record, numbers entry
+inputs (computed by the oracle): what remains there is rounding (Lab 28 record, numbers entry
 "Gradient parity").
 """
 import numpy as np
