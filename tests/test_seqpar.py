@@ -1,7 +1,8 @@
 """Sequence sharding (sliding_window_flash_gb300.seqpar) on the CPU over gloo: the halo exchange
 and the return of halo gradients, with the fp64 oracle as each rank's compute, must reproduce the
 unsharded oracle on the whole sequence.  World sizes 2 and 3; windows shorter than a chunk, equal
-to it, and spanning several ranks (so a rank's halo comes from more than one rank)."""
+to it, and spanning several ranks (so a rank's halo comes from more than one rank).  A rank that
+dies before the exchange makes the other rank's exchange raise rather than hang."""
 import os
 import socket
 
@@ -167,3 +168,45 @@ def test_sharded_kernels_rank_by_rank(swa, world, L_rank, W, D):
     for n in ("o", "dq", "dk", "dv"):
         rel = np.linalg.norm(got[n] - ref[n]) / np.linalg.norm(ref[n])
         assert rel <= 1e-2, (n, rel)
+
+
+def _failing_worker(rank, world, port, out):
+    """Rank 0 fails right after joining the group and leaves; rank 1 then needs its halo from
+    rank 0 and must end the exchange with an error, not wait forever."""
+    import datetime
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=10))
+    if rank == 0:
+        os._exit(3)  # a rank that dies between steps, with nothing of its own in flight
+    case = _case(world, 7)
+    full = si.make_inputs(case)
+    sl = slice(rank * L, (rank + 1) * L)
+    q, k, v = (full[n][:, :, sl].contiguous() for n in ("q", "k", "v"))
+    try:
+        seqpar.seq_fwd(q, k, v, 7, case.softmax_scale, fwd_fn=_oracle_fwd)
+        out[rank] = ("returned", False, "")
+    except Exception as e:  # the peer is gone: gloo reports it as a RuntimeError
+        out[rank] = ("raised", isinstance(e, RuntimeError), f"{type(e).__name__}: {e}")
+
+
+def test_dead_peer_ends_the_halo_exchange_with_an_error():
+    """Failure is made on the host: one rank exits before the halo exchange.  The surviving rank's
+    exchange raises (connection closed or the group's 10 s timeout) instead of hanging."""
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    procs = [ctx.Process(target=_failing_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    try:
+        for p in procs:
+            p.join(timeout=120)
+        assert procs[0].exitcode == 3
+        assert procs[1].exitcode == 0, "the surviving rank hung or crashed"
+        assert 1 in out and out[1][0] == "raised" and out[1][1], out.get(1)
+    finally:
+        for p in procs:
+            if p.is_alive():
+                p.kill()
