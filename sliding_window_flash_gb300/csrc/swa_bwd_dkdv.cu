@@ -59,7 +59,8 @@ struct DkdvCfg {
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;  // + TMEM address and abort flag
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
-  // P^T is written over the first 64 columns of S^T, dS^T over the first 64 of dP^T.
+  // Once dP^T has been read, P^T and dS^T go over its columns: in each half-row's 64 columns,
+  // P^T over the first 32 and dS^T over the last 32 (bf16 pairs).
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 256 + D;
   static constexpr int kThreads = 352;
   static constexpr int kComputeThreads = 256;

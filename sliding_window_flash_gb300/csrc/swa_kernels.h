@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 namespace swa {
 
@@ -65,10 +66,13 @@ struct Problem {
 
 // Streaming multiprocessors of the current device (cached per device); persistent kernels launch
 // one CTA per SM.
+// The cache is filled under a mutex, so host threads calling concurrently see a complete value.
 inline int sm_count() {
+  static std::mutex mu;
   static int cached[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lk(mu);
   if (cached[dev] == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)

@@ -64,8 +64,11 @@ def _exchange(sends, recvs, group):
     """Posts every send and receive of one round and waits for all of them."""
     import torch.distributed as dist
 
-    ops = [dist.P2POp(dist.isend, buf, peer, group) for peer, buf in sends]
-    ops += [dist.P2POp(dist.irecv, buf, peer, group) for peer, buf in recvs]
+    def glob(peer):  # plans number ranks inside `group`; P2POp's peer is a global rank
+        return peer if group is None else dist.get_global_rank(group, peer)
+
+    ops = [dist.P2POp(dist.isend, buf, glob(peer), group) for peer, buf in sends]
+    ops += [dist.P2POp(dist.irecv, buf, glob(peer), group) for peer, buf in recvs]
     if ops:
         for req in dist.batch_isend_irecv(ops):
             req.wait()

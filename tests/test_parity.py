@@ -1,5 +1,6 @@
 """GPU parity: the CUDA library (through its C ABI) against the fp64 oracle on the same seeded bf16
-inputs.  Bar: norm-wise relative error <= 1e-2 for O, dQ, dK, dV and max |LSE difference| <= 1e-3.
+inputs.  Bar: norm-wise relative error <= 1e-2 for O, dQ, dK, dV, over the whole tensor and over
+every (batch, head) plane separately, and max |LSE difference| <= 1e-3.
 
 Where the exact gradient is zero (window 1, or N = 1, for dQ and dK) a relative error is undefined;
 there the GPU gradient's norm must be <= 1e-2 of the same gradient's norm at window 2 on the same
@@ -41,10 +42,40 @@ def run_gpu(swa, case, inputs, backward=True):
     return {k: to_np(v) for k, v in out.items()}
 
 
+def worst_head_and_row(x, ref):
+    """(b, head, row) of the largest row error of a [B, H, L, D] comparison, and that error."""
+    err = np.linalg.norm(np.asarray(x, dtype=np.float64) - ref, axis=-1)
+    b, h, r = np.unravel_index(np.argmax(err), err.shape)
+    return (int(b), int(h), int(r)), float(err[b, h, r])
+
+
+def check_per_head(key, x, ref, tol=REL_TOL):
+    """Norm-wise relative error <= tol for every (b, head) plane of a [B, H, L, D] tensor, so that
+    an error confined to one head or one tile cannot hide in the norm of the whole tensor.  A plane
+    whose reference is zero must come back within tol of the whole reference's norm."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    ntot = np.linalg.norm(ref)
+    for b in range(ref.shape[0]):
+        for h in range(ref.shape[1]):
+            nh = np.linalg.norm(ref[b, h])
+            dh = np.linalg.norm(x[b, h] - ref[b, h])
+            ok = dh <= tol * nh if nh > 0 else dh <= tol * ntot
+            if not ok:
+                where, row_err = worst_head_and_row(x, ref)
+                raise AssertionError(
+                    f"{key}: head (b={b}, h={h}) relative error {dh / max(nh, 1e-300):.3e} > {tol}; "
+                    f"worst row overall (b, h, row) = {where}, row error norm {row_err:.3e}")
+
+
 def check_against_oracle(case, gpu, ref, ref_w2=None, backward=True):
     assert np.all(np.isfinite(gpu["o"])) and np.all(np.isfinite(gpu["lse"]))
-    assert rel_err(gpu["o"], ref["o"]) <= REL_TOL, ("o", rel_err(gpu["o"], ref["o"]))
-    assert np.max(np.abs(gpu["lse"] - ref["lse"])) <= LSE_TOL
+    assert rel_err(gpu["o"], ref["o"]) <= REL_TOL, ("o", rel_err(gpu["o"], ref["o"]),
+                                                    worst_head_and_row(gpu["o"], ref["o"]))
+    check_per_head("o", gpu["o"], ref["o"])
+    dl = np.abs(gpu["lse"] - ref["lse"])
+    assert np.max(dl) <= LSE_TOL, ("lse", float(np.max(dl)),
+                                   tuple(int(i) for i in np.unravel_index(np.argmax(dl), dl.shape)))
     if not backward:
         return
     for key in ("dq", "dk", "dv"):
@@ -58,7 +89,8 @@ def check_against_oracle(case, gpu, ref, ref_w2=None, backward=True):
         else:
             assert nref > 0
             e = rel_err(gpu[key], ref[key])
-            assert e <= REL_TOL, (key, e)
+            assert e <= REL_TOL, (key, e, worst_head_and_row(gpu[key], ref[key]))
+            check_per_head(key, gpu[key], ref[key])
 
 
 def _oracle_full(case, inputs):

@@ -118,6 +118,54 @@ def test_autograd_wrapper_two_ranks():
         np.testing.assert_allclose(got, ref[name], rtol=1e-10, atol=1e-12, err_msg=name)
 
 
+def _subgroup_worker(rank, world, members, W, port, out):
+    """A sequence-parallel subgroup inside a larger job: the ranks in `members` shard one sequence
+    among themselves (group rank g, which torch assigns in order of global rank, holds chunk g);
+    the others take no part in the exchange."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    group = dist.new_group(members)  # every rank takes part in creating the group
+    if rank in members:
+        g = dist.get_rank(group)
+        case = _case(len(members), W)
+        full = si.make_inputs(case)
+        sl = slice(g * L, (g + 1) * L)
+        q, k, v, do = (full[n][:, :, sl].contiguous() for n in ("q", "k", "v", "do"))
+        o, lse, k_ext, v_ext = seqpar.seq_fwd(q, k, v, W, case.softmax_scale, group=group,
+                                              fwd_fn=_oracle_fwd)
+        dq, dk, dv = seqpar.seq_bwd(q, k_ext, v_ext, o, do, lse, W, case.softmax_scale,
+                                    group=group, bwd_fn=_oracle_bwd)
+        out[g] = {n: t.numpy() for n, t in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv).items()}
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("members,W", [([1, 3], 30), ([3, 0, 2], 40)])
+def test_sharded_over_a_subgroup(members, W):
+    """Sharding over a subgroup of a 4-rank job (group ranks differ from global ranks) reproduces
+    the unsharded oracle: the exchange addresses the global ranks of the group's members."""
+    from oracle import swa_oracle as orc
+
+    world = 4
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    procs = [ctx.Process(target=_subgroup_worker, args=(r, world, members, W, port, out))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+        assert p.exitcode == 0
+    n = len(members)
+    case = _case(n, W)
+    full = si.make_inputs(case)
+    ref = orc.oracle_backward(full["q"], full["k"], full["v"], full["do"], W, case.softmax_scale)
+    for name in ("o", "lse", "dq", "dk", "dv"):
+        got = np.concatenate([out[g][name] for g in range(n)], axis=2)
+        np.testing.assert_allclose(got, ref[name], rtol=1e-10, atol=1e-12, err_msg=name)
+
+
 @pytest.mark.parametrize("world,W", [(2, 1), (4, 30), (4, 200), (3, 48)])
 def test_plans_match_and_cover(world, W):
     """Every receive has the matching send, and a rank's halo is exactly the min(W - 1, r L)
