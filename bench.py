@@ -98,28 +98,48 @@ def load_peaks() -> dict:
 # Clock sampling during the timed region
 # ------------------------------------------------------------------------------------------------
 
-_CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+_CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+_CLOCK_PERIOD_MS = 10  # the timed region of the default run is ~40 ms: sample densely
+
+
+def _smi_time(stamp: str):
+    """Seconds since the epoch of an nvidia-smi timestamp ('YYYY/MM/DD HH:MM:SS.mmm', local)."""
+    import datetime
+
+    try:
+        return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    except ValueError:
+        return None
 
 
 class ClockSampler:
+    """nvidia-smi polling in the background while the timed region runs.  `mark(start, end)` gives
+    the wall-clock bounds of the timed region; the summary keeps the samples inside it (or, when
+    none landed inside, the ones at most one period from it) and says how many there were."""
+
     def __init__(self, gpu_index: int):
         self.gpu_index = gpu_index
         self.proc = None
+        self.window = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={_CLOCK_FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(_CLOCK_PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         time.sleep(0.3)
         return self
 
+    def mark(self, start: float, end: float):
+        self.window = (start, end)
+
     def __exit__(self, *exc):
+        time.sleep(2 * _CLOCK_PERIOD_MS / 1000)
         self.lines = []
         if self.proc is not None:
             self.proc.terminate()
@@ -131,25 +151,40 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
         return False
 
-    def summary(self) -> dict:
-        sm, mx, reasons = [], [], set()
+    def _parsed(self):
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        rows = []
         for line in getattr(self, "lines", []):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                sm, mx = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
+            reasons = {n for n, val in zip(names, parts[6:10]) if val.lower().startswith("active")}
+            rows.append((_smi_time(parts[0]), sm, mx, reasons))
+        return rows
+
+    def summary(self) -> dict:
+        rows = self._parsed()
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        sel, where = rows, "whole sampler run"
+        if self.window is not None:
+            t0, t1 = self.window
+            inside = [r for r in rows if r[0] is not None and t0 <= r[0] <= t1]
+            slack = _CLOCK_PERIOD_MS / 1000
+            near = [r for r in rows if r[0] is not None and t0 - slack <= r[0] <= t1 + slack]
+            if inside:
+                sel, where = inside, "inside the timed region"
+            elif near:
+                sel, where = near, f"within {_CLOCK_PERIOD_MS} ms of the timed region"
+        reasons = sorted(set().union(*(r[3] for r in sel)))
+        return {"sm_mhz": statistics.median(r[1] for r in sel),
+                "sm_max_mhz": max(r[2] for r in sel), "reasons": reasons, "samples": len(sel),
+                "sm_mhz_min": min(r[1] for r in sel), "period_ms": _CLOCK_PERIOD_MS,
+                "selection": where, "samples_total": len(rows)}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -233,9 +268,125 @@ def oracle_sample(case: si.Case, rows_per_sample: int, samples: int, seed: int =
             "rows": rows_per_sample * samples}
 
 
+def cpu_model() -> str:
+    """The host CPU's model string (lscpu, else /proc/cpuinfo; Arm hosts name no model there)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def host_info() -> dict:
+    return {"cpu_model": cpu_model(), "cpu_count": os.cpu_count(), "blas_threads": _blas_threads(),
+            "note": "BLAS matmuls use blas_threads threads; NumPy's elementwise ops use one"}
+
+
+def _group_rows_seconds(case: si.Case, rows_per_head: int) -> dict:
+    """The oracle's forward + backward of kv group 0 (kv head 0 of batch 0 and its G query heads):
+    the whole group when rows_per_head >= N, else `rows_per_head` consecutive mid-sequence rows of
+    each of the group's heads.  The dense oracle's cost is the same for every row (it scores every
+    key), so the whole group's time is the sample's time x N / rows."""
+    from oracle import swa_oracle as orc
+
+    G = case.Hq // case.Hkv
+    one_group = si.Case(B=1, Hq=G, Hkv=1, N=case.N, D=case.D, W=case.W, do_std=case.do_std,
+                        seed=case.seed)
+    inp = si.make_inputs(one_group)
+    R = min(rows_per_head, case.N)
+    r0 = (case.N - R) // 2
+    rows = np.arange(r0, r0 + R)
+    heads = [(inp["q"][0, g].double().numpy(), inp["do"][0, g].double().numpy()) for g in range(G)]
+    k0, v0 = inp["k"][0, 0].double().numpy(), inp["v"][0, 0].double().numpy()
+    t0 = time.perf_counter()
+    for qh, doh in heads:
+        if R == case.N:
+            orc.head_backward(qh, k0, v0, doh, case.W, case.softmax_scale)
+        else:
+            orc.rows_backward(qh, k0, v0, doh, rows, case.W, case.softmax_scale)
+    dt = time.perf_counter() - t0
+    group_s = dt * case.N / R
+    return {"measured_s": dt,
+            "measured": ("whole kv group" if R == case.N else
+                         f"{R} mid-sequence rows of each of the kv group's {G} query heads"),
+            "group_s" if R == case.N else "group_s_extrapolated": group_s,
+            "all_heads_s_extrapolated": group_s * case.B * case.Hkv}
+
+
+def cpu_baselines(gpu_ms: dict, rows_per_head: int = 2048) -> dict:
+    """The fp64 oracle beside each workload's GPU time: the full oracle for the tiny case and the
+    edge sweep, one kv group (measured, or a row sample of it) for the long layers, the full-causal
+    GQA layer and the mixed step, with the all-heads (all-layers) time extrapolated and labelled."""
+    from oracle import swa_oracle as orc
+
+    out = {"host": host_info()}
+    c = si.tiny_case()
+    inp = si.make_inputs(c)
+    t0 = time.perf_counter()
+    orc.oracle_backward(inp["q"], inp["k"], inp["v"], inp["do"], c.W, c.softmax_scale)
+    out["tiny"] = {"oracle_s": time.perf_counter() - t0, "measured": "full oracle fwd + bwd",
+                   "gpu_ms": gpu_ms.get("tiny")}
+    t0 = time.perf_counter()
+    for c in si.edge_cases():
+        inp = si.make_inputs(c)
+        orc.oracle_backward(inp["q"], inp["k"], inp["v"], inp["do"], c.W, c.softmax_scale)
+    out["edge_sweep"] = {"oracle_s": time.perf_counter() - t0, "cases": len(si.edge_cases()),
+                         "measured": "full oracle fwd + bwd of every case",
+                         "gpu_ms": gpu_ms.get("edge_sweep")}
+    for N in (8192, 16384, 32768):
+        case = si.long_swa_case(N)
+        r = _group_rows_seconds(case, N if N == 8192 else rows_per_head)
+        r["gpu_ms"] = gpu_ms.get(f"long_swa_{N}")
+        out[f"long_swa_{N}"] = r
+    r = _group_rows_seconds(si.gqa_causal_case(), 8192)
+    r["gpu_ms"] = gpu_ms.get("gqa_causal_8k")
+    out["gqa_causal_8k"] = r
+    layers = si.mixed_layer_cases()
+    per = [_group_rows_seconds(layers[i], rows_per_head) for i in (0, 5)]  # a sliding, a full layer
+    n_full = sum(1 for c in layers if c.W >= c.N)
+    tot = per[0]["all_heads_s_extrapolated"] * (len(layers) - n_full) + \
+        per[1]["all_heads_s_extrapolated"] * n_full
+    out["mixed_12_layers"] = {
+        "measured_s": per[0]["measured_s"] + per[1]["measured_s"],
+        "measured": f"{rows_per_head} mid-sequence rows of each query head of kv group 0, in one "
+                    "sliding and one full layer",
+        "layer_group_s_extrapolated": [per[0]["group_s_extrapolated"],
+                                       per[1]["group_s_extrapolated"]],
+        "all_layers_all_heads_s_extrapolated": tot,
+        "gpu_ms": gpu_ms.get("mixed_12_layers"),
+    }
+    return out
+
+
 # ------------------------------------------------------------------------------------------------
 # Our arm
 # ------------------------------------------------------------------------------------------------
+
+def headline_config(case: si.Case, world: int) -> dict:
+    """The `config` of both arms' JSON lines: the long sliding-window layer at N = 32,768."""
+    fl = step_flops(case)
+    return {
+        "workload": "long-context sliding-window layer: B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, "
+                    "fwd + bwd (Delta, dK/dV, dQ)",
+        "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "N": case.N, "D": case.D, "W": case.W,
+        "global_batch": case.B * world,
+        "seq_len": case.N,
+        "parallelism": f"independent layer per rank x{world}" if world > 1 else "single GPU",
+        "l2": "no flush: each step reads Q/dO (268 MB each) and K/V (134 MB each), all larger "
+              "than the 129 MB L2",
+        "flops_per_step": {"fwd": fl["fwd"], "bwd": fl["bwd"]},
+    }
+
 
 def run_ours(args, world, rank, local):
     import sliding_window_flash_gb300 as swa
@@ -279,11 +430,14 @@ def run_ours(args, world, rank, local):
     with ClockSampler(local) as clk:
         barrier(dist, device)
         torch.cuda.synchronize(device)
+        wall0 = time.time()
         start.record(stream)
         for s in range(args.steps):
             one_step(events[s])
         end.record(stream)
         torch.cuda.synchronize(device)
+        wall1 = time.time()
+        clk.mark(wall0, wall1)
         barrier(dist, device)
     swa.swa_check_device(device)
     total_ms = start.elapsed_time(end)
@@ -306,7 +460,11 @@ def run_ours(args, world, rank, local):
         "bwd": fl["bwd"] / ((avg["delta"] + avg["dkdv"] + avg["dq"]) * 1e-3) / 1e12,
     }
     dominant = max(("fwd", "dkdv", "dq"), key=lambda k_: avg[k_])
-    peak_tf = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+    clocks = clk.summary()
+    # The kernels run inside a short region (tens of ms) at the maximum SM clock, which is how the
+    # burst peak was measured; the sustained peak comes from seconds of back-to-back GEMMs under
+    # the power cap at a lower clock.  So the fraction is taken against the burst figure.
+    peak_tf = peaks["bf16_tflops"]
     traffic = _profiled_traffic(dominant)
     algorithmic_bytes = {  # each kernel's compulsory DRAM traffic per launch
         "fwd": 2 * (case.B * case.Hq * case.N * case.D * 2) + 2 * (case.B * case.Hkv * case.N * case.D * 2)
@@ -326,8 +484,16 @@ def run_ours(args, world, rank, local):
         "frac": kern_tflops[dominant] / peak_tf,
         "traffic": traffic,
         "algorithmic_bytes": algorithmic_bytes[dominant],
-        "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a repeated step)",
+        "algorithmic_flops": fl[dominant],
+        "launch_ms": avg[dominant],
+        "peak_source": f"{peaks['source']} bf16 burst (the kernel runs inside a "
+                       f"{total_ms:.0f} ms region at {clocks.get('sm_mhz')} MHz)",
+        "frac_of_sustained": kern_tflops[dominant] / peaks["bf16_tflops_sustained"]
+        if peaks.get("bf16_tflops_sustained") else None,
     }
+    if clocks.get("sm_mhz"):
+        # clock-normalised duration: a kernel slowed only by a lower clock keeps this figure
+        roofline["launch_kcycles"] = avg[dominant] * clocks["sm_mhz"]
     delta_gbs = delta_bytes(case) / (avg["delta"] * 1e-3) / 1e9
 
     result = {
@@ -343,17 +509,7 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {
-            "workload": "long-context sliding-window layer: B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, "
-                        "fwd + bwd (Delta, dK/dV, dQ)",
-            "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "N": case.N, "D": case.D, "W": case.W,
-            "global_batch": case.B * world,
-            "seq_len": case.N,
-            "parallelism": f"independent layer per rank x{world}" if world > 1 else "single GPU",
-            "l2": "no flush: each step reads Q/dO (268 MB each) and K/V (134 MB each), all larger "
-                  "than the 129 MB L2",
-            "flops_per_step": {"fwd": fl["fwd"], "bwd": fl["bwd"]},
-        },
+        "config": headline_config(case, world),
         "gpu_launches": 4 * args.steps,
         "kernels_ms": avg,
         "kernels_tflops": kern_tflops,
@@ -361,7 +517,7 @@ def run_ours(args, world, rank, local):
         "bwd_tflops": kern_tflops["bwd"],
         "delta_gbs": delta_gbs,
         "roofline": roofline,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     del events
 
@@ -375,13 +531,30 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.no_extra:
         result["other_workloads"] = measure_other_workloads(swa, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        smp = oracle_sample(case, rows_per_sample=1024, samples=args.cpu_samples)
+        gpu_ms = measure_small_configs(swa, device)
+        if "memory" in result:
+            for N, ms in zip(result["memory"]["N"], result["memory"]["fwd_bwd_ms"]):
+                gpu_ms[f"long_swa_{N}"] = ms
+        gpu_ms.setdefault("long_swa_32768", ms_step)
+        ow = result.get("other_workloads", {})
+        if "gqa_causal_8k" in ow:
+            gpu_ms["gqa_causal_8k"] = ow["gqa_causal_8k"]["fwd_ms"] + ow["gqa_causal_8k"]["bwd_ms"]
+        if "mixed_12_layers" in ow:
+            gpu_ms["mixed_12_layers"] = ow["mixed_12_layers"]["step_ms"]
+        per = cpu_baselines(gpu_ms, rows_per_head=args.cpu_rows)
+        result["cpu_baseline_per_config"] = per
+        smp = per["long_swa_32768"]
+        G = case.Hq // case.Hkv
+        pairs = args.cpu_rows * case.W * G  # mid-sequence rows each see the whole window
         result["cpu_baseline"] = {
-            "value": smp["value"], "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
-            "sample": f"fp64 NumPy oracle fwd+bwd of {smp['rows']} query rows (blocks of 1024, "
-                      f"mid-sequence) of one head of the N=32768 W=1024 layer, {smp['seconds']:.1f} s; "
+            "value": 14 * case.D * pairs / smp["measured_s"] / 1e12, "unit": UNIT,
+            "cores": per["host"]["blas_threads"], "kind": "oracle",
+            "sample": f"fp64 NumPy oracle fwd + bwd of {args.cpu_rows} mid-sequence query rows of "
+                      f"each of the {G} query heads of one kv group of the N=32768 W=1024 layer, "
+                      f"{smp['measured_s']:.1f} s (window-effective flops of those rows); "
                       "BLAS matmuls threaded, elementwise ops single-threaded",
-            "seconds": smp["seconds"],
+            "seconds": smp["measured_s"],
+            "cpu_model": per["host"]["cpu_model"], "cpu_count": per["host"]["cpu_count"],
         }
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -413,6 +586,37 @@ def _profiled_traffic(kernel: str):
         return None
 
 
+def measure_small_configs(swa, device) -> dict:
+    """GPU fwd + bwd time of the tiny case (mean of 20 calls) and of the whole edge sweep (every
+    case once, after one untimed pass), on preallocated buffers."""
+    stream = torch.cuda.current_stream(device)
+    out = {}
+
+    def run(cases, reps):
+        calls = []
+        for c in cases:
+            inp = si.make_inputs(c, device=str(device))
+            calls.append(_layer_calls(swa, inp, c.W, c.softmax_scale))
+        for f, b in calls:
+            f()
+            b()
+        torch.cuda.synchronize(device)
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            for f, b in calls:
+                f()
+                b()
+        e.record(stream)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(e) / reps
+
+    out["tiny"] = run([si.tiny_case()], 20)
+    out["edge_sweep"] = run(si.edge_cases(), 1)
+    swa.swa_check_device(device)
+    return out
+
+
 def measure_memory(swa, device, D: int = 128) -> dict:
     """Peak device memory of one layer's fwd + bwd versus N (inputs Q, K, V, dO excluded), for the
     long sliding-window layer with head dim D, and the fwd + bwd time at each N."""
@@ -431,13 +635,15 @@ def measure_memory(swa, device, D: int = 128) -> dict:
         torch.cuda.synchronize(device)
         peak = torch.cuda.max_memory_allocated(device)
         # time of one fwd + bwd at this length (after the memory-tracked one; 5 repetitions)
+        ws = torch.empty(swa.swa_attn_bwd_workspace_bytes(case.B, case.Hq, N, D),
+                         dtype=torch.uint8, device=device)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         ev[0].record()
         for _ in range(5):
             swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale, out=o,
                              lse=lse)
             swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
-                             case.softmax_scale, dq=dq, dk=dk, dv=dv)
+                             case.softmax_scale, dq=dq, dk=dk, dv=dv, workspace=ws)
         ev[1].record()
         torch.cuda.synchronize(device)
         ms = ev[0].elapsed_time(ev[1]) / 5
@@ -447,7 +653,7 @@ def measure_memory(swa, device, D: int = 128) -> dict:
         out["N"].append(N)
         out["peak_gb_total"].append(peak / 1e9)
         out["peak_gb_above_inputs"].append((peak - base) / 1e9)
-        del inp, o, lse, dq, dk, dv
+        del inp, o, lse, dq, dk, dv, ws
     a = out["peak_gb_above_inputs"]
     out["ratio_per_doubling"] = [a[i + 1] / a[i] for i in range(len(a) - 1)]
     torch.cuda.empty_cache()
@@ -498,14 +704,38 @@ def measure_e2e(swa, case, device, dist, args, world) -> dict:
             "api": "swa_attn_fwd_bwd_host"}
 
 
+def _layer_calls(swa, inp, W: int, scale: float, causal: bool = True):
+    """Forward and backward calls of one layer on preallocated outputs and workspace, so that a
+    timed repetition launches the kernels and allocates nothing."""
+    q, k, v, do = inp["q"], inp["k"], inp["v"], inp["do"]
+    B, Hq, Lq, D = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    dev = q.device
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if q.dtype == torch.float32:
+        nws = swa.swa_attn_f32_workspace_bytes(B, Hq, Hkv, Lq, Lk, D)
+    else:
+        nws = swa.swa_attn_bwd_workspace_bytes(B, Hq, Lq, D)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    fwd_ws = ws if q.dtype == torch.float32 else None
+
+    def fwd():
+        swa.swa_attn_fwd(q, k, v, W, scale, out=o, lse=lse, causal=causal, workspace=fwd_ws)
+
+    def bwd():
+        swa.swa_attn_bwd(q, k, v, o, do, lse, W, scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                         causal=causal)
+
+    return fwd, bwd
+
+
 def measure_other_workloads(swa, device) -> dict:
-    """Full-causal GQA layer (fwd and bwd timed separately), the headline layer in fp16 and in
-    fp32, a query suffix and a two-sided window over the headline keys, and the 12-layer mixed
-    step."""
+    """Full-causal GQA layer (fwd and bwd timed separately), the headline layer in fp16, fp32, with
+    64- and 256-wide heads, a query suffix and a two-sided window over the headline keys, and the
+    12-layer mixed step with its peak memory.  Outputs and workspaces are allocated before timing."""
     res = {}
-    case = si.gqa_causal_case()
-    inp = si.make_inputs(case, device=str(device))
-    fl = step_flops(case)
     stream = torch.cuda.current_stream(device)
 
     def timed(fn, reps=5):
@@ -519,152 +749,91 @@ def measure_other_workloads(swa, device) -> dict:
         torch.cuda.synchronize(device)
         return a.elapsed_time(b) / reps
 
-    o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale)
-    f_ms = timed(lambda: swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
-                                          out=o, lse=lse))
-    b_ms = timed(lambda: swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
-                                          case.softmax_scale))
-    res["gqa_causal_8k"] = {
-        "workload": "B=1 Hq=32 Hkv=8 N=8192 D=128 full causal",
-        "fwd_ms": f_ms, "bwd_ms": b_ms,
-        "fwd_tflops": fl["fwd"] / (f_ms * 1e-3) / 1e12,
-        "bwd_tflops": fl["bwd"] / (b_ms * 1e-3) / 1e12,
-    }
-    del inp, o, lse
-    torch.cuda.empty_cache()
-
-    # The headline layer with fp16 tensors (swa_attn_fwd_f16 / swa_attn_bwd_f16).
-    case = si.long_swa_case(32768)
-    inp = si.make_inputs(case, device=str(device), dtype=torch.float16)
-    fl = step_flops(case)
-    o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale)
-    f_ms = timed(lambda: swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
-                                          out=o, lse=lse))
-    b_ms = timed(lambda: swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
-                                          case.softmax_scale))
-    res["long_swa_fp16"] = {
-        "workload": "B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, fp16 tensors",
-        "fwd_ms": f_ms, "bwd_ms": b_ms,
-        "fwd_tflops": fl["fwd"] / (f_ms * 1e-3) / 1e12,
-        "bwd_tflops": fl["bwd"] / (b_ms * 1e-3) / 1e12,
-        "fwd_bwd_tflops": (fl["fwd"] + fl["bwd"]) / ((f_ms + b_ms) * 1e-3) / 1e12,
-    }
-    del inp, o, lse
-    torch.cuda.empty_cache()
-
-    # The headline layer with 64-wide heads.
-    case = dataclasses.replace(si.long_swa_case(32768), D=64)
-    inp = si.make_inputs(case, device=str(device))
-    fl = step_flops(case)
-    o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale)
-    f_ms = timed(lambda: swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
-                                          out=o, lse=lse))
-    b_ms = timed(lambda: swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
-                                          case.softmax_scale))
-    res["long_swa_d64"] = {
-        "workload": "B=1 Hq=32 Hkv=16 N=32768 D=64 W=1024",
-        "fwd_ms": f_ms, "bwd_ms": b_ms,
-        "fwd_tflops": fl["fwd"] / (f_ms * 1e-3) / 1e12,
-        "bwd_tflops": fl["bwd"] / (b_ms * 1e-3) / 1e12,
-        "fwd_bwd_tflops": (fl["fwd"] + fl["bwd"]) / ((f_ms + b_ms) * 1e-3) / 1e12,
-    }
-    del inp, o, lse
-    torch.cuda.empty_cache()
-
-    # The headline layer with 256-wide heads (Gemma 4's sliding layers): half-tile kernels.
-    case = dataclasses.replace(si.long_swa_case(32768), D=256)
-    inp = si.make_inputs(case, device=str(device))
-    fl = step_flops(case)
-    o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale)
-    f_ms = timed(lambda: swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
-                                          out=o, lse=lse))
-    b_ms = timed(lambda: swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
-                                          case.softmax_scale))
-    res["long_swa_d256"] = {
-        "workload": "B=1 Hq=32 Hkv=16 N=32768 D=256 W=1024",
-        "fwd_ms": f_ms, "bwd_ms": b_ms,
-        "fwd_tflops": fl["fwd"] / (f_ms * 1e-3) / 1e12,
-        "bwd_tflops": fl["bwd"] / (b_ms * 1e-3) / 1e12,
-        "fwd_bwd_tflops": (fl["fwd"] + fl["bwd"]) / ((f_ms + b_ms) * 1e-3) / 1e12,
-    }
-    del inp, o, lse
-    torch.cuda.empty_cache()
-
-    # The headline layer with fp32 tensors (swa_attn_fwd_f32 / swa_attn_bwd_f32: rounding to bf16
-    # and widening of the results inside the timed calls).
-    case = si.long_swa_case(32768)
-    inp = si.make_inputs(case, device=str(device), dtype=torch.float32)
-    fl = step_flops(case)
-    ws = torch.empty(swa.swa_attn_f32_workspace_bytes(case.B, case.Hq, case.Hkv, case.N, case.N,
-                                                      case.D), dtype=torch.uint8, device=device)
-    o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
-                              workspace=ws)
-    grads = [torch.empty_like(inp[k_]) for k_ in ("q", "k", "v")]
-    f_ms = timed(lambda: swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
-                                          out=o, lse=lse, workspace=ws))
-    b_ms = timed(lambda: swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
-                                          case.softmax_scale, dq=grads[0], dk=grads[1],
-                                          dv=grads[2], workspace=ws))
-    res["long_swa_fp32"] = {
-        "workload": "B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, fp32 tensors (bf16 tensor-core "
-                    "operands)",
-        "fwd_ms": f_ms, "bwd_ms": b_ms,
-        "fwd_tflops": fl["fwd"] / (f_ms * 1e-3) / 1e12,
-        "bwd_tflops": fl["bwd"] / (b_ms * 1e-3) / 1e12,
-        "fwd_bwd_tflops": (fl["fwd"] + fl["bwd"]) / ((f_ms + b_ms) * 1e-3) / 1e12,
-    }
-    del inp, o, lse, ws, grads
-    torch.cuda.empty_cache()
-
-    # Queries shorter than keys and a two-sided window (swa_attn_fwd_ex / swa_attn_bwd_ex).
-    for name, Lq, causal, what in (
-            ("suffix_queries_8k_of_32k", 8192, True,
-             "B=1 Hq=32 Hkv=16 Lq=8192 Lk=32768 D=128 W=1024 causal, queries = the last 8192 "
-             "key positions"),
-            ("twosided_32k", 32768, False,
-             "B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024 two-sided (|i - j| < W)")):
-        case = si.long_swa_case(32768)
-        inp = si.make_inputs(case, device=str(device))
-        for key in ("q", "do"):
-            inp[key] = inp[key][:, :, case.N - Lq:].contiguous()
+    def layer(name, what, case, dtype=torch.bfloat16, Lq=None, causal=True, both=True):
+        inp = si.make_inputs(case, device=str(device), dtype=dtype)
+        if Lq is not None:
+            for key in ("q", "do"):
+                inp[key] = inp[key][:, :, case.N - Lq:].contiguous()
+        Lq = case.N if Lq is None else Lq
         pairs = window_pairs(Lq, case.N, case.W, causal) * case.B * case.Hq
-        o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale,
-                                  causal=causal)
-        f_ms = timed(lambda: swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W,
-                                              case.softmax_scale, out=o, lse=lse, causal=causal))
-        b_ms = timed(lambda: swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse,
-                                              case.W, case.softmax_scale, causal=causal))
-        res[name] = {
-            "workload": what, "pairs_per_head": pairs // (case.B * case.Hq),
-            "fwd_ms": f_ms, "bwd_ms": b_ms,
-            "fwd_tflops": 4 * case.D * pairs / (f_ms * 1e-3) / 1e12,
-            "bwd_tflops": 10 * case.D * pairs / (b_ms * 1e-3) / 1e12,
-            "fwd_bwd_tflops": 14 * case.D * pairs / ((f_ms + b_ms) * 1e-3) / 1e12,
-        }
-        del inp, o, lse
+        fwd, bwd = _layer_calls(swa, inp, case.W, case.softmax_scale, causal)
+        f_ms = timed(fwd)
+        b_ms = timed(bwd)
+        r = {"workload": what, "fwd_ms": f_ms, "bwd_ms": b_ms,
+             "fwd_tflops": 4 * case.D * pairs / (f_ms * 1e-3) / 1e12,
+             "bwd_tflops": 10 * case.D * pairs / (b_ms * 1e-3) / 1e12}
+        if both:
+            r["fwd_bwd_tflops"] = 14 * case.D * pairs / ((f_ms + b_ms) * 1e-3) / 1e12
+        if Lq != case.N or not causal:
+            r["pairs_per_head"] = pairs // (case.B * case.Hq)
+        res[name] = r
+        del inp, fwd, bwd
         torch.cuda.empty_cache()
 
+    layer("gqa_causal_8k", "B=1 Hq=32 Hkv=8 N=8192 D=128 full causal", si.gqa_causal_case(),
+          both=False)
+    long32 = si.long_swa_case(32768)
+    layer("long_swa_fp16", "B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, fp16 tensors", long32,
+          dtype=torch.float16)
+    layer("long_swa_d64", "B=1 Hq=32 Hkv=16 N=32768 D=64 W=1024",
+          dataclasses.replace(long32, D=64))
+    layer("long_swa_d256", "B=1 Hq=32 Hkv=16 N=32768 D=256 W=1024",
+          dataclasses.replace(long32, D=256))
+    layer("long_swa_fp32", "B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, fp32 tensors", long32,
+          dtype=torch.float32)
+    layer("suffix_queries_8k_of_32k", "B=1 Hq=32 Hkv=16 Lq=8192 Lk=32768 D=128 W=1024 causal, "
+          "queries = the last 8192 key positions", long32, Lq=8192)
+    layer("twosided_32k", "B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024 two-sided (|i - j| < W)", long32,
+          causal=False)
+    res["mixed_12_layers"] = measure_mixed_step(swa, device, timed)
+    return res
+
+
+def measure_mixed_step(swa, device, timed) -> dict:
+    """The 12-layer mixed step (layers 5 and 11 full causal, the rest W = 1024; N = 30,553): the
+    forward of every layer (O and LSE kept), then the backward from layer 11 down to 0.  Each layer
+    has its own inputs, O and LSE; the layers' gradients share one set of buffers, as a training
+    step hands each layer's gradients on before the next backward.  Peak memory is the most torch
+    held during the step, with and without the inputs."""
     layers = si.mixed_layer_cases()
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats(device)
+    before = torch.cuda.memory_allocated(device)
     data = [si.make_inputs(c, device=str(device)) for c in layers]
-    outs = [None] * len(layers)
+    torch.cuda.synchronize(device)
+    inputs_bytes = torch.cuda.memory_allocated(device) - before
+    c0 = layers[0]
+    outs = [(torch.empty_like(d["q"]),
+             torch.empty((c0.B, c0.Hq, c0.N), dtype=torch.float32, device=device)) for d in data]
+    dq, dk, dv = (torch.empty_like(data[0]["q"]), torch.empty_like(data[0]["k"]),
+                  torch.empty_like(data[0]["v"]))
+    ws = torch.empty(swa.swa_attn_bwd_workspace_bytes(c0.B, c0.Hq, c0.N, c0.D), dtype=torch.uint8,
+                     device=device)
 
     def mixed_step():
         for i, c in enumerate(layers):
-            outs[i] = swa.swa_attn_fwd(data[i]["q"], data[i]["k"], data[i]["v"], c.W, c.softmax_scale)
+            swa.swa_attn_fwd(data[i]["q"], data[i]["k"], data[i]["v"], c.W, c.softmax_scale,
+                             out=outs[i][0], lse=outs[i][1])
         for i in reversed(range(len(layers))):
             c = layers[i]
             swa.swa_attn_bwd(data[i]["q"], data[i]["k"], data[i]["v"], outs[i][0], data[i]["do"],
-                             outs[i][1], c.W, c.softmax_scale)
+                             outs[i][1], c.W, c.softmax_scale, dq=dq, dk=dk, dv=dv, workspace=ws)
 
     m_ms = timed(mixed_step, reps=3)
+    torch.cuda.synchronize(device)
+    peak = torch.cuda.max_memory_allocated(device) - before
     tot = sum(step_flops(c)["fwd"] + step_flops(c)["bwd"] for c in layers)
-    res["mixed_12_layers"] = {
+    res = {
         "workload": "12 layers (W=1024 except layers 5 and 11 full causal), B=1 Hq=32 Hkv=16 "
                     "N=30553 D=128, fwd all then bwd 11..0",
         "step_ms": m_ms,
         "tflops": tot / (m_ms * 1e-3) / 1e12,
+        "peak_gb": peak / 1e9,
+        "peak_gb_above_inputs": (peak - inputs_bytes) / 1e9,
+        "inputs_gb": inputs_bytes / 1e9,
     }
-    del data, outs
+    del data, outs, dq, dk, dv, ws
     torch.cuda.empty_cache()
     return res
 
@@ -674,13 +843,17 @@ def measure_other_workloads(swa, device) -> dict:
 # ------------------------------------------------------------------------------------------------
 
 def run_reference(args, world, rank, local):
+    """The fp64 oracle on the host cores, on the headline workload: each step is a bounded sample
+    of it (`--ref-rows` mid-sequence query rows of one query head, forward + backward), and the
+    value counts the window-effective flops of the sampled rows."""
     if rank != 0:
         return
     case = si.long_swa_case(32768)
+    R = args.ref_rows
     for _ in range(args.warmup):
-        oracle_sample(case, rows_per_sample=256, samples=1)
+        oracle_sample(case, rows_per_sample=R, samples=1)
     t0 = time.perf_counter()
-    smp = oracle_sample(case, rows_per_sample=256, samples=args.steps)
+    smp = oracle_sample(case, rows_per_sample=R, samples=args.steps)
     dt = time.perf_counter() - t0
     val = smp["value"]
     result = {
@@ -697,14 +870,12 @@ def run_reference(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {
-            "workload": "long-context sliding-window layer: B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, "
-                        "fwd + bwd; each step = 256 query rows of one head on the CPU oracle",
-        },
+        "config": headline_config(case, world),
         "cpu_baseline": {
             "value": val, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
-            "sample": f"{args.steps} steps x 256 query rows (mid-sequence) of one head, fp64 NumPy "
-                      "oracle fwd+bwd",
+            "sample": f"{args.steps} steps x {R} query rows (mid-sequence) of one head of the "
+                      "workload, fp64 NumPy oracle fwd + bwd",
+            "cpu_model": cpu_model(), "cpu_count": os.cpu_count(),
         },
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -722,7 +893,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-samples", type=int, default=8)
+    ap.add_argument("--ref-rows", type=int, default=256,
+                    help="query rows per step of the reference arm's oracle sample")
+    ap.add_argument("--cpu-rows", type=int, default=2048,
+                    help="query rows per head in the oracle's row samples of the long layers")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":
