@@ -140,14 +140,21 @@ swa_status swa_attn_bwd_ex(const void* q, const void* k, const void* v, const vo
  * fp32 tensors: the general forms above with q, k, v, o, dO, dq, dk, dv in IEEE fp32.
  * The tensor cores take bf16 operands, so every input element is rounded once to the nearest bf16
  * (ties to even) on the device; scores, accumulators, lse and Delta stay fp32, and the results are
- * widened to fp32.  In the backward, Delta is formed from fp32 O and the bf16-rounded dO that the
- * dP contraction sees.  The pages' gradient sweep runs fp32 inputs alongside the 16-bit ones
- * (Lab 28, numbers entry "Gradient parity, small shapes").
+ * widened to fp32.  The forward's lse is then corrected to fp32 accuracy: q and k are also split
+ * into bf16 high and low parts, and the first-order change of the log-sum-exp under the scores'
+ * missing low-part products, scale (<q_hi, P k_lo> + <q_lo, P k_hi>) per row, is added, with
+ * P k_hi and P k_lo taken from two more runs of the forward kernel (v replaced by k_hi, k_lo; the
+ * same scores give the same P).  What remains is second order in the rounding, ~1e-5 for
+ * unit-scale inputs.  O and the gradients keep bf16 tensor-core operands (as P and dS always
+ * are).  In the backward, Delta is formed from fp32 O and the bf16-rounded dO that the dP
+ * contraction sees.  The pages' gradient sweep runs fp32 inputs alongside the 16-bit ones (Lab 28,
+ * numbers entry "Gradient parity, small shapes").
  *   workspace : device scratch of at least swa_attn_f32_workspace_bytes(B,Hq,Hkv,Lq,Lk,D) bytes,
- *               16-byte aligned, owned by the caller (the bf16 copies and Delta live there; it
- *               holds nothing between calls).  Too small or NULL: SWA_ERR_WORKSPACE.
+ *               16-byte aligned, owned by the caller (the bf16 copies, residuals and Delta live
+ *               there; it holds nothing between calls).  Too small or NULL: SWA_ERR_WORKSPACE.
  * Shapes, windows, causal and errors as in the general forms; every pointer 16-byte aligned.
- * A forward is three launches (round q, k, v; attention; widen o), a backward five.
+ * A forward is six launches (round and split q, k, v; attention three times; lse correction;
+ * widen o), a backward five.
  */
 size_t swa_attn_f32_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D);
 swa_status swa_attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,

@@ -291,9 +291,11 @@ namespace {
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Byte offsets of the workspace regions: bf16 copies of q, k, v, a query-shaped slot (o in the
-// forward, dO in the backward), bf16 dq, dk, dv, then Delta (fp32).
+// forward, dO in the backward), bf16 dq, dk, dv, Delta (fp32), then the forward's log-sum-exp
+// correction: the bf16 residuals of q and k and a second query-shaped slot.  In the forward the dq
+// slot holds P k_hi, the new slot P k_lo, and Delta's rows the repeated passes' log-sum-exp.
 struct F32Layout {
-  size_t q16, k16, v16, a16, dq16, dk16, dv16, delta, total;
+  size_t q16, k16, v16, a16, dq16, dk16, dv16, delta, qlo16, klo16, c16, total;
   long long q_units, k_units;  // 8-element units of a query / key tensor
 };
 
@@ -311,6 +313,9 @@ F32Layout f32_layout(int B, int Hq, int Hkv, int Lq, int Lk, int D) {
   L.dk16 = off; off += kb;
   L.dv16 = off; off += kb;
   L.delta = off; off += round256(static_cast<size_t>(B) * Hq * Lq * sizeof(float));
+  L.qlo16 = off; off += qb;
+  L.klo16 = off; off += kb;
+  L.c16 = off; off += qb;
   L.total = off;
   L.q_units = static_cast<long long>(qe / 8);
   L.k_units = static_cast<long long>(ke / 8);
@@ -336,9 +341,14 @@ swa_status f32_prologue(int B, int Hq, int Hkv, int Lq, int Lk, int D, int windo
   return SWA_OK;
 }
 
+// q, k, v rounded to bf16; with `split`, also the bf16 residuals of q and k.
 swa::RoundJob round_qkv(const float* q, const float* k, const float* v, uint8_t* ws,
-                        const F32Layout& L) {
+                        const F32Layout& L, bool split = false) {
   swa::RoundJob j{};
+  if (split) {
+    j.lo[0] = reinterpret_cast<uint16_t*>(ws + L.qlo16);
+    j.lo[1] = reinterpret_cast<uint16_t*>(ws + L.klo16);
+  }
   j.src[0] = q; j.dst[0] = reinterpret_cast<uint16_t*>(ws + L.q16);
   j.src[1] = k; j.dst[1] = reinterpret_cast<uint16_t*>(ws + L.k16);
   j.src[2] = v; j.dst[2] = reinterpret_cast<uint16_t*>(ws + L.v16);
@@ -368,9 +378,19 @@ swa_status swa_attn_fwd_f32(const float* q, const float* k, const float* v, floa
   if (st != SWA_OK) return st;
   const F32Layout L = f32_layout(B, Hq, Hkv, Lq, Lk, D);
   auto* ws = static_cast<uint8_t*>(workspace);
-  if (swa::launch_round_bf16(round_qkv(q, k, v, ws, L), stream) != cudaSuccess) return SWA_ERR_CUDA;
+  if (swa::launch_round_bf16(round_qkv(q, k, v, ws, L, true), stream) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  // O and LSE from the bf16 operands; then P k_hi and P k_lo (the same scores, so the same P)
+  // and the first-order log-sum-exp correction for the residuals of q and k.
+  float* lse_rep = reinterpret_cast<float*>(ws + L.delta);
   if (swa::launch_fwd(pb, ws + L.q16, ws + L.k16, ws + L.v16, ws + L.a16, lse, stream) !=
-      cudaSuccess)
+          cudaSuccess ||
+      swa::launch_fwd(pb, ws + L.q16, ws + L.k16, ws + L.k16, ws + L.dq16, lse_rep, stream) !=
+          cudaSuccess ||
+      swa::launch_fwd(pb, ws + L.q16, ws + L.k16, ws + L.klo16, ws + L.c16, lse_rep, stream) !=
+          cudaSuccess ||
+      swa::launch_lse_correct(pb, ws + L.q16, ws + L.qlo16, ws + L.dq16, ws + L.c16, lse,
+                              stream) != cudaSuccess)
     return SWA_ERR_CUDA;
   swa::WidenJob w{};
   w.src[0] = reinterpret_cast<const uint16_t*>(ws + L.a16);

@@ -6,13 +6,25 @@
 // The gradient sweep of "Off NVIDIA, you fix the platform yourself" (Lab 28 record, numbers entry
 // "Gradient parity, small shapes") runs fp32 inputs alongside the 16-bit ones.
 //
-// Three bandwidth-bound kernels, each a grid-stride walk over 8-element units (D is a multiple of
+// The log-sum-exp is brought to fp32 accuracy by a split of q and k into bf16 high and low parts,
+// x = x_hi + x_lo (+ at most 2^-17 |x|).  The forward's scores s_ij = scale <q_hi_i, k_hi_j> miss
+// e_ij = scale (<q_hi_i, k_lo_j> + <q_lo_i, k_hi_j>) (+ the negligible <q_lo, k_lo>), and
+//   LSE_i(s + e) = LSE_i(s) + sum_j P_ij e_ij + O(max_j e_ij^2),
+// where P is the forward's softmax.  The first-order term is
+//   scale (<q_hi_i, (P k_lo)_i> + <q_lo_i, (P k_hi)_i>),
+// and P k_lo and P k_hi are the forward run again with k_lo and k_hi in place of v: the same
+// scores, hence the same P.  |e| is a few 1e-3 for unit-scale inputs, so the second-order
+// remainder is ~1e-5.
+//
+// Four bandwidth-bound kernels, each a grid-stride walk over 8-element units (D is a multiple of
 // 8, so a unit never crosses a row):
-//   round   up to four fp32 tensors -> bf16 (two 16-byte loads, one 16-byte store per unit);
+//   round   up to four fp32 tensors -> bf16 (two 16-byte loads, one 16-byte store per unit), and
+//           optionally the residual x - bf16(x) -> bf16 as well;
 //   widen   up to four bf16 tensors -> fp32 (one 16-byte load, two 16-byte stores per unit);
 //   delta   Delta_i = sum_d bf16(dO_id) * O_id from fp32 O and dO, writing bf16(dO) on the way,
 //           so Delta is formed from the same rounded dO that the dP = dO V^T contraction uses
-//           (with a one-key window dP - Delta then vanishes exactly, as the exact gradient does).
+//           (with a one-key window dP - Delta then vanishes exactly, as the exact gradient does);
+//   lse     the first-order log-sum-exp correction above, one row per D/8 lanes.
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 
@@ -40,6 +52,18 @@ __global__ void __launch_bounds__(kThreads) swa_round_bf16_kernel(const RoundJob
     r.z = pack_bf16x2(b.x, b.y);
     r.w = pack_bf16x2(b.z, b.w);
     reinterpret_cast<uint4*>(job.dst[t])[i] = r;
+    if (job.lo[t] != nullptr) {
+      // x - bf16(x) is exact in fp32 (it is the bits of x below bf16's eight); rounded to bf16 it
+      // leaves x - hi - lo within 2^-17 |x|.
+      const float2 h0 = Elem<false>::unpack(r.x), h1 = Elem<false>::unpack(r.y);
+      const float2 h2 = Elem<false>::unpack(r.z), h3 = Elem<false>::unpack(r.w);
+      uint4 l;
+      l.x = pack_bf16x2(a.x - h0.x, a.y - h0.y);
+      l.y = pack_bf16x2(a.z - h1.x, a.w - h1.y);
+      l.z = pack_bf16x2(b.x - h2.x, b.y - h2.y);
+      l.w = pack_bf16x2(b.z - h3.x, b.w - h3.y);
+      reinterpret_cast<uint4*>(job.lo[t])[i] = l;
+    }
   }
 }
 
@@ -102,6 +126,49 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// lse_i += scale * sum_d (q_hi[i,d] b[i,d] + q_lo[i,d] a[i,d]), one row per D/8 lanes with one
+// 16-byte load of each of the four bf16 tensors per lane, as in the Delta kernels.
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+    swa_lse_correct_kernel(const uint16_t* __restrict__ qh, const uint16_t* __restrict__ ql,
+                           const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
+                           float* __restrict__ lse, float scale, long long rows) {
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const int sub = lane % kLanesPerRow;
+  const long long warp_global =
+      (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long warps_total = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long base = warp_global * kRowsPerWarp; base < rows;
+       base += warps_total * kRowsPerWarp) {
+    const long long row = base + lane / kLanesPerRow;
+    float acc = 0.f;
+    if (row < rows) {
+      const long long u = row * (D / 8) + sub;  // 16-byte unit of this lane
+      const uint4 vh = __ldg(reinterpret_cast<const uint4*>(qh) + u);
+      const uint4 vl = __ldg(reinterpret_cast<const uint4*>(ql) + u);
+      const uint4 va = __ldg(reinterpret_cast<const uint4*>(a) + u);
+      const uint4 vb = __ldg(reinterpret_cast<const uint4*>(b) + u);
+      const uint32_t h4[4] = {vh.x, vh.y, vh.z, vh.w}, l4[4] = {vl.x, vl.y, vl.z, vl.w};
+      const uint32_t a4[4] = {va.x, va.y, va.z, va.w}, b4[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const float2 fh = Elem<false>::unpack(h4[p]), fl = Elem<false>::unpack(l4[p]);
+        const float2 fa = Elem<false>::unpack(a4[p]), fb = Elem<false>::unpack(b4[p]);
+        acc = fmaf(fh.x, fb.x, acc);
+        acc = fmaf(fh.y, fb.y, acc);
+        acc = fmaf(fl.x, fa.x, acc);
+        acc = fmaf(fl.y, fa.y, acc);
+      }
+    }
+#pragma unroll
+    for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
+      acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (sub == 0 && row < rows) lse[row] += scale * acc;
+  }
+}
+
 // A whole number of waves of resident 256-thread blocks over the SMs, or fewer when the work is
 // smaller.
 unsigned grid_for(long long threads_needed) {
@@ -138,6 +205,28 @@ cudaError_t launch_delta_f32(const Problem& pb, const float* o, const float* dO,
     swa_delta_f32_kernel<128><<<grid_for(lanes), kThreads, 0, stream>>>(o, dO, delta, pd, rows);
   else if (pb.D == 256)
     swa_delta_f32_kernel<256><<<grid_for(lanes), kThreads, 0, stream>>>(o, dO, delta, pd, rows);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_correct(const Problem& pb, const void* q_hi, const void* q_lo,
+                               const void* a, const void* b, float* lse, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(pb.B) * pb.Hq * pb.span.Lq;
+  const long long lanes = rows * (pb.D / 8);
+  const auto* ph = static_cast<const uint16_t*>(q_hi);
+  const auto* pl = static_cast<const uint16_t*>(q_lo);
+  const auto* pa = static_cast<const uint16_t*>(a);
+  const auto* pb16 = static_cast<const uint16_t*>(b);
+  if (pb.D == 64)
+    swa_lse_correct_kernel<64><<<grid_for(lanes), kThreads, 0, stream>>>(ph, pl, pa, pb16, lse,
+                                                                         pb.scale, rows);
+  else if (pb.D == 128)
+    swa_lse_correct_kernel<128><<<grid_for(lanes), kThreads, 0, stream>>>(ph, pl, pa, pb16, lse,
+                                                                          pb.scale, rows);
+  else if (pb.D == 256)
+    swa_lse_correct_kernel<256><<<grid_for(lanes), kThreads, 0, stream>>>(ph, pl, pa, pb16, lse,
+                                                                          pb.scale, rows);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

@@ -114,6 +114,7 @@ constexpr int kMaxJobTensors = 4;
 struct RoundJob {  // fp32 -> bf16, round to nearest even
   const float* src[kMaxJobTensors];
   uint16_t* dst[kMaxJobTensors];
+  uint16_t* lo[kMaxJobTensors];  // if set: the residual x - bf16(x), itself rounded to bf16
   long long end[kMaxJobTensors];
 };
 struct WidenJob {  // bf16 -> fp32, exact
@@ -126,5 +127,10 @@ cudaError_t launch_widen_bf16(const WidenJob& job, cudaStream_t stream);
 // Delta from fp32 O and dO, also writing dO rounded to bf16 (Delta uses the rounded dO).
 cudaError_t launch_delta_f32(const Problem& pb, const float* o, const float* dO, float* delta,
                              void* do16, cudaStream_t stream);
+// First-order correction of the log-sum-exp for the residuals of a split of q and k into bf16
+// high and low parts: lse += scale * (<q_hi, b> + <q_lo, a>) per query row, where a and b are the
+// forward's outputs with k_hi and k_lo in place of v (all four [B, Hq, Lq, D] bf16).
+cudaError_t launch_lse_correct(const Problem& pb, const void* q_hi, const void* q_lo,
+                               const void* a, const void* b, float* lse, cudaStream_t stream);
 
 }  // namespace swa

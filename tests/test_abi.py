@@ -141,8 +141,8 @@ def _bwd_f32(lib, B=1, Hq=2, Hkv=1, Lq=16, Lk=40, D=64, W=4, causal=1, scale=0.1
 
 
 def test_f32_workspace_size():
-    """Bytes: bf16 copies of q, k, v, a query-shaped slot, dq, dk, dv, then fp32 Delta, each
-    region rounded up to 256 bytes."""
+    """Bytes: bf16 copies of q, k, v, a query-shaped slot, dq, dk, dv, fp32 Delta, then the bf16
+    residuals of q and k and a second query-shaped slot, each region rounded up to 256 bytes."""
     import sliding_window_flash_gb300 as swa
 
     lib = swa.load()
@@ -152,8 +152,8 @@ def test_f32_workspace_size():
 
     B, Hq, Hkv, Lq, Lk, D = 2, 4, 2, 100, 300, 128
     qb, kb = r(B * Hq * Lq * D * 2), r(B * Hkv * Lk * D * 2)
-    assert _f32_need(lib, B, Hq, Hkv, Lq, Lk, D) == 3 * qb + 4 * kb + r(B * Hq * Lq * 4)
-    assert swa.swa_attn_f32_workspace_bytes(B, Hq, Hkv, Lq, Lk, D) == 3 * qb + 4 * kb + r(
+    assert _f32_need(lib, B, Hq, Hkv, Lq, Lk, D) == 5 * qb + 5 * kb + r(B * Hq * Lq * 4)
+    assert swa.swa_attn_f32_workspace_bytes(B, Hq, Hkv, Lq, Lk, D) == 5 * qb + 5 * kb + r(
         B * Hq * Lq * 4)
     assert _f32_need(lib, Lq=41) == 0 and _f32_need(lib, D=96) == 0 and _f32_need(lib, B=0) == 0
 
