@@ -406,77 +406,92 @@ def run_ours(args, world, rank, local):
     lse = torch.empty(case.B, case.Hq, case.N, dtype=torch.float32, device=device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     delta = torch.empty(case.B, case.Hq, case.N, dtype=torch.float32, device=device)
+    ws_fused = torch.empty(swa.swa_attn_bwd_fused_workspace_bytes(case.B, case.Hq, case.N, case.D),
+                           dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
+    # kernels of one step, in launch order (the backward's three phases after the forward)
+    names = {"fused": ("fwd", "delta", "fused", "dq_convert"),
+             "split": ("fwd", "delta", "dkdv", "dq")}
 
-    n_ev = 5  # fwd | delta | dkdv | dq boundaries
-    def one_step(evs=None):
+    def one_step(path, evs=None):
         if evs is not None:
             evs[0].record(stream)
         swa.swa_attn_fwd(q, k, v, case.W, case.softmax_scale, out=o, lse=lse)
         marks = None
         if evs is not None:
             marks = lambda i: evs[i + 1].record(stream)
-        swa.swa_attn_bwd_phases(q, k, v, o, do, lse, case.W, case.softmax_scale,
-                                dq=dq, dk=dk, dv=dv, delta=delta, between=marks)
+        if path == "fused":
+            swa.swa_attn_bwd_phases(q, k, v, o, do, lse, case.W, case.softmax_scale, dq=dq, dk=dk,
+                                    dv=dv, between=marks, fused=True, workspace=ws_fused)
+        else:
+            swa.swa_attn_bwd_phases(q, k, v, o, do, lse, case.W, case.softmax_scale, dq=dq, dk=dk,
+                                    dv=dv, delta=delta, between=marks)
 
-    for _ in range(args.warmup):
-        one_step()
-    torch.cuda.synchronize(device)
-    swa.swa_check_device(device)
-
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    def timed_steps(path, steps, clk=None):
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
         barrier(dist, device)
         torch.cuda.synchronize(device)
         wall0 = time.time()
         start.record(stream)
-        for s in range(args.steps):
-            one_step(events[s])
+        for s_ in range(steps):
+            one_step(path, events[s_])
         end.record(stream)
         torch.cuda.synchronize(device)
-        wall1 = time.time()
-        clk.mark(wall0, wall1)
+        if clk is not None:
+            clk.mark(wall0, time.time())
         barrier(dist, device)
+        swa.swa_check_device(device)
+        per = {n: [] for n in names[path]}
+        for evs in events:
+            for i, n in enumerate(names[path]):
+                per[n].append(evs[i].elapsed_time(evs[i + 1]))
+        return start.elapsed_time(end), {n_: sum(v_) / len(v_) for n_, v_ in per.items()}
+
+    path = args.bwd
+    for _ in range(args.warmup):
+        one_step(path)
+    torch.cuda.synchronize(device)
     swa.swa_check_device(device)
-    total_ms = start.elapsed_time(end)
+    with ClockSampler(local) as clk:
+        total_ms, avg = timed_steps(path, args.steps, clk)
     total_ms = max_over_ranks(dist, total_ms, device)
     ms_step = total_ms / args.steps
-    per = {"fwd": [], "delta": [], "dkdv": [], "dq": []}
-    for evs in events:
-        per["fwd"].append(evs[0].elapsed_time(evs[1]))
-        per["delta"].append(evs[1].elapsed_time(evs[2]))
-        per["dkdv"].append(evs[2].elapsed_time(evs[3]))
-        per["dq"].append(evs[3].elapsed_time(evs[4]))
-    avg = {key: sum(vals) / len(vals) for key, vals in per.items()}
     step_total = fl["fwd"] + fl["bwd"]
     value = aggregate_tflops(world, step_total, args.steps, total_ms)
+    bwd_ms = sum(avg[n] for n in names[path][1:])
 
-    kern_tflops = {
-        "fwd": fl["fwd"] / (avg["fwd"] * 1e-3) / 1e12,
-        "dkdv": fl["dkdv"] / (avg["dkdv"] * 1e-3) / 1e12,
-        "dq": fl["dq"] / (avg["dq"] * 1e-3) / 1e12,
-        "bwd": fl["bwd"] / ((avg["delta"] + avg["dkdv"] + avg["dq"]) * 1e-3) / 1e12,
-    }
-    dominant = max(("fwd", "dkdv", "dq"), key=lambda k_: avg[k_])
+    kern_tflops = {"fwd": fl["fwd"] / (avg["fwd"] * 1e-3) / 1e12,
+                   "bwd": fl["bwd"] / (bwd_ms * 1e-3) / 1e12}
+    if path == "fused":
+        kern_tflops["fused"] = fl["bwd"] / (avg["fused"] * 1e-3) / 1e12
+    else:
+        kern_tflops["dkdv"] = fl["dkdv"] / (avg["dkdv"] * 1e-3) / 1e12
+        kern_tflops["dq"] = fl["dq"] / (avg["dq"] * 1e-3) / 1e12
+    dominant = max((n for n in names[path] if n in kern_tflops), key=lambda k_: avg[k_])
     clocks = clk.summary()
     # The kernels run inside a short region (tens of ms) at the maximum SM clock, which is how the
     # burst peak was measured; the sustained peak comes from seconds of back-to-back GEMMs under
     # the power cap at a lower clock.  So the fraction is taken against the burst figure.
     peak_tf = peaks["bf16_tflops"]
     traffic = _profiled_traffic(dominant)
+    q_bytes = case.B * case.Hq * case.N * case.D * 2
+    k_bytes = case.B * case.Hkv * case.N * case.D * 2
+    row_bytes = case.B * case.Hq * case.N * 4
+    acc_bytes = case.B * case.Hq * ((case.N + 127) // 128) * 128 * case.D * 4
     algorithmic_bytes = {  # each kernel's compulsory DRAM traffic per launch
-        "fwd": 2 * (case.B * case.Hq * case.N * case.D * 2) + 2 * (case.B * case.Hkv * case.N * case.D * 2)
-               + case.B * case.Hq * case.N * 4,
-        "dkdv": 2 * (case.B * case.Hq * case.N * case.D * 2) + 4 * (case.B * case.Hkv * case.N * case.D * 2)
-                + 2 * case.B * case.Hq * case.N * 4,
-        "dq": 3 * (case.B * case.Hq * case.N * case.D * 2) + 2 * (case.B * case.Hkv * case.N * case.D * 2)
-              + 2 * case.B * case.Hq * case.N * 4,
+        "fwd": 2 * q_bytes + 2 * k_bytes + row_bytes,
+        "dkdv": 2 * q_bytes + 4 * k_bytes + 2 * row_bytes,
+        "dq": 3 * q_bytes + 2 * k_bytes + 2 * row_bytes,
+        # as dK/dV, plus reading and writing back the fp32 dQ accumulator (which the L2 cannot hold)
+        "fused": 2 * q_bytes + 4 * k_bytes + 2 * row_bytes + 2 * acc_bytes,
     }
+    kernel_names = {"fwd": "swa_fwd_kernel<128>", "dkdv": "swa_dkdv_kernel<128>",
+                    "dq": "swa_dq_kernel<128>", "fused": "swa_fused_bwd_kernel<128>"}
+    dom_flops = fl["bwd"] if dominant == "fused" else fl[dominant]
     roofline = {
-        "kernel": {"fwd": "swa_fwd_kernel<128>", "dkdv": "swa_dkdv_kernel<128>",
-                   "dq": "swa_dq_kernel<128>"}[dominant],
+        "kernel": kernel_names[dominant],
         "bound": "tensor",
         "achieved": kern_tflops[dominant],
         "peak": peak_tf,
@@ -484,7 +499,7 @@ def run_ours(args, world, rank, local):
         "frac": kern_tflops[dominant] / peak_tf,
         "traffic": traffic,
         "algorithmic_bytes": algorithmic_bytes[dominant],
-        "algorithmic_flops": fl[dominant],
+        "algorithmic_flops": dom_flops,
         "launch_ms": avg[dominant],
         "peak_source": f"{peaks['source']} bf16 burst (the kernel runs inside a "
                        f"{total_ms:.0f} ms region at {clocks.get('sm_mhz')} MHz)",
@@ -494,7 +509,21 @@ def run_ours(args, world, rank, local):
     if clocks.get("sm_mhz"):
         # clock-normalised duration: a kernel slowed only by a lower clock keeps this figure
         roofline["launch_kcycles"] = avg[dominant] * clocks["sm_mhz"]
-    delta_gbs = delta_bytes(case) / (avg["delta"] * 1e-3) / 1e9
+    # the other backward path, timed the same way right after (reported, not the headline)
+    other = "split" if path == "fused" else "fused"
+    for _ in range(3):
+        one_step(other)
+    o_ms, o_avg = timed_steps(other, args.steps)
+    o_bwd = sum(o_avg[n] for n in names[other][1:])
+    bwd_other = {"path": other, "ms_per_step": o_ms / args.steps, "kernels_ms": o_avg,
+                 "bwd_ms": o_bwd, "bwd_tflops": fl["bwd"] / (o_bwd * 1e-3) / 1e12,
+                 "fwd_bwd_tflops": step_total / (o_ms / args.steps * 1e-3) / 1e12}
+    if other == "split":
+        bwd_other["kernels_tflops"] = {"dkdv": fl["dkdv"] / (o_avg["dkdv"] * 1e-3) / 1e12,
+                                       "dq": fl["dq"] / (o_avg["dq"] * 1e-3) / 1e12}
+    # the fused path's preprocess also zeroes the fp32 dQ accumulator (acc_bytes written)
+    delta_gbs = (delta_bytes(case) + (acc_bytes if path == "fused" else 0)) / \
+        (avg["delta"] * 1e-3) / 1e9
 
     result = {
         "metric": METRIC,
@@ -511,6 +540,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic",
         "config": headline_config(case, world),
         "gpu_launches": 4 * args.steps,
+        "bwd_path": path,
         "kernels_ms": avg,
         "kernels_tflops": kern_tflops,
         "fwd_tflops": kern_tflops["fwd"],
@@ -518,12 +548,13 @@ def run_ours(args, world, rank, local):
         "delta_gbs": delta_gbs,
         "roofline": roofline,
         "clocks": clocks,
+        "bwd_other_path": bwd_other,
     }
-    del events
 
     if rank == 0 and not args.no_memory:
         result["memory"] = measure_memory(swa, device)
         result["peak_gb"] = result["memory"]["peak_gb_total"][-1]
+        result["memory_fused_bwd"] = measure_memory(swa, device, fused=True)
         # the same layer with 256-wide heads, the shape of the pages' backward-memory figure
         result["memory_d256"] = measure_memory(swa, device, D=256)
     if not args.no_e2e:
@@ -617,10 +648,12 @@ def measure_small_configs(swa, device) -> dict:
     return out
 
 
-def measure_memory(swa, device, D: int = 128) -> dict:
+def measure_memory(swa, device, D: int = 128, fused: bool = False) -> dict:
     """Peak device memory of one layer's fwd + bwd versus N (inputs Q, K, V, dO excluded), for the
-    long sliding-window layer with head dim D, and the fwd + bwd time at each N."""
-    out = {"D": D, "N": [], "peak_gb_total": [], "peak_gb_above_inputs": []}
+    long sliding-window layer with head dim D, and the fwd + bwd time at each N, on the split
+    (default) or the fused backward."""
+    out = {"D": D, "bwd_path": "fused" if fused else "split", "N": [], "peak_gb_total": [],
+           "peak_gb_above_inputs": []}
     for N in (8192, 16384, 32768):
         case = dataclasses.replace(si.long_swa_case(N), D=D)
         torch.cuda.synchronize(device)
@@ -631,19 +664,20 @@ def measure_memory(swa, device, D: int = 128) -> dict:
         base = torch.cuda.memory_allocated(device)
         o, lse = swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale)
         dq, dk, dv = swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
-                                      case.softmax_scale)
+                                      case.softmax_scale, fused=fused)
         torch.cuda.synchronize(device)
         peak = torch.cuda.max_memory_allocated(device)
         # time of one fwd + bwd at this length (after the memory-tracked one; 5 repetitions)
-        ws = torch.empty(swa.swa_attn_bwd_workspace_bytes(case.B, case.Hq, N, D),
-                         dtype=torch.uint8, device=device)
+        nws = (swa.swa_attn_bwd_fused_workspace_bytes if fused else
+               swa.swa_attn_bwd_workspace_bytes)(case.B, case.Hq, N, D)
+        ws = torch.empty(nws, dtype=torch.uint8, device=device)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         ev[0].record()
         for _ in range(5):
             swa.swa_attn_fwd(inp["q"], inp["k"], inp["v"], case.W, case.softmax_scale, out=o,
                              lse=lse)
             swa.swa_attn_bwd(inp["q"], inp["k"], inp["v"], o, inp["do"], lse, case.W,
-                             case.softmax_scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+                             case.softmax_scale, dq=dq, dk=dk, dv=dv, workspace=ws, fused=fused)
         ev[1].record()
         torch.cuda.synchronize(device)
         ms = ev[0].elapsed_time(ev[1]) / 5
@@ -808,8 +842,8 @@ def measure_mixed_step(swa, device, timed) -> dict:
              torch.empty((c0.B, c0.Hq, c0.N), dtype=torch.float32, device=device)) for d in data]
     dq, dk, dv = (torch.empty_like(data[0]["q"]), torch.empty_like(data[0]["k"]),
                   torch.empty_like(data[0]["v"]))
-    ws = torch.empty(swa.swa_attn_bwd_workspace_bytes(c0.B, c0.Hq, c0.N, c0.D), dtype=torch.uint8,
-                     device=device)
+    ws = torch.empty(swa.swa_attn_bwd_workspace_bytes(c0.B, c0.Hq, c0.N, c0.D),
+                     dtype=torch.uint8, device=device)
 
     def mixed_step():
         for i, c in enumerate(layers):
@@ -889,6 +923,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--bwd", choices=("fused", "split"), default="split",
+                    help="backward path of the timed step (the other is timed after it)")
     ap.add_argument("--no-memory", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true")

@@ -213,6 +213,55 @@ swa_status swa_attn_bwd_dq(const void* q, const void* k, const void* v, const vo
                            cudaStream_t stream);
 
 /*
+ * Fused backward: the same gradients as swa_attn_bwd_ex, with one kernel for dK, dV and dQ.  Per
+ * (key block, query tile) pair it runs the backward's five contractions once each (the split
+ * backward's dQ kernel recomputes S and dP), following the window walk of "Off NVIDIA, you fix the
+ * platform yourself" (Lab 28, "What did fixing it take?", "Method and disclosure": tiles outside the
+ * window skipped, edge tiles masked, dK / dV of key tiles no query visits written as zeros).  dK and
+ * dV accumulate on chip over each kv group as in the split path; every query tile's dQ gets one fp32
+ * partial per key block of its window, added into an fp32 accumulator in the workspace with vector
+ * reduce-adds at the L2, then scaled and rounded once by a small kernel.  Launches: Delta (also
+ * zeroing the accumulator), the fused kernel, the dQ rounding.
+ *   Speed: on GB300 the split backward is faster.  The accumulator's reduce-adds (a 64 KB fp32
+ *   partial per 128 x 128 tile pair) are bounded by the L2's reduction throughput, which costs more
+ *   than the split path's recomputation of S and dP; the fused form is kept for callers who want
+ *   one pass over the key blocks.
+ *   Determinism: dK and dV equal the split path's bit for bit; the order of the fp32 additions into
+ *   dQ's accumulator varies between runs, so dQ can differ in the last bits from run to run (the
+ *   split swa_attn_bwd / swa_attn_bwd_ex is the bit-reproducible path).
+ *   workspace : device scratch of at least swa_attn_bwd_fused_workspace_bytes(B,Hq,Lq,D) bytes,
+ *               16-byte aligned, owned by the caller: Delta (fp32 [B,Hq,Lq], rounded up to 256
+ *               bytes), then the accumulator (B*Hq*ceil(Lq/128)*128*D fp32).  Nothing is kept
+ *               between calls.  Too small or NULL: SWA_ERR_WORKSPACE.
+ *   D = 256 has no fused kernel: the call runs the split backward (the size function then returns
+ *   the Delta bytes alone).
+ * Shapes, windows, causal, f16 and errors as in swa_attn_bwd_ex.
+ */
+size_t swa_attn_bwd_fused_workspace_bytes(int B, int Hq, int Lq, int D);
+swa_status swa_attn_bwd_fused(const void* q, const void* k, const void* v, const void* o,
+                              const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                              int B, int Hq, int Hkv, int Lq, int Lk, int D, int window,
+                              int causal, float scale, int f16, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The three phases swa_attn_bwd_fused runs, one by one (bf16, Lq = Lk = N, causal, D in {64, 128};
+ * D = 256: SWA_ERR_UNSUPPORTED), e.g. to time each kernel.  `workspace` is swa_attn_bwd_fused's.
+ *   swa_attn_bwd_fused_preprocess : Delta, and the accumulator zeroed.
+ *   swa_attn_bwd_fused_dkdv       : dk, dv, and every dQ partial added into the accumulator.
+ *   swa_attn_bwd_fused_dq         : dq = scale * accumulator, rounded to bf16.
+ */
+swa_status swa_attn_bwd_fused_preprocess(const void* o, const void* dO, void* workspace,
+                                         size_t workspace_bytes, int B, int Hq, int N, int D,
+                                         cudaStream_t stream);
+swa_status swa_attn_bwd_fused_dkdv(const void* q, const void* k, const void* v, const void* dO,
+                                   const float* lse, void* dk, void* dv, void* workspace,
+                                   size_t workspace_bytes, int B, int Hq, int Hkv, int N, int D,
+                                   int window, float scale, cudaStream_t stream);
+swa_status swa_attn_bwd_fused_dq(void* dq, const void* workspace, size_t workspace_bytes, int B,
+                                 int Hq, int N, int D, float scale, cudaStream_t stream);
+
+/*
  * Backward without any caller-provided workspace and without allocating: the same computation and
  * kernels as swa_attn_bwd, but the per-row Delta scratch lives in a fixed array of device memory
  * that is part of the library image (SWA_NOALLOC_MAX_ROWS fp32 values, 16 MiB; every GPU that loads

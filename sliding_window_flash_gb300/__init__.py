@@ -28,6 +28,7 @@ __all__ = [
     "swa_attn_fwd",
     "swa_attn_bwd",
     "swa_attn_bwd_workspace_bytes",
+    "swa_attn_bwd_fused_workspace_bytes",
     "swa_attn_f32_workspace_bytes",
     "swa_attn_fwd_bwd_host",
     "swa_attn_host_workspace_bytes",
@@ -83,6 +84,17 @@ SIGNATURES = {
     "swa_attn_bwd_dkdv": (_c_int, [_vp] * 8 + [_c_int] * 6 + [_c_float, _vp]),
     "swa_attn_bwd_dq": (_c_int, [_vp] * 7 + [_c_int] * 6 + [_c_float, _vp]),
     "swa_attn_bwd_noalloc": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_c_float, _vp]),
+    "swa_attn_bwd_fused_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
+    "swa_attn_bwd_fused": (
+        _c_int,
+        [_vp] * 9 + [_c_int] * 8 + [_c_float, _c_int, _vp, ctypes.c_size_t, _vp],
+    ),
+    "swa_attn_bwd_fused_preprocess": (_c_int, [_vp] * 3 + [ctypes.c_size_t] + [_c_int] * 4 + [_vp]),
+    "swa_attn_bwd_fused_dkdv": (
+        _c_int,
+        [_vp] * 8 + [ctypes.c_size_t] + [_c_int] * 6 + [_c_float, _vp],
+    ),
+    "swa_attn_bwd_fused_dq": (_c_int, [_vp] * 2 + [ctypes.c_size_t] + [_c_int] * 4 + [_c_float, _vp]),
     "swa_strerror": (ctypes.c_char_p, [_c_int]),
     "swa_check_device": (_c_int, [_vp]),
     "swa_selftest_wait_timeout": (_c_int, [_vp]),
@@ -225,11 +237,21 @@ def swa_attn_bwd_workspace_bytes(B: int, Hq: int, N: int, D: int) -> int:
     return int(load().swa_attn_bwd_workspace_bytes(B, Hq, N, D))
 
 
+def swa_attn_bwd_fused_workspace_bytes(B: int, Hq: int, Lq: int, D: int) -> int:
+    return int(load().swa_attn_bwd_fused_workspace_bytes(B, Hq, Lq, D))
+
+
 def swa_attn_bwd(q, k, v, o, do, lse, window: int, scale: Optional[float] = None,
-                 dq=None, dk=None, dv=None, workspace=None, causal: bool = True) -> Tuple:
+                 dq=None, dk=None, dv=None, workspace=None, causal: bool = True,
+                 fused: bool = False) -> Tuple:
     """Backward of sum(do * o): returns (dq, dk, dv) in q's dtype (bf16, fp16 or fp32), dk/dv
-    summed over each kv group.  Shapes, window and workspace as in swa_attn_fwd (bf16 and fp16
-    calls take a Delta workspace of swa_attn_bwd_workspace_bytes)."""
+    summed over each kv group.  Shapes, window and workspace as in swa_attn_fwd.
+
+    bf16 / fp16: ``fused=False`` (default) runs the split, bit-reproducible swa_attn_bwd /
+    swa_attn_bwd_ex (workspace of swa_attn_bwd_workspace_bytes), the faster path on GB300;
+    ``fused=True`` runs swa_attn_bwd_fused (one kernel for dK, dV and dQ; workspace of
+    swa_attn_bwd_fused_workspace_bytes; dQ's fp32 additions run in a varying order).  fp32 tensors
+    always take the split path."""
     import torch
 
     lib = load()
@@ -256,11 +278,18 @@ def swa_attn_bwd(q, k, v, o, do, lse, window: int, scale: Optional[float] = None
         if rc != 0:
             raise SwaError(rc, name)
         return dq, dk, dv
-    ws_bytes = int(lib.swa_attn_bwd_workspace_bytes(B, Hq, Lq, D))
+    if fused:
+        ws_bytes = int(lib.swa_attn_bwd_fused_workspace_bytes(B, Hq, Lq, D))
+    else:
+        ws_bytes = int(lib.swa_attn_bwd_workspace_bytes(B, Hq, Lq, D))
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size())
-    if Lq == Lk and causal:
+    if fused:
+        name = "swa_attn_bwd_fused"
+        rc = lib.swa_attn_bwd_fused(*ptrs, B, Hq, Hkv, Lq, Lk, D, int(window), int(bool(causal)),
+                                    _scale(scale, D), int(f16), *ws, st)
+    elif Lq == Lk and causal:
         name = "swa_attn_bwd_f16" if f16 else "swa_attn_bwd"
         rc = getattr(lib, name)(*ptrs, B, Hq, Hkv, Lq, D, int(window), _scale(scale, D), *ws, st)
     else:
@@ -273,12 +302,17 @@ def swa_attn_bwd(q, k, v, o, do, lse, window: int, scale: Optional[float] = None
 
 
 def swa_attn_bwd_phases(q, k, v, o, do, lse, window: int, scale: Optional[float] = None,
-                        dq=None, dk=None, dv=None, delta=None, between=None) -> Tuple:
-    """The backward as its three C-ABI phases (preprocess, dK/dV, dQ) on the current stream.
-
-    Same kernels and results as swa_attn_bwd.  ``between(i)`` (optional) is called before phase i
-    and after the last one (i = 0..3), e.g. to record CUDA events around each kernel.
+                        dq=None, dk=None, dv=None, delta=None, between=None, fused: bool = False,
+                        workspace=None) -> Tuple:
+    """The backward as its three C-ABI phases on the current stream: split (preprocess, dK/dV,
+    dQ; ``delta`` is the Delta buffer) or, with ``fused=True``, the fused backward's (preprocess
+    with the accumulator zeroed, the fused dK/dV/dQ kernel, dQ from the accumulator;
+    ``workspace`` as for swa_attn_bwd_fused).  Same kernels and results as swa_attn_bwd.
+    ``between(i)`` (optional) is called before phase i and after the last one (i = 0..3), e.g. to
+    record CUDA events around each kernel.
     """
+    if fused:
+        return _fused_phases(q, k, v, o, do, lse, window, scale, dq, dk, dv, workspace, between)
     import torch
 
     lib = load()
@@ -313,6 +347,45 @@ def swa_attn_bwd_phases(q, k, v, o, do, lse, window: int, scale: Optional[float]
                              delta.data_ptr(), dq.data_ptr(), B, Hq, Hkv, N, D, int(window), sc, st)
     if rc != 0:
         raise SwaError(rc, "swa_attn_bwd_dq")
+    mark(3)
+    return dq, dk, dv
+
+
+def _fused_phases(q, k, v, o, do, lse, window, scale, dq, dk, dv, workspace, between):
+    import torch
+
+    lib = load()
+    B, Hq, Hkv, N, Lk, D = _dims(q, k)
+    if Lk != N:
+        raise ValueError("the phase entry points take equal query and key lengths")
+    sc = _scale(scale, D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, name, hs in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq),
+                        (dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
+        _check_tensor(t, name, (B, hs, N, D), torch.bfloat16)
+    _check_tensor(lse, "lse", (B, Hq, N), torch.float32)
+    n = int(lib.swa_attn_bwd_fused_workspace_bytes(B, Hq, N, D))
+    if workspace is None:
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    st = _stream_handle(q.device)
+    mark = between or (lambda i: None)
+    mark(0)
+    rc = lib.swa_attn_bwd_fused_preprocess(o.data_ptr(), do.data_ptr(), *ws, B, Hq, N, D, st)
+    if rc != 0:
+        raise SwaError(rc, "swa_attn_bwd_fused_preprocess")
+    mark(1)
+    rc = lib.swa_attn_bwd_fused_dkdv(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                                     lse.data_ptr(), dk.data_ptr(), dv.data_ptr(), *ws, B, Hq, Hkv,
+                                     N, D, int(window), sc, st)
+    if rc != 0:
+        raise SwaError(rc, "swa_attn_bwd_fused_dkdv")
+    mark(2)
+    rc = lib.swa_attn_bwd_fused_dq(dq.data_ptr(), *ws, B, Hq, N, D, sc, st)
+    if rc != 0:
+        raise SwaError(rc, "swa_attn_bwd_fused_dq")
     mark(3)
     return dq, dk, dv
 

@@ -240,6 +240,111 @@ swa_status swa_attn_bwd_dq(const void* q, const void* k, const void* v, const vo
                                                                                     : SWA_ERR_CUDA;
 }
 
+// ---- Fused backward: Delta and the zeroed dQ accumulator, one kernel for dK, dV and the dQ
+// partials, then dQ from the accumulator.  Workspace: Delta (256-byte rounded), then the
+// accumulator (D <= 128); D = 256 has no fused kernel and runs the split backward on Delta alone.
+
+size_t swa_attn_bwd_fused_workspace_bytes(int B, int Hq, int Lq, int D) {
+  if (B < 1 || Hq < 1 || Lq < 1 || (D != 64 && D != 128 && D != 256)) return 0;
+  const size_t delta = swa_attn_bwd_workspace_bytes(B, Hq, Lq, D);
+  return D == 256 ? delta : delta + swa::dq_acc_bytes(B, Hq, Lq, D);
+}
+
+swa_status swa_attn_bwd_fused(const void* q, const void* k, const void* v, const void* o,
+                              const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                              int B, int Hq, int Hkv, int Lq, int Lk, int D, int window,
+                              int causal, float scale, int f16, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return SWA_ERR_INVALID_ARG;
+  if ((causal != 0 && causal != 1) || (f16 != 0 && f16 != 1)) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_shape(B, Hq, Hkv, Lq, Lk, D, window, scale);
+  if (st != SWA_OK) return st;
+  if (!workspace || workspace_bytes < swa_attn_bwd_fused_workspace_bytes(B, Hq, Lq, D))
+    return SWA_ERR_WORKSPACE;
+  if (D == 256)
+    return swa_attn_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lk, D, window, causal,
+                           scale, f16, workspace, workspace_bytes, stream);
+  const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return SWA_ERR_MISALIGNED;
+  unsigned* err = nullptr;
+  if ((st = current_device(&err)) != SWA_OK) return st;
+  const swa::Problem pb = make_problem_ex(B, Hq, Hkv, Lq, Lk, D, window, causal, scale, err, f16);
+  float* delta = static_cast<float*>(workspace);
+  float* acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                        swa_attn_bwd_workspace_bytes(B, Hq, Lq, D));
+  if (swa::launch_bwd_delta_zero_acc(pb, o, dO, delta, acc, stream) != cudaSuccess ||
+      swa::launch_bwd_fused(pb, q, k, v, dO, lse, delta, acc, dk, dv, stream) != cudaSuccess ||
+      swa::launch_dq_from_acc(pb, acc, dq, stream) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  return SWA_OK;
+}
+
+namespace {
+
+// Shared checks of the fused backward's phase entry points (bf16, Lq = Lk = N, causal).
+swa_status fused_phase_setup(int B, int Hq, int Hkv, int N, int D, int window, float scale,
+                             const void* workspace, size_t workspace_bytes,
+                             std::initializer_list<const void*> ptrs, swa::Problem* pb,
+                             float** delta, float** acc) {
+  for (const void* p : ptrs)
+    if (!p) return SWA_ERR_INVALID_ARG;
+  swa_status st = check_sizes(B, Hq, Hkv, N, D, window, scale);
+  if (st != SWA_OK) return st;
+  if (D == 256) return SWA_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < swa_attn_bwd_fused_workspace_bytes(B, Hq, N, D))
+    return SWA_ERR_WORKSPACE;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return SWA_ERR_MISALIGNED;
+  if (!aligned16(workspace)) return SWA_ERR_MISALIGNED;
+  unsigned* err = nullptr;
+  if ((st = current_device(&err)) != SWA_OK) return st;
+  *pb = make_problem(B, Hq, Hkv, N, D, window, scale, err);
+  *delta = static_cast<float*>(const_cast<void*>(workspace));
+  *acc = reinterpret_cast<float*>(static_cast<uint8_t*>(const_cast<void*>(workspace)) +
+                                  swa_attn_bwd_workspace_bytes(B, Hq, N, D));
+  return SWA_OK;
+}
+
+}  // namespace
+
+swa_status swa_attn_bwd_fused_preprocess(const void* o, const void* dO, void* workspace,
+                                         size_t workspace_bytes, int B, int Hq, int N, int D,
+                                         cudaStream_t stream) {
+  swa::Problem pb;
+  float *delta = nullptr, *acc = nullptr;
+  swa_status st = fused_phase_setup(B, Hq, Hq, N, D, 1, 1.f, workspace, workspace_bytes, {o, dO},
+                                    &pb, &delta, &acc);
+  if (st != SWA_OK) return st;
+  return swa::launch_bwd_delta_zero_acc(pb, o, dO, delta, acc, stream) == cudaSuccess
+             ? SWA_OK
+             : SWA_ERR_CUDA;
+}
+
+swa_status swa_attn_bwd_fused_dkdv(const void* q, const void* k, const void* v, const void* dO,
+                                   const float* lse, void* dk, void* dv, void* workspace,
+                                   size_t workspace_bytes, int B, int Hq, int Hkv, int N, int D,
+                                   int window, float scale, cudaStream_t stream) {
+  swa::Problem pb;
+  float *delta = nullptr, *acc = nullptr;
+  swa_status st = fused_phase_setup(B, Hq, Hkv, N, D, window, scale, workspace, workspace_bytes,
+                                    {q, k, v, dO, lse, dk, dv}, &pb, &delta, &acc);
+  if (st != SWA_OK) return st;
+  return swa::launch_bwd_fused(pb, q, k, v, dO, lse, delta, acc, dk, dv, stream) == cudaSuccess
+             ? SWA_OK
+             : SWA_ERR_CUDA;
+}
+
+swa_status swa_attn_bwd_fused_dq(void* dq, const void* workspace, size_t workspace_bytes, int B,
+                                 int Hq, int N, int D, float scale, cudaStream_t stream) {
+  swa::Problem pb;
+  float *delta = nullptr, *acc = nullptr;
+  swa_status st = fused_phase_setup(B, Hq, Hq, N, D, 1, scale, workspace, workspace_bytes, {dq},
+                                    &pb, &delta, &acc);
+  if (st != SWA_OK) return st;
+  return swa::launch_dq_from_acc(pb, acc, dq, stream) == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
 const char* swa_strerror(swa_status status) {
   switch (status) {
     case SWA_OK: return "SWA_OK";

@@ -12,11 +12,14 @@
 namespace swa {
 namespace {
 
+// With dq_acc set (the fused backward), the grid also zeroes the acc_floats floats of the dQ
+// accumulator, with 16-byte stores in a grid-stride walk of its own.
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) swa_delta_kernel(const uint16_t* __restrict__ o,
                                                         const uint16_t* __restrict__ dO,
                                                         float* __restrict__ delta,
-                                                        long long rows) {
+                                                        long long rows, float* __restrict__ dq_acc,
+                                                        long long acc_floats) {
   constexpr int kLanesPerRow = D / 8;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const int lane = static_cast<int>(threadIdx.x & 31);
@@ -46,12 +49,22 @@ __global__ void __launch_bounds__(256) swa_delta_kernel(const uint16_t* __restri
       acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (sub == 0 && row < rows) delta[row] = acc;
   }
+  if (dq_acc != nullptr) {
+    const long long n4 = acc_floats / 4;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; u < n4;
+         u += stride)
+      reinterpret_cast<float4*>(dq_acc)[u] = z;
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_delta(const Problem& pb, const void* o, const void* dO, float* delta,
-                             cudaStream_t stream) {
+namespace {
+
+cudaError_t delta_impl(const Problem& pb, const void* o, const void* dO, float* delta,
+                       float* dq_acc, cudaStream_t stream) {
   const long long rows = static_cast<long long>(pb.B) * pb.Hq * pb.span.Lq;
   constexpr int kThreads = 256;
   const long long rows_per_block = (kThreads / 32) * (32 / (pb.D / 8));
@@ -61,21 +74,36 @@ cudaError_t launch_bwd_delta(const Problem& pb, const void* o, const void* dO, f
   const auto* po = static_cast<const uint16_t*>(o);
   const auto* pd = static_cast<const uint16_t*>(dO);
   const dim3 grid(static_cast<unsigned>(blocks));
+  const long long acc_floats =
+      dq_acc != nullptr ? static_cast<long long>(dq_acc_bytes(pb.B, pb.Hq, pb.span.Lq, pb.D) / 4) : 0;
   if (pb.D == 64 && !pb.f16)
-    swa_delta_kernel<64, false><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
+    swa_delta_kernel<64, false><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows, dq_acc, acc_floats);
   else if (pb.D == 64)
-    swa_delta_kernel<64, true><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
+    swa_delta_kernel<64, true><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows, dq_acc, acc_floats);
   else if (pb.D == 128 && !pb.f16)
-    swa_delta_kernel<128, false><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
+    swa_delta_kernel<128, false><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows, dq_acc, acc_floats);
   else if (pb.D == 128)
-    swa_delta_kernel<128, true><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
-  else if (pb.D == 256 && !pb.f16)
-    swa_delta_kernel<256, false><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
-  else if (pb.D == 256)
-    swa_delta_kernel<256, true><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows);
+    swa_delta_kernel<128, true><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows, dq_acc, acc_floats);
+  else if (pb.D == 256 && !pb.f16 && dq_acc == nullptr)
+    swa_delta_kernel<256, false><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows, nullptr, 0);
+  else if (pb.D == 256 && dq_acc == nullptr)
+    swa_delta_kernel<256, true><<<grid, kThreads, 0, stream>>>(po, pd, delta, rows, nullptr, 0);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_delta(const Problem& pb, const void* o, const void* dO, float* delta,
+                             cudaStream_t stream) {
+  return delta_impl(pb, o, dO, delta, nullptr, stream);
+}
+
+cudaError_t launch_bwd_delta_zero_acc(const Problem& pb, const void* o, const void* dO,
+                                      float* delta, float* dq_acc, cudaStream_t stream) {
+  if (dq_acc == nullptr) return cudaErrorInvalidValue;
+  return delta_impl(pb, o, dO, delta, dq_acc, stream);
 }
 
 }  // namespace swa

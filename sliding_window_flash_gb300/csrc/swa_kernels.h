@@ -94,6 +94,30 @@ cudaError_t launch_bwd_dq(const Problem& pb, const void* q, const void* k, const
                           const void* dO, const float* lse, const float* delta, void* dq,
                           cudaStream_t stream);
 
+// Fused backward (swa_bwd_fused.cu): dK, dV and the dQ partials of every (key block, query tile)
+// pair in one kernel.  dQ accumulates in fp32, tile-major: block (bhq, qb) holds query rows
+// [128 qb, 128 qb + 128) of plane bhq, as groups of 4 head-dimension columns: column c of block
+// row r sits at (c / 4) * 512 + r * 4 + c % 4, so the 4 columns of 32 consecutive rows (one warp's
+// vector reduce-add) are 512 contiguous bytes.  Offsets in floats.
+__host__ __device__ inline size_t dq_acc_offset(int bhq, int qb, int row, int col, int nqb, int D) {
+  return (static_cast<size_t>(bhq) * nqb + qb) * (static_cast<size_t>(kBlockM) * D) +
+         static_cast<size_t>(col / 4) * (kBlockM * 4) + row * 4 + col % 4;
+}
+// Bytes of the accumulator for B x Hq planes of Lq query rows.
+inline size_t dq_acc_bytes(int B, int Hq, int Lq, int D) {
+  const size_t nqb = static_cast<size_t>((Lq + kBlockM - 1) / kBlockM);
+  return static_cast<size_t>(B) * Hq * nqb * kBlockM * D * sizeof(float);
+}
+cudaError_t launch_bwd_fused(const Problem& pb, const void* q, const void* k, const void* v,
+                             const void* dO, const float* lse, const float* delta, float* dq_acc,
+                             void* dk, void* dv, cudaStream_t stream);
+// Delta as launch_bwd_delta, also zeroing the whole accumulator.
+cudaError_t launch_bwd_delta_zero_acc(const Problem& pb, const void* o, const void* dO,
+                                      float* delta, float* dq_acc, cudaStream_t stream);
+// dq = scale * accumulator, rounded to the element type (rows [0, Lq) of every plane).
+cudaError_t launch_dq_from_acc(const Problem& pb, const float* dq_acc, void* dq,
+                               cudaStream_t stream);
+
 // Head dimension 256 (swa_d256.cu): the same operations with half-tile streaming; dK and dV come
 // from two kernels.  launch_fwd / launch_bwd_dq / launch_bwd_dkdv dispatch here for D = 256.
 cudaError_t launch_fwd_d256(const Problem& pb, const void* q, const void* k, const void* v,

@@ -147,6 +147,14 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// dst[0..3] += {a, b, c, d} in fp32, performed at the L2 (relaxed, no return value); dst 16-byte
+// aligned.
+__device__ __forceinline__ void red_add_v4_f32(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 // ------------------------------------------------------------------------------------------------
 // tcgen05: TMEM allocation
 // ------------------------------------------------------------------------------------------------
@@ -344,6 +352,63 @@ __device__ __forceinline__ void umma_ts_mnmajor_x8_split(uint32_t d_tmem, uint32
       "add.u32 ra, %1, 88;\n\tadd.s64 rb, %2, 896;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
       "}" ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 8 MMAs along K = 128 with A K-major (128B-swizzled, two 64-column chunks 16 KB apart: K-step ks
+// at 32 (ks % 4) bytes inside chunk ks / 4) and B MN-major (one 128-byte row per K index, so K-step
+// ks starts 2048 bytes further).  Both operands in shared memory.
+__device__ __forceinline__ void umma_ss_kA_mnB_x8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b64 ra, rb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %3, %3;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 128;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 256;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 384;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 1024;\n\tadd.s64 rb, %2, 512;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 1026;\n\tadd.s64 rb, %2, 640;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 1028;\n\tadd.s64 rb, %2, 768;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 1030;\n\tadd.s64 rb, %2, 896;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "}" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 8 MMAs along K = 128 with A and B both MN-major in shared memory (one 128-byte row per K index:
+// K-step ks starts 2048 bytes further in both).
+__device__ __forceinline__ void umma_ss_mnA_mnB_x8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b64 ra, rb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %3, %3;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "add.s64 ra, %1, 128;\n\tadd.s64 rb, %2, 128;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 256;\n\tadd.s64 rb, %2, 256;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 384;\n\tadd.s64 rb, %2, 384;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 512;\n\tadd.s64 rb, %2, 512;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 640;\n\tadd.s64 rb, %2, 640;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 768;\n\tadd.s64 rb, %2, 768;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "add.s64 ra, %1, 896;\n\tadd.s64 rb, %2, 896;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+      "}" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 

@@ -1,6 +1,9 @@
-"""GPU: results are deterministic.  No kernel uses atomics; dK / dV sum the query heads of a group
-in a fixed order in TMEM, and dQ accumulates its key blocks in a fixed order, so repeated calls on
-the same inputs are bit-identical — on the long layer, at D = 256, and for fp16."""
+"""GPU: the split backward is deterministic.  Its kernels use no atomics; dK / dV sum the query
+heads of a group in a fixed order in TMEM, and dQ accumulates its key blocks in a fixed order, so
+repeated calls on the same inputs are bit-identical — on the long layer, at D = 256, and for fp16.
+The fused backward adds dQ's partials in fp32 in whatever order the key blocks finish: its dK and
+dV are still bit-identical (to each other across runs and to the split path's), its dQ agrees with
+the split path's to within a few bf16 units."""
 import dataclasses
 
 import pytest
@@ -11,10 +14,10 @@ import swa_inputs as si
 pytestmark = pytest.mark.gpu
 
 
-def _run(swa, g, case):
+def _run(swa, g, case, fused=False):
     o, lse = swa.swa_attn_fwd(g["q"], g["k"], g["v"], case.W, case.softmax_scale)
     dq, dk, dv = swa.swa_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, case.W,
-                                  case.softmax_scale)
+                                  case.softmax_scale, fused=fused)
     return [t.clone() for t in (o, lse, dq, dk, dv)]
 
 
@@ -29,4 +32,21 @@ def test_repeated_calls_are_bit_identical(swa, D, dtype, reps):
         again = _run(swa, g, case)
         for a, b in zip(first, again):
             assert torch.equal(a, b)
+    swa.swa_check_device()
+
+
+@pytest.mark.parametrize("D,dtype", [(128, torch.bfloat16), (64, torch.bfloat16),
+                                     (128, torch.float16)])
+def test_fused_dkdv_exact_dq_close(swa, D, dtype):
+    dev = torch.device("cuda:0")
+    case = dataclasses.replace(si.long_swa_case(8192), D=D)
+    g = si.make_inputs(case, device=str(dev), dtype=dtype)
+    split = _run(swa, g, case, fused=False)
+    for _ in range(2):
+        fused = _run(swa, g, case, fused=True)
+        for a, b in zip(split[:2] + split[3:], fused[:2] + fused[3:]):  # o, lse, dk, dv
+            assert torch.equal(a, b)
+        dq_s, dq_f = split[2].float(), fused[2].float()
+        rel = (torch.linalg.vector_norm(dq_f - dq_s) / torch.linalg.vector_norm(dq_s)).item()
+        assert rel <= 2e-3, rel
     swa.swa_check_device()

@@ -19,7 +19,7 @@ from oracle import swa_oracle as orc
 pytestmark = pytest.mark.gpu
 
 
-def _gpu(swa, case, poison=False):
+def _gpu(swa, case, poison=False, fused=False):
     dev = torch.device("cuda:0")
     inp = si.make_inputs(case)
     g = {k: v.to(dev) for k, v in inp.items()}
@@ -31,7 +31,7 @@ def _gpu(swa, case, poison=False):
             t.fill_(float("nan"))
     swa.swa_attn_fwd(g["q"], g["k"], g["v"], case.W, case.softmax_scale, out=o, lse=lse)
     swa.swa_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, case.W, case.softmax_scale,
-                     dq=dq, dk=dk, dv=dv)
+                     dq=dq, dk=dk, dv=dv, fused=fused)
     swa.swa_check_device()
     return inp, {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
 
@@ -60,8 +60,8 @@ def test_window_one(swa, N, D, G):
 def test_window_at_least_length_is_causal(swa, N):
     a_case = si.Case(B=1, Hq=4, Hkv=2, N=N, D=128, W=N, seed=12)
     b_case = si.Case(B=1, Hq=4, Hkv=2, N=N, D=128, W=10 * N, seed=12)
-    _, a = _gpu(swa, a_case)
-    _, b = _gpu(swa, b_case)
+    _, a = _gpu(swa, a_case, fused=False)  # the split path: bit-reproducible
+    _, b = _gpu(swa, b_case, fused=False)
     for key in a:
         assert torch.equal(a[key], b[key]), key
 
@@ -95,8 +95,11 @@ def test_last_key_block_gradients(swa):
     (64, torch.bfloat16, 1, 500, 3, True),
     (128, torch.float16, 129, 129, 1, False),
     (256, torch.float32, 257, 257, 300, False),
+    (128, torch.bfloat16, 100, 700, 30, True),   # the same, D = 128 (fused and split below)
+    (64, torch.float16, 300, 300, 7, False),
 ])
-def test_every_output_written_on_every_path(swa, D, dtype, Lq, Lk, W, causal):
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "split"])
+def test_every_output_written_on_every_path(swa, D, dtype, Lq, Lk, W, causal, fused):
     """Outputs pre-filled with NaN come back finite for every head dim, element type, query
     offset and window kind (key blocks that no query sees must be written as zeros)."""
     dev = torch.device("cuda:0")
@@ -111,7 +114,7 @@ def test_every_output_written_on_every_path(swa, D, dtype, Lq, Lk, W, causal):
     swa.swa_attn_fwd(g["q"], g["k"], g["v"], W, case.softmax_scale, out=o, lse=lse,
                      causal=causal)
     swa.swa_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, W, case.softmax_scale, dq=dq,
-                     dk=dk, dv=dv, causal=causal)
+                     dk=dk, dv=dv, causal=causal, fused=fused)
     swa.swa_check_device()
     for name, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
         assert torch.isfinite(t.float()).all(), name

@@ -42,7 +42,8 @@ def test_noalloc_matches_workspace_backward(swa, case):
     for c in (case, other, case):
         g = {k: v.to(dev) for k, v in si.make_inputs(c).items()}
         o, lse = swa.swa_attn_fwd(g["q"], g["k"], g["v"], c.W, c.softmax_scale)
-        ref = swa.swa_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, c.W, c.softmax_scale)
+        ref = swa.swa_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, c.W, c.softmax_scale,
+                               fused=False)
         for _ in range(2):
             got = _noalloc_bwd(lib, g, o, lse, c, stream)
             swa.swa_check_device()
