@@ -658,6 +658,7 @@ def measure_memory(swa, device, D: int = 128, fused: bool = False) -> dict:
         case = dataclasses.replace(si.long_swa_case(N), D=D)
         torch.cuda.synchronize(device)
         torch.cuda.empty_cache()
+        before = torch.cuda.memory_allocated(device)  # what the process holds besides this layer
         inp = si.make_inputs(case, device=str(device))
         torch.cuda.synchronize(device)
         torch.cuda.reset_peak_memory_stats(device)
@@ -685,7 +686,7 @@ def measure_memory(swa, device, D: int = 128, fused: bool = False) -> dict:
         out.setdefault("fwd_bwd_ms", []).append(ms)
         out.setdefault("fwd_bwd_tflops", []).append((fl["fwd"] + fl["bwd"]) / (ms * 1e-3) / 1e12)
         out["N"].append(N)
-        out["peak_gb_total"].append(peak / 1e9)
+        out["peak_gb_total"].append((peak - before) / 1e9)  # the layer's inputs + fwd + bwd
         out["peak_gb_above_inputs"].append((peak - base) / 1e9)
         del inp, o, lse, dq, dk, dv, ws
     a = out["peak_gb_above_inputs"]

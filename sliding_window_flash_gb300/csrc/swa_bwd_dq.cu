@@ -313,15 +313,33 @@ __global__ void __launch_bounds__(352, 1)
     bool prev_in = false;
     int g = 0;  // key blocks consumed so far by this CTA
     bool ok = true;
+    // LSE and Delta of this thread's row in the next tile, loaded a whole tile ahead so that
+    // the loads' latency hides behind the current tile.  Rows past the end see P = 0 (their LSE
+    // is taken as +inf), so they add nothing.
+    float nxt_lse = SWA_POS_INF, nxt_dlt = 0.f;
+    auto fetch_rows = [&](int tn) {
+      if (tn >= a.ntiles) return;
+      const DqTile fn = dq_tile(tn, a, sp);
+      const int rn = fn.q0 + r;
+      if (rn < sp.Lq) {
+        const size_t gn = static_cast<size_t>(fn.bh) * sp.Lq + rn;
+        nxt_lse = a.lse[gn];
+        nxt_dlt = a.delta[gn];
+      } else {
+        nxt_lse = SWA_POS_INF;
+        nxt_dlt = 0.f;
+      }
+    };
+    fetch_rows(static_cast<int>(blockIdx.x));
     for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
       const DqTile f = dq_tile(t, a, sp);
       const int q0 = f.q0;
       const int row = q0 + r;
       const bool in_range = row < sp.Lq;
       const size_t grow = static_cast<size_t>(f.bh) * sp.Lq + row;
-      // Rows past the end see P = 0 (their LSE is taken as +inf), so they add nothing.
-      const float lse2 = in_range ? a.lse[grow] * kLog2e : SWA_POS_INF;
-      const float dlt = in_range ? a.delta[grow] : 0.f;
+      const float lse2 = nxt_lse == SWA_POS_INF ? SWA_POS_INF : nxt_lse * kLog2e;
+      const float dlt = nxt_dlt;
+      fetch_rows(t + tile_step);
       for (int j = 0; j < f.nkv; ++j) {
         const int gg = g + j;
         const int k0 = (f.kb_lo + j) * kBlockN;

@@ -121,8 +121,8 @@ def test_fused_workspace_too_small_is_refused(swa):
     n = swa.swa_attn_bwd_fused_workspace_bytes(case.B, case.Hq, case.N, case.D)
     ws = torch.empty(n, dtype=torch.uint8, device=dev)
     swa.swa_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, case.W, case.softmax_scale,
-                     workspace=ws)
+                     workspace=ws, fused=True)
     with pytest.raises(swa.SwaError):
         swa.swa_attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, case.W, case.softmax_scale,
-                         workspace=ws[:n - 16])
+                         workspace=ws[:n - 16], fused=True)
     swa.swa_check_device()
