@@ -29,13 +29,17 @@
 //              from two warps because one warp's TMA copies complete at only ~40 B/clk on this
 //              GPU, less than one key block (64 KB of K and V) per MMA period needs.
 //   warp 9     MMA issuer and TMEM owner (converged warp, one elected lane issues): S_j = Q K_j^T
-//              into one of two TMEM S buffers; O += P_j V_j with P_j read from TMEM (A operand).
-//              S_{j+1} is issued before O += P_j V_j so the tensor core computes the next scores
-//              while the softmax warps work on this block.  tcgen05.mma operations of one thread
-//              run in issue order, which orders every TMEM reuse below.
+//              into one of kSBufs TMEM S buffers; O += P_j V_j with P_j read from TMEM (A operand).
+//              The S products run kSBufs blocks ahead of the P V products, across tiles, so the
+//              tensor core computes the next scores while the softmax warps work on this block.
+//              tcgen05.mma operations of one thread run in issue order, which orders every TMEM
+//              reuse below.
 //   warp 10    output: one TMA tensor store per staged O tile, then frees that Q buffer.
-// TMEM columns: [0,128) S buffer 0, [128,256) S buffer 1, [256, 256+D) O, then two 64-column
-// P buffers (128 bf16 per row, two per column).
+// TMEM columns: D = 64: three S buffers at [0,384), P_j over the first 32 of each half-row's 64
+// columns of its S buffer, O at [384,448).  D = 128: two S buffers at [0,256), O at [256,384), two
+// 64-column P buffers at [384,512).
+// D = 128 with an even number of query heads per kv head runs on CTA pairs instead
+// (swa_fwd_pair.cu).
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 #include "swa_tmap.h"
@@ -69,10 +73,17 @@ struct FwdCfg {
   static constexpr int kKEmpty = kKFull + kKStages;
   static constexpr int kVFull = kKEmpty + kKStages;
   static constexpr int kVEmpty = kVFull + kVStages;
-  static constexpr int kSFull = kVEmpty + kVStages;  // 2
-  static constexpr int kPFull = kSFull + 2;          // 2
-  static constexpr int kPVDone = kPFull + 2;         // 2
-  static constexpr int kXch = kPVDone + 2;           // [4 lane quarters][2 slots]
+  // S buffers in TMEM: the S products run kSBufs blocks ahead of the P V products, which the K
+  // ring must keep fed (a K tile lands ~2,400 cycles after its copy is issued, longer than one
+  // block's softmax).  D = 64 (four K stages): three buffers, P written over S.  D = 128 (three K
+  // stages): two S buffers and two P buffers of their own (P over S with two buffers measured
+  // slower).
+  static constexpr bool kPOverS = (D == 64);
+  static constexpr int kSBufs = kPOverS ? 3 : 2;
+  static constexpr int kSFull = kVEmpty + kVStages;  // kSBufs
+  static constexpr int kPFull = kSFull + kSBufs;     // kSBufs
+  static constexpr int kPVDone = kPFull + kSBufs;    // kSBufs
+  static constexpr int kXch = kPVDone + kSBufs;      // [4 lane quarters][2 slots]
   static constexpr int kOEmpty = kXch + 8;           // the O accumulator has been read
   static constexpr int kOutFull = kOEmpty + 1;       // 2: staged O tile complete, per Q buffer
   static constexpr int kDrain = kOutFull + 2;
@@ -80,9 +91,11 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;  // + TMEM address and abort flag
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;  // buffer b at kColS + 128 b
-  static constexpr uint32_t kColO = 256;
-  static constexpr uint32_t kColP = 256 + D;  // buffer b at kColP + 64 b
+  // Buffer b at kColS + 128 b holds S_g (fp32) for blocks g = b mod kSBufs; P_g (bf16 pairs) goes
+  // over the first 32 of each half-row's 64 columns (kPOverS) or into P buffer g & 1 at kColP.
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColO = 128 * kSBufs;
+  static constexpr uint32_t kColP = kColO + D;  // two 64-column buffers (D = 128 only)
   static constexpr int kThreads = 384;
   static constexpr int kComputeThreads = 256;
 };
@@ -138,10 +151,12 @@ __global__ void __launch_bounds__(384, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::kQFull + b), 1);
       mbar_init(bar(C::kQEmpty + b), 1);
+      mbar_init(bar(C::kOutFull + b), C::kComputeThreads / 32);
+    }
+    for (int b = 0; b < C::kSBufs; ++b) {
       mbar_init(bar(C::kSFull + b), 1);
       mbar_init(bar(C::kPFull + b), C::kComputeThreads / 32);
       mbar_init(bar(C::kPVDone + b), 1);
-      mbar_init(bar(C::kOutFull + b), C::kComputeThreads / 32);
     }
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bar(C::kKFull + s), 1);
@@ -235,10 +250,11 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockM, kBlockN, false, false);
     constexpr uint32_t kIdO = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockM, D, false, true);
-    // S_gg = Q K_gg^T into S buffer gg & 1.  That buffer was last read by the softmax warps for
-    // block gg - 2, whose P_FULL the P V of gg - 2 (issued earlier) already waited for.
+    // S_gg = Q K_gg^T into buffer gg mod kSBufs.  The buffer last held P_{gg-kSBufs}, which the P V
+    // of that block, issued before this, reads: tcgen05.mma operations of one thread run in issue
+    // order.
     auto issue_s = [&](int gg, uint32_t sQ) -> bool {
-      const int s = gg % C::kKStages, n = gg / C::kKStages, sb = gg & 1;
+      const int s = gg % C::kKStages, n = gg / C::kKStages, sb = gg % C::kSBufs;
       if (!warp_wait(bar(C::kKFull + s), n & 1, &abort_flag, a.err)) return false;
       tc_fence_after();
       umma_ss_kmajor_d<D>(tmem + C::kColS + 128u * sb, smem_desc_sw128(sQ, 16, 1024),
@@ -247,31 +263,62 @@ __global__ void __launch_bounds__(384, 1)
       umma_commit_w(bar(C::kKEmpty + s));
       return true;
     };
+    // O += P_gg V_gg.  P over S: keys 16 ks .. 16 ks + 15 at packed column 8 ks + 32 (ks / 4) of
+    // buffer gg mod kSBufs (each half-row's P over the first 32 of its 64 columns); else at column
+    // 8 ks of P buffer gg & 1.
     auto issue_pv = [&](int gg, bool first) -> bool {
-      const int s = gg % C::kVStages, n = gg / C::kVStages, pb = gg & 1;
-      if (!warp_wait(bar(C::kPFull + pb), (gg >> 1) & 1, &abort_flag, a.err)) return false;
+      const int s = gg % C::kVStages, n = gg / C::kVStages, pb = gg % C::kSBufs;
+      if (!warp_wait(bar(C::kPFull + pb), (gg / C::kSBufs) & 1, &abort_flag, a.err)) return false;
       if (!warp_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
       tc_fence_after();
-      umma_ts_mnmajor_x8(tmem + C::kColO, tmem + C::kColP + 64u * pb,
-                         smem_desc_sw128(sV0 + s * C::kTileBytes, C::kChunkBytes, 1024), kIdO,
-                         first ? 0u : 1u);
+      const uint64_t vdesc = smem_desc_sw128(sV0 + s * C::kTileBytes, C::kChunkBytes, 1024);
+      if constexpr (C::kPOverS)
+        umma_ts_mnmajor_x8_split(tmem + C::kColO, tmem + C::kColS + 128u * pb, vdesc, kIdO,
+                                 first ? 0u : 1u);
+      else
+        umma_ts_mnmajor_x8(tmem + C::kColO, tmem + C::kColP + 64u * pb, vdesc, kIdO,
+                           first ? 0u : 1u);
       umma_commit_w(bar(C::kPVDone + pb));
       umma_commit_w(bar(C::kVEmpty + s));
       return true;
     };
-    int g = 0;  // key blocks issued so far by this CTA
-    bool ok = true;
+    // The S products run up to kSBufs blocks ahead of the P V products over the CTA's whole walk
+    // (across tiles): S of block gg + kSBufs is issued right after P_gg V_gg, so the softmax warps do
+    // not wait for scores, and no extra barrier is needed.  S of a tile may be issued only once
+    // every P V of the tile two before it has been: its Q buffer is that tile's output staging
+    // area, refilled after the store.
+    int s_t = static_cast<int>(blockIdx.x), s_it = 0, s_j = 0, s_g = 0;
+    FwdTile s_f = fwd_tile(s_t < a.ntiles ? s_t : 0, a, sp);
+    auto issue_next_s = [&]() -> bool {
+      if (s_t >= a.ntiles) return true;
+      if (s_j == 0 &&
+          !warp_wait(bar(C::kQFull + (s_it & 1)), (s_it >> 1) & 1, &abort_flag, a.err))
+        return false;
+      if (!issue_s(s_g, sQ0 + (s_it & 1) * C::kTileBytes)) return false;
+      ++s_g;
+      if (++s_j == s_f.nkv) {
+        s_j = 0;
+        s_t += tile_step;
+        ++s_it;
+        if (s_t < a.ntiles) s_f = fwd_tile(s_t, a, sp);
+      }
+      return true;
+    };
+    // Issues S up to (excluding) block s_limit, for tiles below tiles_done + 2.
+    auto fill_s = [&](int s_limit, int tiles_done) -> bool {
+      while (s_t < a.ntiles && s_g < s_limit && s_it < tiles_done + 2)
+        if (!issue_next_s()) return false;
+      return true;
+    };
+    bool ok = fill_s(C::kSBufs, 0);
+    int g = 0;  // key blocks whose P V has been issued
     for (int t = blockIdx.x, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
       const FwdTile f = fwd_tile(t, a, sp);
-      const uint32_t sQ = sQ0 + (it & 1) * C::kTileBytes;
-      ok = warp_wait(bar(C::kQFull + (it & 1)), (it >> 1) & 1, &abort_flag, a.err);
-      if (ok) ok = issue_s(g, sQ);
       for (int j = 0; ok && j < f.nkv; ++j) {
-        if (j + 1 < f.nkv) ok = issue_s(g + j + 1, sQ);
         // The first P V of a tile overwrites O: the previous tile's epilogue must have read it.
-        if (ok && j == 0 && it > 0)
-          ok = warp_wait(bar(C::kOEmpty), (it - 1) & 1, &abort_flag, a.err);
+        if (j == 0 && it > 0) ok = warp_wait(bar(C::kOEmpty), (it - 1) & 1, &abort_flag, a.err);
         if (ok) ok = issue_pv(g + j, j == 0);
+        if (ok) ok = fill_s(g + j + 1 + C::kSBufs, it + (j + 1 == f.nkv ? 1 : 0));
       }
       g += f.nkv;
     }
@@ -327,8 +374,8 @@ __global__ void __launch_bounds__(384, 1)
       for (int j = 0; j < f.nkv; ++j) {
         const int gg = g + j;
         const int k0 = (f.kb_lo + j) * kBlockN;
-        const int sb = gg & 1;
-        if (!(ok = warp_wait(bar(C::kSFull + sb), (gg >> 1) & 1, &abort_flag, a.err))) break;
+        const int sb = gg % C::kSBufs;
+        if (!(ok = warp_wait(bar(C::kSFull + sb), (gg / C::kSBufs) & 1, &abort_flag, a.err))) break;
         tc_fence_after();
         float x[64];  // raw scores S (the scale is applied inside the exponent below)
         {
@@ -407,15 +454,17 @@ __global__ void __launch_bounds__(384, 1)
         }
         l += bsum;
 
-        // P buffer (gg & 1) was last read by the P V of block gg - 2.
-        if (gg >= 2 &&
-            !(ok = warp_wait(bar(C::kPVDone + sb), ((gg - 2) >> 1) & 1, &abort_flag, a.err)))
-          break;
+        // A P buffer of its own was last read by the P V of block gg - 2.
+        if constexpr (!C::kPOverS) {
+          if (gg >= 2 &&
+              !(ok = warp_wait(bar(C::kPVDone + sb), ((gg - 2) >> 1) & 1, &abort_flag, a.err)))
+            break;
+        }
         // Rescaling O needs this tile's P V of block gg - 1 (and so every earlier one) to have
         // landed; a tile's first block needs none (its P V overwrites O).
         if (j >= 1 && __any_sync(0xffffffffu, resc)) {
-          if (!(ok = warp_wait(bar(C::kPVDone + (sb ^ 1)), ((gg - 1) >> 1) & 1, &abort_flag,
-                               a.err)))
+          if (!(ok = warp_wait(bar(C::kPVDone + (gg - 1) % C::kSBufs), ((gg - 1) / C::kSBufs) & 1,
+                               &abort_flag, a.err)))
             break;
           tc_fence_after();
 #pragma unroll
@@ -431,8 +480,12 @@ __global__ void __launch_bounds__(384, 1)
         } else {
           tc_fence_after();
         }
-        // keys [64h, 64h+64) -> packed P columns [32h, 32h+32)
-        tmem_st32(tmem + lane_base + C::kColP + 64u * sb + 32u * h, pk);
+        // keys [64h, 64h+64) -> packed P over the first 32 of the 64 S columns this thread read, or
+        // columns [32h, 32h+32) of P buffer gg & 1
+        if constexpr (C::kPOverS)
+          tmem_st32(tmem + lane_base + C::kColS + 128u * sb + 64u * h, pk);
+        else
+          tmem_st32(tmem + lane_base + C::kColP + 64u * sb + 32u * h, pk);
         tmem_wait_st();
         warp_arrive(bar(C::kPFull + sb));
       }
@@ -443,7 +496,8 @@ __global__ void __launch_bounds__(384, 1)
       float l_other = 0.f;
       if (!(ok = exchange(l, &l_other))) break;
       const int last = g - 1;
-      if (!(ok = warp_wait(bar(C::kPVDone + (last & 1)), (last >> 1) & 1, &abort_flag, a.err)))
+      if (!(ok = warp_wait(bar(C::kPVDone + last % C::kSBufs), (last / C::kSBufs) & 1, &abort_flag,
+                           a.err)))
         break;
       tc_fence_after();
       constexpr int kHalf = D / 2;
@@ -523,6 +577,7 @@ cudaError_t launch_fwd_d(const Problem& pb, const void* q, const void* k, const 
 cudaError_t launch_fwd(const Problem& pb, const void* q, const void* k, const void* v, void* o,
                        float* lse, cudaStream_t stream) {
   if (pb.D == 256) return launch_fwd_d256(pb, q, k, v, o, lse, stream);
+  if (fwd_pair_applies(pb)) return launch_fwd_pair(pb, q, k, v, o, lse, stream);
   if (pb.D == 64)
     return pb.f16 ? launch_fwd_d<64, true>(pb, q, k, v, o, lse, stream)
                   : launch_fwd_d<64, false>(pb, q, k, v, o, lse, stream);

@@ -85,6 +85,11 @@ inline int sm_count() {
 // Launchers (each returns the launch's cudaError_t).
 cudaError_t launch_fwd(const Problem& pb, const void* q, const void* k, const void* v, void* o,
                        float* lse, cudaStream_t stream);
+// Forward on CTA pairs (swa_fwd_pair.cu): D = 128 with an even number of query heads per kv
+// head; launch_fwd dispatches there when it applies.
+bool fwd_pair_applies(const Problem& pb);
+cudaError_t launch_fwd_pair(const Problem& pb, const void* q, const void* k, const void* v,
+                            void* o, float* lse, cudaStream_t stream);
 cudaError_t launch_bwd_delta(const Problem& pb, const void* o, const void* dO, float* delta,
                              cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const Problem& pb, const void* q, const void* k, const void* v,

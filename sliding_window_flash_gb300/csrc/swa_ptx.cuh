@@ -462,6 +462,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// 32 lanes x 16 columns.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      SWA_W8(0), SWA_W8(8)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -569,6 +578,224 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   const bool ok = mbar_wait_slow(bar, parity, abort_flag, err);
   return __all_sync(0xffffffffu, ok);
+}
+
+// ------------------------------------------------------------------------------------------------
+// CTA pairs (cluster of two CTAs on one TPC sharing tcgen05.mma.cta_group::2 operations)
+// ------------------------------------------------------------------------------------------------
+// An M = 256 pair MMA issued by rank 0 computes rows [0, 128) into rank 0's TMEM and rows
+// [128, 256) into rank 1's, each from its own CTA's A operand (shared memory or TMEM, at the same
+// address in both); B's N columns are split between the pair, [0, N/2) in rank 0's shared memory
+// and [N/2, N) in rank 1's, at the same address.  A kernel that uses pairs uses cta_group::2 for
+// every tcgen05 allocation, MMA and commit.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs; orders each CTA's prior shared-memory writes (barrier inits
+// included) before the other's later accesses.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address, in the cluster window, of the same shared-memory offset in rank 0 of the pair.
+__device__ __forceinline__ uint32_t mapa_rank0(uint32_t saddr) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(saddr));
+  return r;
+}
+
+// Arrive on a barrier given by its cluster-window address (default semantics: the data handed
+// over is TMEM, ordered by the tcgen05 fences around the arrive and the wait, or shared memory
+// written by TMA and read by the tensor core).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// mbar_wait_slow with acquire at cluster scope (barriers that the other CTA of a pair arrives on).
+static __device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity,
+                                                           volatile int* abort_flag,
+                                                           unsigned* err_word) {
+  const long long t0 = clock64();
+  for (unsigned it = 0; it < kWaitPollLimit; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 15u) == 0u) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kWaitCycleLimit) break;
+    }
+  }
+  *abort_flag = 1;
+  atomicOr(err_word, kErrWaitTimeout);
+  return false;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, unsigned* err_word) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  return mbar_wait_cluster_slow(bar, parity, abort_flag, err_word);
+}
+
+__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, unsigned* err) {
+  if (__all_sync(0xffffffffu, mbar_try_wait_cluster(bar, parity))) return true;
+  const bool ok = mbar_wait_cluster_slow(bar, parity, abort_flag, err);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// warp_arrive on the barrier at the same offset in rank 0 of the pair.
+__device__ __forceinline__ void warp_arrive_rank0(uint32_t bar) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31u) == 0u) mbar_arrive_cluster(mapa_rank0(bar));
+}
+
+// One warp in each CTA of the pair, collectively: both receive the same TMEM address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Arrives once on the barrier at offset `bar` in both CTAs of the pair when every tcgen05
+// operation issued so far by the issuing thread has completed.
+__device__ __forceinline__ void umma2_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(bar),
+      "h"(static_cast<unsigned short>(3))
+      : "memory");
+}
+
+// Pair MMAs along K over the head dimension D (64 or 128): A and B K-major, 128B-swizzled.  A is
+// each CTA's 128-row tile (64-column chunks 16 KB apart), B each CTA's 64-row half (chunks 8 KB
+// apart).  K-step ks starts 32 bytes further inside a chunk; every fourth step moves to the next.
+template <int D>
+__device__ __forceinline__ void umma2_ss_kmajor_d(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  static_assert(D == 64 || D == 128, "head dim");
+  if constexpr (D == 128) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 ra, rb;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, %3, %3;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 2;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], ra, rb, %3, t;\n\t"
+        "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 4;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], ra, rb, %3, t;\n\t"
+        "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 6;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], ra, rb, %3, t;\n\t"
+        "add.s64 ra, %1, 1024;\n\tadd.s64 rb, %2, 512;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], ra, rb, %3, t;\n\t"
+        "add.s64 ra, %1, 1026;\n\tadd.s64 rb, %2, 514;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], ra, rb, %3, t;\n\t"
+        "add.s64 ra, %1, 1028;\n\tadd.s64 rb, %2, 516;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], ra, rb, %3, t;\n\t"
+        "add.s64 ra, %1, 1030;\n\tadd.s64 rb, %2, 518;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], ra, rb, %3, t;\n\t"
+        "}" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 ra, rb;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, %3, %3;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 2;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], ra, rb, %3, t;\n\t"
+        "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 4;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], ra, rb, %3, t;\n\t"
+        "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 6;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], ra, rb, %3, t;\n\t"
+        "}" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+
+// umma2_ts_mnmajor_x8 with A's K-step ks at column 8 ks + 32 (ks / 4): two 32-column halves 64
+// columns apart.
+__device__ __forceinline__ void umma2_ts_mnmajor_x8_split(uint32_t d_tmem, uint32_t a_tmem,
+                                                          uint64_t b_desc, uint32_t idesc,
+                                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 ra;\n\t.reg .b64 rb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %3, %3;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.s32 ra, %1, 8;\n\tadd.s64 rb, %2, 128;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.s32 ra, %1, 16;\n\tadd.s64 rb, %2, 256;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.s32 ra, %1, 24;\n\tadd.s64 rb, %2, 384;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.s32 ra, %1, 64;\n\tadd.s64 rb, %2, 512;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.s32 ra, %1, 72;\n\tadd.s64 rb, %2, 640;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.s32 ra, %1, 80;\n\tadd.s64 rb, %2, 768;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.s32 ra, %1, 88;\n\tadd.s64 rb, %2, 896;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "}" ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 8 pair MMAs along K = 128 with A (bf16 pairs, K-step ks at column 8 ks) in each CTA's TMEM and
+// B MN-major, 128B-swizzled in each CTA's shared memory (one 128-byte row per K index: K-step ks
+// starts 2048 bytes further).
+__device__ __forceinline__ void umma2_ts_mnmajor_x8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                    uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 ra;\n\t.reg .b64 rb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %3, %3;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.s32 ra, %1, 8;\n\tadd.s64 rb, %2, 128;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.s32 ra, %1, 16;\n\tadd.s64 rb, %2, 256;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.s32 ra, %1, 24;\n\tadd.s64 rb, %2, 384;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.s32 ra, %1, 32;\n\tadd.s64 rb, %2, 512;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.s32 ra, %1, 40;\n\tadd.s64 rb, %2, 640;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.s32 ra, %1, 48;\n\tadd.s64 rb, %2, 768;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "add.s32 ra, %1, 56;\n\tadd.s64 rb, %2, 896;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+      "}" ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // Stages 16 packed bf16 pairs = columns [c0, c0 + 32) of row `row` of a 128-row tile whose
