@@ -471,6 +471,7 @@ cudaError_t launch_bwd_dq(const Problem& pb, const void* q, const void* k, const
                           const void* dO, const float* lse, const float* delta, void* dq,
                           cudaStream_t stream) {
   if (pb.D == 256) return launch_dq_d256(pb, q, k, v, dO, lse, delta, dq, stream);
+  if (dq_pair_applies(pb)) return launch_dq_pair(pb, q, k, v, dO, lse, delta, dq, stream);
   if (pb.D == 64)
     return pb.f16 ? launch_dq_d<64, true>(pb, q, k, v, dO, lse, delta, dq, stream)
                   : launch_dq_d<64, false>(pb, q, k, v, dO, lse, delta, dq, stream);

@@ -98,6 +98,12 @@ cudaError_t launch_bwd_dkdv(const Problem& pb, const void* q, const void* k, con
 cudaError_t launch_bwd_dq(const Problem& pb, const void* q, const void* k, const void* v,
                           const void* dO, const float* lse, const float* delta, void* dq,
                           cudaStream_t stream);
+// dQ on CTA pairs (swa_bwd_dq_pair.cu): D = 128 with an even number of query heads per kv head;
+// launch_bwd_dq dispatches there when it applies.
+bool dq_pair_applies(const Problem& pb);
+cudaError_t launch_dq_pair(const Problem& pb, const void* q, const void* k, const void* v,
+                           const void* dO, const float* lse, const float* delta, void* dq,
+                           cudaStream_t stream);
 
 // Fused backward (swa_bwd_fused.cu): dK, dV and the dQ partials of every (key block, query tile)
 // pair in one kernel.  dQ accumulates in fp32, tile-major: block (bhq, qb) holds query rows
