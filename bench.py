@@ -487,8 +487,12 @@ def run_ours(args, world, rank, local):
         # as dK/dV, plus reading and writing back the fp32 dQ accumulator (which the L2 cannot hold)
         "fused": 2 * q_bytes + 4 * k_bytes + 2 * row_bytes + 2 * acc_bytes,
     }
-    kernel_names = {"fwd": "swa_fwd_kernel<128>", "dkdv": "swa_dkdv_kernel<128>",
-                    "dq": "swa_dq_kernel<128>", "fused": "swa_fused_bwd_kernel<128>"}
+    # D = 128 with an even number of query heads per kv head runs the forward and dQ on CTA pairs.
+    pair = case.D == 128 and (case.Hq // case.Hkv) % 2 == 0
+    kernel_names = {"fwd": "swa_fwd_pair_kernel<128>" if pair else "swa_fwd_kernel<128>",
+                    "dkdv": "swa_dkdv_kernel<128>",
+                    "dq": "swa_dq_pair_kernel<128>" if pair else "swa_dq_kernel<128>",
+                    "fused": "swa_fused_bwd_kernel<128>"}
     dom_flops = fl["bwd"] if dominant == "fused" else fl[dominant]
     roofline = {
         "kernel": kernel_names[dominant],
@@ -512,16 +516,18 @@ def run_ours(args, world, rank, local):
     # The timed region is short (~40 ms at the default 20 steps), so only a few clock samples land
     # in it; the same step then runs untimed for ~0.5 s under the sampler, to show the clock that
     # this load holds (reported beside the timed region's samples, not instead of them).
-    with ClockSampler(local) as soak:
-        soak_steps = max(1, int(500.0 / max(ms_step, 1e-3)))
-        torch.cuda.synchronize(device)
-        w0 = time.time()
-        for _ in range(soak_steps):
-            one_step(path)
-        torch.cuda.synchronize(device)
-        soak.mark(w0, time.time())
-    clocks_soak = soak.summary()
-    clocks_soak["steps"] = soak_steps
+    clocks_soak = None
+    if not args.no_soak:
+        with ClockSampler(local) as soak:
+            soak_steps = max(1, int(500.0 / max(ms_step, 1e-3)))
+            torch.cuda.synchronize(device)
+            w0 = time.time()
+            for _ in range(soak_steps):
+                one_step(path)
+            torch.cuda.synchronize(device)
+            soak.mark(w0, time.time())
+        clocks_soak = soak.summary()
+        clocks_soak["steps"] = soak_steps
     # the other backward path, timed the same way right after (reported, not the headline)
     other = "split" if path == "fused" else "fused"
     for _ in range(3):
@@ -944,6 +950,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-soak", action="store_true",
+                    help="skip the untimed clock soak after the timed region (profiler runs)")
     ap.add_argument("--ref-rows", type=int, default=256,
                     help="query rows per step of the reference arm's oracle sample")
     ap.add_argument("--cpu-rows", type=int, default=2048,
