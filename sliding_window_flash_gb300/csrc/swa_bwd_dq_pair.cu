@@ -15,14 +15,15 @@
 // so each SM loads 48 KB per key block instead of 64, which leaves room for a fourth K stage: a K
 // tile is held from S_j until dQ_j completes, and three stages could not cover the copy latency.
 //
-// Warp roles (352 threads per CTA): warps 0-7 compute (as swa_bwd_dq.cu; the S-read, dP-read,
-// dS-written and dQ-read handshakes arrive on rank 0's barriers, 16 arrivals from both CTAs);
+// Warp roles (352 threads per CTA): warps 0-7 compute (as swa_bwd_dq.cu; the S-read, dS-written
+// and dQ-read handshakes arrive on rank 0's barriers, 16 arrivals from both CTAs);
 // warp 8 TMA producer of this CTA's Q and dO (per tile) and K pieces; warp 10 of its V halves;
 // warp 9 rank 0: MMA issuer for the pair (commits arrive on the barriers of both CTAs), rank 1:
 // relay — waits for each of its own copies in the order rank 0 consumes them and arrives on rank
 // 0's matching barrier.
-// TMEM (each CTA, allocated for the pair): [0,128) S, [128,256) dP, [256,384) dQ, [384,512) dS x 2
-// (bf16 pairs).
+// TMEM (each CTA, allocated for the pair): [0,128) S, [128,384) two dP buffers, [384,512) dQ.  dS_g
+// (bf16 pairs) goes over the first 32 of each half-row's 64 columns of dP buffer g & 1, so dP of
+// the next block is computed into the other buffer while the compute warps work on this one.
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 #include "swa_tmap.h"
@@ -56,9 +57,8 @@ struct DqPairCfg {
   static constexpr int kVEmpty = kVFull + kVStages;
   static constexpr int kSFull = kVEmpty + kVStages;
   static constexpr int kSEmpty = kSFull + 1;    // rank 0's: both CTAs have read S
-  static constexpr int kDPFull = kSEmpty + 1;
-  static constexpr int kDPEmpty = kDPFull + 1;  // rank 0's: both CTAs have read dP
-  static constexpr int kDSFull = kDPEmpty + 1;  // 2, rank 0's: both CTAs' dS written
+  static constexpr int kDPFull = kSEmpty + 1;   // 2 (one per dP buffer)
+  static constexpr int kDSFull = kDPFull + 2;   // 2, rank 0's: both CTAs' dS written
   static constexpr int kDQDone = kDSFull + 2;
   static constexpr int kDQEmpty = kDQDone + 1;  // rank 0's: both epilogues have read dQ
   static constexpr int kDrain = kDQEmpty + 1;
@@ -66,7 +66,7 @@ struct DqPairCfg {
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;  // + TMEM address and abort flag
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 384;  // dP buffer b at kColDP + 128 b
   static constexpr int kThreads = 352;
   static constexpr int kComputeThreads = 256;
   static constexpr uint32_t kPairWarps = 2 * kComputeThreads / 32;
@@ -151,8 +151,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
     }
     mbar_init(bar(C::kSFull), 1);
     mbar_init(bar(C::kSEmpty), C::kPairWarps);
-    mbar_init(bar(C::kDPFull), 1);
-    mbar_init(bar(C::kDPEmpty), C::kPairWarps);
+    mbar_init(bar(C::kDPFull + 0), 1);
+    mbar_init(bar(C::kDPFull + 1), 1);
     mbar_init(bar(C::kDSFull + 0), C::kPairWarps);
     mbar_init(bar(C::kDSFull + 1), C::kPairWarps);
     mbar_init(bar(C::kDQDone), 1);
@@ -241,6 +241,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
   } else if (warp == 9 && lead) {
     // ------------------------------------------------------------------ MMA issuer (the pair)
     // Per tile: S_0, dP_0, then per block j: S_{j+1}, dP_{j+1}, dQ += dS_j K_j (as swa_bwd_dq.cu).
+    // dP_gg goes into buffer gg & 1, which last held dS_{gg-2}: dQ_{gg-2} was issued before it and
+    // tcgen05.mma operations of one thread run in issue order, so no wait is needed.
     constexpr uint32_t kIdSq = idesc_f16kind(Elem<F16>::kMmaFmt, 2 * kBlockM, kBlockN, false, false);
     constexpr uint32_t kIdDq = idesc_f16kind(Elem<F16>::kMmaFmt, 2 * kBlockM, D, false, true);
     auto issue_s = [&](int gg) -> bool {  // S = Q K_gg^T once S_{gg-1} has been read
@@ -254,26 +256,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
       umma2_commit_w(bar(C::kSFull));
       return true;
     };
-    auto issue_dp = [&](int gg, bool tile_last) -> bool {  // dP = dO V_gg^T once dP_{gg-1} read
+    auto issue_dp = [&](int gg, bool tile_last) -> bool {  // dP = dO V_gg^T into buffer gg & 1
       const int s = gg % C::kVStages, n = gg / C::kVStages;
       if (!warp_wait_cluster(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
-      if (gg >= 1 && !warp_wait_cluster(bar(C::kDPEmpty), (gg - 1) & 1, &abort_flag, a.err))
-        return false;
       tc_fence_after();
-      umma2_ss_kmajor_d<D>(tmem + C::kColDP, smem_desc_sw128(sDO, 16, 1024),
+      umma2_ss_kmajor_d<D>(tmem + C::kColDP + 128u * (gg & 1), smem_desc_sw128(sDO, 16, 1024),
                            smem_desc_sw128(sV0 + s * C::kHalfBytes, 16, 1024), kIdSq, 0u);
-      umma2_commit_w(bar(C::kDPFull));
+      umma2_commit_w(bar(C::kDPFull + (gg & 1)));
       umma2_commit_w(bar(C::kVEmpty + s));
       if (tile_last) umma2_commit_w(bar(C::kQDEmpty));  // every S and dP of the tile is issued
       return true;
     };
-    auto issue_dq = [&](int gg, bool first, bool tile_last) -> bool {  // dQ += dS K_gg
+    // dQ += dS_gg K_gg with dS_gg in dP buffer gg & 1: keys 16 ks .. 16 ks + 15 at packed column
+    // 8 ks + 32 (ks / 4).
+    auto issue_dq = [&](int gg, bool first, bool tile_last) -> bool {
       const int s = gg % C::kKStages, db = gg & 1;
       if (!warp_wait_cluster(bar(C::kDSFull + db), (gg >> 1) & 1, &abort_flag, a.err))
         return false;
       tc_fence_after();
-      umma2_ts_mnmajor_x8(tmem + C::kColDQ, tmem + C::kColDS + 64u * db,
-                          smem_desc_sw128(sKQ(s), C::kKColBytes, 1024), kIdDq, first ? 0u : 1u);
+      umma2_ts_mnmajor_x8_split(tmem + C::kColDQ, tmem + C::kColDP + 128u * db,
+                                smem_desc_sw128(sKQ(s), C::kKColBytes, 1024), kIdDq,
+                                first ? 0u : 1u);
       umma2_commit_w(bar(C::kKEmpty + s));
       if (tile_last) umma2_commit_w(bar(C::kDQDone));
       return true;
@@ -423,17 +426,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
             p[2 * c + 1] = ex2(tt.y);
           }
         }
-        // dP_gg landing also means dQ_{gg-2} has finished reading dS buffer (gg & 1).
-        if (!(ok = warp_wait(bar(C::kDPFull), gg & 1, &abort_flag, a.err))) break;
+        const uint32_t dp_col = tmem + lane_base + C::kColDP + 128u * (gg & 1) + 64u * h;
+        if (!(ok = warp_wait(bar(C::kDPFull + (gg & 1)), (gg >> 1) & 1, &abort_flag, a.err))) break;
         tc_fence_after();
         {
           uint32_t rr[2][32];
-          tmem_ld32(tmem + lane_base + C::kColDP + 64u * h, rr[0]);
-          tmem_ld32(tmem + lane_base + C::kColDP + 64u * h + 32u, rr[1]);
+          tmem_ld32(dp_col, rr[0]);
+          tmem_ld32(dp_col + 32u, rr[1]);
           tmem_wait_ld_all();
           reg_fence(rr[0]);
           reg_fence(rr[1]);
-          warp_arrive_rank0(bar(C::kDPEmpty));
           uint32_t pk[32];
           const float2 neg_d2 = make_float2(-dlt, -dlt);
 #pragma unroll
@@ -445,8 +447,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
                                                     neg_d2));
             pk[i] = Elem<F16>::pack(ds.x, ds.y);
           }
-          // dS columns [64h, 64h+64) -> packed TMEM columns [32h, 32h+32) of dS buffer (gg & 1).
-          tmem_st32(tmem + lane_base + C::kColDS + 64u * (gg & 1) + 32u * h, pk);
+          // dS columns [64h, 64h+64) -> packed over the first 32 of the 64 dP columns just read.
+          tmem_st32(dp_col, pk);
         }
         tmem_wait_st();
         warp_arrive_rank0(bar(C::kDSFull + (gg & 1)));
