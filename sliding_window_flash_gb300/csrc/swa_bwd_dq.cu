@@ -19,9 +19,11 @@
 // split over two threads; warp 8 TMA producer of Q and dO (per tile) and of the K ring; warp 10
 // TMA producer of the V ring; warp 9 MMA issuer and TMEM owner.  Loads are issued from two warps
 // because one warp's TMA copies complete at only ~40 B/clk on this GPU, less than one key block
-// (64 KB of K and V) per MMA period needs.  dS goes back to TMEM (two buffers)
-// and is the A operand of dQ += dS K_j.
-// TMEM columns: [0,128) S, [128,256) dP, [256, 256+D) dQ, [256+D, 384+D) dS x 2 (bf16 pairs).
+// (64 KB of K and V) per MMA period needs.  dS goes back to TMEM over the dP it was formed from and
+// is the A operand of dQ += dS K_j.
+// TMEM columns: [0,128) S, [128,384) two dP buffers, [384, 384+D) dQ.  dS_g (bf16 pairs) goes over
+// the first 32 of each half-row's 64 columns of dP buffer g & 1, so dP of the next block is
+// computed into the other buffer while the compute warps work on this one.
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 #include "swa_tmap.h"
@@ -49,9 +51,8 @@ struct DqCfg {
   static constexpr int kVEmpty = kVFull + kVStages;
   static constexpr int kSFull = kVEmpty + kVStages;
   static constexpr int kSEmpty = kSFull + 1;
-  static constexpr int kDPFull = kSEmpty + 1;
-  static constexpr int kDPEmpty = kDPFull + 1;
-  static constexpr int kDSFull = kDPEmpty + 1;  // 2 (one per dS buffer)
+  static constexpr int kDPFull = kSEmpty + 1;   // 2 (one per dP buffer)
+  static constexpr int kDSFull = kDPFull + 2;   // 2 (one per dP buffer)
   static constexpr int kDQDone = kDSFull + 2;   // a tile's last dQ MMA has completed
   static constexpr int kDQEmpty = kDQDone + 1;  // the epilogue has read the dQ accumulator
   static constexpr int kDrain = kDQEmpty + 1;
@@ -59,7 +60,7 @@ struct DqCfg {
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;  // + TMEM address and abort flag
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 384;  // dP buffer b at kColDP + 128 b
   static constexpr int kThreads = 352;
   static constexpr int kComputeThreads = 256;
 };
@@ -125,8 +126,8 @@ __global__ void __launch_bounds__(352, 1)
     }
     mbar_init(bar(C::kSFull), 1);
     mbar_init(bar(C::kSEmpty), C::kComputeThreads / 32);
-    mbar_init(bar(C::kDPFull), 1);
-    mbar_init(bar(C::kDPEmpty), C::kComputeThreads / 32);
+    mbar_init(bar(C::kDPFull + 0), 1);
+    mbar_init(bar(C::kDPFull + 1), 1);
     mbar_init(bar(C::kDSFull + 0), C::kComputeThreads / 32);
     mbar_init(bar(C::kDSFull + 1), C::kComputeThreads / 32);
     mbar_init(bar(C::kDQDone), 1);
@@ -211,8 +212,9 @@ __global__ void __launch_bounds__(352, 1)
     // ------------------------------------------------------------------ MMA issuer
     // Per tile: S_0, dP_0, then per block j: S_{j+1}, dP_{j+1}, dQ += dS_j K_j.  The next block's
     // S and dP are computed as soon as the compute warps have read this block's, so they never
-    // wait on dQ_j.  dS alternates between two TMEM buffers: dP_{g+2} runs after dQ_g, so when the
-    // compute warps see dP_{g+2} the buffer of dS_g is free again.  Block counters run across tiles.
+    // wait on dQ_j.  dP_g goes into buffer g & 1, which last held dS_{g-2}: dQ_{g-2} was issued
+    // before it and tcgen05.mma operations of one thread run in issue order, so no wait is needed.
+    // Block counters run across tiles.
     constexpr uint32_t kIdSq = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockM, kBlockN, false, false);  // S, dP
     constexpr uint32_t kIdDq = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockM, D, false, true);         // dQ += dS K
     auto issue_s = [&](int gg) -> bool {  // S = Q K_gg^T once S_{gg-1} has been read
@@ -225,25 +227,26 @@ __global__ void __launch_bounds__(352, 1)
       umma_commit_w(bar(C::kSFull));
       return true;
     };
-    auto issue_dp = [&](int gg, bool tile_last) -> bool {  // dP = dO V_gg^T once dP_{gg-1} read
+    auto issue_dp = [&](int gg, bool tile_last) -> bool {  // dP = dO V_gg^T into buffer gg & 1
       const int s = gg % C::kVStages, n = gg / C::kVStages;
       if (!warp_wait(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
-      if (gg >= 1 && !warp_wait(bar(C::kDPEmpty), (gg - 1) & 1, &abort_flag, a.err)) return false;
       tc_fence_after();
-      umma_ss_kmajor_d<D>(tmem + C::kColDP, smem_desc_sw128(sDO, 16, 1024),
+      umma_ss_kmajor_d<D>(tmem + C::kColDP + 128u * (gg & 1), smem_desc_sw128(sDO, 16, 1024),
                           smem_desc_sw128(sV0 + s * C::kTileBytes, 16, 1024), kIdSq, 0u);
-      umma_commit_w(bar(C::kDPFull));
+      umma_commit_w(bar(C::kDPFull + (gg & 1)));
       umma_commit_w(bar(C::kVEmpty + s));
       if (tile_last) umma_commit_w(bar(C::kQDEmpty));  // every S and dP of the tile is issued
       return true;
     };
-    auto issue_dq = [&](int gg, bool first, bool tile_last) -> bool {  // dQ += dS K_gg
+    // dQ += dS_gg K_gg with dS_gg in dP buffer gg & 1: keys 16 ks .. 16 ks + 15 at packed column
+    // 8 ks + 32 (ks / 4).
+    auto issue_dq = [&](int gg, bool first, bool tile_last) -> bool {
       const int s = gg % C::kKStages, db = gg & 1;
       if (!warp_wait(bar(C::kDSFull + db), (gg >> 1) & 1, &abort_flag, a.err)) return false;
       tc_fence_after();
-      umma_ts_mnmajor_x8(tmem + C::kColDQ, tmem + C::kColDS + 64u * db,
-                         smem_desc_sw128(sK0 + s * C::kTileBytes, C::kChunkBytes, 1024), kIdDq,
-                         first ? 0u : 1u);
+      umma_ts_mnmajor_x8_split(tmem + C::kColDQ, tmem + C::kColDP + 128u * db,
+                               smem_desc_sw128(sK0 + s * C::kTileBytes, C::kChunkBytes, 1024),
+                               kIdDq, first ? 0u : 1u);
       umma_commit_w(bar(C::kKEmpty + s));
       if (tile_last) umma_commit_w(bar(C::kDQDone));
       return true;
@@ -381,17 +384,16 @@ __global__ void __launch_bounds__(352, 1)
           }
         }
 
-        // dP_gg landing also means dQ_{gg-2} has finished reading dS buffer (gg & 1).
-        if (!(ok = warp_wait(bar(C::kDPFull), gg & 1, &abort_flag, a.err))) break;
+        const uint32_t dp_col = tmem + lane_base + C::kColDP + 128u * (gg & 1) + 64u * h;
+        if (!(ok = warp_wait(bar(C::kDPFull + (gg & 1)), (gg >> 1) & 1, &abort_flag, a.err))) break;
         tc_fence_after();
         {
           uint32_t rr[2][32];
-          tmem_ld32(tmem + lane_base + C::kColDP + 64u * h, rr[0]);
-          tmem_ld32(tmem + lane_base + C::kColDP + 64u * h + 32u, rr[1]);
+          tmem_ld32(dp_col, rr[0]);
+          tmem_ld32(dp_col + 32u, rr[1]);
           tmem_wait_ld_all();
           reg_fence(rr[0]);
           reg_fence(rr[1]);
-          warp_arrive(bar(C::kDPEmpty));
           // dS = P (dP - Delta), two columns per packed FADD / FMUL.
           uint32_t pk[32];
           const float2 neg_d2 = make_float2(-dlt, -dlt);
@@ -404,8 +406,8 @@ __global__ void __launch_bounds__(352, 1)
                                                     neg_d2));
             pk[i] = Elem<F16>::pack(ds.x, ds.y);
           }
-          // dS columns [64h, 64h+64) -> packed TMEM columns [32h, 32h+32) of dS buffer (gg & 1).
-          tmem_st32(tmem + lane_base + C::kColDS + 64u * (gg & 1) + 32u * h, pk);
+          // dS columns [64h, 64h+64) -> packed over the first 32 of the 64 dP columns just read.
+          tmem_st32(dp_col, pk);
         }
         tmem_wait_st();
         warp_arrive(bar(C::kDSFull + (gg & 1)));
