@@ -49,9 +49,8 @@ struct DkdvCfg {
   static constexpr int kSFull = kDOEmpty + kDOStages;
   static constexpr int kSEmpty = kSFull + 1;  // every compute warp has read S^T
   static constexpr int kDPFull = kSEmpty + 1;
-  static constexpr int kPFull = kDPFull + 1;
-  static constexpr int kDSFull = kPFull + 1;
-  static constexpr int kVecFull = kDSFull + 1;  // 2 slots
+  static constexpr int kPFull = kDPFull + 1;  // P^T and dS^T written (one arrival per warp)
+  static constexpr int kVecFull = kPFull + 1;  // 2 slots
   static constexpr int kDone = kVecFull + 2;
   static constexpr int kOutFull = kDone + 1;  // staged dK / dV tiles complete (one arrival per warp)
   static constexpr int kDrain = kOutFull + 1;
@@ -117,8 +116,21 @@ __global__ void __launch_bounds__(352, 1)
   const int q_int_hi = (k0 + kBlockN <= sp.Lk)
                            ? min(k0 + sp.dmax - sp.off - (kBlockM - 1), sp.Lq - kBlockM)
                            : -1;
-  auto tile_q0 = [&](int t) { return (qb_lo + t % nq) * kBlockM; };
-  auto tile_bhq = [&](int t) { return b * a.Hq + hk * a.G + t / nq; };
+  // Tile t of the walk is query head gi of the group and query block qb_lo + qi, t = gi nq + qi.
+  // Each role advances (qi, gi) tile by tile: dividing t by nq costs an integer division per tile,
+  // whose reciprocal queues behind the compute warps' exponentials.
+  struct WalkPos {
+    int qi = 0, gi = 0;
+  };
+  auto advance = [&](WalkPos& w) {
+    if (++w.qi == nq) {
+      w.qi = 0;
+      ++w.gi;
+    }
+  };
+  const int bhq0 = b * a.Hq + hk * a.G;
+  auto pos_q0 = [&](const WalkPos& w) { return (qb_lo + w.qi) * kBlockM; };
+  auto pos_bhq = [&](const WalkPos& w) { return bhq0 + w.gi; };
 
   if (T == 0) {
     // No query sees this key block: its dK and dV rows are zero.  Written straight from the
@@ -143,7 +155,6 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(bar(C::kSEmpty), C::kComputeThreads / 32);
     mbar_init(bar(C::kDPFull), 1);
     mbar_init(bar(C::kPFull), C::kComputeThreads / 32);
-    mbar_init(bar(C::kDSFull), C::kComputeThreads / 32);
     mbar_init(bar(C::kVecFull + 0), C::kComputeThreads / 32);
     mbar_init(bar(C::kVecFull + 1), C::kComputeThreads / 32);
     mbar_init(bar(C::kDone), 1);
@@ -170,15 +181,16 @@ __global__ void __launch_bounds__(352, 1)
         tma_load_3d(sK + h * C::kChunkBytes, &tm_k, bar(C::kKVFull), 64 * h, k0, bhk);
       int last_q[C::kQStages];
       for (int s = 0; s < C::kQStages; ++s) last_q[s] = -1;
-      for (int t = 0; t < T; ++t) {
+      WalkPos wp;
+      for (int t = 0; t < T; ++t, advance(wp)) {
         const int sq = t % C::kQStages, nqs = t / C::kQStages;
         if (t >= C::kQStages && !mbar_wait(bar(C::kQEmpty + sq), (nqs - 1) & 1, &abort_flag, a.err))
           break;
         const uint32_t sQ = sQ0 + sq * C::kTileBytes;
         mbar_arrive_expect_tx(bar(C::kQFull + sq), C::kTileBytes);
         for (int h = 0; h < C::kChunks; ++h)
-          tma_load_3d(sQ + h * C::kChunkBytes, &tm_q, bar(C::kQFull + sq), 64 * h, tile_q0(t),
-                      tile_bhq(t));
+          tma_load_3d(sQ + h * C::kChunkBytes, &tm_q, bar(C::kQFull + sq), 64 * h, pos_q0(wp),
+                      pos_bhq(wp));
         last_q[sq] = t;
       }
       drain_wait(bar(C::kKVFull), 0, a.err);
@@ -195,7 +207,8 @@ __global__ void __launch_bounds__(352, 1)
         tma_load_3d(sV + h * C::kChunkBytes, &tm_v, bar(C::kKVFull), 64 * h, k0, bhk);
       int last_do[C::kDOStages];
       for (int s = 0; s < C::kDOStages; ++s) last_do[s] = -1;
-      for (int t = 0; t < T; ++t) {
+      WalkPos wp;
+      for (int t = 0; t < T; ++t, advance(wp)) {
         const int sd = t % C::kDOStages, nds = t / C::kDOStages;
         if (t >= C::kDOStages &&
             !mbar_wait(bar(C::kDOEmpty + sd), (nds - 1) & 1, &abort_flag, a.err))
@@ -203,8 +216,8 @@ __global__ void __launch_bounds__(352, 1)
         const uint32_t sDO = sDO0 + sd * C::kTileBytes;
         mbar_arrive_expect_tx(bar(C::kDOFull + sd), C::kTileBytes);
         for (int h = 0; h < C::kChunks; ++h)
-          tma_load_3d(sDO + h * C::kChunkBytes, &tm_do, bar(C::kDOFull + sd), 64 * h, tile_q0(t),
-                      tile_bhq(t));
+          tma_load_3d(sDO + h * C::kChunkBytes, &tm_do, bar(C::kDOFull + sd), 64 * h, pos_q0(wp),
+                      pos_bhq(wp));
         last_do[sd] = t;
       }
       drain_wait(bar(C::kKVFull), 0, a.err);
@@ -244,10 +257,13 @@ __global__ void __launch_bounds__(352, 1)
         return true;
       };
       // acc += X^T B_t with X^T (bf16 pairs) in TMEM at column a_col and B_t = dO_t or Q_t (MN-major)
+      // (wait_bar < 0: no wait, the operand's barrier has already been waited for)
       auto issue_acc = [&](int t, int wait_bar, uint32_t a_col, uint32_t b_tile,
                            uint32_t d_col) -> bool {
-        if (!warp_wait(bar(wait_bar), t & 1, &abort_flag, a.err)) return false;
-        tc_fence_after();
+        if (wait_bar >= 0) {
+          if (!warp_wait(bar(wait_bar), t & 1, &abort_flag, a.err)) return false;
+          tc_fence_after();
+        }
         // query columns 16 ks .. 16 ks + 15 sit at packed column 8 ks + 32 (ks / 4)
         umma_ts_mnmajor_x8_split(tmem + d_col, tmem + a_col,
                                  smem_desc_sw128(b_tile, C::kChunkBytes, 1024), kIdAcc,
@@ -263,7 +279,8 @@ __global__ void __launch_bounds__(352, 1)
         ok = issue_acc(t, C::kPFull, C::kColDP, sDO0 + sd * C::kTileBytes, C::kColDV);  // dV
         if (!ok) break;
         umma_commit_w(bar(C::kDOEmpty + sd));
-        ok = issue_acc(t, C::kDSFull, C::kColDP + 32u, sQ0 + sq * C::kTileBytes, C::kColDK);  // dK
+        // dK: dS^T was written with P^T, under the same barrier
+        ok = issue_acc(t, -1, C::kColDP + 32u, sQ0 + sq * C::kTileBytes, C::kColDK);
         if (!ok) break;
         umma_commit_w(bar(C::kQEmpty + sq));
         if (t + 1 < T) ok = issue_dp(t + 1);
@@ -284,19 +301,21 @@ __global__ void __launch_bounds__(352, 1)
     // for query q0 + r.  The raw value is kept until it is stored, so the load's latency hides
     // behind a whole tile.
     float nxt = 0.f;
-    auto fetch_row = [&](int t) {
-      const int q = tile_q0(t) + r;
+    auto fetch_row = [&](const WalkPos& w) {
+      const int q = pos_q0(w) + r;
       if (q < sp.Lq) {
-        const size_t gi = static_cast<size_t>(tile_bhq(t)) * sp.Lq + q;
+        const size_t gi = static_cast<size_t>(pos_bhq(w)) * sp.Lq + q;
         nxt = h == 0 ? a.lse[gi] : a.delta[gi];
       } else {  // queries past the end contribute P = 0
         nxt = h == 0 ? SWA_POS_INF : 0.f;
       }
     };
-    if (T > 0) fetch_row(0);
+    WalkPos wcur, wnext;  // tiles t and t + 1
+    advance(wnext);
+    if (T > 0) fetch_row(wcur);
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      const int q0 = tile_q0(t);
+    for (int t = 0; t < T; ++t, advance(wcur), advance(wnext)) {
+      const int q0 = pos_q0(wcur);
       // Slot t & 1 was last read in tile t - 2; every compute thread has finished that tile
       // (dK_{t-2}, which needed all of them, precedes dP_{t-1}, which this thread has seen).
       // Stored negated (-LSE log2(e) and -Delta), the addends of the packed FFMA / FADD below.
@@ -309,7 +328,7 @@ __global__ void __launch_bounds__(352, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::kVecFull + (t & 1)));
       if (!(ok = warp_wait(bar(C::kVecFull + (t & 1)), (t >> 1) & 1, &abort_flag, a.err))) break;
-      if (t + 1 < T) fetch_row(t + 1);
+      if (t + 1 < T) fetch_row(wnext);
 
       if (!(ok = warp_wait(bar(C::kSFull), t & 1, &abort_flag, a.err))) break;
       tc_fence_after();
@@ -392,7 +411,6 @@ __global__ void __launch_bounds__(352, 1)
       }
       tmem_wait_st();
       warp_arrive(bar(C::kPFull));
-      warp_arrive(bar(C::kDSFull));
     }
     if (ok && warp_wait(bar(C::kDone), 0, &abort_flag, a.err)) {
       tc_fence_after();
