@@ -73,6 +73,7 @@ struct DqArgs {
   Span span;
   float scale, scale_log2;
   unsigned* err;
+  FastDiv divBH, divHq, divG;  // tile index decomposition
 };
 
 struct DqTile {
@@ -82,9 +83,12 @@ struct DqTile {
 // Tile t: heaviest query blocks first (the causal case gives later blocks more key blocks).
 __device__ __forceinline__ DqTile dq_tile(int t, const DqArgs& a, const Span sp) {
   DqTile f;
-  const int qb = a.nqb - 1 - t / a.BH;
-  f.bh = t % a.BH;
-  f.bhk = (f.bh / a.Hq) * a.Hkv + (f.bh % a.Hq) / a.G;
+  const uint32_t tq = a.divBH.div(static_cast<uint32_t>(t));
+  const int qb = a.nqb - 1 - static_cast<int>(tq);
+  f.bh = t - static_cast<int>(tq) * a.BH;
+  const uint32_t b = a.divHq.div(static_cast<uint32_t>(f.bh));
+  f.bhk = static_cast<int>(b) * a.Hkv +
+          static_cast<int>(a.divG.div(static_cast<uint32_t>(f.bh) - b * static_cast<uint32_t>(a.Hq)));
   f.q0 = qb * kBlockM;
   f.kb_lo = sp.first_kblock(f.q0);
   f.nkv = sp.last_kblock(f.q0) - f.kb_lo + 1;
@@ -462,6 +466,9 @@ cudaError_t launch_dq_d(const Problem& pb, const void* q, const void* k, const v
   a.scale = pb.scale;
   a.scale_log2 = pb.scale * kLog2e;
   a.err = pb.err;
+  a.divBH = FastDiv(static_cast<uint32_t>(a.BH));
+  a.divHq = FastDiv(static_cast<uint32_t>(a.Hq));
+  a.divG = FastDiv(static_cast<uint32_t>(a.G));
   const int grid = a.ntiles < sm_count() ? a.ntiles : sm_count();
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tdo, tk, tv, a);
   return cudaGetLastError();

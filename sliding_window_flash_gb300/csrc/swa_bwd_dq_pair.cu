@@ -81,6 +81,7 @@ struct DqPairArgs {
   Span span;
   float scale, scale_log2;
   unsigned* err;
+  FastDiv divBHKP, divGP, divHkv;  // tile index decomposition (divGP: G / 2)
 };
 
 struct DqPairTile {
@@ -91,11 +92,13 @@ struct DqPairTile {
 __device__ __forceinline__ DqPairTile dq_pair_tile(int t, const DqPairArgs& a, const Span sp,
                                                    uint32_t rank) {
   DqPairTile f;
-  const int qb = a.nqb - 1 - t / a.BHKP;
-  const int rem = t % a.BHKP;
-  const int gp = rem % (a.G / 2);
-  f.bhk = rem / (a.G / 2);
-  const int b = f.bhk / a.Hkv, hk = f.bhk % a.Hkv;
+  const uint32_t tq = a.divBHKP.div(static_cast<uint32_t>(t));
+  const int qb = a.nqb - 1 - static_cast<int>(tq);
+  const uint32_t rem = static_cast<uint32_t>(t) - tq * static_cast<uint32_t>(a.BHKP);
+  f.bhk = static_cast<int>(a.divGP.div(rem));
+  const int gp = static_cast<int>(rem) - f.bhk * (a.G / 2);
+  const int b = static_cast<int>(a.divHkv.div(static_cast<uint32_t>(f.bhk)));
+  const int hk = f.bhk - b * a.Hkv;
   f.bh = b * a.Hq + hk * a.G + 2 * gp + static_cast<int>(rank);
   f.q0 = qb * kBlockM;
   f.kb_lo = sp.first_kblock(f.q0);
@@ -527,6 +530,9 @@ cudaError_t launch_dq_pair_d(const Problem& pb, const void* q, const void* k, co
   a.scale = pb.scale;
   a.scale_log2 = pb.scale * kLog2e;
   a.err = pb.err;
+  a.divBHKP = FastDiv(static_cast<uint32_t>(a.BHKP));
+  a.divGP = FastDiv(static_cast<uint32_t>(a.G / 2));
+  a.divHkv = FastDiv(static_cast<uint32_t>(a.Hkv));
   const int clusters = max_dq_pair_clusters<D, F16>();
   const int nclusters = a.ntiles < clusters ? a.ntiles : clusters;
   kern<<<2 * nclusters, C::kThreads, C::kSmemBytes, stream>>>(tq, tdo, tk64, tk128, tv64, a);

@@ -107,6 +107,7 @@ struct FwdArgs {
   Span span;
   float scale_log2;  // scale * log2(e)
   unsigned* err;
+  FastDiv divBH, divHq, divG;  // tile index decomposition
 };
 
 struct FwdTile {
@@ -116,9 +117,12 @@ struct FwdTile {
 // Tile t: heaviest query blocks first (the causal case gives later blocks more key blocks).
 __device__ __forceinline__ FwdTile fwd_tile(int t, const FwdArgs& a, const Span sp) {
   FwdTile f;
-  const int qb = a.nqb - 1 - t / a.BH;
-  f.bh = t % a.BH;
-  f.bhk = (f.bh / a.Hq) * a.Hkv + (f.bh % a.Hq) / a.G;
+  const uint32_t tq = a.divBH.div(static_cast<uint32_t>(t));
+  const int qb = a.nqb - 1 - static_cast<int>(tq);
+  f.bh = t - static_cast<int>(tq) * a.BH;
+  const uint32_t b = a.divHq.div(static_cast<uint32_t>(f.bh));
+  f.bhk = static_cast<int>(b) * a.Hkv +
+          static_cast<int>(a.divG.div(static_cast<uint32_t>(f.bh) - b * static_cast<uint32_t>(a.Hq)));
   f.q0 = qb * kBlockM;
   f.kb_lo = sp.first_kblock(f.q0);
   f.nkv = sp.last_kblock(f.q0) - f.kb_lo + 1;
@@ -567,6 +571,9 @@ cudaError_t launch_fwd_d(const Problem& pb, const void* q, const void* k, const 
   a.ntiles = a.nqb * a.BH;
   a.scale_log2 = pb.scale * kLog2e;
   a.err = pb.err;
+  a.divBH = FastDiv(static_cast<uint32_t>(a.BH));
+  a.divHq = FastDiv(static_cast<uint32_t>(a.Hq));
+  a.divG = FastDiv(static_cast<uint32_t>(a.G));
   const int grid = a.ntiles < sm_count() ? a.ntiles : sm_count();
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();

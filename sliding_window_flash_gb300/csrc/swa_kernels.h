@@ -64,6 +64,31 @@ struct Problem {
   int f16 = 0;    // element type of every tensor but LSE / Delta: 0 = bf16, 1 = fp16
 };
 
+// Division by a divisor fixed for a launch, without a divide instruction: for 0 <= n < 2^31 and
+// 1 <= d < 2^31, n / d = (umulhi(n, m) + n) >> s with s = ceil(log2 d) and
+// m = floor(2^32 (2^s - d) / d) + 1 (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994; umulhi(n, m) <= n, so the sum does not overflow 32 bits).  Persistent
+// kernels split their tile index with it: a runtime division costs a MUFU reciprocal, which queues
+// behind the softmax exponentials.
+struct FastDiv {
+  uint32_t d = 1, m = 1, s = 0;
+  FastDiv() = default;
+  explicit FastDiv(uint32_t divisor) : d(divisor) {
+    s = 0;
+    while ((1ull << s) < d) ++s;
+    m = static_cast<uint32_t>((((1ull << 32) * ((1ull << s) - d)) / d) + 1);
+  }
+  __host__ __device__ uint32_t div(uint32_t n) const {
+#ifdef __CUDA_ARCH__
+    const uint32_t hi = __umulhi(n, m);
+#else
+    const uint32_t hi = static_cast<uint32_t>((static_cast<uint64_t>(n) * m) >> 32);
+#endif
+    return (hi + n) >> s;
+  }
+  __host__ __device__ uint32_t mod(uint32_t n) const { return n - div(n) * d; }
+};
+
 // Streaming multiprocessors of the current device (cached per device); persistent kernels launch
 // one CTA per SM.
 // The cache is filled under a mutex, so host threads calling concurrently see a complete value.

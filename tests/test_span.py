@@ -48,3 +48,18 @@ def test_span_check_rejects_planted_mistakes(tmp_path, old, new):
     (hdr / "swa_kernels.h").write_text(src.replace(old, new))
     r = _build(tmp_path, str(hdr))
     assert r.returncode == 1 and r.stdout.startswith("mismatch"), r.stdout
+
+
+def test_fastdiv_matches_division(tmp_path):
+    """swa::FastDiv, which the persistent kernels use to split their tile index, against the
+    built-in division and remainder (tests/fastdiv_check.cpp)."""
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None or not os.path.exists(os.path.join(CUDA_INC, "cuda_runtime.h")):
+        pytest.skip("needs a host C++ compiler and the CUDA headers")
+    exe = str(tmp_path / "fastdiv_check")
+    subprocess.run([cxx, "-std=c++17", "-O2", f"-I{CSRC}", f"-I{CUDA_INC}",
+                    os.path.join(ROOT, "tests", "fastdiv_check.cpp"), "-o", exe],
+                   check=True, capture_output=True, text=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert re.match(r"ok \d+", r.stdout)
