@@ -376,14 +376,16 @@ def headline_config(case: si.Case, world: int) -> dict:
     """The `config` of both arms' JSON lines: the long sliding-window layer at N = 32,768."""
     fl = step_flops(case)
     return {
-        "workload": "long-context sliding-window layer: B=1 Hq=32 Hkv=16 N=32768 D=128 W=1024, "
-                    "fwd + bwd (Delta, dK/dV, dQ)",
+        "workload": f"long-context sliding-window layer: B={case.B} Hq={case.Hq} Hkv={case.Hkv} "
+                    f"N={case.N} D={case.D} W={case.W}, fwd + bwd (Delta, dK/dV, dQ)",
         "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "N": case.N, "D": case.D, "W": case.W,
         "global_batch": case.B * world,
         "seq_len": case.N,
         "parallelism": f"independent layer per rank x{world}" if world > 1 else "single GPU",
-        "l2": "no flush: each step reads Q/dO (268 MB each) and K/V (134 MB each), all larger "
-              "than the 129 MB L2",
+        "l2": f"no flush: each step reads Q/dO ({case.B * case.Hq * case.N * case.D * 2 / 1e6:.0f} "
+              f"MB each) and K/V ({case.B * case.Hkv * case.N * case.D * 2 / 1e6:.0f} MB each), "
+              "all larger than the 129 MB L2" if case.N >= 32768 else
+              "no flush (a profiling size: the per-tensor footprint may fit in the 129 MB L2)",
         "flops_per_step": {"fwd": fl["fwd"], "bwd": fl["bwd"]},
     }
 
@@ -395,7 +397,7 @@ def run_ours(args, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     dist = dist_init(world, device)
-    case = si.long_swa_case(32768)
+    case = dataclasses.replace(si.long_swa_case(args.seq_len), D=args.head_dim)
     case = si.Case(**{**case.__dict__, "seed": rank})
     fl = step_flops(case)
     peaks = load_peaks()
@@ -475,7 +477,8 @@ def run_ours(args, world, rank, local):
     # burst peak was measured; the sustained peak comes from seconds of back-to-back GEMMs under
     # the power cap at a lower clock.  So the fraction is taken against the burst figure.
     peak_tf = peaks["bf16_tflops"]
-    traffic = _profiled_traffic(dominant)
+    # the committed counters are of the headline layer's kernels
+    traffic = _profiled_traffic(dominant) if (case.N, case.D) == (32768, 128) else None
     q_bytes = case.B * case.Hq * case.N * case.D * 2
     k_bytes = case.B * case.Hkv * case.N * case.D * 2
     row_bytes = case.B * case.Hq * case.N * 4
@@ -487,12 +490,17 @@ def run_ours(args, world, rank, local):
         # as dK/dV, plus reading and writing back the fp32 dQ accumulator (which the L2 cannot hold)
         "fused": 2 * q_bytes + 4 * k_bytes + 2 * row_bytes + 2 * acc_bytes,
     }
-    # D = 128 with an even number of query heads per kv head runs the forward and dQ on CTA pairs.
+    # D = 128 with an even number of query heads per kv head runs the forward and dQ on CTA pairs;
+    # D = 256 has kernels of its own (dK and dV two of them).
     pair = case.D == 128 and (case.Hq // case.Hkv) % 2 == 0
-    kernel_names = {"fwd": "swa_fwd_pair_kernel<128>" if pair else "swa_fwd_kernel<128>",
-                    "dkdv": "swa_dkdv_kernel<128>",
-                    "dq": "swa_dq_pair_kernel<128>" if pair else "swa_dq_kernel<128>",
-                    "fused": "swa_fused_bwd_kernel<128>"}
+    if case.D == 256:
+        kernel_names = {"fwd": "swa_fwd256_kernel", "dkdv": "swa_dv256_kernel + swa_dk256_kernel",
+                        "dq": "swa_dq256_kernel", "fused": "swa_fused_bwd_kernel<256>"}
+    else:
+        kernel_names = {"fwd": f"swa_fwd_pair_kernel<{case.D}>" if pair else f"swa_fwd_kernel<{case.D}>",
+                        "dkdv": f"swa_dkdv_kernel<{case.D}>",
+                        "dq": f"swa_dq_pair_kernel<{case.D}>" if pair else f"swa_dq_kernel<{case.D}>",
+                        "fused": f"swa_fused_bwd_kernel<{case.D}>"}
     dom_flops = fl["bwd"] if dominant == "fused" else fl[dominant]
     roofline = {
         "kernel": kernel_names[dominant],
@@ -528,18 +536,21 @@ def run_ours(args, world, rank, local):
             soak.mark(w0, time.time())
         clocks_soak = soak.summary()
         clocks_soak["steps"] = soak_steps
-    # the other backward path, timed the same way right after (reported, not the headline)
+    # the other backward path, timed the same way right after (reported, not the headline; the
+    # fused backward has no D = 256 form)
     other = "split" if path == "fused" else "fused"
-    for _ in range(3):
-        one_step(other)
-    o_ms, o_avg = timed_steps(other, args.steps)
-    o_bwd = sum(o_avg[n] for n in names[other][1:])
-    bwd_other = {"path": other, "ms_per_step": o_ms / args.steps, "kernels_ms": o_avg,
-                 "bwd_ms": o_bwd, "bwd_tflops": fl["bwd"] / (o_bwd * 1e-3) / 1e12,
-                 "fwd_bwd_tflops": step_total / (o_ms / args.steps * 1e-3) / 1e12}
-    if other == "split":
-        bwd_other["kernels_tflops"] = {"dkdv": fl["dkdv"] / (o_avg["dkdv"] * 1e-3) / 1e12,
-                                       "dq": fl["dq"] / (o_avg["dq"] * 1e-3) / 1e12}
+    bwd_other = None
+    if case.D != 256:
+        for _ in range(3):
+            one_step(other)
+        o_ms, o_avg = timed_steps(other, args.steps)
+        o_bwd = sum(o_avg[n] for n in names[other][1:])
+        bwd_other = {"path": other, "ms_per_step": o_ms / args.steps, "kernels_ms": o_avg,
+                     "bwd_ms": o_bwd, "bwd_tflops": fl["bwd"] / (o_bwd * 1e-3) / 1e12,
+                     "fwd_bwd_tflops": step_total / (o_ms / args.steps * 1e-3) / 1e12}
+        if other == "split":
+            bwd_other["kernels_tflops"] = {"dkdv": fl["dkdv"] / (o_avg["dkdv"] * 1e-3) / 1e12,
+                                           "dq": fl["dq"] / (o_avg["dq"] * 1e-3) / 1e12}
     # the fused path's preprocess also zeroes the fp32 dQ accumulator (acc_bytes written)
     delta_gbs = (delta_bytes(case) + (acc_bytes if path == "fused" else 0)) / \
         (avg["delta"] * 1e-3) / 1e9
@@ -952,6 +963,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-soak", action="store_true",
                     help="skip the untimed clock soak after the timed region (profiler runs)")
+    ap.add_argument("--seq-len", type=int, default=32768,
+                    help="sequence length of the timed layer (profiler runs on a smaller layer; "
+                         "the headline is 32768)")
+    ap.add_argument("--head-dim", type=int, choices=(64, 128, 256), default=128,
+                    help="head dimension of the timed layer (profiler runs; the headline is 128)")
     ap.add_argument("--ref-rows", type=int, default=256,
                     help="query rows per step of the reference arm's oracle sample")
     ap.add_argument("--cpu-rows", type=int, default=2048,
