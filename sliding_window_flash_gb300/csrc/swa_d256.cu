@@ -1486,6 +1486,7 @@ cudaError_t launch_fwd_d256(const Problem& pb, const void* q, const void* k, con
 cudaError_t launch_dq_d256(const Problem& pb, const void* q, const void* k, const void* v,
                            const void* dO, const float* lse, const float* delta, void* dq,
                            cudaStream_t stream) {
+  if (dq256_pair_applies(pb)) return launch_dq256_pair(pb, q, k, v, dO, lse, delta, dq, stream);
   return pb.f16 ? dq256<true>(pb, q, k, v, dO, lse, delta, dq, stream)
                 : dq256<false>(pb, q, k, v, dO, lse, delta, dq, stream);
 }
