@@ -1479,6 +1479,7 @@ cudaError_t dkdv256(const Problem& pb, const void* q, const void* k, const void*
 
 cudaError_t launch_fwd_d256(const Problem& pb, const void* q, const void* k, const void* v,
                             void* o, float* lse, cudaStream_t stream) {
+  if (fwd256_pair_applies(pb)) return launch_fwd256_pair(pb, q, k, v, o, lse, stream);
   return pb.f16 ? fwd256<true>(pb, q, k, v, o, lse, stream)
                 : fwd256<false>(pb, q, k, v, o, lse, stream);
 }
