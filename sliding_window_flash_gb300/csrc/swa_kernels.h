@@ -166,6 +166,12 @@ cudaError_t launch_dq_d256(const Problem& pb, const void* q, const void* k, cons
 bool fwd256_pair_applies(const Problem& pb);
 cudaError_t launch_fwd256_pair(const Problem& pb, const void* q, const void* k, const void* v,
                                void* o, float* lse, cudaStream_t stream);
+// D = 256 dK and dV on CTA pairs over neighbouring key blocks (swa_d256_dkdv_pair.cu);
+// launch_dkdv_d256 dispatches there when it applies.
+bool dkdv256_pair_applies(const Problem& pb);
+cudaError_t launch_dkdv256_pair(const Problem& pb, const void* q, const void* k, const void* v,
+                                const void* dO, const float* lse, const float* delta, void* dk,
+                                void* dv, cudaStream_t stream);
 // D = 256 dQ on CTA pairs (swa_d256_dq_pair.cu), for an even number of query heads per kv head;
 // launch_dq_d256 dispatches there when it applies.
 bool dq256_pair_applies(const Problem& pb);
