@@ -490,12 +490,14 @@ def run_ours(args, world, rank, local):
         # as dK/dV, plus reading and writing back the fp32 dQ accumulator (which the L2 cannot hold)
         "fused": 2 * q_bytes + 4 * k_bytes + 2 * row_bytes + 2 * acc_bytes,
     }
-    # D = 128 with an even number of query heads per kv head runs the forward and dQ on CTA pairs;
-    # D = 256 has kernels of its own (dK and dV two of them).
-    pair = case.D == 128 and (case.Hq // case.Hkv) % 2 == 0
+    # An even number of query heads per kv head runs the forward and dQ on CTA pairs at D = 128
+    # and 256; D = 256 has kernels of its own (dK and dV two of them, always on CTA pairs).
+    pair = case.D in (128, 256) and (case.Hq // case.Hkv) % 2 == 0
     if case.D == 256:
-        kernel_names = {"fwd": "swa_fwd256_kernel", "dkdv": "swa_dv256_kernel + swa_dk256_kernel",
-                        "dq": "swa_dq256_kernel", "fused": "swa_fused_bwd_kernel<256>"}
+        kernel_names = {"fwd": "swa_fwd256_pair_kernel" if pair else "swa_fwd256_kernel",
+                        "dkdv": "swa_dv256_pair_kernel + swa_dk256_pair_kernel",
+                        "dq": "swa_dq256_pair_kernel" if pair else "swa_dq256_kernel",
+                        "fused": "swa_fused_bwd_kernel<256>"}
     else:
         kernel_names = {"fwd": f"swa_fwd_pair_kernel<{case.D}>" if pair else f"swa_fwd_kernel<{case.D}>",
                         "dkdv": f"swa_dkdv_kernel<{case.D}>",

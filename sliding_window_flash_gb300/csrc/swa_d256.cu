@@ -1,6 +1,9 @@
-// swa_d256.cu — sliding-window attention with head dimension 256 on sm_103a: forward, dQ, dV and
-// dK kernels ("Off NVIDIA, you fix the platform yourself", Lab 28 record, numbers entry "Attention
-// backward memory": Gemma 4's sliding layers use 256-wide heads).
+// swa_d256.cu — sliding-window attention with head dimension 256 on sm_103a: the single-CTA
+// forward and dQ kernels ("Off NVIDIA, you fix the platform yourself", Lab 28 record, numbers
+// entry "Attention backward memory": Gemma 4's sliding layers use 256-wide heads), which run when
+// the number of query heads per kv head is odd, and the D = 256 entry points.  An even number of
+// query heads per kv head runs the forward and dQ on CTA pairs (swa_d256_fwd_pair.cu,
+// swa_d256_dq_pair.cu); dK and dV always run on CTA pairs (swa_d256_dkdv_pair.cu).
 //
 // The D <= 128 kernels keep whole 128-row operand tiles in shared memory and both dK and dV in
 // TMEM.  At D = 256 a 128-row tile is 64 KB and dK + dV alone would fill the 512 TMEM columns, so
@@ -26,10 +29,7 @@
 namespace swa {
 namespace {
 
-using d256::ds_transposed;
-using d256::key_epilogue;
 using d256::mask64;
-using d256::p_transposed;
 
 constexpr int kD = 256;
 constexpr int kHalfBytes = kBlockM * 128 * 2;  // one half-tile: 128 rows x 128 columns, 16-bit
@@ -96,11 +96,8 @@ struct Args256 {
   float* lse_out;        // forward output
   const float* delta;
   uint16_t* dq;          // dQ kernel output (bf16 or fp16 elements)
-  uint16_t* dk;          // dK / dV kernel outputs, for key blocks no query sees (zeros)
-  uint16_t* dv;
   int BH, Hq, Hkv, G;    // B * Hq, heads, G = Hq / Hkv
-  int nqb, ntiles;       // query-tile kernels: query blocks per head, B * Hq * nqb
-  int BHK;               // key-block kernels: B * Hkv
+  int nqb, ntiles;       // query blocks per head, B * Hq * nqb
   Span span;
   float scale, scale_log2;  // softmax scale, scale * log2(e)
   unsigned* err;
@@ -815,484 +812,6 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ================================================================================================
-// Key-block kernels (dV, dK): one CTA per 128-row key block of one (batch, kv head), walking for
-// each of the G query heads of the group the query blocks that can see the block (as the D <= 128
-// dK / dV kernel does), transposed so the key rows sit on TMEM lanes; the accumulator sums over
-// the whole group (the grouped-query reduction, no atomics).  A key block no query sees stores
-// zeros.
-// ================================================================================================
-struct KWalk {
-  int bhk, k0, qb_lo, nq, T;   // T = G * nq (query head, query block) tiles
-  int q_int_lo, q_int_hi;      // query tiles q0 in [q_int_lo, q_int_hi] need no mask
-  int b, hk;
-  __device__ int q0(int t) const { return (qb_lo + t % nq) * kBlockM; }
-};
-
-__device__ __forceinline__ KWalk kwalk(const Args256& a, const Span& sp) {
-  KWalk w;
-  const int kb = static_cast<int>(blockIdx.x) / a.BHK;
-  w.bhk = static_cast<int>(blockIdx.x) % a.BHK;
-  w.b = w.bhk / a.Hkv;
-  w.hk = w.bhk % a.Hkv;
-  w.k0 = kb * kBlockN;
-  w.qb_lo = sp.first_qblock(w.k0);
-  const int qb_hi = sp.last_qblock(w.k0);
-  w.nq = qb_hi >= w.qb_lo ? qb_hi - w.qb_lo + 1 : 0;
-  w.T = a.G * w.nq;
-  w.q_int_lo = w.k0 + kBlockN - 1 + sp.dmin - sp.off;
-  w.q_int_hi = (w.k0 + kBlockN <= sp.Lk)
-                   ? min(w.k0 + sp.dmax - sp.off - (kBlockM - 1), sp.Lq - kBlockM)
-                   : -1;
-  return w;
-}
-
-__device__ __forceinline__ int walk_bhq(const KWalk& w, const Args256& a, int t) {
-  return w.b * a.Hq + w.hk * a.G + t / w.nq;
-}
-
-
-// ------------------------------------------------------------------------------------------------
-// dV = sum over the walk of P_t^T dO_t.  Warps (352 threads): 0-7 compute (warp w: key rows
-// 32 (w % 4).., query columns [64 h, 64 h + 64), h = w / 4), 8 and 10 TMA producers (warp 8 also
-// loads K once), 9 MMA issuer and TMEM owner.  S^T is double-buffered: S^T_{t+1} is computed while
-// the compute warps turn S^T_t into P^T_t, which is written over S^T_t and read by dV += P^T dO.
-// Ring order: Q_0, then per tile t: Q_{t+1} (if any), dO_t (two halves each).
-// TMEM: [0,128) S^T / P^T buffer 0, [128,256) buffer 1, [256,512) dV.
-// ------------------------------------------------------------------------------------------------
-struct V256 {
-  static constexpr int kSlots = 5;
-  static constexpr int kOffK = 0;
-  static constexpr int kOffRing = kOffK + kFullBytes;
-  static constexpr int kOffRow = kOffRing + kSlots * kHalfBytes;  // [2 slots][128] -LSE log2(e)
-  static constexpr int kOffBar = kOffRow + 2 * kBlockM * 4;
-  static constexpr int kKFull = 0;
-  static constexpr int kFull = 1;
-  static constexpr int kEmpty = kFull + kSlots;
-  static constexpr int kSFull = kEmpty + kSlots;  // 2
-  static constexpr int kPFull = kSFull + 2;       // 2
-  static constexpr int kVecFull = kPFull + 2;     // 2
-  static constexpr int kDone = kVecFull + 2;
-  static constexpr int kOutFull = kDone + 1;
-  static constexpr int kDrain = kOutFull + 1;
-  static constexpr int kNumBars = kDrain + 1;
-  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 48;
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-  static constexpr uint32_t kColS = 0, kColAcc = 256;
-  static constexpr int kThreads = 352;
-};
-
-template <bool F16>
-__global__ void __launch_bounds__(352, 1)
-    swa_dv256_kernel(const __grid_constant__ CUtensorMap tm_q,
-                     const __grid_constant__ CUtensorMap tm_do,
-                     const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_dv, const Args256 a) {
-  using C = V256;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = smem_raw;
-  if (!smem_base_ok(smem, a.err)) return;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
-  int& abort_flag = *reinterpret_cast<int*>(tmem_slot + 1);
-  int* s_last = reinterpret_cast<int*>(tmem_slot + 4);  // producers' last fills
-  auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const uint32_t sK = smem_u32(smem + C::kOffK);
-  float* s_rows = reinterpret_cast<float*>(smem + C::kOffRow);
-  const Ring<C::kSlots> rg{smem_u32(smem + C::kOffRing), bar(C::kFull), bar(C::kEmpty)};
-  const Span sp = a.span;
-  const KWalk w = kwalk(a, sp);
-  if (w.T == 0) {  // no query sees this key block: its dV rows are zero
-    zero_key_rows(a.dv, nullptr, w.bhk, w.k0, sp.Lk, kD);
-    return;
-  }
-
-  const uint32_t warp = warp_id(), lane = lane_id();
-  if (threadIdx.x == 0) {
-    abort_flag = 0;
-    mbar_init(bar(C::kKFull), 1);
-    for (int s = 0; s < C::kSlots; ++s) {
-      mbar_init(bar(C::kFull + s), 1);
-      mbar_init(bar(C::kEmpty + s), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(C::kSFull + b), 1);
-      mbar_init(bar(C::kPFull + b), 8);
-      mbar_init(bar(C::kVecFull + b), 8);
-    }
-    mbar_init(bar(C::kDone), 1);
-    mbar_init(bar(C::kOutFull), 8);
-    mbar_init(bar(C::kDrain), 1);
-    fence_barrier_init();
-  }
-  if (warp == 9) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 8 || warp == 10) {
-    // ------------------------------------------------------------ K once; Q / dO ring
-    const int p = warp == 8 ? 0 : 1;
-    int last[C::kSlots];  // lane 0: last item loaded per slot
-    for (int s = 0; s < C::kSlots; ++s) last[s] = -1;
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_do);
-      if (p == 0) {
-        tma_prefetch_desc(&tm_k);
-        mbar_arrive_expect_tx(bar(C::kKFull), kFullBytes);
-        for (int c = 0; c < 4; ++c)
-          tma_load_3d(sK + c * kChunk, &tm_k, bar(C::kKFull), 64 * c, w.k0, w.bhk);
-      }
-      int i = 0;
-      bool ok = true;
-      auto put_tile = [&](const CUtensorMap* m, int t) {
-        for (int hf = 0; hf < 2; ++hf, ++i) {
-          if (!ok || (i & 1) != p) continue;
-          ok = ring_load(rg, i, Item{m, hf, w.q0(t), walk_bhq(w, a, t)}, &abort_flag, a.err);
-          if (ok) last[i % C::kSlots] = i;
-        }
-      };
-      if (w.T > 0) put_tile(&tm_q, 0);
-      for (int t = 0; ok && t < w.T; ++t) {
-        if (t + 1 < w.T) put_tile(&tm_q, t + 1);
-        put_tile(&tm_do, t);
-      }
-      if (p == 0) drain_wait(bar(C::kKFull), 0, a.err);
-    }
-    ring_drain(rg, last, s_last, p, lane, a.err);
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdS = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockN, kBlockM, false, false);
-    constexpr uint32_t kIdAcc = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockN, 128, false, true);
-    int i = 0;
-    auto issue_s = [&](int t) -> bool {  // S^T_t = K_lo Q_lo^T + K_hi Q_hi^T into buffer t & 1
-      const uint32_t d = tmem + C::kColS + 128u * (t & 1);
-      for (int hf = 0; hf < 2; ++hf, ++i) {
-        if (!warp_wait(rg.full(i), rg.parity(i), &abort_flag, a.err)) return false;
-        tc_fence_after();
-        umma_ss_kmajor_x8(d, smem_desc_sw128(sK + hf * kHalfBytes, 16, 1024),
-                          smem_desc_sw128(rg.slot(i), 16, 1024), kIdS, hf);
-        umma_commit_w(rg.empty(i));
-      }
-      umma_commit_w(bar(C::kSFull + (t & 1)));
-      return true;
-    };
-    auto issue_dv = [&](int t) -> bool {  // dV[:, 128 hf ..] (+)= P_t^T dO_t[:, 128 hf ..]
-      const int pb = t & 1;
-      if (!warp_wait(bar(C::kPFull + pb), (t >> 1) & 1, &abort_flag, a.err)) return false;
-      for (int hf = 0; hf < 2; ++hf, ++i) {
-        if (!warp_wait(rg.full(i), rg.parity(i), &abort_flag, a.err)) return false;
-        tc_fence_after();
-        umma_ts_mnmajor_x8_split(tmem + C::kColAcc + 128u * hf, tmem + C::kColS + 128u * pb,
-                                 smem_desc_sw128(rg.slot(i), kChunk, 1024), kIdAcc,
-                                 t > 0 ? 1u : 0u);
-        umma_commit_w(rg.empty(i));
-      }
-      return true;
-    };
-    bool ok = warp_wait(bar(C::kKFull), 0, &abort_flag, a.err);
-    if (ok && w.T > 0) ok = issue_s(0);
-    for (int t = 0; ok && t < w.T; ++t) {
-      if (t + 1 < w.T) ok = issue_s(t + 1);  // buffer (t+1)&1 last held P^T_{t-1}, read by dV_{t-1}
-      if (ok) ok = issue_dv(t);
-    }
-    if (ok) umma_commit_w(bar(C::kDone));
-    umma_commit_w(bar(C::kDrain));
-    warp_drain_wait(bar(C::kDrain), 0, a.err);
-  } else {
-    // ------------------------------------------------------------ compute (warps 0-7)
-    const int r = static_cast<int>(threadIdx.x & 127);  // key row within the block = TMEM lane
-    const uint32_t h = warp >> 2;
-    const int key = w.k0 + r;
-    const int vis_lo = key + sp.dmin - sp.off, vis_hi = key + sp.dmax - sp.off;
-    const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
-    float nxt = 0.f;  // LSE of query q0(t) + r, fetched a tile ahead (h = 0 threads)
-    auto fetch_row = [&](int t) {
-      const int q = w.q0(t) + r;
-      nxt = q < sp.Lq ? a.lse[static_cast<size_t>(walk_bhq(w, a, t)) * sp.Lq + q] : SWA_POS_INF;
-    };
-    if (w.T > 0 && h == 0) fetch_row(0);
-    bool ok = true;
-    for (int t = 0; t < w.T; ++t) {
-      const int q0 = w.q0(t);
-      // Slot t & 1 was last read in tile t - 2; every warp has since arrived for tile t - 1.
-      float* nl2 = s_rows + (t & 1) * kBlockM;
-      if (h == 0) nl2[r] = -nxt * kLog2e;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::kVecFull + (t & 1)));
-      if (!(ok = warp_wait(bar(C::kVecFull + (t & 1)), (t >> 1) & 1, &abort_flag, a.err))) break;
-      if (t + 1 < w.T && h == 0) fetch_row(t + 1);
-      if (!(ok = warp_wait(bar(C::kSFull + (t & 1)), (t >> 1) & 1, &abort_flag, a.err))) break;
-      tc_fence_after();
-      const uint32_t s_col = tmem + lane_base + C::kColS + 128u * (t & 1) + 64u * h;
-      float p[64];
-      const int base = q0 + 64 * static_cast<int>(h);
-      p_transposed(p, s_col, nl2 + 64 * h, a.scale_log2, !(q0 >= w.q_int_lo && q0 <= w.q_int_hi),
-                   vis_lo - base, vis_hi - base);
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = Elem<F16>::pack(p[2 * c], p[2 * c + 1]);
-      tmem_st32(s_col, pk);
-      tmem_wait_st();
-      warp_arrive(bar(C::kPFull + (t & 1)));
-    }
-    if (ok && warp_wait(bar(C::kDone), 0, &abort_flag, a.err)) {
-      tc_fence_after();
-      // dV -> 16-bit, staged in the K buffer (every MMA has completed).
-      key_epilogue<F16>(tmem + lane_base + C::kColAcc, sK, r, h, 1.f, w.T == 0, bar(C::kOutFull),
-                        &tm_dv, w.k0, w.bhk, &abort_flag, a.err);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 9) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-// ------------------------------------------------------------------------------------------------
-// dK = scale * sum over the walk of dS_t^T Q_t, dS^T = P^T (dP^T - Delta), dP^T = V dO^T.
-// Warps (352 threads): 0-7 compute, 8 and 10 TMA producers (warp 8 also loads K, warp 10 V, once
-// each), 9 MMA issuer and TMEM owner.  S^T_{t+1} is issued as soon as the compute warps have read
-// S^T_t; dS^T goes over the dP^T columns it came from and is the A operand of dK += dS^T Q_t,
-// after which dP^T_{t+1} is issued.  Q_t is streamed twice (for S^T, then for dK) because the
-// ring holds only three half-tiles next to K and V.
-// Ring order: Q_0, dO_0, then per tile t: Q_{t+1} (if any), Q_t, dO_{t+1} (if any).
-// TMEM: [0,128) S^T, [128,256) dP^T / dS^T, [256,512) dK.
-// ------------------------------------------------------------------------------------------------
-struct K256 {
-  static constexpr int kSlots = 3;
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = kOffK + kFullBytes;
-  static constexpr int kOffRing = kOffV + kFullBytes;
-  static constexpr int kOffRow = kOffRing + kSlots * kHalfBytes;  // [2 slots][-LSE log2e | -Delta]
-  static constexpr int kOffBar = kOffRow + 2 * 2 * kBlockM * 4;
-  static constexpr int kKVFull = 0;
-  static constexpr int kFull = 1;
-  static constexpr int kEmpty = kFull + kSlots;
-  static constexpr int kSFull = kEmpty + kSlots;
-  static constexpr int kSEmpty = kSFull + 1;
-  static constexpr int kDPFull = kSEmpty + 1;
-  static constexpr int kDSFull = kDPFull + 1;
-  static constexpr int kVecFull = kDSFull + 1;  // 2
-  static constexpr int kDone = kVecFull + 2;
-  static constexpr int kOutFull = kDone + 1;
-  static constexpr int kDrain = kOutFull + 1;
-  static constexpr int kNumBars = kDrain + 1;
-  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 48;
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
-  static constexpr int kThreads = 352;
-};
-
-template <bool F16>
-__global__ void __launch_bounds__(352, 1)
-    swa_dk256_kernel(const __grid_constant__ CUtensorMap tm_q,
-                     const __grid_constant__ CUtensorMap tm_do,
-                     const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_dk, const Args256 a) {
-  using C = K256;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = smem_raw;
-  if (!smem_base_ok(smem, a.err)) return;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
-  int& abort_flag = *reinterpret_cast<int*>(tmem_slot + 1);
-  int* s_last = reinterpret_cast<int*>(tmem_slot + 4);  // producers' last fills
-  auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const uint32_t sK = smem_u32(smem + C::kOffK);
-  const uint32_t sV = smem_u32(smem + C::kOffV);
-  float* s_rows = reinterpret_cast<float*>(smem + C::kOffRow);
-  const Ring<C::kSlots> rg{smem_u32(smem + C::kOffRing), bar(C::kFull), bar(C::kEmpty)};
-  const Span sp = a.span;
-  const KWalk w = kwalk(a, sp);
-  if (w.T == 0) {  // no query sees this key block: its dK rows are zero
-    zero_key_rows(a.dk, nullptr, w.bhk, w.k0, sp.Lk, kD);
-    return;
-  }
-
-  const uint32_t warp = warp_id(), lane = lane_id();
-  if (threadIdx.x == 0) {
-    abort_flag = 0;
-    mbar_init(bar(C::kKVFull), 2);  // one arrival per producer warp
-    for (int s = 0; s < C::kSlots; ++s) {
-      mbar_init(bar(C::kFull + s), 1);
-      mbar_init(bar(C::kEmpty + s), 1);
-    }
-    mbar_init(bar(C::kSFull), 1);
-    mbar_init(bar(C::kSEmpty), 8);
-    mbar_init(bar(C::kDPFull), 1);
-    mbar_init(bar(C::kDSFull), 8);
-    mbar_init(bar(C::kVecFull + 0), 8);
-    mbar_init(bar(C::kVecFull + 1), 8);
-    mbar_init(bar(C::kDone), 1);
-    mbar_init(bar(C::kOutFull), 8);
-    mbar_init(bar(C::kDrain), 1);
-    fence_barrier_init();
-  }
-  if (warp == 9) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 8 || warp == 10) {
-    // ------------------------------------------------------------ K / V once; Q / dO ring
-    const int p = warp == 8 ? 0 : 1;
-    int last[C::kSlots];  // lane 0: last item loaded per slot
-    for (int s = 0; s < C::kSlots; ++s) last[s] = -1;
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_do);
-      {
-        const CUtensorMap* m = p == 0 ? &tm_k : &tm_v;
-        const uint32_t dst = p == 0 ? sK : sV;
-        mbar_arrive_expect_tx(bar(C::kKVFull), kFullBytes);
-        for (int c = 0; c < 4; ++c)
-          tma_load_3d(dst + c * kChunk, m, bar(C::kKVFull), 64 * c, w.k0, w.bhk);
-      }
-      int i = 0;
-      bool ok = true;
-      auto put_tile = [&](const CUtensorMap* m, int t) {
-        for (int hf = 0; hf < 2; ++hf, ++i) {
-          if (!ok || (i & 1) != p) continue;
-          ok = ring_load(rg, i, Item{m, hf, w.q0(t), walk_bhq(w, a, t)}, &abort_flag, a.err);
-          if (ok) last[i % C::kSlots] = i;
-        }
-      };
-      if (w.T > 0) {
-        put_tile(&tm_q, 0);
-        put_tile(&tm_do, 0);
-      }
-      for (int t = 0; ok && t < w.T; ++t) {
-        if (t + 1 < w.T) put_tile(&tm_q, t + 1);
-        put_tile(&tm_q, t);
-        if (t + 1 < w.T) put_tile(&tm_do, t + 1);
-      }
-      drain_wait(bar(C::kKVFull), 0, a.err);
-    }
-    ring_drain(rg, last, s_last, p, lane, a.err);
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdS = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockN, kBlockM, false, false);
-    constexpr uint32_t kIdAcc = idesc_f16kind(Elem<F16>::kMmaFmt, kBlockN, 128, false, true);
-    int i = 0;
-    auto product_d = [&](uint32_t d, uint32_t a_tile) -> bool {  // (+)= A_hf B_hf^T over D
-      for (int hf = 0; hf < 2; ++hf, ++i) {
-        if (!warp_wait(rg.full(i), rg.parity(i), &abort_flag, a.err)) return false;
-        tc_fence_after();
-        umma_ss_kmajor_x8(d, smem_desc_sw128(a_tile + hf * kHalfBytes, 16, 1024),
-                          smem_desc_sw128(rg.slot(i), 16, 1024), kIdS, hf);
-        umma_commit_w(rg.empty(i));
-      }
-      return true;
-    };
-    auto issue_s = [&](int t) -> bool {  // S^T = K Q_t^T once S^T_{t-1} has been read
-      if (t >= 1 && !warp_wait(bar(C::kSEmpty), (t - 1) & 1, &abort_flag, a.err)) return false;
-      if (!product_d(tmem + C::kColS, sK)) return false;
-      umma_commit_w(bar(C::kSFull));
-      return true;
-    };
-    auto issue_dp = [&]() -> bool {  // dP^T = V dO_t^T, after dK of the previous tile
-      if (!product_d(tmem + C::kColDP, sV)) return false;
-      umma_commit_w(bar(C::kDPFull));
-      return true;
-    };
-    auto issue_dk = [&](int t) -> bool {  // dK[:, 128 hf ..] (+)= dS_t^T Q_t[:, 128 hf ..]
-      if (!warp_wait(bar(C::kDSFull), t & 1, &abort_flag, a.err)) return false;
-      for (int hf = 0; hf < 2; ++hf, ++i) {
-        if (!warp_wait(rg.full(i), rg.parity(i), &abort_flag, a.err)) return false;
-        tc_fence_after();
-        umma_ts_mnmajor_x8_split(tmem + C::kColAcc + 128u * hf, tmem + C::kColDP,
-                                 smem_desc_sw128(rg.slot(i), kChunk, 1024), kIdAcc,
-                                 t > 0 ? 1u : 0u);
-        umma_commit_w(rg.empty(i));
-      }
-      return true;
-    };
-    bool ok = warp_wait(bar(C::kKVFull), 0, &abort_flag, a.err);
-    if (ok && w.T > 0) ok = issue_s(0);
-    if (ok && w.T > 0) ok = issue_dp();
-    for (int t = 0; ok && t < w.T; ++t) {
-      if (t + 1 < w.T) ok = issue_s(t + 1);
-      if (ok) ok = issue_dk(t);
-      if (ok && t + 1 < w.T) ok = issue_dp();
-    }
-    if (ok) umma_commit_w(bar(C::kDone));
-    umma_commit_w(bar(C::kDrain));
-    warp_drain_wait(bar(C::kDrain), 0, a.err);
-  } else {
-    // ------------------------------------------------------------ compute (warps 0-7)
-    const int r = static_cast<int>(threadIdx.x & 127);
-    const uint32_t h = warp >> 2;
-    const int key = w.k0 + r;
-    const int vis_lo = key + sp.dmin - sp.off, vis_hi = key + sp.dmax - sp.off;
-    const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
-    // h = 0 threads fetch LSE, h = 1 threads Delta, of query q0(t) + r, a tile ahead.
-    float nxt = 0.f;
-    auto fetch_row = [&](int t) {
-      const int q = w.q0(t) + r;
-      if (q < sp.Lq) {
-        const size_t gi = static_cast<size_t>(walk_bhq(w, a, t)) * sp.Lq + q;
-        nxt = h == 0 ? a.lse[gi] : a.delta[gi];
-      } else {
-        nxt = h == 0 ? SWA_POS_INF : 0.f;
-      }
-    };
-    if (w.T > 0) fetch_row(0);
-    bool ok = true;
-    for (int t = 0; t < w.T; ++t) {
-      const int q0 = w.q0(t);
-      float* nl2 = s_rows + (t & 1) * 2 * kBlockM;  // -LSE log2(e)
-      float* nd = nl2 + kBlockM;                     // -Delta
-      if (h == 0)
-        nl2[r] = -nxt * kLog2e;
-      else
-        nd[r] = -nxt;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::kVecFull + (t & 1)));
-      if (!(ok = warp_wait(bar(C::kVecFull + (t & 1)), (t >> 1) & 1, &abort_flag, a.err))) break;
-      if (t + 1 < w.T) fetch_row(t + 1);
-      if (!(ok = warp_wait(bar(C::kSFull), t & 1, &abort_flag, a.err))) break;
-      tc_fence_after();
-      float p[64];
-      const int base = q0 + 64 * static_cast<int>(h);
-      p_transposed(p, tmem + lane_base + C::kColS + 64u * h, nl2 + 64 * h, a.scale_log2,
-                   !(q0 >= w.q_int_lo && q0 <= w.q_int_hi), vis_lo - base, vis_hi - base);
-      warp_arrive(bar(C::kSEmpty));  // S^T_{t+1} may overwrite S^T_t now
-      if (!(ok = warp_wait(bar(C::kDPFull), t & 1, &abort_flag, a.err))) break;
-      tc_fence_after();
-      ds_transposed<F16>(tmem + lane_base + C::kColDP + 64u * h, nd + 64 * h, p);
-      tmem_wait_st();
-      warp_arrive(bar(C::kDSFull));
-    }
-    if (ok && warp_wait(bar(C::kDone), 0, &abort_flag, a.err)) {
-      tc_fence_after();
-      // dK * scale -> 16-bit, staged in the K buffer (every MMA has completed).
-      key_epilogue<F16>(tmem + lane_base + C::kColAcc, sK, r, h, a.scale, w.T == 0,
-                        bar(C::kOutFull), &tm_dk, w.k0, w.bhk, &abort_flag, a.err);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 9) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-// ================================================================================================
 // Host launchers
 // ================================================================================================
 Args256 make_args(const Problem& pb, const float* lse, const float* delta, void* dq,
@@ -1300,7 +819,6 @@ Args256 make_args(const Problem& pb, const float* lse, const float* delta, void*
   Args256 a;
   a.lse = lse;
   a.lse_out = lse_out;
-  a.dk = a.dv = nullptr;
   a.delta = delta;
   a.dq = static_cast<uint16_t*>(dq);
   a.BH = pb.B * pb.Hq;
@@ -1309,7 +827,6 @@ Args256 make_args(const Problem& pb, const float* lse, const float* delta, void*
   a.G = pb.Hq / pb.Hkv;
   a.nqb = (pb.span.Lq + kBlockM - 1) / kBlockM;
   a.ntiles = a.nqb * a.BH;
-  a.BHK = pb.B * pb.Hkv;
   a.span = pb.span;
   a.scale = pb.scale;
   a.scale_log2 = pb.scale * kLog2e;
@@ -1360,30 +877,6 @@ cudaError_t dq256(const Problem& pb, const void* q, const void* k, const void* v
   return cudaGetLastError();
 }
 
-template <bool F16>
-cudaError_t dkdv256(const Problem& pb, const void* q, const void* k, const void* v,
-                    const void* dO, const float* lse, const float* delta, void* dk, void* dv,
-                    cudaStream_t stream) {
-  CUtensorMap tq, tdo, tk, tv, tdk, tdv;
-  if (!qmap(&tq, q, pb) || !qmap(&tdo, dO, pb) || !kmap(&tk, k, pb) || !kmap(&tv, v, pb) ||
-      !kmap(&tdk, dk, pb) || !kmap(&tdv, dv, pb))
-    return cudaErrorInvalidValue;
-  Args256 a = make_args(pb, lse, delta, nullptr);
-  a.dk = static_cast<uint16_t*>(dk);
-  a.dv = static_cast<uint16_t*>(dv);
-  const unsigned grid = static_cast<unsigned>((pb.span.Lk + kBlockN - 1) / kBlockN) *
-                        static_cast<unsigned>(a.BHK);
-  auto kk = swa_dk256_kernel<F16>;
-  cudaError_t e = set_smem(kk, K256::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  kk<<<grid, K256::kThreads, K256::kSmemBytes, stream>>>(tq, tdo, tk, tv, tdk, a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  auto kv = swa_dv256_kernel<F16>;
-  if ((e = set_smem(kv, V256::kSmemBytes)) != cudaSuccess) return e;
-  kv<<<grid, V256::kThreads, V256::kSmemBytes, stream>>>(tq, tdo, tk, tdv, a);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 cudaError_t launch_fwd_d256(const Problem& pb, const void* q, const void* k, const void* v,
@@ -1404,10 +897,7 @@ cudaError_t launch_dq_d256(const Problem& pb, const void* q, const void* k, cons
 cudaError_t launch_dkdv_d256(const Problem& pb, const void* q, const void* k, const void* v,
                              const void* dO, const float* lse, const float* delta, void* dk,
                              void* dv, cudaStream_t stream) {
-  if (dkdv256_pair_applies(pb))
-    return launch_dkdv256_pair(pb, q, k, v, dO, lse, delta, dk, dv, stream);
-  return pb.f16 ? dkdv256<true>(pb, q, k, v, dO, lse, delta, dk, dv, stream)
-                : dkdv256<false>(pb, q, k, v, dO, lse, delta, dk, dv, stream);
+  return launch_dkdv256_pair(pb, q, k, v, dO, lse, delta, dk, dv, stream);
 }
 
 }  // namespace swa
