@@ -13,8 +13,10 @@
 // cores.  Q, P, O, the softmax and the epilogue stay per CTA, as in swa_fwd.cu.
 //
 // Warp roles (384 threads per CTA):
-//   warps 0-7  softmax of this CTA's rows (as swa_fwd.cu); the P and O-read handshakes arrive on
-//              rank 0's barriers (16 arrivals: both CTAs' softmax warps).
+//   warps 0-7  softmax of this CTA's rows: warp w owns 16 whole rows (TMEM lanes 32 (w % 4) +
+//              16 (w / 4) ..), read with the 16x256b TMEM shape, so that each row lies in four
+//              threads of one warp; the P and O-read handshakes arrive on rank 0's barriers (16
+//              arrivals: both CTAs' softmax warps).
 //   warp 8     TMA producer of this CTA's Q and K halves; warp 11 of its V halves.
 //   warp 9     rank 0: MMA issuer for the pair; commits arrive on the barriers of both CTAs.
 //              rank 1: relay — waits for each of its own Q / K / V copies, in the order rank 0
@@ -22,8 +24,8 @@
 //              count its own copy and rank 1's relay).
 //   warp 10    output: TMA store of this CTA's O tile.
 // TMEM (each CTA, allocated for the pair): three 128-column S buffers at [0,384) — buffer b holds
-// S_g for the blocks g = b mod 3, then P_g (bf16 pairs) over the first 32 of each half-row's 64
-// columns — and O at [384,512).  With three buffers and the deep K ring that half-tiles leave room
+// S_g for the blocks g = b mod 3, then P_g over its first 64 columns (16-bit pairs: keys 2c and
+// 2c + 1 in column c) — and O at [384,512).  With three buffers and the deep K ring that half-tiles leave room
 // for, the S products run up to three blocks ahead of the P V products.
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
@@ -51,8 +53,7 @@ struct FwdPairCfg {
   static constexpr int kOffQ = 0;  // 2 buffers
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kKHalfBytes;
-  static constexpr int kOffRed = kOffV + kVStages * kVHalfBytes;  // [2 slots][2 halves][128] fp32
-  static constexpr int kOffBar = kOffRed + 2 * 2 * kBlockM * 4;
+  static constexpr int kOffBar = kOffV + kVStages * kVHalfBytes;
   static constexpr int kQFull = 0;   // 2
   static constexpr int kQEmpty = 2;  // 2
   static constexpr int kKFull = 4;
@@ -63,8 +64,7 @@ struct FwdPairCfg {
   static constexpr int kSFull = kVEmpty + kVStages;  // kSBufs
   static constexpr int kPFull = kSFull + kSBufs;     // kSBufs (rank 0's: both CTAs' softmax warps)
   static constexpr int kPVDone = kPFull + kSBufs;    // kSBufs
-  static constexpr int kXch = kPVDone + kSBufs;      // [4 lane quarters][2 slots]
-  static constexpr int kOEmpty = kXch + 8;           // rank 0's: both CTAs have read O
+  static constexpr int kOEmpty = kPVDone + kSBufs;   // rank 0's: both CTAs have read O
   static constexpr int kOutFull = kOEmpty + 1;       // 2
   static constexpr int kDrain = kOutFull + 2;
   static constexpr int kNumBars = kDrain + 1;
@@ -129,7 +129,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
   const uint32_t sQ0 = smem_u32(smem + C::kOffQ);
   const uint32_t sK0 = smem_u32(smem + C::kOffK);
   const uint32_t sV0 = smem_u32(smem + C::kOffV);
-  float* s_red = reinterpret_cast<float*>(smem + C::kOffRed);
   const uint32_t rank = cluster_rank();
   const bool lead = rank == 0u;
   const int tile0 = static_cast<int>(blockIdx.x >> 1);
@@ -159,7 +158,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
       mbar_init(bar(C::kVFull + s), full_count);
       mbar_init(bar(C::kVEmpty + s), 1);
     }
-    for (int x = 0; x < 8; ++x) mbar_init(bar(C::kXch + x), 2);
     mbar_init(bar(C::kOEmpty), C::kPairWarps);
     mbar_init(bar(C::kDrain), 1);
     fence_barrier_init();
@@ -292,8 +290,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
       umma2_commit_w(bar(C::kKEmpty + s));
       return true;
     };
-    // O += P_gg V_gg with P_gg in buffer gg mod 3 (keys 16 ks .. 16 ks + 15 at packed column
-    // 8 ks + 32 (ks / 4)); a tile's first P V overwrites O once both CTAs' epilogues have read it.
+    // O += P_gg V_gg with P_gg in buffer gg mod 3 (keys 16 ks .. 16 ks + 15 at packed columns
+    // 8 ks .. 8 ks + 7); a tile's first P V overwrites O once both CTAs' epilogues have read it.
     auto on_pv = [&](int gg, int it, int j) -> bool {
       const int s = gg % C::kVStages, n = gg / C::kVStages, pb = gg % C::kSBufs;
       if (j == 0 && it > 0 &&
@@ -303,7 +301,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
         return false;
       if (!warp_wait_cluster(bar(C::kVFull + s), n & 1, &abort_flag, a.err)) return false;
       tc_fence_after();
-      umma2_ts_mnmajor_x8_split(tmem + C::kColO, tmem + C::kColS + 128u * pb,
+      umma2_ts_mnmajor_x8(tmem + C::kColO, tmem + C::kColS + 128u * pb,
                                 smem_desc_sw128(sV0 + s * C::kVHalfBytes, C::kVHalfBytes, 1024),
                                 kIdO, j == 0 ? 0u : 1u);
       umma2_commit_w(bar(C::kPVDone + pb));
@@ -348,42 +346,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
     }
   } else {
     // ------------------------------------------------------------------ softmax (warps 0-7)
-    const int r = static_cast<int>(threadIdx.x & 127);
-    const uint32_t h = warp >> 2;
-    const uint32_t quarter = warp & 3u;
-    const uint32_t lane_base = (quarter * 32u) << 16;
+    // Thread t of warp w holds rows R0 = 32 (w % 4) + 16 (w / 4) + t / 4 and R1 = R0 + 8 of the
+    // tile, and of every group j (0..15) of 8 columns the columns 8j + 2kq, 8j + 2kq + 1 (kq =
+    // t % 4): x[4j], x[4j+1] of R0 and x[4j+2], x[4j+3] of R1.  Row maxima and sums combine the four
+    // threads kq = 0..3 with two shuffles; P goes back as packed pairs, column 4j + kq of each row,
+    // which is the 16x128b store layout.
+    const uint32_t lane0 = 32u * (warp & 3u) + 16u * (warp >> 2);
+    const uint32_t lane_base = lane0 << 16;
+    const int r0 = static_cast<int>(lane0 + (lane >> 2));  // R0 (R1 = R0 + 8)
+    const int kq = static_cast<int>(lane & 3u);
     const float sl2 = a.scale_log2;
-    int xn = 0;
-    auto exchange = [&](float v, float* other) -> bool {
-      float* red = s_red + (xn & 1) * 2 * kBlockM;
-      red[h * kBlockM + r] = v;
-      __syncwarp();
-      const uint32_t xb = bar(C::kXch + quarter * 2 + (xn & 1));
-      if (lane == 0) mbar_arrive(xb);
-      if (!warp_wait(xb, (xn >> 1) & 1, &abort_flag, a.err)) return false;
-      *other = red[(h ^ 1u) * kBlockM + r];
-      ++xn;
-      return true;
+    auto row_max = [](float v) {
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+      return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+    };
+    auto row_sum = [](float v) {
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      return v + __shfl_xor_sync(0xffffffffu, v, 2);
     };
     int g = 0;
     bool ok = true;
     for (int t = tile0, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
       const PairTile f = fwd_pair_tile(t, a, sp, rank);
       const int q0 = f.q0;
-      const int row = q0 + r;
-      float m_ref = SWA_NEG_INF;
-      float l = 0.f;
+      const int row0 = q0 + r0, row1 = row0 + 8;
+      float m0 = SWA_NEG_INF, m1 = SWA_NEG_INF;  // reference max (log2 domain) of rows R0, R1
+      float l0 = 0.f, l1 = 0.f;                  // partial sums over this thread's columns
       for (int j = 0; j < f.nkv; ++j) {
         const int gg = g + j;
         const int k0 = (f.kb_lo + j) * kBlockN;
         const int sb = gg % C::kSBufs;
         if (!(ok = warp_wait(bar(C::kSFull + sb), (gg / C::kSBufs) & 1, &abort_flag, a.err))) break;
         tc_fence_after();
+        const uint32_t s_addr = tmem + lane_base + C::kColS + 128u * sb;
         float x[64];
         {
           uint32_t rr[2][32];
-          tmem_ld32(tmem + lane_base + C::kColS + 128u * sb + 64u * h, rr[0]);
-          tmem_ld32(tmem + lane_base + C::kColS + 128u * sb + 64u * h + 32u, rr[1]);
+          tmem_ld16x256_x8(s_addr, rr[0]);
+          tmem_ld16x256_x8(s_addr + 64u, rr[1]);
           tmem_wait_ld_all();
           reg_fence(rr[0]);
           reg_fence(rr[1]);
@@ -391,58 +391,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
           for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(rr[i >> 5][i & 31]);
         }
         if (!sp.interior(q0, k0)) {
-          const int rel = row + sp.off - k0 - 64 * static_cast<int>(h);
-          const int lo = rel - sp.dmax;
-          const int hi = min(rel - sp.dmin, sp.Lk - 1 - k0 - 64 * static_cast<int>(h));
+          // column 8 (i / 4) + 2 kq + (i & 1) of row R0 (i % 4 < 2) or R1, visible to that row and
+          // inside the key sequence
+          const int rel0 = row0 + sp.off - k0 - 2 * kq, rel1 = rel0 + 8;
+          const int lo0 = rel0 - sp.dmax, hi0 = min(rel0 - sp.dmin, sp.Lk - 1 - k0 - 2 * kq);
+          const int lo1 = rel1 - sp.dmax, hi1 = min(rel1 - sp.dmin, sp.Lk - 1 - k0 - 2 * kq);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) x[c] = (c >= lo && c <= hi) ? x[c] : SWA_NEG_INF;
-        }
-        uint32_t pk[32];
-        auto exponentiate = [&](float m) -> float {
-          const float2 scale2 = make_float2(sl2, sl2), neg_m2 = make_float2(-m, -m);
-          float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                           make_float2(0.f, 0.f)};
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float2 tt = __ffma2_rn(make_float2(x[2 * c], x[2 * c + 1]), scale2, neg_m2);
-            const float2 e = make_float2(ex2(tt.x), ex2(tt.y));
-            rs2[c & 3] = __fadd2_rn(rs2[c & 3], e);
-            pk[c] = Elem<F16>::pack(e.x, e.y);
+          for (int i = 0; i < 64; ++i) {
+            const int c = 8 * (i >> 2) + (i & 1);
+            const bool vis = (i & 2) ? (c >= lo1 && c <= hi1) : (c >= lo0 && c <= hi0);
+            x[i] = vis ? x[i] : SWA_NEG_INF;
           }
-          return ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) +
-                 ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
+        }
+        uint32_t pk[32];  // pk[2j] row R0, pk[2j+1] row R1: packed column 4j + kq
+        float b0 = 0.f, b1 = 0.f;
+        auto exponentiate = [&](float mu0, float mu1) {
+          const float2 scale2 = make_float2(sl2, sl2);
+          const float2 n0 = make_float2(-mu0, -mu0), n1 = make_float2(-mu1, -mu1);
+          float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+          float2 u0 = make_float2(0.f, 0.f), u1 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const float2 t0 = __ffma2_rn(make_float2(x[4 * jj], x[4 * jj + 1]), scale2, n0);
+            const float2 t1 = __ffma2_rn(make_float2(x[4 * jj + 2], x[4 * jj + 3]), scale2, n1);
+            const float2 e0 = make_float2(ex2(t0.x), ex2(t0.y));
+            const float2 e1 = make_float2(ex2(t1.x), ex2(t1.y));
+            if (jj & 1) {
+              u0 = __fadd2_rn(u0, e0);
+              u1 = __fadd2_rn(u1, e1);
+            } else {
+              s0 = __fadd2_rn(s0, e0);
+              s1 = __fadd2_rn(s1, e1);
+            }
+            pk[2 * jj] = Elem<F16>::pack(e0.x, e0.y);
+            pk[2 * jj + 1] = Elem<F16>::pack(e1.x, e1.y);
+          }
+          b0 = (s0.x + s0.y) + (u0.x + u0.y);
+          b1 = (s1.x + s1.y) + (u1.x + u1.y);
         };
+        // One pass against the running reference max; redone exactly on a tile's first block or
+        // when a row's block sum exceeds 2^12 (the four threads of a row decide alike).
         bool redo = true;
-        float bsum = 0.f;
-        if (__all_sync(0xffffffffu, m_ref != SWA_NEG_INF)) {
-          bsum = exponentiate(m_ref);
-          float other;
-          if (!(ok = exchange(bsum, &other))) break;
-          redo = __any_sync(0xffffffffu, !(bsum + other <= kFastSumLimit));
+        if (__all_sync(0xffffffffu, m0 != SWA_NEG_INF && m1 != SWA_NEG_INF)) {
+          exponentiate(m0, m1);
+          redo = __any_sync(0xffffffffu,
+                            !(row_sum(b0) <= kFastSumLimit) || !(row_sum(b1) <= kFastSumLimit));
         }
         bool resc = false;
-        float factor = 1.f;
+        float f0 = 1.f, f1 = 1.f;  // rescale factors of rows R0, R1
         if (redo) {
-          float m8[8];
+          float a0 = x[0], a1 = x[2], c0 = x[1], c1 = x[3];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) m8[i] = x[i];
-#pragma unroll
-          for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
-          float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
-          float mx_other;
-          if (!(ok = exchange(mx, &mx_other))) break;
-          mx = fmaxf(mx, mx_other);
-          const float m_new = fmaxf(m_ref, mx);
-          resc = m_new > m_ref + kRescaleThreshold;
-          if (resc) {
-            factor = ex2(m_ref - m_new);
-            l *= factor;
-            m_ref = m_new;
+          for (int jj = 1; jj < 16; ++jj) {
+            a0 = fmaxf(a0, x[4 * jj]);
+            c0 = fmaxf(c0, x[4 * jj + 1]);
+            a1 = fmaxf(a1, x[4 * jj + 2]);
+            c1 = fmaxf(c1, x[4 * jj + 3]);
           }
-          bsum = exponentiate((m_ref == SWA_NEG_INF) ? 0.f : m_ref);
+          const float mx0 = row_max(fmaxf(a0, c0)) * sl2, mx1 = row_max(fmaxf(a1, c1)) * sl2;
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          if (mn0 > m0 + kRescaleThreshold) {
+            f0 = ex2(m0 - mn0);  // 0 when m0 is -inf
+            l0 *= f0;
+            m0 = mn0;
+            resc = true;
+          }
+          if (mn1 > m1 + kRescaleThreshold) {
+            f1 = ex2(m1 - mn1);
+            l1 *= f1;
+            m1 = mn1;
+            resc = true;
+          }
+          exponentiate((m0 == SWA_NEG_INF) ? 0.f : m0, (m1 == SWA_NEG_INF) ? 0.f : m1);
         }
-        l += bsum;
+        l0 += b0;
+        l1 += b1;
 
         // Rescaling O needs this tile's P V of block gg - 1 to have landed.
         if (j >= 1 && __any_sync(0xffffffffu, resc)) {
@@ -451,20 +474,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
             break;
           tc_fence_after();
 #pragma unroll
-          for (int c0 = 0; c0 < D / 2; c0 += 32) {
-            const uint32_t oc = tmem + lane_base + C::kColO + (D / 2) * h + c0;
+          for (int hc = 0; hc < D / 64; ++hc) {
+            const uint32_t oc = tmem + lane_base + C::kColO + 64u * hc;
             uint32_t rr[32];
-            tmem_ld32(oc, rr);
+            tmem_ld16x256_x8(oc, rr);
             tmem_wait_ld(rr);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * factor);
-            tmem_st32(oc, rr);
+            for (int i = 0; i < 32; ++i)
+              rr[i] = __float_as_uint(__uint_as_float(rr[i]) * ((i & 2) ? f1 : f0));
+            tmem_st16x256_x8(oc, rr);
           }
         } else {
           tc_fence_after();
         }
-        // keys [64h, 64h+64) -> packed P over the first 32 of the 64 S columns this thread read
-        tmem_st32(tmem + lane_base + C::kColS + 128u * sb + 64u * h, pk);
+        // packed P over the first 64 columns of the buffer (this warp's rows of S have been read)
+        tmem_st16x128_x16(s_addr, pk);
         tmem_wait_st();
         warp_arrive_rank0(bar(C::kPFull + sb));
       }
@@ -472,37 +496,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
       g += f.nkv;
 
       // ---------------------------------------------------------------- tile epilogue
-      float l_other = 0.f;
-      if (!(ok = exchange(l, &l_other))) break;
+      const float lr0 = row_sum(l0), lr1 = row_sum(l1);
       const int last = g - 1;
       if (!(ok = warp_wait(bar(C::kPVDone + last % C::kSBufs), (last / C::kSBufs) & 1, &abort_flag,
                            a.err)))
         break;
       tc_fence_after();
-      constexpr int kHalf = D / 2;
-      uint32_t rr[kHalf / 32][32];
+      uint32_t ro[D / 64][32];
 #pragma unroll
-      for (int c4 = 0; c4 < kHalf / 32; ++c4)
-        tmem_ld32(tmem + lane_base + C::kColO + kHalf * h + 32u * c4, rr[c4]);
+      for (int hc = 0; hc < D / 64; ++hc) tmem_ld16x256_x8(tmem + lane_base + C::kColO + 64u * hc, ro[hc]);
       tmem_wait_ld_all();
 #pragma unroll
-      for (int c4 = 0; c4 < kHalf / 32; ++c4) reg_fence(rr[c4]);
+      for (int hc = 0; hc < D / 64; ++hc) reg_fence(ro[hc]);
       warp_arrive_rank0(bar(C::kOEmpty));
 
-      const float l_row = l + l_other;
-      const float inv_l = 1.f / l_row;
-      const float m_use = (m_ref == SWA_NEG_INF) ? 0.f : m_ref;
-      if (row < sp.Lq && h == 0)
-        a.lse[static_cast<size_t>(f.bh) * sp.Lq + row] = (m_use + log2f(l_row)) * kLn2;
+      const float inv0 = 1.f / lr0, inv1 = 1.f / lr1;
+      if (kq == 0) {
+        const size_t base = static_cast<size_t>(f.bh) * sp.Lq;
+        if (row0 < sp.Lq)
+          a.lse[base + row0] = (((m0 == SWA_NEG_INF) ? 0.f : m0) + log2f(lr0)) * kLn2;
+        if (row1 < sp.Lq)
+          a.lse[base + row1] = (((m1 == SWA_NEG_INF) ? 0.f : m1) + log2f(lr1)) * kLn2;
+      }
+      // O / l -> 16-bit, staged in the Q buffer in the swizzled layout of the TMA map: group j of
+      // 64-column chunk hc is 16-byte unit j of the row, this thread's pair its word kq.
       const uint32_t sQ = sQ0 + (it & 1) * C::kTileBytes;
 #pragma unroll
-      for (int c4 = 0; c4 < kHalf / 32; ++c4) {
-        uint32_t pk[16];
+      for (int hc = 0; hc < D / 64; ++hc) {
+        const uint32_t chunk = sQ + hc * C::kChunkBytes + 4u * kq;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = Elem<F16>::pack(__uint_as_float(rr[c4][2 * i]) * inv_l,
-                                  __uint_as_float(rr[c4][2 * i + 1]) * inv_l);
-        stage_row32_sw128(sQ, r, kHalf * h + 32u * c4, pk);
+        for (int jj = 0; jj < 8; ++jj) {
+          st_shared_b32(chunk + sw128_offset(r0, jj),
+                        Elem<F16>::pack(__uint_as_float(ro[hc][4 * jj]) * inv0,
+                                        __uint_as_float(ro[hc][4 * jj + 1]) * inv0));
+          st_shared_b32(chunk + sw128_offset(r0 + 8, jj),
+                        Elem<F16>::pack(__uint_as_float(ro[hc][4 * jj + 2]) * inv1,
+                                        __uint_as_float(ro[hc][4 * jj + 3]) * inv1));
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();

@@ -432,6 +432,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+// 16 lanes x 8 groups of 8 columns (16x256b shape, 8 repetitions): with L the lane in taddr,
+// thread t receives, for group j, r[4j], r[4j+1] = columns 8j + 2(t%4), +1 of lane L + t/4 and
+// r[4j+2], r[4j+3] = the same columns of lane L + 8 + t/4.  Issues the load (no wait).
+__device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : SWA_R8(0), SWA_R8(8), SWA_R8(16), SWA_R8(24)
+      : "r"(taddr));
+}
+
 // Waits for this thread's outstanding TMEM loads; `r` is passed through so that no use of the
 // loaded registers can be scheduled before the wait.
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
@@ -455,6 +467,29 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      SWA_W8(0), SWA_W8(8), SWA_W8(16), SWA_W8(24)
+      : "memory");
+}
+
+// The store counterpart of tmem_ld16x256_x8 (same register layout).
+__device__ __forceinline__ void tmem_st16x256_x8(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      SWA_W8(0), SWA_W8(8), SWA_W8(16), SWA_W8(24)
+      : "memory");
+}
+
+// 16 lanes x 16 groups of 4 columns (16x128b shape, 16 repetitions): thread t writes r[2j] to
+// column 4j + t%4 of lane L + t/4 and r[2j+1] to the same column of lane L + 8 + t/4.
+__device__ __forceinline__ void tmem_st16x128_x16(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x16.b32 [%0], "
       "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
       "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
           taddr),
@@ -515,6 +550,10 @@ struct Elem {
       return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
   }
 };
+
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t a) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
