@@ -135,6 +135,24 @@ def test_d256_unvisited_keys_get_exact_zeros(swa, causal):
     assert np.abs(gpu["dv"][:, :, first_seen:]).max() > 0
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_d256_key_block_pair_half_unvisited(swa, causal):
+    """dK and dV run on CTA pairs over neighbouring key blocks, which walk the union of the two
+    blocks' query blocks.  Here no query sees keys below 700, so of the pair (512..639, 640..767)
+    the first block is unvisited while the second is partly visited: the first must come out as
+    exact zeros and the second match the oracle."""
+    sh = Shape(1, 2, 1, 100, 1000, 201, causal=causal, seed=6)
+    inp, scale = _inputs(sh)
+    gpu = _run(swa, sh, inp, scale)
+    first_seen = (sh.Lk - sh.Lq) - (sh.W - 1)
+    assert first_seen == 700 and 640 <= first_seen < 768  # inside key block 5, block 4 unseen
+    assert np.all(gpu["dk"][:, :, :first_seen] == 0.0)
+    assert np.all(gpu["dv"][:, :, :first_seen] == 0.0)
+    ref = orc.oracle_backward(inp["q"], inp["k"], inp["v"], inp["do"], sh.W, scale,
+                              causal=sh.causal)
+    _check(gpu, ref, None, sh.W)
+
+
 def test_d256_autograd(swa):
     """The autograd wrapper at D = 256 matches the explicit calls."""
     sh = Shape(1, 2, 1, 256, 256, 64, seed=5)
