@@ -23,16 +23,13 @@
 // half of K, VC the head-dim half of V.
 // TMEM (each CTA, allocated for the pair): [0,128) S / P buffer 0, [128,256) S / P buffer 1,
 // [256,512) O.
+#include "swa_d256.cuh"
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 #include "swa_tmap.h"
 
 namespace swa {
 namespace {
-
-// The running-max policy of the other forward kernels (exact softmax either way).
-constexpr float kRescaleThresholdP256 = 8.0f;
-constexpr float kFastSumLimitP256 = 4096.0f;
 
 struct FwdP256 {
   static constexpr int kD = 256;
@@ -312,168 +309,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
                [&](int i, bool, int, int) { return relay(full(i), parity(i)); });
   } else {
     // ------------------------------------------------------------ softmax (warps 0-7)
-    const int r = static_cast<int>(threadIdx.x & 127);  // row within the tile == TMEM lane
-    const uint32_t h = warp >> 2;                          // column half of every score tile
-    const uint32_t quarter = warp & 3u;
-    const uint32_t lane_base = (quarter * 32u) << 16;
-    const float sl2 = a.scale_log2;
-    int xn = 0;  // exchanges done so far
-    // Swap a per-row value with the thread that owns the other half of the row (slot xn & 1 was
-    // last used two exchanges ago, and the partner passed the exchange in between only after
-    // reading it).
-    auto exchange = [&](float v, float* other) -> bool {
-      float* red = s_red + (xn & 1) * 2 * kBlockM;
-      red[h * kBlockM + r] = v;
-      __syncwarp();
-      const uint32_t xb = bar(C::kXch + quarter * 2 + (xn & 1));
-      if (lane == 0) mbar_arrive(xb);
-      if (!warp_wait(xb, (xn >> 1) & 1, &abort_flag, a.err)) return false;
-      *other = red[(h ^ 1u) * kBlockM + r];
-      ++xn;
-      return true;
-    };
-    int g = 0;
-    bool ok = true;
-    for (int t = tile0, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
-      const FwdP256Tile f = fwdp256_tile(t, a, sp, rank);
-      const int q0 = f.q0;
-      const int row = q0 + r;
-      float m_ref = SWA_NEG_INF;  // reference max (log2 domain) that P and l are taken against
-      float l = 0.f;              // partial row sum over this thread's half of the columns
-      for (int j = 0; j < f.nkv; ++j) {
-        const int gg = g + j;
-        const int k0 = (f.kb_lo + j) * kBlockN;
-        const int sb = gg & 1;
-        if (!(ok = warp_wait(bar(C::kSFull + sb), (gg >> 1) & 1, &abort_flag, a.err))) break;
-        tc_fence_after();
-        const uint32_t s_col = tmem + lane_base + C::kColS + 128u * sb + 64u * h;
-        float x[64];  // raw scores S (the scale is applied inside the exponent)
-        {
-          uint32_t rr[2][32];
-          tmem_ld32(s_col, rr[0]);
-          tmem_ld32(s_col + 32u, rr[1]);
-          tmem_wait_ld_all();
-          reg_fence(rr[0]);
-          reg_fence(rr[1]);
-#pragma unroll
-          for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(rr[c >> 5][c & 31]);
-        }
-        if (!sp.interior(q0, k0)) {
-          // Columns c (keys k0 + 64h + c) visible to row `row`, and inside the key sequence.
-          const int rel = row + sp.off - k0 - 64 * static_cast<int>(h);
-          const int lo = rel - sp.dmax;
-          const int hi = min(rel - sp.dmin, sp.Lk - 1 - k0 - 64 * static_cast<int>(h));
-#pragma unroll
-          for (int c = 0; c < 64; ++c) x[c] = (c >= lo && c <= hi) ? x[c] : SWA_NEG_INF;
-        }
-        uint32_t pk[32];
-        auto exponentiate = [&](float m) -> float {
-          const float2 scale2 = make_float2(sl2, sl2), neg_m2 = make_float2(-m, -m);
-          float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                           make_float2(0.f, 0.f)};
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float2 tt = __ffma2_rn(make_float2(x[2 * c], x[2 * c + 1]), scale2, neg_m2);
-            const float2 e = make_float2(ex2(tt.x), ex2(tt.y));
-            rs2[c & 3] = __fadd2_rn(rs2[c & 3], e);
-            pk[c] = Elem<F16>::pack(e.x, e.y);
-          }
-          return ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) +
-                 ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
-        };
-        // One pass against the running reference max; redone exactly on a tile's first block or
-        // when a row's block sum exceeds 2^12 (both halves of a row decide alike).
-        bool redo = true;
-        float bsum = 0.f;
-        if (__all_sync(0xffffffffu, m_ref != SWA_NEG_INF)) {
-          bsum = exponentiate(m_ref);
-          float other;
-          if (!(ok = exchange(bsum, &other))) break;
-          redo = __any_sync(0xffffffffu, !(bsum + other <= kFastSumLimitP256));
-        }
-        bool resc = false;
-        float factor = 1.f;
-        if (redo) {
-          float m8[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) m8[c] = x[c];
-#pragma unroll
-          for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
-          float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
-          float mx_other;
-          if (!(ok = exchange(mx, &mx_other))) break;
-          mx = fmaxf(mx, mx_other);
-          const float m_new = fmaxf(m_ref, mx);
-          resc = m_new > m_ref + kRescaleThresholdP256;
-          if (resc) {
-            factor = ex2(m_ref - m_new);  // 0 when m_ref is -inf
-            l *= factor;
-            m_ref = m_new;
-          }
-          bsum = exponentiate((m_ref == SWA_NEG_INF) ? 0.f : m_ref);
-        }
-        l += bsum;
-        // Rescaling O needs this tile's P V of block gg - 1 (and so every earlier one) to have
-        // landed; a tile's first block needs none (its P V overwrites O).
-        if (j >= 1 && __any_sync(0xffffffffu, resc)) {
-          if (!(ok = warp_wait(bar(C::kPVDone + (sb ^ 1)), ((gg - 1) >> 1) & 1, &abort_flag,
-                               a.err)))
-            break;
-          tc_fence_after();
-#pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
-            const uint32_t oc = tmem + lane_base + C::kColO + 128u * h + c0;
-            uint32_t rr[32];
-            tmem_ld32(oc, rr);
-            tmem_wait_ld(rr);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * factor);
-            tmem_st32(oc, rr);
-          }
-        } else {
-          tc_fence_after();
-        }
-        // keys [64h, 64h + 64) -> packed P over the first 32 of this thread's S columns (the
-        // landing of S_gg implies P V_{gg-2}, which read the previous P here, has completed).
-        tmem_st32(s_col, pk);
-        tmem_wait_st();
-        warp_arrive_rank0(bar(C::kPFull + sb));
-      }
-      if (!ok) break;
-      g += f.nkv;
-
-      // ---------------------------------------------------------- tile epilogue
-      float l_other = 0.f;
-      if (!(ok = exchange(l, &l_other))) break;
-      const int last = g - 1;
-      if (!(ok = warp_wait(bar(C::kPVDone + (last & 1)), (last >> 1) & 1, &abort_flag, a.err)))
-        break;
-      tc_fence_after();
-      const float l_row = l + l_other;
-      const float inv_l = 1.f / l_row;
-      const float m_use = (m_ref == SWA_NEG_INF) ? 0.f : m_ref;
-      if (row < sp.Lq && h == 0)
-        a.lse[static_cast<size_t>(f.bh) * sp.Lq + row] = (m_use + log2f(l_row)) * kLn2;
-      // O / l -> 16-bit, staged in the Q buffer (every S of the tile has completed) in the
-      // swizzled layout of the TMA map; warp 10 stores it.
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kColO + 128u * h + 32u * c4, rr);
-        tmem_wait_ld(rr);
-        uint32_t o16[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          o16[c] = Elem<F16>::pack(__uint_as_float(rr[2 * c]) * inv_l,
-                                   __uint_as_float(rr[2 * c + 1]) * inv_l);
-        stage_row32_sw128(sQ, r, 128u * h + 32u * c4, o16);
-      }
-      warp_arrive_rank0(bar(C::kOEmpty));  // the next tile's first P V may overwrite O now
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::kOutFull));
-    }
+    static_assert(C::kPFull - C::kSFull == d256::FwdBar::kPFull &&
+                      C::kPVDone - C::kSFull == d256::FwdBar::kPVDone &&
+                      C::kXch - C::kSFull == d256::FwdBar::kXch &&
+                      C::kOEmpty - C::kSFull == d256::FwdBar::kOEmpty &&
+                      C::kOutFull - C::kSFull == d256::FwdBar::kOutFull,
+                  "softmax barrier layout");
+    const d256::FwdSoftmax cx{tmem + C::kColS, sQ,        s_red,      bar(C::kSFull),
+                              &abort_flag,     a.err,     a.scale_log2, a.lse};
+    d256::fwd_softmax<F16, true>(cx, sp, tile0, tile_step, a.ntiles,
+                                 [&](int t) { return fwdp256_tile(t, a, sp, rank); });
   }
 
   // Every cross-CTA arrival and every pair MMA (rank 0 waited for its drain) is complete once both
