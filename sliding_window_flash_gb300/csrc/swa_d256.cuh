@@ -1,6 +1,7 @@
-// swa_d256.cuh — device helpers shared by the head-dimension-256 kernels (swa_d256.cu and the
+// swa_d256.cuh — device code shared by the head-dimension-256 kernels (swa_d256.cu and the
 // CTA-pair kernels next to it): the score-column mask, the transposed probabilities and dS of
-// the key-block kernels and their accumulator epilogue.
+// the key-block kernels and their accumulator epilogue, and the compute warps of the forward and
+// dQ kernels (one routine each for the single-CTA and the pair kernel).
 #pragma once
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
@@ -322,6 +323,155 @@ __device__ __forceinline__ void fwd_softmax(const FwdSoftmax& cx, const Span& sp
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(FwdBar::kOutFull));
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// The dQ kernels' compute warps (warps 0-7 of the D = 256 dQ kernels, single-CTA and pair): two
+// threads per query row as in the forward; per key block P = exp(scale S - LSE) (window-masked)
+// and dS = P (dP - Delta) go back over the dP columns as packed pairs; each tile's dQ * scale is
+// read out of TMEM and stored to global memory directly (rows past Lq are not written).
+// ------------------------------------------------------------------------------------------------
+struct DqBar {
+  static constexpr int kSFull = 0;   // S of the block landed
+  static constexpr int kSEmpty = 1;  // S read (rank 0's in a pair)
+  static constexpr int kDPFull = 2;  // dP of the block landed
+  static constexpr int kDSFull = 3;  // dS written (rank 0's in a pair)
+  static constexpr int kDQDone = 4;  // the tile's last dQ product has completed
+  static constexpr int kDQEmpty = 5; // dQ read out (rank 0's in a pair)
+};
+
+// Runs the compute warps over the CTA's tiles tile0, tile0 + tile_step, .. < a.ntiles.  TMEM: S at
+// tmem + 0, dP / dS at + 128, dQ at + 256; `bars` is the address of the first of the six
+// consecutive barriers of DqBar.  `a` supplies lse, delta, dq, scale, scale_log2, err and ntiles;
+// tile_of(t) the tile's plane bh, first query q0, first key block kb_lo and block count nkv.
+template <bool F16, bool kPair, typename Args, typename TileOf>
+__device__ __forceinline__ void dq_compute(const Args& a, const Span& sp, uint32_t tmem,
+                                           uint32_t bars, volatile int* abort_flag, int tile0,
+                                           int tile_step, TileOf tile_of) {
+  const uint32_t warp = warp_id();
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  auto arrive = [](uint32_t b) {
+    if constexpr (kPair)
+      warp_arrive_rank0(b);
+    else
+      warp_arrive(b);
+  };
+  const int r = static_cast<int>(threadIdx.x & 127);  // query row within the tile = TMEM lane
+  const uint32_t h = warp >> 2;                          // column half of every score tile
+  const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
+  const float sl2 = a.scale_log2;
+  int g = 0;
+  bool ok = true;
+  // LSE and Delta of this thread's row in the next tile, loaded a whole tile ahead so that
+  // the loads' latency hides behind the current tile.  Rows past the end see P = 0 (their LSE
+  // is taken as +inf), so they add nothing.
+  float nxt_lse = SWA_POS_INF, nxt_dlt = 0.f;
+  auto fetch_rows = [&](int tn) {
+    if (tn >= a.ntiles) return;
+    const auto fn = tile_of(tn);
+    const int rn = fn.q0 + r;
+    if (rn < sp.Lq) {
+      const size_t gn = static_cast<size_t>(fn.bh) * sp.Lq + rn;
+      nxt_lse = a.lse[gn];
+      nxt_dlt = a.delta[gn];
+    } else {
+      nxt_lse = SWA_POS_INF;
+      nxt_dlt = 0.f;
+    }
+  };
+  fetch_rows(tile0);
+  for (int t = tile0, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
+    const auto f = tile_of(t);
+    const int q0 = f.q0;
+    const int row = q0 + r;
+    const bool in_range = row < sp.Lq;
+    const size_t grow = static_cast<size_t>(f.bh) * sp.Lq + row;
+    const float lse2 = nxt_lse == SWA_POS_INF ? SWA_POS_INF : nxt_lse * kLog2e;
+    const float dlt = nxt_dlt;
+    fetch_rows(t + tile_step);
+    for (int j = 0; j < f.nkv; ++j) {
+      const int gg = g + j;
+      const int k0 = (f.kb_lo + j) * kBlockN;
+      if (!(ok = warp_wait(bar(DqBar::kSFull), gg & 1, abort_flag, a.err))) break;
+      tc_fence_after();
+      float p[64];
+      {
+        uint32_t rr[2][32];
+        tmem_ld32(tmem + lane_base + 64u * h, rr[0]);
+        tmem_ld32(tmem + lane_base + 64u * h + 32u, rr[1]);
+        tmem_wait_ld_all();
+        reg_fence(rr[0]);
+        reg_fence(rr[1]);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p[c] = __uint_as_float(rr[c >> 5][c & 31]);
+      }
+      arrive(bar(DqBar::kSEmpty));
+      if (!sp.interior(q0, k0)) {
+        const int rel = row + sp.off - k0 - 64 * static_cast<int>(h);
+        mask64(p, rel - sp.dmax, min(rel - sp.dmin, sp.Lk - 1 - k0 - 64 * static_cast<int>(h)),
+               SWA_NEG_INF);
+      }
+      {
+        const float2 scale2 = make_float2(sl2, sl2), neg_l2 = make_float2(-lse2, -lse2);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float2 tt = __ffma2_rn(make_float2(p[2 * c], p[2 * c + 1]), scale2, neg_l2);
+          p[2 * c] = ex2(tt.x);
+          p[2 * c + 1] = ex2(tt.y);
+        }
+      }
+      // dP_gg landing also means dQ_{gg-1} has finished reading the previous dS here.
+      if (!(ok = warp_wait(bar(DqBar::kDPFull), gg & 1, abort_flag, a.err))) break;
+      tc_fence_after();
+      {
+        const uint32_t dcol = tmem + lane_base + 128u + 64u * h;
+        uint32_t rr[2][32];
+        tmem_ld32(dcol, rr[0]);
+        tmem_ld32(dcol + 32u, rr[1]);
+        tmem_wait_ld_all();
+        reg_fence(rr[0]);
+        reg_fence(rr[1]);
+        uint32_t pk[32];
+        const float2 neg_d2 = make_float2(-dlt, -dlt);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const uint32_t d0 = rr[c >> 4][(2 * c) & 31], d1 = rr[c >> 4][(2 * c + 1) & 31];
+          const float2 ds = __fmul2_rn(
+              make_float2(p[2 * c], p[2 * c + 1]),
+              __fadd2_rn(make_float2(__uint_as_float(d0), __uint_as_float(d1)), neg_d2));
+          pk[c] = Elem<F16>::pack(ds.x, ds.y);
+        }
+        tmem_st32(dcol, pk);  // over the first 32 of this thread's dP columns
+      }
+      tmem_wait_st();
+      arrive(bar(DqBar::kDSFull));
+    }
+    if (!ok) break;
+    g += f.nkv;
+
+    // ---------------------------------------------------------- tile epilogue
+    if (!(ok = warp_wait(bar(DqBar::kDQDone), it & 1, abort_flag, a.err))) break;
+    tc_fence_after();
+    uint16_t* dst_row = a.dq + grow * 256 + 128 * h;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      uint32_t rr[32];
+      tmem_ld32(tmem + lane_base + 256u + 128u * h + 32u * c4, rr);
+      tmem_wait_ld(rr);
+      if (in_range) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          pk[c] = Elem<F16>::pack(__uint_as_float(rr[2 * c]) * a.scale,
+                                  __uint_as_float(rr[2 * c + 1]) * a.scale);
+        uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c4);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      }
+    }
+    arrive(bar(DqBar::kDQEmpty));  // the next tile's first dQ may overwrite the accumulator
   }
 }
 

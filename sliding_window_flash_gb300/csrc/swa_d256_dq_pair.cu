@@ -24,6 +24,7 @@
 // Ring order per tile of n key blocks: KH_0, VH_0, then per block j: KH_{j+1} (if any), KC_j,
 // VH_{j+1} (if any) — KH / VH the key halves of K / V, KC the head-dim half of K.
 // TMEM (each CTA, allocated for the pair): [0,128) S, [128,256) dP / dS, [256,512) dQ.
+#include "swa_d256.cuh"
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 #include "swa_tmap.h"
@@ -320,123 +321,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
                [&](int i, int, int, int) { return relay(full(i), parity(i)); });
   } else {
     // ------------------------------------------------------------ compute (warps 0-7)
-    const int r = static_cast<int>(threadIdx.x & 127);  // query row within the tile = TMEM lane
-    const uint32_t h = warp >> 2;                          // column half of every score tile
-    const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
-    const float sl2 = a.scale_log2;
-    int g = 0;
-    bool ok = true;
-    // LSE and Delta of this thread's row in the next tile, loaded a whole tile ahead.  Rows past
-    // the end see P = 0 (their LSE is taken as +inf), so they add nothing.
-    float nxt_lse = SWA_POS_INF, nxt_dlt = 0.f;
-    auto fetch_rows = [&](int tn) {
-      if (tn >= a.ntiles) return;
-      const DqP256Tile fn = dqp256_tile(tn, a, sp, rank);
-      const int rn = fn.q0 + r;
-      if (rn < sp.Lq) {
-        const size_t gn = static_cast<size_t>(fn.bh) * sp.Lq + rn;
-        nxt_lse = a.lse[gn];
-        nxt_dlt = a.delta[gn];
-      } else {
-        nxt_lse = SWA_POS_INF;
-        nxt_dlt = 0.f;
-      }
-    };
-    fetch_rows(tile0);
-    for (int t = tile0, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
-      const DqP256Tile f = dqp256_tile(t, a, sp, rank);
-      const int q0 = f.q0;
-      const int row = q0 + r;
-      const bool in_range = row < sp.Lq;
-      const size_t grow = static_cast<size_t>(f.bh) * sp.Lq + row;
-      const float lse2 = nxt_lse == SWA_POS_INF ? SWA_POS_INF : nxt_lse * kLog2e;
-      const float dlt = nxt_dlt;
-      fetch_rows(t + tile_step);
-      for (int j = 0; j < f.nkv; ++j) {
-        const int gg = g + j;
-        const int k0 = (f.kb_lo + j) * kBlockN;
-        if (!(ok = warp_wait(bar(C::kSFull), gg & 1, &abort_flag, a.err))) break;
-        tc_fence_after();
-        float p[64];
-        {
-          uint32_t rr[2][32];
-          tmem_ld32(tmem + lane_base + C::kColS + 64u * h, rr[0]);
-          tmem_ld32(tmem + lane_base + C::kColS + 64u * h + 32u, rr[1]);
-          tmem_wait_ld_all();
-          reg_fence(rr[0]);
-          reg_fence(rr[1]);
-#pragma unroll
-          for (int c = 0; c < 64; ++c) p[c] = __uint_as_float(rr[c >> 5][c & 31]);
-        }
-        warp_arrive_rank0(bar(C::kSEmpty));
-        if (!sp.interior(q0, k0)) {
-          const int rel = row + sp.off - k0 - 64 * static_cast<int>(h);
-          const int lo = rel - sp.dmax;
-          const int hi = min(rel - sp.dmin, sp.Lk - 1 - k0 - 64 * static_cast<int>(h));
-#pragma unroll
-          for (int c = 0; c < 64; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : SWA_NEG_INF;
-        }
-        {
-          const float2 scale2 = make_float2(sl2, sl2), neg_l2 = make_float2(-lse2, -lse2);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float2 tt = __ffma2_rn(make_float2(p[2 * c], p[2 * c + 1]), scale2, neg_l2);
-            p[2 * c] = ex2(tt.x);
-            p[2 * c + 1] = ex2(tt.y);
-          }
-        }
-        // dP_gg landing also means dQ_{gg-1} has finished reading the previous dS here.
-        if (!(ok = warp_wait(bar(C::kDPFull), gg & 1, &abort_flag, a.err))) break;
-        tc_fence_after();
-        {
-          const uint32_t dcol = tmem + lane_base + C::kColDP + 64u * h;
-          uint32_t rr[2][32];
-          tmem_ld32(dcol, rr[0]);
-          tmem_ld32(dcol + 32u, rr[1]);
-          tmem_wait_ld_all();
-          reg_fence(rr[0]);
-          reg_fence(rr[1]);
-          uint32_t pk[32];
-          const float2 neg_d2 = make_float2(-dlt, -dlt);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const uint32_t d0 = rr[c >> 4][(2 * c) & 31], d1 = rr[c >> 4][(2 * c + 1) & 31];
-            const float2 ds = __fmul2_rn(
-                make_float2(p[2 * c], p[2 * c + 1]),
-                __fadd2_rn(make_float2(__uint_as_float(d0), __uint_as_float(d1)), neg_d2));
-            pk[c] = Elem<F16>::pack(ds.x, ds.y);
-          }
-          tmem_st32(dcol, pk);  // over the first 32 of this thread's dP columns
-        }
-        tmem_wait_st();
-        warp_arrive_rank0(bar(C::kDSFull));
-      }
-      if (!ok) break;
-      g += f.nkv;
-
-      // ---------------------------------------------------------- tile epilogue
-      if (!(ok = warp_wait(bar(C::kDQDone), it & 1, &abort_flag, a.err))) break;
-      tc_fence_after();
-      uint16_t* dst_row = a.dq + grow * C::kD + 128 * h;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kColDQ + 128u * h + 32u * c4, rr);
-        tmem_wait_ld(rr);
-        if (in_range) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            pk[c] = Elem<F16>::pack(__uint_as_float(rr[2 * c]) * a.scale,
-                                    __uint_as_float(rr[2 * c + 1]) * a.scale);
-          uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c4);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-        }
-      }
-      warp_arrive_rank0(bar(C::kDQEmpty));  // the next tile's first dQ may overwrite it
-    }
+    static_assert(C::kSEmpty - C::kSFull == d256::DqBar::kSEmpty &&
+                      C::kDPFull - C::kSFull == d256::DqBar::kDPFull &&
+                      C::kDSFull - C::kSFull == d256::DqBar::kDSFull &&
+                      C::kDQDone - C::kSFull == d256::DqBar::kDQDone &&
+                      C::kDQEmpty - C::kSFull == d256::DqBar::kDQEmpty && C::kColDP == 128 &&
+                      C::kColDQ == 256,
+                  "dQ compute layout");
+    d256::dq_compute<F16, true>(a, sp, tmem + C::kColS, bar(C::kSFull), &abort_flag, tile0,
+                                tile_step, [&](int t) { return dqp256_tile(t, a, sp, rank); });
   }
 
   // Every cross-CTA arrival and every pair MMA (rank 0 waited for its drain) is complete once both
