@@ -24,6 +24,7 @@
 // TMEM (each CTA, allocated for the pair): [0,128) S, [128,384) two dP buffers, [384,512) dQ.  dS_g
 // (bf16 pairs) goes over the first 32 of each half-row's 64 columns of dP buffer g & 1, so dP of
 // the next block is computed into the other buffer while the compute warps work on this one.
+#include "swa_bwd_dq.cuh"
 #include "swa_kernels.h"
 #include "swa_ptx.cuh"
 #include "swa_tmap.h"
@@ -329,140 +330,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
     }
   } else {
     // ------------------------------------------------------------------ compute (warps 0-7)
-    const int r = static_cast<int>(threadIdx.x & 127);  // query row within the tile = TMEM lane
-    const uint32_t h = warp >> 2;                          // column half of every tile
-    const uint32_t lane_base = ((warp & 3u) * 32u) << 16;
-    const float sl2 = a.scale_log2;
-    // dQ * scale of tile `pit` -> 16-bit, written straight from registers.
-    auto epilogue = [&](int pit, size_t pgrow, bool pin) -> bool {
-      if (!warp_wait(bar(C::kDQDone), pit & 1, &abort_flag, a.err)) return false;
-      tc_fence_after();
-      constexpr int kHalf = D / 2;
-      uint32_t rr[kHalf / 32][32];
-#pragma unroll
-      for (int c4 = 0; c4 < kHalf / 32; ++c4)
-        tmem_ld32(tmem + lane_base + C::kColDQ + kHalf * h + 32u * c4, rr[c4]);
-      tmem_wait_ld_all();
-#pragma unroll
-      for (int c4 = 0; c4 < kHalf / 32; ++c4) reg_fence(rr[c4]);
-      warp_arrive_rank0(bar(C::kDQEmpty));  // the next tile's first dQ may overwrite it
-      if (pin) {
-        uint16_t* dst_row = a.dq + pgrow * D + kHalf * h;
-#pragma unroll
-        for (int c4 = 0; c4 < kHalf / 32; ++c4) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = Elem<F16>::pack(__uint_as_float(rr[c4][2 * i]) * a.scale,
-                                    __uint_as_float(rr[c4][2 * i + 1]) * a.scale);
-          uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c4);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-        }
-      }
-      return true;
-    };
-    int prev_it = -1;
-    size_t prev_grow = 0;
-    bool prev_in = false;
-    int g = 0;
-    bool ok = true;
-    float nxt_lse = SWA_POS_INF, nxt_dlt = 0.f;
-    auto fetch_rows = [&](int tn) {
-      if (tn >= a.ntiles) return;
-      const DqPairTile fn = dq_pair_tile(tn, a, sp, rank);
-      const int rn = fn.q0 + r;
-      if (rn < sp.Lq) {
-        const size_t gn = static_cast<size_t>(fn.bh) * sp.Lq + rn;
-        nxt_lse = a.lse[gn];
-        nxt_dlt = a.delta[gn];
-      } else {
-        nxt_lse = SWA_POS_INF;
-        nxt_dlt = 0.f;
-      }
-    };
-    fetch_rows(tile0);
-    for (int t = tile0, it = 0; ok && t < a.ntiles; t += tile_step, ++it) {
-      const DqPairTile f = dq_pair_tile(t, a, sp, rank);
-      const int q0 = f.q0;
-      const int row = q0 + r;
-      const bool in_range = row < sp.Lq;
-      const size_t grow = static_cast<size_t>(f.bh) * sp.Lq + row;
-      const float lse2 = nxt_lse == SWA_POS_INF ? SWA_POS_INF : nxt_lse * kLog2e;
-      const float dlt = nxt_dlt;
-      fetch_rows(t + tile_step);
-      for (int j = 0; j < f.nkv; ++j) {
-        const int gg = g + j;
-        const int k0 = (f.kb_lo + j) * kBlockN;
-        if (!(ok = warp_wait(bar(C::kSFull), gg & 1, &abort_flag, a.err))) break;
-        tc_fence_after();
-        float p[64];
-        {
-          uint32_t rr[2][32];
-          tmem_ld32(tmem + lane_base + C::kColS + 64u * h, rr[0]);
-          tmem_ld32(tmem + lane_base + C::kColS + 64u * h + 32u, rr[1]);
-          tmem_wait_ld_all();
-          reg_fence(rr[0]);
-          reg_fence(rr[1]);
-#pragma unroll
-          for (int i = 0; i < 64; ++i) p[i] = __uint_as_float(rr[i >> 5][i & 31]);
-        }
-        warp_arrive_rank0(bar(C::kSEmpty));
-        if (j == 0 && prev_it >= 0) {  // the previous tile's epilogue
-          if (!(ok = epilogue(prev_it, prev_grow, prev_in))) break;
-          prev_it = -1;
-        }
-        if (!sp.interior(q0, k0)) {
-          const int rel = row + sp.off - k0 - 64 * static_cast<int>(h);
-          const int lo = rel - sp.dmax;
-          const int hi = min(rel - sp.dmin, sp.Lk - 1 - k0 - 64 * static_cast<int>(h));
-#pragma unroll
-          for (int c = 0; c < 64; ++c) p[c] = (c >= lo && c <= hi) ? p[c] : SWA_NEG_INF;
-        }
-        {
-          const float2 scale2 = make_float2(sl2, sl2), neg_l2 = make_float2(-lse2, -lse2);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float2 tt = __ffma2_rn(make_float2(p[2 * c], p[2 * c + 1]), scale2, neg_l2);
-            p[2 * c] = ex2(tt.x);
-            p[2 * c + 1] = ex2(tt.y);
-          }
-        }
-        const uint32_t dp_col = tmem + lane_base + C::kColDP + 128u * (gg & 1) + 64u * h;
-        if (!(ok = warp_wait(bar(C::kDPFull + (gg & 1)), (gg >> 1) & 1, &abort_flag, a.err))) break;
-        tc_fence_after();
-        {
-          uint32_t rr[2][32];
-          tmem_ld32(dp_col, rr[0]);
-          tmem_ld32(dp_col + 32u, rr[1]);
-          tmem_wait_ld_all();
-          reg_fence(rr[0]);
-          reg_fence(rr[1]);
-          uint32_t pk[32];
-          const float2 neg_d2 = make_float2(-dlt, -dlt);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const uint32_t d0 = rr[i >> 4][(2 * i) & 31], d1 = rr[i >> 4][(2 * i + 1) & 31];
-            const float2 ds = __fmul2_rn(make_float2(p[2 * i], p[2 * i + 1]),
-                                         __fadd2_rn(make_float2(__uint_as_float(d0),
-                                                                __uint_as_float(d1)),
-                                                    neg_d2));
-            pk[i] = Elem<F16>::pack(ds.x, ds.y);
-          }
-          // dS columns [64h, 64h+64) -> packed over the first 32 of the 64 dP columns just read.
-          tmem_st32(dp_col, pk);
-        }
-        tmem_wait_st();
-        warp_arrive_rank0(bar(C::kDSFull + (gg & 1)));
-      }
-      if (!ok) break;
-      g += f.nkv;
-      prev_it = it;
-      prev_grow = grow;
-      prev_in = in_range;
-    }
-    if (ok && prev_it >= 0) epilogue(prev_it, prev_grow, prev_in);
+    static_assert(C::kSEmpty - C::kSFull == dqc::DqBar::kSEmpty &&
+                      C::kDPFull - C::kSFull == dqc::DqBar::kDPFull &&
+                      C::kDSFull - C::kSFull == dqc::DqBar::kDSFull &&
+                      C::kDQDone - C::kSFull == dqc::DqBar::kDQDone &&
+                      C::kDQEmpty - C::kSFull == dqc::DqBar::kDQEmpty && C::kColS == dqc::kColS &&
+                      C::kColDP == dqc::kColDP && C::kColDQ == dqc::kColDQ,
+                  "dQ compute layout");
+    dqc::dq_compute<D, F16, true>(a, sp, tmem, bar(C::kSFull), &abort_flag, tile0, tile_step,
+                                  [&](int t) { return dq_pair_tile(t, a, sp, rank); });
   }
 
   // Every cross-CTA arrival and every pair MMA (rank 0 waited for its drain) is complete once both
