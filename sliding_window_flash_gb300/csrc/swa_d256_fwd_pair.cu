@@ -332,29 +332,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
 }
 
 template <bool F16>
-int max_fwd256_pair_clusters() {
-  static std::mutex mu;
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return sm_count() / 2;
-  std::lock_guard<std::mutex> lk(mu);
-  if (cached[dev] == 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * (sm_count() / 2)));
-    cfg.blockDim = dim3(FwdP256::kThreads);
-    cfg.dynamicSmemBytes = FwdP256::kSmemBytes;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, swa_fwd256_pair_kernel<F16>, &cfg) != cudaSuccess ||
-        n <= 0) {
-      cudaGetLastError();
-      n = sm_count() / 2;
-    }
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
-template <bool F16>
 cudaError_t launch_fwd256_pair_t(const Problem& pb, const void* q, const void* k, const void* v,
                                  void* o, float* lse, cudaStream_t stream) {
   using C = FwdP256;
@@ -383,7 +360,7 @@ cudaError_t launch_fwd256_pair_t(const Problem& pb, const void* q, const void* k
   a.divBHKP = FastDiv(static_cast<uint32_t>(a.BHKP));
   a.divGP = FastDiv(static_cast<uint32_t>(a.G / 2));
   a.divHkv = FastDiv(static_cast<uint32_t>(a.Hkv));
-  const int clusters = max_fwd256_pair_clusters<F16>();
+  const int clusters = max_pair_clusters<swa_fwd256_pair_kernel<F16>>(C::kThreads, C::kSmemBytes);
   const int nclusters = a.ntiles < clusters ? a.ntiles : clusters;
   kern<<<2 * nclusters, C::kThreads, C::kSmemBytes, stream>>>(tq, tk64, tv128, to, a);
   return cudaGetLastError();

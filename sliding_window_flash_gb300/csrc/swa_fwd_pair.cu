@@ -550,32 +550,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
   }
 }
 
-// Clusters of two that can be resident at once with this kernel's shared memory (cached per
-// device and kernel instance).
-template <int D, bool F16>
-int max_pair_clusters() {
-  using C = FwdPairCfg<D>;
-  static std::mutex mu;
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return sm_count() / 2;
-  std::lock_guard<std::mutex> lk(mu);
-  if (cached[dev] == 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * (sm_count() / 2)));
-    cfg.blockDim = dim3(C::kThreads);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, swa_fwd_pair_kernel<D, F16>, &cfg) != cudaSuccess ||
-        n <= 0) {
-      cudaGetLastError();
-      n = sm_count() / 2;
-    }
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
 template <int D, bool F16>
 cudaError_t launch_fwd_pair_d(const Problem& pb, const void* q, const void* k, const void* v,
                               void* o, float* lse, cudaStream_t stream) {
@@ -605,7 +579,7 @@ cudaError_t launch_fwd_pair_d(const Problem& pb, const void* q, const void* k, c
   a.divBHKP = FastDiv(static_cast<uint32_t>(a.BHKP));
   a.divGP = FastDiv(static_cast<uint32_t>(a.G / 2));
   a.divHkv = FastDiv(static_cast<uint32_t>(a.Hkv));
-  const int clusters = max_pair_clusters<D, F16>();
+  const int clusters = max_pair_clusters<swa_fwd_pair_kernel<D, F16>>(C::kThreads, C::kSmemBytes);
   const int nclusters = a.ntiles < clusters ? a.ntiles : clusters;
   kern<<<2 * nclusters, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();

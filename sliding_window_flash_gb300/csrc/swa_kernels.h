@@ -107,6 +107,31 @@ inline int sm_count() {
   return cached[dev];
 }
 
+// Clusters of two CTAs of the pair kernel `Kernel` (launched with `threads` threads and `smem` bytes
+// of dynamic shared memory) that can be resident at once, cached per device and kernel; half the
+// SM count when the occupancy query fails.
+template <auto Kernel>
+int max_pair_clusters(int threads, int smem) {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return sm_count() / 2;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * (sm_count() / 2)));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, Kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = sm_count() / 2;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 // Launchers (each returns the launch's cudaError_t).
 cudaError_t launch_fwd(const Problem& pb, const void* q, const void* k, const void* v, void* o,
                        float* lse, cudaStream_t stream);
