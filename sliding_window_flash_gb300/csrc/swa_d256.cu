@@ -68,27 +68,6 @@ __device__ __forceinline__ bool ring_load(const Ring<kSlots>& rg, int i, const I
   return true;
 }
 
-// Before the CTA exits, no copy may be in flight.  Called by all 32 lanes of both producer
-// warps, `last` being lane 0's last item per slot: the two warps publish their `last` in
-// `s_last` ([2][kSlots] ints) and meet at named barrier 1, then one lane waits (bounded) for the
-// final fill of every slot.  Only the final fill's phase parity is unambiguous: with an odd slot
-// count the producers alternate within a slot, so a producer's own last fill may be followed by
-// the other's, after which the barrier has moved two phases on.
-template <int kSlots>
-__device__ __forceinline__ void ring_drain(const Ring<kSlots>& rg, const int (&last)[kSlots],
-                                           int* s_last, int p, uint32_t lane, unsigned* err) {
-  if (lane == 0)
-    for (int s = 0; s < kSlots; ++s) s_last[p * kSlots + s] = last[s];
-  __syncwarp();
-  named_barrier_sync(1, 64);
-  if (p == 0 && lane == 0) {
-    for (int s = 0; s < kSlots; ++s) {
-      const int f = max(s_last[s], s_last[kSlots + s]);
-      if (f >= 0) drain_wait(rg.full(f), rg.parity(f), err);
-    }
-  }
-}
-
 struct Args256 {
   const float* lse;      // backward input
   float* lse_out;        // forward output
@@ -227,7 +206,7 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
-    ring_drain(rg, last, s_last, p, lane, a.err);
+    d256::drain_ring<C::kSlots>(last, s_last, p, lane, [&](int i) { return rg.full(i); }, a.err);
   } else if (warp == 10) {
     // ------------------------------------------------------------ Q loads, O stores
     auto load_q = [&](int t) {
@@ -447,7 +426,7 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
-    ring_drain(rg, last, s_last, p, lane, a.err);
+    d256::drain_ring<C::kSlots>(last, s_last, p, lane, [&](int i) { return rg.full(i); }, a.err);
   } else if (warp == 10) {
     // ------------------------------------------------------------ Q and dO of each tile
     if (lane == 0) {

@@ -11,6 +11,28 @@ namespace d256 {
 
 constexpr int kChunk = kBlockM * 128;  // one 64-column chunk: 128 rows x 128 bytes
 
+// Before a CTA exits no copy may be in flight.  Called by all 32 lanes of both producer warps of
+// a two-producer ring (p = 0, 1), `last` being lane 0's last item per slot and full(i) the
+// barrier item i completes: the two warps publish their `last` in `s_last` ([2][kSlots] ints),
+// meet at named barrier 1, then one lane waits (bounded) for the final fill of every slot.  Only
+// the final fill's phase parity (item / kSlots) is unambiguous: the producers alternate within a
+// slot, so a producer's own last fill may be followed by the other's, after which the barrier has
+// moved two phases on.
+template <int kSlots, typename FullOf>
+__device__ __forceinline__ void drain_ring(const int (&last)[kSlots], int* s_last, int p,
+                                           uint32_t lane, FullOf full, unsigned* err) {
+  if (lane == 0)
+    for (int s = 0; s < kSlots; ++s) s_last[p * kSlots + s] = last[s];
+  __syncwarp();
+  named_barrier_sync(1, 64);
+  if (p == 0 && lane == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      const int fin = max(s_last[s], s_last[kSlots + s]);
+      if (fin >= 0) drain_wait(full(fin), static_cast<uint32_t>((fin / kSlots) & 1), err);
+    }
+  }
+}
+
 // Column mask of one half-row of scores: keeps columns [lo, hi] of 64, sets the rest to `fill`.
 __device__ __forceinline__ void mask64(float (&x)[64], int lo, int hi, float fill) {
 #pragma unroll
@@ -211,10 +233,8 @@ __device__ __forceinline__ void fwd_softmax(const FwdSoftmax& cx, const Span& sp
       if (!sp.interior(q0, k0)) {
         // Columns c (keys k0 + 64h + c) visible to row `row`, and inside the key sequence.
         const int rel = row + sp.off - k0 - 64 * static_cast<int>(h);
-        const int lo = rel - sp.dmax;
-        const int hi = min(rel - sp.dmin, sp.Lk - 1 - k0 - 64 * static_cast<int>(h));
-#pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = (c >= lo && c <= hi) ? x[c] : SWA_NEG_INF;
+        mask64(x, rel - sp.dmax, min(rel - sp.dmin, sp.Lk - 1 - k0 - 64 * static_cast<int>(h)),
+               SWA_NEG_INF);
       }
       uint32_t pk[32];
       auto exponentiate = [&](float m) -> float {

@@ -245,18 +245,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
       });
       if (p == 0) drain_wait(bar(C::kKFull), 0, a.err);
     }
-    // No copy may be in flight when the CTA exits; only a slot's final fill (the later of the two
-    // producers' last) has an unambiguous parity.
-    if (lane == 0)
-      for (int s = 0; s < C::kSlots; ++s) s_last[p * C::kSlots + s] = last[s];
-    __syncwarp();
-    named_barrier_sync(1, 64);
-    if (p == 0 && lane == 0) {
-      for (int s = 0; s < C::kSlots; ++s) {
-        const int fin = max(s_last[s], s_last[C::kSlots + s]);
-        if (fin >= 0) drain_wait(full(fin), parity(fin), a.err);
-      }
-    }
+    d256::drain_ring<C::kSlots>(last, s_last, p, lane, full, a.err);
   } else if (warp == 9 && lead) {
     // ------------------------------------------------------------ MMA issuer (the pair)
     constexpr uint32_t kIdS = idesc_f16kind(Elem<F16>::kMmaFmt, 2 * kBlockN, kBlockM, false, false);
@@ -502,16 +491,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
       });
       drain_wait(bar(C::kKVFull), 0, a.err);
     }
-    if (lane == 0)
-      for (int s = 0; s < C::kSlots; ++s) s_last[p * C::kSlots + s] = last[s];
-    __syncwarp();
-    named_barrier_sync(1, 64);
-    if (p == 0 && lane == 0) {
-      for (int s = 0; s < C::kSlots; ++s) {
-        const int fin = max(s_last[s], s_last[C::kSlots + s]);
-        if (fin >= 0) drain_wait(full(fin), parity(fin), a.err);
-      }
-    }
+    d256::drain_ring<C::kSlots>(last, s_last, p, lane, full, a.err);
   } else if (warp == 9 && lead) {
     // ------------------------------------------------------------ MMA issuer (the pair)
     constexpr uint32_t kIdS = idesc_f16kind(Elem<F16>::kMmaFmt, 2 * kBlockN, kBlockM, false, false);

@@ -214,18 +214,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
                    return true;
                  });
     }
-    // No copy may be in flight when the CTA exits.  The producers alternate within a slot, so only
-    // the slot's final fill (the later of the two producers' last) has an unambiguous parity.
-    if (lane == 0)
-      for (int s = 0; s < C::kSlots; ++s) s_last[p * C::kSlots + s] = last[s];
-    __syncwarp();
-    named_barrier_sync(1, 64);
-    if (p == 0 && lane == 0) {
-      for (int s = 0; s < C::kSlots; ++s) {
-        const int fin = max(s_last[s], s_last[C::kSlots + s]);
-        if (fin >= 0) drain_wait(full(fin), parity(fin), a.err);
-      }
-    }
+    d256::drain_ring<C::kSlots>(last, s_last, p, lane, full, a.err);
   } else if (warp == 10) {
     // ------------------------------------------------------------ Q and dO of each tile
     if (lane == 0) {
