@@ -551,8 +551,8 @@ struct HostPipe {
   cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
   cudaEvent_t fork = nullptr, join_in = nullptr, join_comp = nullptr, join_out = nullptr;
   cudaEvent_t in_fwd[kMaxHostSlots] = {}, in_done[kMaxHostSlots] = {},
-              fwd_done[kMaxHostSlots] = {}, comp_done[kMaxHostSlots] = {},
-              out_done[kMaxHostSlots] = {};
+              fwd_done[kMaxHostSlots] = {}, dkdv_done[kMaxHostSlots] = {},
+              comp_done[kMaxHostSlots] = {}, out_done[kMaxHostSlots] = {};
 };
 std::mutex g_pipe_mu;
 HostPipe g_pipe[kMaxDevices];
@@ -576,6 +576,7 @@ swa_status host_pipe(HostPipe** out) {
     for (int i = 0; ok && i < kMaxHostSlots; ++i)
       ok = cudaEventCreateWithFlags(&hp.in_fwd[i], ef) == cudaSuccess &&
            cudaEventCreateWithFlags(&hp.in_done[i], ef) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.dkdv_done[i], ef) == cudaSuccess &&
            cudaEventCreateWithFlags(&hp.fwd_done[i], ef) == cudaSuccess &&
            cudaEventCreateWithFlags(&hp.comp_done[i], ef) == cudaSuccess &&
            cudaEventCreateWithFlags(&hp.out_done[i], ef) == cudaSuccess;
@@ -702,21 +703,23 @@ swa_status swa_attn_fwd_bwd_host(const void* q, const void* k, const void* v, co
     if (swa::launch_bwd_delta(pb, so, sdo, sdelta, hp->comp) != cudaSuccess ||
         swa::launch_bwd_dkdv(pb, sq, sk, sv, sdo, slse, sdelta, sdk, sdv, hp->comp) !=
             cudaSuccess ||
+        cudaEventRecord(hp->dkdv_done[slot], hp->comp) != cudaSuccess ||
         swa::launch_bwd_dq(pb, sq, sk, sv, sdo, slse, sdelta, sdq, hp->comp) != cudaSuccess ||
         cudaEventRecord(hp->comp_done[slot], hp->comp) != cudaSuccess) {
       result = SWA_ERR_CUDA;
       break;
     }
     // outputs of chunk c: O and LSE as soon as the forward has written them (the backward only
-    // reads them), the gradients after the backward
+    // reads them), dK and dV once their kernel is done (while dQ is computed), then dQ
     if (cudaStreamWaitEvent(hp->out, hp->fwd_done[slot], 0) != cudaSuccess ||
         !d2h(at(o, u0 * q_unit), so, n * q_unit) || !d2h(at(lse, u0 * l_unit), slse, n * l_unit) ||
+        cudaStreamWaitEvent(hp->out, hp->dkdv_done[slot], 0) != cudaSuccess ||
+        !d2h(at(dk, u0 * k_unit), sdk, n * k_unit) || !d2h(at(dv, u0 * k_unit), sdv, n * k_unit) ||
         cudaStreamWaitEvent(hp->out, hp->comp_done[slot], 0) != cudaSuccess) {
       result = SWA_ERR_CUDA;
       break;
     }
-    if (!d2h(at(dq, u0 * q_unit), sdq, n * q_unit) || !d2h(at(dk, u0 * k_unit), sdk, n * k_unit) ||
-        !d2h(at(dv, u0 * k_unit), sdv, n * k_unit) ||
+    if (!d2h(at(dq, u0 * q_unit), sdq, n * q_unit) ||
         cudaEventRecord(hp->out_done[slot], hp->out) != cudaSuccess) {
       result = SWA_ERR_CUDA;
       break;
